@@ -1,0 +1,403 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV cache hot path on GB300.
+
+Headline: paged decode attention KV-read GB/s (and sequences/s) at the LLaMA-2-7B layer shape
+-- 32 sequences, 32 query = 32 KV heads, head_dim 128, fp16, block_size 16, context lengths
+uniform in [1, 4096], physical blocks from a seeded permutation of a pool sized 110% of need.
+One step = one pass of the decode hot path over that batch: slot indexing of the 32 new tokens
+-> paged append of their K/V -> split-K paged decode attention over L+1 tokens -> split merge.
+value = KV bytes the attention reads per step (sum(L+1) x 32 heads x 128 x 2 B x 2) / step time.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): each rank runs its own batch (seed + rank), weak scaling,
+no collective on the data path; value = all ranks' KV bytes / the slowest rank's time.
+--impl reference times the CPU oracle (fp64 C) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV-read GB/s and seqs/s at 7B shape; % of GB300 HBM peak"
+WORKLOAD = ("LLaMA-2-7B-shape single-layer paged decode: 32 seqs, 32 q heads = 32 KV heads, head_dim 128, "
+            "fp16, block_size 16, context U[1,4096] + 1 appended token, pool 110% of need, permuted block ids")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, path: str):
+        self.path = path
+        self.proc = None
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _reduce_max(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _reduce_sum(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def _barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------------------------- CPU oracle
+
+def oracle_decode_rate(w, budget_s: float, max_seqs=None):
+    """Time the fp64 CPU oracle on a decode pass over a subset of the batch.
+
+    Returns (GB/s of KV read, seconds per pass, sequences in the sample, threads)."""
+    import oracle
+    from oracle import steps
+    nseq = w.num_seqs if max_seqs is None else max(1, min(w.num_seqs, max_seqs))
+    r = steps.decode_step(w)   # builds the oracle's own pool (slots + appends), untimed
+    lens = w.decode_lens.copy()
+    lens[nseq:] = 0
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.paged_decode(w.q, w.model_dtype, r["pool"], oracle.contiguous_strides(w.num_blocks, w.num_kv_heads,
+                                                                                      w.block_size, w.head_dim),
+                            w.kv_dtype, w.num_blocks, w.block_tables, lens, w.num_kv_heads, w.block_size,
+                            float(w.scale), w.k_scale, w.v_scale)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    kv = int(lens.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    return kv / dt / 1e9, dt, nseq, oracle.num_threads(), reps
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_cache_134_gb300 import workloads as W
+    oracle.build()
+    w = W.decode7b()
+    # size each step: a subset of the sequences so that warmup + steps stay within ~60 s
+    _, t_full, _, threads, _ = oracle_decode_rate(w, 0.0)
+    per_step = 60.0 / max(1, args.steps + args.warmup)
+    nseq = max(1, min(w.num_seqs, int(w.num_seqs * per_step / max(t_full, 1e-9))))
+    from oracle import steps
+    import oracle as O
+    r = steps.decode_step(w)
+    lens = w.decode_lens.copy()
+    lens[nseq:] = 0
+    st = O.contiguous_strides(w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+
+    def step():
+        O.paged_decode(w.q, w.model_dtype, r["pool"], st, w.kv_dtype, w.num_blocks, w.block_tables, lens,
+                       w.num_kv_heads, w.block_size, float(w.scale))
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    kv = int(lens.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    gbs = kv / dt / 1e9
+    sample = f"decode attention of the first {nseq} of {w.num_seqs} sequences per step (KV {kv / 1e6:.1f} MB)"
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "seqs_per_s": round(nseq / dt, 3),
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------------------------- GPU path
+
+def _time_loop(fn, steps, stream):
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / 1e3
+
+
+def secondary_prefill(P, W, gpu_path, peaks, reps=20):
+    """Packed causal prefill of 5256 tokens (lengths 128..2048), 32 heads, D=128, fp16, bs=16."""
+    w = W.prefill()
+    md = gpu_path.TORCH_DT[w.dtype]
+    cache = gpu_path.new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.dtype, w.dtype)
+    q, k, v = gpu_path.dev(w.q, md), gpu_path.dev(w.k, md), gpu_path.dev(w.v, md)
+    cu, tables = gpu_path.dev(w.cu_seqlens), gpu_path.dev(w.block_tables)
+    out = torch.empty_like(q)
+
+    def step():
+        P.packed_prefill_attention(q, k, v, cu, w.max_seqlen, tables, cache, float(w.scale), out=out)
+
+    try:
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+    except Exception as e:  # reported, not hidden
+        cache.close()
+        return {"status": f"unavailable: {e}"}
+    cache.profile_start()
+    dt = _time_loop(step, reps, torch.cuda.current_stream()) / reps
+    prof = cache.profile_read()
+    err = cache.check_error()
+    cache.close()
+    kern = prof["prefill_ms"] / max(1, prof["prefill_launches"]) / 1e3
+    tflops = w.flops() / kern / 1e12
+    return {"workload": "packed causal prefill, lengths 128,200,512,1024,2048,256,64,1024 (5256 tokens), "
+                        "32 heads, D=128, fp16, bs=16", "tokens_per_s": round(w.total_tokens / dt, 1),
+            "ms": round(dt * 1e3, 4), "kernel_ms": round(kern * 1e3, 4), "tflops": round(tflops, 2),
+            "causal_gflop": round(w.flops() / 1e9, 3),
+            "frac_of_bf16_peak": round(tflops / peaks[1], 4), "device_errors": err}
+
+
+def secondary_append(P, W, gpu_path, peaks, reps=20):
+    """Bulk paged append of 5256 tokens x 32 heads x 128 fp16 (86 MB read + 86 MB written)."""
+    w = W.prefill()
+    md = gpu_path.TORCH_DT[w.dtype]
+    cache = gpu_path.new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.dtype, w.dtype)
+    k, v = gpu_path.dev(w.k, md), gpu_path.dev(w.v, md)
+    seq = np.repeat(np.arange(len(w.lengths), dtype=np.int32), w.lengths)
+    pos = np.concatenate([np.arange(n, dtype=np.int32) for n in w.lengths])
+    slots = P.paged_slot_mapping(gpu_path.dev(w.block_tables), gpu_path.dev(seq), gpu_path.dev(pos), w.block_size)
+    for _ in range(3):
+        P.paged_kv_append(cache, k, v, slots)
+    torch.cuda.synchronize()
+    cache.profile_start()
+    _time_loop(lambda: P.paged_kv_append(cache, k, v, slots), reps, torch.cuda.current_stream())
+    prof = cache.profile_read()
+    cache.close()
+    kern = prof["append_ms"] / max(1, prof["append_launches"]) / 1e3
+    nbytes = 2 * (k.numel() + v.numel()) * 2 + slots.numel() * 8
+    return {"workload": "bulk append of 5256 tokens, 32 KV heads, D=128, fp16", "kernel_ms": round(kern * 1e3, 4),
+            "gbs": round(nbytes / kern / 1e9, 1), "frac_of_hbm": round(nbytes / kern / 1e9 / peaks[0], 4)}
+
+
+def run_ours(args):
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import paged_kv_cache_134_gb300 as P
+    from paged_kv_cache_134_gb300 import workloads as W
+    from paged_kv_cache_134_gb300 import runner as G
+
+    peaks = _peaks()
+    w = W.decode7b(seed=1002 + rank)
+    cache = G.new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype, w.model_dtype)
+    G.fill_cache(cache, w)
+    x = G.DecodeInputs(w)
+    cache.reserve(w.num_seqs, w.num_q_heads, w.max_blocks)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    step = lambda: G.decode_step(cache, x)  # noqa: E731
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert cache.check_error() == 0
+
+    # ---- timed region: inputs resident in HBM; KV (1.07 GB/step) is larger than L2 (129 MB)
+    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
+        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, f"/tmp/pkv_clocks_{rank}.csv")
+    time.sleep(0.2)
+    launches0 = P.kernel_launches()
+    cache.profile_start()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    elapsed = _time_loop(step, args.steps, stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    prof = cache.profile_read()
+    launches = P.kernel_launches() - launches0
+    clocks = sampler.stop()
+    assert cache.check_error() == 0
+
+    kv_bytes = w.kv_read_bytes()
+    elapsed_max = _reduce_max(elapsed, ws)
+    total_bytes = _reduce_sum(float(kv_bytes) * args.steps, ws)
+    total_seqs = _reduce_sum(float(w.num_seqs) * args.steps, ws)
+    value = total_bytes / elapsed_max / 1e9
+    dec_kernel_s = prof["decode_ms"] / max(1, prof["decode_launches"]) / 1e3
+    achieved = kv_bytes / dec_kernel_s / 1e9
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
+    h = {name: t.cpu().pin_memory() for name, t in (("q", x.q), ("k", x.new_k), ("v", x.new_v), ("tables", x.tables),
+                                                     ("pos", x.positions), ("lens", x.lens))}
+    h_out = torch.empty(x.out.shape, dtype=x.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        x.q.copy_(h["q"], non_blocking=True)
+        x.new_k.copy_(h["k"], non_blocking=True)
+        x.new_v.copy_(h["v"], non_blocking=True)
+        x.tables.copy_(h["tables"], non_blocking=True)
+        x.positions.copy_(h["pos"], non_blocking=True)
+        x.lens.copy_(h["lens"], non_blocking=True)
+        G.decode_step(cache, x)
+        h_out.copy_(x.out, non_blocking=True)
+
+    e2e_steps = max(10, min(args.steps, 1000))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    e2e_t = _reduce_max(_time_loop(e2e_step, e2e_steps, stream), ws)
+    e2e_value = _reduce_sum(float(kv_bytes) * e2e_steps, ws) / e2e_t / 1e9
+
+    secondary = {}
+    if rank == 0 and not args.skip_secondary:
+        secondary["prefill"] = secondary_prefill(P, W, G, peaks)
+        secondary["append"] = secondary_append(P, W, G, peaks)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.skip_cpu:
+        gbs, t_pass, nseq, threads, reps = oracle_decode_rate(w, budget_s=args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"full decode attention pass over all {nseq} sequences, repeated {reps}x "
+                         f"({t_pass:.2f} s per pass, fp64 C, OpenMP)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(elapsed_max / args.steps * 1e3, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                       "num_blocks": w.num_blocks, "tokens_attended": int(w.decode_lens.sum()),
+                       "kv_bytes_per_step": kv_bytes, "per_rank_seed": "1002 + rank",
+                       "l2": "inputs larger than L2 (KV read per step 1.07 GB vs 129 MB L2)",
+                       "split_tokens": int(os.environ.get("PAGEDKV_SPLIT_TOKENS", "256")),
+                       "parallelism": f"replicas x{ws} (one independent batch per GPU)"},
+            "seqs_per_s": round(total_seqs / elapsed_max, 1),
+            "seqs_per_s_32_layers": round(total_seqs / elapsed_max / 32, 1),
+            "hbm_frac": round(value / peaks[0], 4),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks[0], "unit": "GB/s",
+                         "frac": round(achieved / peaks[0], 4), "traffic": None,
+                         "kernel": "pkv_decode::decode_kernel<128,1,f16,f16>",
+                         "kernel_ms": round(dec_kernel_s * 1e3, 5),
+                         "peak_source": f"{peaks[3]} hbm_gbs (MEASURED_PEAKS.json)",
+                         "algorithmic_bytes": "KV read: sum(L+1) x Hkv x D x 2 B x 2 (K and V) per launch"},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "secondary": secondary,
+        }
+        print(json.dumps(line), flush=True)
+    cache.close()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-secondary", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

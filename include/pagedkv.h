@@ -1,0 +1,165 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged KV cache library.
+ *
+ * What it computes (the passages each call restates are named per call):
+ *   a paged KV cache is one flat device pool cut into num_blocks equal blocks of
+ *   block_size tokens; each sequence owns a block table whose entry i names the
+ *   physical block holding its logical block i ("PagedAttention 与前缀缓存",
+ *   2kiu.com, sections 2.1-2.2).  Token t of sequence s lives in physical block
+ *   block_table[s][t / block_size] at offset t % block_size ("Paged KV Cache 与
+ *   Packed Sequence", discosf.com, section 2.2).
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument except the cache handle and the outputs of
+ *     kv_cache_view / kv_cache_check_error / kv_cache_profile_read is a DEVICE
+ *     pointer owned by the caller, 16-byte aligned for q/k/v/out, valid until the
+ *     work queued on `stream` has finished.  The library owns only what a cache
+ *     handle holds: the block pool, the FP8 scales, a device error word and the
+ *     split-K workspace of the decode.
+ *   - `stream` is a cudaStream_t passed as void*; 0 is the legacy default stream.
+ *     Every call only enqueues work on it and returns; nothing synchronises except
+ *     kv_cache_check_error and kv_cache_profile_read.
+ *   - Dtypes: PKV_F16 / PKV_BF16 / PKV_FP8_E4M3.  q, k, v and out are in the
+ *     cache's model dtype (fp16 or bf16); the pool is in its KV dtype.
+ *   - Return value: PKV_OK or a negative pkv_status; pkv_last_error() gives a
+ *     message for the calling thread's last failure.  Host-side validation fails
+ *     before anything is enqueued.  Data that only the device sees (block ids,
+ *     slots, lengths, cu_seqlens) is checked in the kernels: the offending element
+ *     is skipped, a bit is or-ed into the cache's device error word, and the
+ *     kernel carries on; nothing traps.
+ *   - Supported shapes: head_dim in {64, 128}; block_size in {8, 16, 32};
+ *     num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pkv_cache *pkv_cache_t; /* opaque; created by kv_cache_create */
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_EINVAL = -1,       /* bad argument (null pointer, size, alignment, dtype mix) */
+    PKV_ENOMEM = -2,       /* device allocation failed */
+    PKV_ECUDA = -3,        /* a CUDA runtime call or launch failed */
+    PKV_EUNSUPPORTED = -4, /* shape outside the supported set */
+    PKV_EDEVICE = -5       /* kv_cache_check_error found device-side errors */
+} pkv_status;
+
+/* bits of the device error word */
+#define PKV_DEVERR_BLOCK_ID 1u   /* a needed block-table entry was outside [0, num_blocks) */
+#define PKV_DEVERR_SLOT 2u       /* an append slot was >= num_blocks * block_size */
+#define PKV_DEVERR_LENGTH 4u     /* a length needed more than max_blocks_per_seq blocks */
+#define PKV_DEVERR_CU_SEQLENS 8u /* cu_seqlens decreasing, or a length above max_seqlen */
+#define PKV_DEVERR_TIMEOUT 16u   /* a bounded wait inside a kernel gave up */
+
+/* Create a cache: cudaMalloc a pool of num_blocks blocks, each holding K and V of
+ * block_size tokens x num_kv_heads heads x head_dim, in kv_dtype (zero-filled).
+ * model_dtype is the dtype of q/k/v/out used with this cache; it must equal
+ * kv_dtype unless kv_dtype is PKV_FP8_E4M3.  The pool is the "flat device pool of
+ * equal blocks" of 2kiu.com section 2.2 / discosf.com section 2.1.  Pool layout
+ * (see kv_cache_view): [num_blocks][2 = K,V][num_kv_heads][block_size][head_dim],
+ * so one (block, K|V, head) tile is block_size*head_dim contiguous elements.
+ * On failure *out is untouched. */
+int kv_cache_create(int64_t num_blocks, int block_size, int num_kv_heads, int head_dim, pkv_dtype kv_dtype,
+                    pkv_dtype model_dtype, pkv_cache_t *out);
+
+/* Free everything the handle owns (synchronises the device first).  NULL is a no-op. */
+int kv_cache_destroy(pkv_cache_t cache);
+
+/* FP8 caches: copy per-KV-head fp32 scales (device arrays of num_kv_heads floats) into
+ * the cache.  Stored code = E4M3(fp32(x) / scale[head]), rounded to nearest-even and
+ * saturated to +-448; readers multiply the code's value by the scale (the one-byte
+ * cache of 2kiu.com section 1.1).  Scales must be finite and > 0; EINVAL for other caches. */
+int kv_cache_set_scales(pkv_cache_t cache, const float *k_scale, const float *v_scale, void *stream);
+
+/* Describe the pool for tests and initialisation: *base = device address of the pool,
+ * strides_elems = element strides of the (block, K|V, head, offset, dim) axes,
+ * *num_bytes = pool size in bytes.  The library keeps ownership. */
+int kv_cache_view(pkv_cache_t cache, void **base, int64_t strides_elems[5], int64_t *num_bytes);
+
+/* Pre-size the decode split-K workspace for up to max_seqs x max_q_heads rows and tables
+ * of max_blocks_per_seq entries, so that later decode calls allocate nothing. */
+int kv_cache_reserve(pkv_cache_t cache, int max_seqs, int max_q_heads, int max_blocks_per_seq);
+
+/* Synchronise the device, return the device error word's bits in *device_code and clear
+ * it.  Returns PKV_EDEVICE when any bit was set, PKV_OK otherwise. */
+int kv_cache_check_error(pkv_cache_t cache, int *device_code);
+
+/* Message for the calling thread's most recent non-OK return ("" if none). */
+const char *pkv_last_error(void);
+
+/* Slot indexing (discosf.com section 2.2; 2kiu.com section 4.1 step 3):
+ *   slot_mapping[i] = block_tables[seq_ids[i]][positions[i] / block_size] * block_size
+ *                     + positions[i] % block_size                       (int64)
+ * or -1 when seq_ids[i] is outside [0, num_rows), positions[i] < 0, the logical block is
+ * >= max_blocks_per_seq, or the table entry is negative.
+ * block_tables: int32 [num_rows][max_blocks_per_seq], row-major.  seq_ids, positions:
+ * int32 [num_tokens].  slot_mapping: int64 [num_tokens] (written).  Exact integer work. */
+int paged_slot_mapping(const int32_t *block_tables, int num_rows, int max_blocks_per_seq, const int32_t *seq_ids,
+                       const int32_t *positions, int64_t num_tokens, int block_size, int64_t *slot_mapping,
+                       void *stream);
+
+/* Paged KV append (2kiu.com section 4.1 step 3 and section 6.3; discosf.com section 4.3
+ * step 2): for each token j with slot = slot_mapping[j] >= 0, write k[j] and v[j]
+ * ([num_tokens][num_kv_heads][head_dim], model dtype) into block slot / block_size at
+ * offset slot % block_size.  fp16/bf16 caches store the bits unchanged; FP8 caches store
+ * E4M3(fp32(x) / scale[head]) (see kv_cache_set_scales).  Negative slots are padding and
+ * skipped; slots >= num_blocks*block_size are skipped and set PKV_DEVERR_SLOT.  Two
+ * tokens with the same slot in one call: which one lands is unspecified. */
+int paged_kv_append(pkv_cache_t cache, const void *k, const void *v, const int64_t *slot_mapping,
+                    int64_t num_tokens, void *stream);
+
+/* Paged decode attention (2kiu.com section 2.3: walk the block table, mask the tail
+ * block by the true length; section 3.3: prefix blocks are read per sequence):
+ *   out[s][h] = sum_{t < L_s} softmax_t(scale * q[s][h] . K_t) V_t,  L_s = context_lens[s],
+ * K_t/V_t read from block block_tables[s][t / block_size], offset t % block_size, KV head
+ * h / (num_q_heads / num_kv_heads).  q, out: [num_seqs][num_q_heads][head_dim] model dtype;
+ * block_tables: int32 [num_seqs][max_blocks_per_seq]; entries past ceil(L_s/block_size)
+ * are never read.  L_s == 0 gives a zero row.  fp32 accumulation and softmax; the output
+ * is rounded to the model dtype (nearest-even).  num_seqs <= 1024.  Runs a split-K pass
+ * over block-aligned chunks of each sequence plus a merge; split boundaries depend only on
+ * L_s, so results do not depend on block placement.  The workspace grows (cudaMalloc) on
+ * demand unless kv_cache_reserve covered the call. */
+int paged_decode_attention(const void *q, pkv_cache_t cache, const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *context_lens, int num_seqs, int num_q_heads, float scale, void *out,
+                           void *stream);
+
+/* Packed causal prefill (discosf.com sections 3.1-3.3 and 4.2): sequences packed back to
+ * back, sequence i owning rows [cu_seqlens[i], cu_seqlens[i+1]):
+ *   out[cu_i + r][h] = sum_{c <= r} softmax_c(scale * q[cu_i + r][h] . k[cu_i + c][g]) v[cu_i + c][g]
+ * with g = h / (num_q_heads / num_kv_heads); no attention across sequences.  The same call
+ * writes every token's k/v into the cache at block_tables[i][r / block_size], offset
+ * r % block_size (the bytes paged_kv_append would write).  q, out: [T][num_q_heads][head_dim];
+ * k, v: [T][num_kv_heads][head_dim] (model dtype, T = cu_seqlens[num_seqs]);
+ * cu_seqlens: int32 [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0; max_seqlen >= every
+ * length.  fp16/bf16 caches only (EUNSUPPORTED for FP8).  Q.K^T and P.V run on the tensor
+ * cores (tcgen05, fp32 accumulation in tensor memory); P is rounded to the model dtype for P.V. */
+int packed_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens, int num_seqs,
+                             int max_seqlen, const int32_t *block_tables, int max_blocks_per_seq, pkv_cache_t cache,
+                             int num_q_heads, float scale, void *out, void *stream);
+
+/* Profiling.  Between kv_cache_profile_start and kv_cache_profile_read the library records
+ * CUDA events around each main kernel it launches for this cache (decode split-K kernel,
+ * prefill kernel, append kernel) on the launch stream.  kv_cache_profile_read synchronises
+ * those events and returns the summed device time per kind (milliseconds) and launch
+ * counts, then stops recording.  pkv_kernel_launches counts every kernel this library
+ * launched in the process (all caches and free functions). */
+typedef struct {
+    int64_t decode_launches, prefill_launches, append_launches;
+    double decode_ms, prefill_ms, append_ms;
+} pkv_profile_t;
+int kv_cache_profile_start(pkv_cache_t cache);
+int kv_cache_profile_read(pkv_cache_t cache, pkv_profile_t *out);
+int64_t pkv_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H */

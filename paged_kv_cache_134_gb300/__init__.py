@@ -1,0 +1,11 @@
+"""GB300-native paged KV cache: paged append, paged decode attention and packed causal
+prefill, hand-written CUDA for sm_103a behind the C ABI declared in include/pagedkv.h.
+
+``binding`` marshals torch tensors into that ABI (no computation in Python);
+``workloads`` generates the seeded synthetic inputs; ``build`` compiles the library.
+"""
+from .binding import (KVCache, PagedKVError, kernel_launches, lib, packed_prefill_attention,  # noqa: F401
+                      paged_decode_attention, paged_kv_append, paged_slot_mapping)
+
+__all__ = ["KVCache", "PagedKVError", "kernel_launches", "lib", "packed_prefill_attention",
+           "paged_decode_attention", "paged_kv_append", "paged_slot_mapping"]

@@ -1,0 +1,248 @@
+"""Thin ctypes binding over the C ABI of ``libpagedkv.so`` (include/pagedkv.h).
+
+Argument marshalling only: tensors are checked for device, dtype, shape and contiguity and
+passed as raw device pointers together with torch's current CUDA stream.  Every step of the
+hot path runs in the library's kernels.  If the library has not been built, every call
+raises ``RuntimeError``: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libpagedkv.so")
+
+PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
+_DT = {"f16": PKV_F16, "bf16": PKV_BF16, "fp8": PKV_FP8_E4M3}
+_TORCH = {PKV_F16: torch.float16, PKV_BF16: torch.bfloat16}
+DEVERR = {1: "block id", 2: "slot", 4: "length", 8: "cu_seqlens", 16: "timeout"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"pagedkv status {status}: {msg}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library {LIB_PATH} is not built; run __graft_entry__.build() "
+                               "(paged_kv_cache_134_gb300.build.build()) on a machine with nvcc")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.kv_cache_create.argtypes = [i64, i32, i32, i32, i32, i32, ctypes.POINTER(vp)]
+        L.kv_cache_destroy.argtypes = [vp]
+        L.kv_cache_set_scales.argtypes = [vp, vp, vp, vp]
+        L.kv_cache_view.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        L.kv_cache_reserve.argtypes = [vp, i32, i32, i32]
+        L.kv_cache_check_error.argtypes = [vp, ctypes.POINTER(i32)]
+        L.pkv_last_error.restype = ctypes.c_char_p
+        L.paged_slot_mapping.argtypes = [vp, i32, i32, vp, vp, i64, i32, vp, vp]
+        L.paged_kv_append.argtypes = [vp, vp, vp, vp, i64, vp]
+        L.paged_decode_attention.argtypes = [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]
+        L.packed_prefill_attention.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, vp, i32, ctypes.c_float, vp, vp]
+        L.kv_cache_profile_start.argtypes = [vp]
+        L.kv_cache_profile_read.argtypes = [vp, ctypes.c_void_p]
+        L.pkv_kernel_launches.restype = i64
+        _lib = L
+        return L
+
+
+class _Profile(ctypes.Structure):
+    _fields_ = [("decode_launches", ctypes.c_int64), ("prefill_launches", ctypes.c_int64),
+                ("append_launches", ctypes.c_int64), ("decode_ms", ctypes.c_double),
+                ("prefill_ms", ctypes.c_double), ("append_ms", ctypes.c_double)]
+
+
+def _check(status: int):
+    if status != 0:
+        raise PagedKVError(status, lib().pkv_last_error().decode(errors="replace"))
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _req(t: torch.Tensor, name: str, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+class _DevMem:
+    """Exposes a raw device range through __cuda_array_interface__ for a zero-copy torch view."""
+
+    def __init__(self, ptr: int, nbytes: int, owner):
+        self.__cuda_array_interface__ = {"shape": (int(nbytes),), "typestr": "|u1", "data": (int(ptr), False),
+                                         "version": 3, "strides": None}
+        self._owner = owner
+
+
+class KVCache:
+    """A block pool on the current CUDA device (kv_cache_create)."""
+
+    def __init__(self, num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
+                 kv_dtype: str = "f16", model_dtype: Optional[str] = None):
+        L = lib()
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        self.num_kv_heads, self.head_dim = int(num_kv_heads), int(head_dim)
+        self.kv_dtype = kv_dtype
+        self.model_dtype = model_dtype or (kv_dtype if kv_dtype != "fp8" else "bf16")
+        h = ctypes.c_void_p()
+        _check(L.kv_cache_create(self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim,
+                                 _DT[kv_dtype], _DT[self.model_dtype], ctypes.byref(h)))
+        self._h = h
+        self.torch_dtype = _TORCH[_DT[self.model_dtype]]
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if self._h is None:
+            raise RuntimeError("cache is closed")
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            lib().kv_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def view(self):
+        """(uint8 tensor over the whole pool, element strides of (block, K|V, head, offset, dim))."""
+        base = ctypes.c_void_p()
+        st = (ctypes.c_int64 * 5)()
+        nbytes = ctypes.c_int64()
+        _check(lib().kv_cache_view(self.handle, ctypes.byref(base), st, ctypes.byref(nbytes)))
+        raw = torch.as_tensor(_DevMem(base.value, nbytes.value, self), device="cuda")
+        return raw, [int(x) for x in st]
+
+    def pool_elems(self) -> torch.Tensor:
+        """The pool as a flat tensor of raw elements (int16 for 16-bit caches, uint8 for FP8)."""
+        raw, _ = self.view()
+        return raw if self.kv_dtype == "fp8" else raw.view(torch.int16)
+
+    def set_scales(self, k_scale: torch.Tensor, v_scale: torch.Tensor):
+        _req(k_scale, "k_scale", torch.float32, 1)
+        _req(v_scale, "v_scale", torch.float32, 1)
+        if k_scale.numel() != self.num_kv_heads or v_scale.numel() != self.num_kv_heads:
+            raise ValueError("one scale per KV head")
+        _check(lib().kv_cache_set_scales(self.handle, _ptr(k_scale), _ptr(v_scale), _stream()))
+
+    def reserve(self, max_seqs: int, max_q_heads: int, max_blocks_per_seq: int):
+        _check(lib().kv_cache_reserve(self.handle, int(max_seqs), int(max_q_heads), int(max_blocks_per_seq)))
+
+    def check_error(self) -> int:
+        """Synchronise and return (and clear) the device error bits; 0 when clean."""
+        code = ctypes.c_int(0)
+        st = lib().kv_cache_check_error(self.handle, ctypes.byref(code))
+        if st not in (0, -5):
+            _check(st)
+        return int(code.value)
+
+    def profile_start(self):
+        _check(lib().kv_cache_profile_start(self.handle))
+
+    def profile_read(self) -> dict:
+        p = _Profile()
+        _check(lib().kv_cache_profile_read(self.handle, ctypes.byref(p)))
+        return {k: getattr(p, k) for k, _ in _Profile._fields_}
+
+
+def kernel_launches() -> int:
+    return int(lib().pkv_kernel_launches())
+
+
+def paged_slot_mapping(block_tables: torch.Tensor, seq_ids: torch.Tensor, positions: torch.Tensor,
+                       block_size: int, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    _req(block_tables, "block_tables", torch.int32, 2)
+    _req(seq_ids, "seq_ids", torch.int32, 1)
+    _req(positions, "positions", torch.int32, 1)
+    n = positions.numel()
+    if seq_ids.numel() != n:
+        raise ValueError("seq_ids and positions differ in length")
+    if out is None:
+        out = torch.empty(n, dtype=torch.int64, device=positions.device)
+    _req(out, "out", torch.int64, 1)
+    _check(lib().paged_slot_mapping(_ptr(block_tables), block_tables.shape[0], block_tables.shape[1],
+                                    _ptr(seq_ids), _ptr(positions), n, int(block_size), _ptr(out), _stream()))
+    return out
+
+
+def paged_kv_append(cache: KVCache, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor) -> None:
+    _req(k, "k", cache.torch_dtype, 3)
+    _req(v, "v", cache.torch_dtype, 3)
+    _req(slot_mapping, "slot_mapping", torch.int64, 1)
+    n = k.shape[0]
+    if tuple(k.shape) != (n, cache.num_kv_heads, cache.head_dim) or k.shape != v.shape:
+        raise ValueError(f"k/v must be [T, {cache.num_kv_heads}, {cache.head_dim}]")
+    if slot_mapping.numel() != n:
+        raise ValueError("slot_mapping length != number of tokens")
+    _check(lib().paged_kv_append(cache.handle, _ptr(k), _ptr(v), _ptr(slot_mapping), n, _stream()))
+
+
+def paged_decode_attention(q: torch.Tensor, cache: KVCache, block_tables: torch.Tensor,
+                           context_lens: torch.Tensor, scale: float,
+                           out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    _req(q, "q", cache.torch_dtype, 3)
+    _req(block_tables, "block_tables", torch.int32, 2)
+    _req(context_lens, "context_lens", torch.int32, 1)
+    S, hq, d = q.shape
+    if d != cache.head_dim or block_tables.shape[0] != S or context_lens.numel() != S:
+        raise ValueError("shape mismatch between q, block_tables and context_lens")
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, "out", cache.torch_dtype, 3)
+    _check(lib().paged_decode_attention(_ptr(q), cache.handle, _ptr(block_tables), block_tables.shape[1],
+                                        _ptr(context_lens), S, hq, ctypes.c_float(scale), _ptr(out), _stream()))
+    return out
+
+
+def packed_prefill_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                             max_seqlen: int, block_tables: torch.Tensor, cache: KVCache, scale: float,
+                             out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _req(t, name, cache.torch_dtype, 3)
+    _req(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _req(block_tables, "block_tables", torch.int32, 2)
+    T, hq, d = q.shape
+    if k.shape != (T, cache.num_kv_heads, d) or v.shape != k.shape or d != cache.head_dim:
+        raise ValueError("q/k/v shape mismatch")
+    nseq = cu_seqlens.numel() - 1
+    if block_tables.shape[0] != nseq:
+        raise ValueError("one block-table row per sequence")
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, "out", cache.torch_dtype, 3)
+    _check(lib().packed_prefill_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseq, int(max_seqlen),
+                                          _ptr(block_tables), block_tables.shape[1], cache.handle, hq,
+                                          ctypes.c_float(scale), _ptr(out), _stream()))
+    return out

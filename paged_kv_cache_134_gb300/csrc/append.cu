@@ -1,0 +1,133 @@
+// Slot indexing and paged KV append.
+//
+// Slot indexing: token t of sequence s goes to physical block block_table[s][t / bs] at
+// offset t % bs ("Paged KV Cache 与 Packed Sequence", discosf.com, section 2.2).
+// Append: the new token's K/V is written at exactly that (block, offset) and nowhere else
+// ("PagedAttention 与前缀缓存", 2kiu.com, section 4.1 step 3 and section 6.3).
+//
+// Both are HBM-bound scatter/gather work: 16-byte vector loads and stores, one thread per
+// 16-byte source chunk, consecutive threads on consecutive chunks of a (token, K|V, head)
+// row so that every warp moves whole contiguous 256-byte rows.
+#include "device_common.cuh"
+#include "pkv_internal.h"
+
+namespace {
+
+__global__ void slot_mapping_kernel(const int32_t *__restrict__ tables, int rows, int max_blocks,
+                                    const int32_t *__restrict__ seq_ids, const int32_t *__restrict__ positions,
+                                    int64_t n, int bs, int64_t *__restrict__ out) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int s = seq_ids[i], p = positions[i];
+        int64_t slot = -1;
+        if (s >= 0 && s < rows && p >= 0) {
+            const int lb = p / bs;
+            if (lb < max_blocks) {
+                const int b = tables[(int64_t)s * max_blocks + lb];
+                if (b >= 0) slot = (int64_t)b * bs + p % bs;
+            }
+        }
+        out[i] = slot;
+    }
+}
+
+struct AppendArgs {
+    const uint4 *k, *v;   // [n][Hkv][D] model dtype, viewed as 16-byte chunks
+    const int64_t *slots;
+    char *pool;
+    const float *k_scale, *v_scale;
+    unsigned int *err;
+    int64_t n, num_slots;
+    int hkv, bs, chunks_per_row; // chunks_per_row = D / 8
+    int64_t tile_elems;          // bs * D
+    int d;
+};
+
+// KVT: 0 = 16-bit cache (bit copy), 2 = E4M3 cache; MT = model dtype for the E4M3 path
+template <int KVT, int MT>
+__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+    const int64_t per_token = 2LL * a.hkv * a.chunks_per_row;
+    const int64_t total = a.n * per_token;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t j = i / per_token;
+        const int rem = static_cast<int>(i - j * per_token);
+        const int kv = rem / (a.hkv * a.chunks_per_row);
+        const int hc = rem - kv * a.hkv * a.chunks_per_row;
+        const int h = hc / a.chunks_per_row;
+        const int c = hc - h * a.chunks_per_row;
+        const int64_t slot = a.slots[j];
+        if (slot < 0) continue;
+        if (slot >= a.num_slots) {
+            if (rem == 0) set_error(a.err, PKV_DEVERR_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / a.bs;
+        const int off = static_cast<int>(slot - blk * a.bs);
+        // element index of (blk, kv, h, off, c*8) in the [NB][2][Hkv][bs][D] pool
+        const int64_t e = ((blk * 2 + kv) * a.hkv + h) * a.tile_elems + (int64_t)off * a.d + c * 8;
+        const uint4 src = (kv ? a.v : a.k)[j * a.hkv * a.chunks_per_row + hc];
+        if constexpr (KVT != PKV_FP8_E4M3) {
+            reinterpret_cast<uint4 *>(a.pool)[e / 8] = src;
+        } else {
+            float f[8];
+            cvt8<MT>(src, f);
+            const float s = (kv ? a.v_scale : a.k_scale)[h];
+            uint2 o;
+            o.x = e4m3x2_from_f32(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
+                  (e4m3x2_from_f32(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
+            o.y = e4m3x2_from_f32(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s)) |
+                  (e4m3x2_from_f32(__fdiv_rn(f[6], s), __fdiv_rn(f[7], s)) << 16);
+            reinterpret_cast<uint2 *>(a.pool)[e / 8] = o;
+        }
+    }
+}
+
+inline int grid_for(int64_t work, int threads, int num_sms) {
+    const int64_t blocks = (work + threads - 1) / threads;
+    const int64_t cap = (int64_t)num_sms * 16;
+    return static_cast<int>(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));
+}
+
+} // namespace
+
+cudaError_t launch_slot_mapping(const int32_t *tables, int rows, int max_blocks, const int32_t *seq_ids,
+                                const int32_t *positions, int64_t n, int bs, int64_t *out, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    slot_mapping_kernel<<<grid_for(n, 256, sms), 256, 0, st>>>(tables, rows, max_blocks, seq_ids, positions, n, bs,
+                                                               out);
+    g_pkv_launches++;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append(pkv_cache *c, const void *k, const void *v, const int64_t *slots, int64_t n,
+                          cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    AppendArgs a;
+    a.k = static_cast<const uint4 *>(k);
+    a.v = static_cast<const uint4 *>(v);
+    a.slots = slots;
+    a.pool = static_cast<char *>(c->pool);
+    a.k_scale = c->k_scale;
+    a.v_scale = c->v_scale;
+    a.err = c->err;
+    a.n = n;
+    a.num_slots = c->num_blocks * c->block_size;
+    a.hkv = c->num_kv_heads;
+    a.bs = c->block_size;
+    a.chunks_per_row = c->head_dim / 8;
+    a.tile_elems = (int64_t)c->block_size * c->head_dim;
+    a.d = c->head_dim;
+    const int64_t work = n * 2 * a.hkv * a.chunks_per_row;
+    const int grid = grid_for(work, 256, c->num_sms);
+    PkvTimer timer(c, PKV_KIND_APPEND, st);
+    if (c->kv_dtype != PKV_FP8_E4M3)
+        append_kernel<PKV_F16, PKV_F16><<<grid, 256, 0, st>>>(a);
+    else if (c->model_dtype == PKV_F16)
+        append_kernel<PKV_FP8_E4M3, PKV_F16><<<grid, 256, 0, st>>>(a);
+    else
+        append_kernel<PKV_FP8_E4M3, PKV_BF16><<<grid, 256, 0, st>>>(a);
+    g_pkv_launches++;
+    return cudaGetLastError();
+}

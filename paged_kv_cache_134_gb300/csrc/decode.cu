@@ -1,0 +1,105 @@
+// Host side of the paged decode: split size, stage count, grid, workspace, launches.
+#include <cstdlib>
+
+#include "decode_impl.cuh"
+
+namespace {
+
+int env_int(const char *name, int dflt) {
+    const char *v = std::getenv(name);
+    if (!v || !*v) return dflt;
+    const int x = std::atoi(v);
+    return x > 0 ? x : dflt;
+}
+
+// target resident CTAs per SM (shared-memory budget per CTA follows from it)
+int ctas_per_sm() { return env_int("PAGEDKV_DECODE_CTAS", 3); }
+
+using DecodeFn = cudaError_t (*)(const pkv_decode::Args &, int, int, int, size_t, cudaStream_t, bool);
+using OccFn = int (*)(int, int, size_t);
+
+void pick(const pkv_cache *c, DecodeFn *fn, OccFn *occ) {
+    if (c->kv_dtype == PKV_F16) {
+        *fn = pkv_decode_f16;
+        *occ = pkv_decode_occupancy_f16;
+    } else if (c->kv_dtype == PKV_BF16) {
+        *fn = pkv_decode_bf16;
+        *occ = pkv_decode_occupancy_bf16;
+    } else if (c->model_dtype == PKV_F16) {
+        *fn = pkv_decode_fp8_f16;
+        *occ = pkv_decode_occupancy_fp8_f16;
+    } else {
+        *fn = pkv_decode_fp8_bf16;
+        *occ = pkv_decode_occupancy_fp8_bf16;
+    }
+}
+
+} // namespace
+
+int decode_split_blocks(const pkv_cache *c) {
+    const int tokens = env_int("PAGEDKV_SPLIT_TOKENS", 256);
+    const int b = tokens / c->block_size;
+    return b > 0 ? b : 1;
+}
+
+int64_t decode_workspace_floats(const pkv_cache *c, int num_seqs, int num_q_heads, int max_splits) {
+    // partial o [rows][D] and (m, l) [rows][2], rows = S * Hq * max_splits; only needed when splits > 1
+    if (max_splits <= 1) return 0;
+    const int64_t rows = (int64_t)num_seqs * num_q_heads * max_splits;
+    return rows * (c->head_dim + 2);
+}
+
+cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) {
+    using namespace pkv_decode;
+    const int G = d.num_q_heads / c->num_kv_heads;
+    Args a;
+    a.q = d.q;
+    a.out = d.out;
+    a.pool = static_cast<const char *>(c->pool);
+    a.k_scale = c->k_scale;
+    a.v_scale = c->v_scale;
+    a.tables = d.tables;
+    a.lens = d.lens;
+    a.ws_o = d.ws_o;
+    a.ws_ml = d.ws_o ? d.ws_o + (int64_t)d.num_seqs * d.num_q_heads * d.max_splits * c->head_dim : nullptr;
+    a.err = c->err;
+    a.num_blocks = c->num_blocks;
+    a.tile_bytes = static_cast<int>(c->tile_bytes);
+    a.kv_stride = (int64_t)c->num_kv_heads * c->tile_bytes;
+    a.blk_stride = 2 * a.kv_stride;
+    a.max_blocks = d.max_blocks;
+    a.num_seqs = d.num_seqs;
+    a.hq = d.num_q_heads;
+    a.hkv = c->num_kv_heads;
+    a.bs = c->block_size;
+    a.split_blocks = d.split_blocks;
+    a.max_splits = d.max_splits;
+    a.qk_scale_log2 = d.scale * 1.4426950408889634f;
+
+    DecodeFn fn;
+    OccFn occ;
+    pick(c, &fn, &occ);
+    // stages: fill the per-CTA shared-memory budget
+    const size_t fixed = smem_bytes(c->head_dim, G, 0, a.tile_bytes, d.num_seqs);
+    const size_t per_stage = smem_bytes(c->head_dim, G, 1, a.tile_bytes, d.num_seqs) - fixed;
+    const int want = ctas_per_sm();
+    const size_t budget = (size_t)(233472 / want) - 1024;
+    int nst = budget > fixed ? static_cast<int>((budget - fixed) / per_stage) : 0;
+    if (nst > 32) nst = 32;
+    if (nst < 2) nst = 2;
+    a.nstages = nst;
+    const size_t smem = smem_bytes(c->head_dim, G, nst, a.tile_bytes, d.num_seqs);
+    int per_sm = occ(c->head_dim, G, smem);
+    if (per_sm < 1) per_sm = 1;
+    const int grid = c->num_sms * per_sm;
+    cudaError_t e;
+    {
+        PkvTimer timer(c, PKV_KIND_DECODE, st);
+        e = fn(a, c->head_dim, G, grid, smem, st, false);
+        g_pkv_launches++;
+    }
+    if (e != cudaSuccess) return e;
+    e = fn(a, c->head_dim, G, 0, 0, st, true);
+    g_pkv_launches++;
+    return e;
+}

@@ -1,0 +1,530 @@
+// Paged decode attention: split-K flash-decoding over block-table entries.
+//
+// What it computes ("PagedAttention 与前缀缓存", 2kiu.com, section 2.3): for every sequence
+// s and query head h, softmax(scale * q . K_t) weighted sum of V_t over the sequence's
+// L_s tokens, where token t lives in physical block block_table[s][t / bs] at offset
+// t % bs; slots of the tail block at or beyond L_s are never used (the page's tail-block
+// warning).  Grouped-query heads: query head h reads KV head h / G, and one pass over a KV
+// head's tiles serves all G query heads that share it, so every K/V byte is read once.
+//
+// Design (GB300, HBM-bound, ~1 flop per byte for G = 1):
+//  * Work unit = (sequence, KV head, split), a split being up to `split_blocks` consecutive
+//    logical blocks.  Splits are block-aligned and depend only on L_s, so the arithmetic
+//    order of every output is fixed by the lengths alone (placement of physical blocks,
+//    sharing of prefix blocks and the batch composition never change a bit).
+//  * Persistent CTAs (a whole number of CTAs per SM) walk a unit list that puts full splits
+//    first and partial tail splits last; units go round-robin over CTAs.
+//  * One producer warp per CTA reads block-table entries (32 at a time, coalesced) and issues
+//    one 1-D bulk async copy (cp.async.bulk, the TMA's linear mode) per (block, K|V, head)
+//    tile into a ring of shared-memory stages, completion tracked by mbarrier transaction
+//    counts.  The pool layout [block][K|V][head][offset][dim] makes each tile one contiguous
+//    bs*D*elt-byte run (4 KB for bs=16, D=128, fp16), so one table lookup yields two large
+//    aligned copies.  The copies carry an L2 evict-first hint: KV is streamed once.
+//  * Four consumer warps take the unit's tiles round-robin.  In a warp, D/8 lanes share a
+//    token (16-byte vector loads from shared memory, conflict-free), partial dot products are
+//    reduced with xor-shuffles, and an online softmax (running max m, sum l, rescaled
+//    accumulator) runs per 16-token chunk with exp2 on prescaled scores.
+//  * At the end of a unit the four warps' (m, l, acc) are merged through shared memory.  A
+//    sequence with one split writes its output row directly; otherwise the unit writes an
+//    fp32 partial (m, l, unnormalised o) and a merge kernel combines the splits in split
+//    order.
+//  * Every mbarrier wait is bounded (PKV_WAIT_LIMIT_NS); a timeout sets PKV_DEVERR_TIMEOUT
+//    and the CTA winds down without further waiting on work that will not arrive.
+#pragma once
+
+#include "device_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv_decode {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxSeqs = 1024;
+
+struct Args {
+    const void *q;
+    void *out;
+    const char *pool;
+    const float *k_scale, *v_scale;
+    const int32_t *tables, *lens;
+    float *ws_o, *ws_ml;
+    unsigned int *err;
+    int64_t num_blocks;
+    int64_t blk_stride;  // bytes between consecutive physical blocks
+    int64_t kv_stride;   // bytes between the K and V halves of a block
+    int tile_bytes;      // one (block, K|V, head) tile
+    int max_blocks, num_seqs, hq, hkv, bs;
+    int split_blocks, max_splits, nstages;
+    float qk_scale_log2; // scale * log2(e)
+};
+
+template <int KVT>
+PKV_DEV void load8(const char *p, float *f) {
+    if constexpr (KVT == PKV_FP8_E4M3) {
+        cvt8_e4m3(*reinterpret_cast<const uint2 *>(p), f);
+    } else {
+        cvt8<KVT>(*reinterpret_cast<const uint4 *>(p), f);
+    }
+}
+
+// Which unit is u: (sequence, KV head, split index, first logical block, tiles).
+struct Unit {
+    int s, kvh, j, blk0, ntiles, nsplit;
+};
+
+PKV_DEV int find_row(const int *pref, int n, int k) {
+    // largest i in [0, n) with pref[i] <= k (pref non-decreasing, pref[0] = 0)
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pref[mid] <= k)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+PKV_DEV Unit unit_info(int u, const int *pf, const int *pp, const int *nb, int S, int hkv, int bps) {
+    Unit r;
+    const int nfull_units = pf[S] * hkv;
+    if (u < nfull_units) {
+        const int k = u / hkv;
+        r.kvh = u - k * hkv;
+        r.s = find_row(pf, S, k);
+        r.j = k - pf[r.s];
+        r.blk0 = r.j * bps;
+        r.ntiles = bps;
+    } else {
+        const int u2 = u - nfull_units;
+        const int k = u2 / hkv;
+        r.kvh = u2 - k * hkv;
+        r.s = find_row(pp, S, k);
+        r.j = pf[r.s + 1] - pf[r.s];
+        r.blk0 = r.j * bps;
+        r.ntiles = nb[r.s] - r.blk0;
+    }
+    r.nsplit = (pf[r.s + 1] - pf[r.s]) + (pp[r.s + 1] - pp[r.s]);
+    return r;
+}
+
+// One tile of `bs` tokens, `valid` of them real, for the G query heads of one KV head.
+template <int D, int G, int KVT>
+PKV_DEV void process_tile(const char *ks, const char *vs, int bs, int valid, const float (&qf)[G][8], float (&m)[G],
+                          float (&l)[G], float (&acc)[G][8], int lane) {
+    constexpr int LPT = D / 8;        // lanes per token
+    constexpr int TPP = 32 / LPT;     // tokens per pass
+    constexpr int MAXP = 16 / TPP;    // passes per 16-token chunk
+    constexpr int EB = (KVT == PKV_FP8_E4M3) ? 1 : 2;
+    const int sub = lane % LPT, grp = lane / LPT;
+    const int ch = bs < 16 ? bs : 16;
+    const int npc = ch / TPP;
+    for (int c0 = 0; c0 < bs; c0 += ch) {
+        if (c0 >= valid) break;
+        float sc[G][MAXP];
+#pragma unroll
+        for (int p = 0; p < MAXP; ++p) {
+            if (p < npc) {
+                const int t = c0 + p * TPP + grp;
+                float kf[8];
+                load8<KVT>(ks + (t * D + sub * 8) * EB, kf);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float d0 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) d0 = fmaf(qf[g][e], kf[e], d0);
+                    sc[g][p] = d0;
+                }
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < MAXP; ++p) {
+            if (p < npc) {
+                const bool live = (c0 + p * TPP + grp) < valid;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float v = sc[g][p];
+#pragma unroll
+                    for (int o = LPT / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    sc[g][p] = live ? v : -INFINITY;
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int p = 0; p < MAXP; ++p)
+                if (p < npc) mx = fmaxf(mx, sc[g][p]);
+#pragma unroll
+            for (int o = LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float mn = fmaxf(m[g], mx); // finite: the chunk holds at least one live token
+            const float alpha = fast_exp2(m[g] - mn);
+            m[g] = mn;
+            l[g] *= alpha;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+#pragma unroll
+            for (int p = 0; p < MAXP; ++p) {
+                if (p < npc) {
+                    const float pr = fast_exp2(sc[g][p] - mn);
+                    sc[g][p] = pr;
+                    l[g] += pr;
+                }
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < MAXP; ++p) {
+            if (p < npc) {
+                const int t = c0 + p * TPP + grp;
+                if (t < valid) {
+                    float vf[8];
+                    load8<KVT>(vs + (t * D + sub * 8) * EB, vf);
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(sc[g][p], vf[e], acc[g][e]);
+                }
+            }
+        }
+    }
+}
+
+template <int D, int G, int MT, int KVT>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
+    using M = ModelT<MT>;
+    using T = typename M::T;
+    constexpr int NCW = kConsumerWarps;
+    constexpr int LPT = D / 8;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int NST = a.nstages;
+    const int S = a.num_seqs;
+    char *ring = reinterpret_cast<char *>(smem);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NST * 2 * a.tile_bytes);
+    uint64_t *empty = full + NST;
+    int *flags = reinterpret_cast<int *>(empty + NST);
+    int *abort_flag = flags + NST;
+    float *mrg = reinterpret_cast<float *>(abort_flag + 4);
+    int *pf = reinterpret_cast<int *>(mrg + NCW * G * (D + 2));
+    int *pp = pf + (S + 1);
+    int *nb = pp + (S + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    // unit list: per sequence, full splits and (0 or 1) partial split
+    const int bps = a.split_blocks;
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+        const int L = a.lens[s];
+        int n = L > 0 ? (L + a.bs - 1) / a.bs : 0;
+        if (n > a.max_blocks) {
+            if (blockIdx.x == 0) set_error(a.err, PKV_DEVERR_LENGTH);
+            n = a.max_blocks;
+        }
+        nb[s] = n;
+        pf[s + 1] = n / bps;
+        pp[s + 1] = (n % bps) ? 1 : 0;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int cf = 0, cp = 0;
+        for (int base = 0; base < S; base += 32) {
+            const int i = base + lane;
+            int vf = i < S ? pf[i + 1] : 0, vp = i < S ? pp[i + 1] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int tf = __shfl_up_sync(0xffffffffu, vf, o), tp = __shfl_up_sync(0xffffffffu, vp, o);
+                if (lane >= o) {
+                    vf += tf;
+                    vp += tp;
+                }
+            }
+            if (i < S) {
+                pf[i + 1] = vf + cf;
+                pp[i + 1] = vp + cp;
+            }
+            cf += __shfl_sync(0xffffffffu, vf, 31);
+            cp += __shfl_sync(0xffffffffu, vp, 31);
+        }
+        if (lane == 0) {
+            pf[0] = 0;
+            pp[0] = 0;
+        }
+    }
+    __syncthreads();
+    const int U = (pf[S] + pp[S]) * a.hkv;
+
+    if (warp == NCW) {
+        // ---------------------------------------------------------------- producer warp
+        const uint64_t policy = l2_policy_evict_first();
+        uint32_t tau = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+            const Unit un = unit_info(u, pf, pp, nb, S, a.hkv, bps);
+            const int32_t *trow = a.tables + (int64_t)un.s * a.max_blocks + un.blk0;
+            const char *head_base = a.pool + (int64_t)un.kvh * a.tile_bytes;
+            for (int i0 = 0; i0 < un.ntiles && ok; i0 += 32) {
+                const int cnt = min(32, un.ntiles - i0);
+                const int myb = lane < cnt ? trow[i0 + lane] : 0;
+                for (int i = 0; i < cnt; ++i) {
+                    const int b = __shfl_sync(0xffffffffu, myb, i);
+                    if (lane == 0) {
+                        const uint32_t stage = tau % NST, round = tau / NST;
+                        if (round > 0 && !mbar_wait(&empty[stage], (round - 1) & 1)) {
+                            // stop issuing; the consumers time out on the stages that never fill
+                            set_error(a.err, PKV_DEVERR_TIMEOUT);
+                            ok = false;
+                        } else if (b >= 0 && b < a.num_blocks) {
+                            flags[stage] = 0;
+                            char *dst = ring + (size_t)stage * 2 * a.tile_bytes;
+                            const char *src = head_base + (int64_t)b * a.blk_stride;
+                            mbar_arrive_expect_tx(&full[stage], 2u * a.tile_bytes);
+                            bulk_g2s_hint(dst, src, a.tile_bytes, &full[stage], policy);
+                            bulk_g2s_hint(dst + a.tile_bytes, src + a.kv_stride, a.tile_bytes, &full[stage], policy);
+                        } else {
+                            flags[stage] = 1;
+                            set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                            mbar_arrive(&full[stage]);
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    ++tau;
+                }
+            }
+        }
+        // drain: the copies of the last stages must land before this CTA's shared memory goes away
+        if (lane == 0) {
+            const uint32_t first = tau > (uint32_t)NST ? tau - NST : 0;
+            for (uint32_t t = first; t < tau; ++t)
+                if (!mbar_wait(&full[t % NST], (t / NST) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------------- consumer warps
+    const int sub = lane % LPT, grp = lane / LPT;
+    const int tid = threadIdx.x; // 0 .. NCW*32-1
+    uint32_t tau = 0;
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+        const Unit un = unit_info(u, pf, pp, nb, S, a.hkv, bps);
+        const int L = a.lens[un.s];
+        float qs = a.qk_scale_log2;
+        if constexpr (KVT == PKV_FP8_E4M3) qs *= a.k_scale[un.kvh];
+        float qf[G][8];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const T *qp = static_cast<const T *>(a.q) + ((int64_t)un.s * a.hq + un.kvh * G + g) * D + sub * 8;
+            const uint4 raw = *reinterpret_cast<const uint4 *>(qp);
+            cvt8<MT>(raw, qf[g]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qf[g][e] *= qs;
+        }
+        float m[G], l[G], acc[G][8];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+        }
+        for (int i = warp; i < un.ntiles; i += NCW) {
+            const uint32_t t = tau + i;
+            const uint32_t stage = t % NST;
+            if (!mbar_wait(&full[stage], (t / NST) & 1)) {
+                set_error(a.err, PKV_DEVERR_TIMEOUT);
+                *reinterpret_cast<volatile int *>(abort_flag) = 1;
+            }
+            if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+            if (!flags[stage]) {
+                const char *ks = ring + (size_t)stage * 2 * a.tile_bytes;
+                const int valid = min(a.bs, L - (un.blk0 + i) * a.bs);
+                process_tile<D, G, KVT>(ks, ks + a.tile_bytes, a.bs, valid, qf, m, l, acc, lane);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+        }
+        tau += un.ntiles;
+        // combine the token groups of this warp
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+            for (int o = LPT; o < 32; o <<= 1) {
+                l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
+            }
+        }
+        if (grp == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float *r = mrg + (warp * G + g) * (D + 2);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) r[sub * 8 + e] = acc[g][e];
+                if (sub == 0) {
+                    r[D] = m[g];
+                    r[D + 1] = l[g];
+                }
+            }
+        }
+        named_barrier_sync(1, NCW * 32);
+        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+        const float vs = (KVT == PKV_FP8_E4M3) ? a.v_scale[un.kvh] : 1.f;
+        for (int o = tid; o < G * D; o += NCW * 32) {
+            const int g = o / D, d = o - g * D;
+            float Mx = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) {
+                const float *r = mrg + (w * G + g) * (D + 2);
+                if (r[D + 1] > 0.f) Mx = fmaxf(Mx, r[D]);
+            }
+            float num = 0.f, den = 0.f;
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) {
+                const float *r = mrg + (w * G + g) * (D + 2);
+                if (r[D + 1] > 0.f) {
+                    const float wt = fast_exp2(r[D] - Mx);
+                    num = fmaf(wt, r[d], num);
+                    den = fmaf(wt, r[D + 1], den);
+                }
+            }
+            const int h = un.kvh * G + g;
+            if (un.nsplit == 1) {
+                const float y = den > 0.f ? (num / den) * vs : 0.f;
+                static_cast<T *>(a.out)[((int64_t)un.s * a.hq + h) * D + d] = M::from_f(y);
+            } else {
+                const int64_t idx = ((int64_t)un.s * a.hq + h) * a.max_splits + un.j;
+                a.ws_o[idx * D + d] = num * vs;
+                if (d == 0) {
+                    a.ws_ml[2 * idx] = Mx;
+                    a.ws_ml[2 * idx + 1] = den;
+                }
+            }
+        }
+        named_barrier_sync(1, NCW * 32);
+    }
+}
+
+// Merge of the per-split partials of sequences with more than one split; zero rows for
+// L_s == 0.  One warp per (sequence, query head); splits are combined in split order.
+template <int D, int MT>
+__global__ void __launch_bounds__(128) merge_kernel(const Args a) {
+    using M = ModelT<MT>;
+    using T = typename M::T;
+    const int wid = blockIdx.x * 4 + threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (wid >= a.num_seqs * a.hq) return;
+    const int s = wid / a.hq;
+    const int L = a.lens[s];
+    int n = L > 0 ? (L + a.bs - 1) / a.bs : 0;
+    if (n > a.max_blocks) n = a.max_blocks;
+    const int nsplit = n / a.split_blocks + ((n % a.split_blocks) ? 1 : 0);
+    if (nsplit == 1) return;
+    T *o = static_cast<T *>(a.out) + (int64_t)wid * D;
+    constexpr int PER = D / 32;
+    if (nsplit == 0) {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) o[lane * PER + e] = M::from_f(0.f);
+        return;
+    }
+    const int64_t base = (int64_t)wid * a.max_splits;
+    float Mx = -INFINITY;
+    for (int j = 0; j < nsplit; ++j)
+        if (a.ws_ml[2 * (base + j) + 1] > 0.f) Mx = fmaxf(Mx, a.ws_ml[2 * (base + j)]);
+    float num[PER], den = 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) num[e] = 0.f;
+    for (int j = 0; j < nsplit; ++j) {
+        const float lj = a.ws_ml[2 * (base + j) + 1];
+        if (!(lj > 0.f)) continue;
+        const float wt = fast_exp2(a.ws_ml[2 * (base + j)] - Mx);
+        den = fmaf(wt, lj, den);
+        const float *src = a.ws_o + (base + j) * D + lane * PER;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) num[e] = fmaf(wt, src[e], num[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < PER; ++e) o[lane * PER + e] = M::from_f(den > 0.f ? num[e] / den : 0.f);
+}
+
+inline size_t smem_bytes(int D, int G, int nst, int tile_bytes, int S) {
+    return (size_t)nst * 2 * tile_bytes + (size_t)nst * (8 + 8 + 4) + 16 + (size_t)kConsumerWarps * G * (D + 2) * 4 +
+           (size_t)(3 * S + 2) * 4;
+}
+
+template <int D, int G, int MT, int KVT>
+cudaError_t launch_t(const Args &a, int grid, size_t smem, cudaStream_t st) {
+    auto kern = decode_kernel<D, G, MT, KVT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D, int MT>
+cudaError_t launch_merge_t(const Args &a, cudaStream_t st) {
+    const int rows = a.num_seqs * a.hq;
+    if (rows == 0) return cudaSuccess;
+    merge_kernel<D, MT><<<(rows + 3) / 4, 128, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+// Dispatch over head_dim and group size for one (model dtype, KV dtype) pair.
+template <int MT, int KVT>
+cudaError_t dispatch(const Args &a, int D, int G, int grid, size_t smem, cudaStream_t st, bool merge) {
+#define PKV_CASE(DD, GG)                                                                                               \
+    if (D == DD && G == GG) return merge ? launch_merge_t<DD, MT>(a, st) : launch_t<DD, GG, MT, KVT>(a, grid, smem, st);
+    PKV_CASE(64, 1)
+    PKV_CASE(64, 2)
+    PKV_CASE(64, 4)
+    PKV_CASE(64, 8)
+    PKV_CASE(128, 1)
+    PKV_CASE(128, 2)
+    PKV_CASE(128, 4)
+    PKV_CASE(128, 8)
+#undef PKV_CASE
+    return cudaErrorInvalidValue;
+}
+
+template <int D, int G, int MT, int KVT>
+int occupancy(size_t smem) {
+    int n = 0;
+    cudaFuncSetAttribute(decode_kernel<D, G, MT, KVT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, G, MT, KVT>, kThreads, smem);
+    return n;
+}
+
+template <int MT, int KVT>
+int occupancy_dispatch(int D, int G, size_t smem) {
+#define PKV_CASE(DD, GG)                                                                                               \
+    if (D == DD && G == GG) return occupancy<DD, GG, MT, KVT>(smem);
+    PKV_CASE(64, 1)
+    PKV_CASE(64, 2)
+    PKV_CASE(64, 4)
+    PKV_CASE(64, 8)
+    PKV_CASE(128, 1)
+    PKV_CASE(128, 2)
+    PKV_CASE(128, 4)
+    PKV_CASE(128, 8)
+#undef PKV_CASE
+    return 0;
+}
+
+} // namespace pkv_decode
+
+// Per (model dtype, KV dtype) entry points, each compiled in its own translation unit.
+cudaError_t pkv_decode_f16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t, bool merge);
+cudaError_t pkv_decode_bf16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t, bool merge);
+cudaError_t pkv_decode_fp8_f16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t,
+                               bool merge);
+cudaError_t pkv_decode_fp8_bf16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t,
+                                bool merge);
+int pkv_decode_occupancy_f16(int D, int G, size_t smem);
+int pkv_decode_occupancy_bf16(int D, int G, size_t smem);
+int pkv_decode_occupancy_fp8_f16(int D, int G, size_t smem);
+int pkv_decode_occupancy_fp8_bf16(int D, int G, size_t smem);

@@ -1,0 +1,88 @@
+// Host-side internals shared by the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "pagedkv.h"
+
+struct pkv_cache {
+    int device = 0;
+    int64_t num_blocks = 0;
+    int block_size = 0, num_kv_heads = 0, head_dim = 0;
+    pkv_dtype kv_dtype = PKV_F16, model_dtype = PKV_F16;
+    int elem_bytes = 2;
+    // pool: [num_blocks][2][Hkv][bs][D] elements
+    void *pool = nullptr;
+    int64_t pool_bytes = 0;
+    int64_t tile_bytes = 0;   // one (block, K|V, head) tile: bs * D * elem
+    float *k_scale = nullptr; // [Hkv] device (FP8 only)
+    float *v_scale = nullptr;
+    unsigned int *err = nullptr; // device error word
+    // split-K workspace of the decode
+    float *ws = nullptr;
+    int64_t ws_bytes = 0;
+    int num_sms = 0;
+    // profiling
+    bool profiling = false;
+    struct Ev {
+        int kind;
+        cudaEvent_t a, b;
+    };
+    std::vector<Ev> events;
+    std::vector<cudaEvent_t> event_pool;
+    std::mutex mu;
+};
+
+enum { PKV_KIND_DECODE = 0, PKV_KIND_PREFILL = 1, PKV_KIND_APPEND = 2 };
+
+// status helpers (api.cu)
+int pkv_fail(int status, const char *fmt, ...);
+int pkv_cuda_fail(cudaError_t e, const char *what);
+extern std::atomic<int64_t> g_pkv_launches;
+
+// profiling bracket around one main-kernel launch (api.cu)
+struct PkvTimer {
+    pkv_cache *c;
+    int kind;
+    cudaStream_t st;
+    cudaEvent_t a = nullptr, b = nullptr;
+    PkvTimer(pkv_cache *c_, int kind_, cudaStream_t st_);
+    ~PkvTimer();
+};
+
+// launchers (one per translation unit); return cudaError_t of the launch
+cudaError_t launch_slot_mapping(const int32_t *tables, int rows, int max_blocks, const int32_t *seq_ids,
+                                const int32_t *positions, int64_t n, int bs, int64_t *out, cudaStream_t st);
+cudaError_t launch_append(pkv_cache *c, const void *k, const void *v, const int64_t *slots, int64_t n,
+                          cudaStream_t st);
+
+struct DecodeLaunch {
+    const void *q;
+    void *out;
+    const int32_t *tables;
+    const int32_t *lens;
+    int max_blocks, num_seqs, num_q_heads;
+    float scale;
+    int split_blocks; // blocks per split
+    int max_splits;
+    float *ws_o;      // [S*Hq*max_splits][D]
+    float *ws_ml;     // [S*Hq*max_splits][2]
+};
+int64_t decode_workspace_floats(const pkv_cache *c, int num_seqs, int num_q_heads, int max_splits);
+int decode_split_blocks(const pkv_cache *c);
+cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st);
+
+struct PrefillLaunch {
+    const void *q, *k, *v;
+    void *out;
+    const int32_t *cu;
+    const int32_t *tables;
+    int num_seqs, max_seqlen, max_blocks, num_q_heads;
+    float scale;
+};
+cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st);
