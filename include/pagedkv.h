@@ -137,13 +137,15 @@ int paged_decode_attention(const void *q, pkv_cache_t cache, const int32_t *bloc
  * with g = h / (num_q_heads / num_kv_heads); no attention across sequences.  The same call
  * writes every token's k/v into the cache at block_tables[i][r / block_size], offset
  * r % block_size (the bytes paged_kv_append would write).  q, out: [T][num_q_heads][head_dim];
- * k, v: [T][num_kv_heads][head_dim] (model dtype, T = cu_seqlens[num_seqs]);
- * cu_seqlens: int32 [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0; max_seqlen >= every
- * length.  fp16/bf16 caches only (EUNSUPPORTED for FP8).  Q.K^T and P.V run on the tensor
+ * k, v: [T][num_kv_heads][head_dim] (model dtype), T = total_tokens = cu_seqlens[num_seqs]
+ * (passed from the host because the tensor maps of the loads need it); cu_seqlens: int32
+ * [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0; max_seqlen >= every length.  A sequence
+ * whose bounds break these rules is skipped and sets PKV_DEVERR_CU_SEQLENS.  fp16/bf16 caches only (EUNSUPPORTED for FP8).  Q.K^T and P.V run on the tensor
  * cores (tcgen05, fp32 accumulation in tensor memory); P is rounded to the model dtype for P.V. */
 int packed_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens, int num_seqs,
-                             int max_seqlen, const int32_t *block_tables, int max_blocks_per_seq, pkv_cache_t cache,
-                             int num_q_heads, float scale, void *out, void *stream);
+                             int max_seqlen, int64_t total_tokens, const int32_t *block_tables,
+                             int max_blocks_per_seq, pkv_cache_t cache, int num_q_heads, float scale, void *out,
+                             void *stream);
 
 /* Profiling.  Between kv_cache_profile_start and kv_cache_profile_read the library records
  * CUDA events around each main kernel it launches for this cache (decode split-K kernel,

@@ -53,7 +53,8 @@ def lib() -> ctypes.CDLL:
         L.paged_slot_mapping.argtypes = [vp, i32, i32, vp, vp, i64, i32, vp, vp]
         L.paged_kv_append.argtypes = [vp, vp, vp, vp, i64, vp]
         L.paged_decode_attention.argtypes = [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]
-        L.packed_prefill_attention.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, vp, i32, ctypes.c_float, vp, vp]
+        L.packed_prefill_attention.argtypes = [vp, vp, vp, vp, i32, i32, i64, vp, i32, vp, i32, ctypes.c_float, vp,
+                                               vp]
         L.kv_cache_profile_start.argtypes = [vp]
         L.kv_cache_profile_read.argtypes = [vp, ctypes.c_void_p]
         L.pkv_kernel_launches.restype = i64
@@ -242,7 +243,7 @@ def packed_prefill_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     if out is None:
         out = torch.empty_like(q)
     _req(out, "out", cache.torch_dtype, 3)
-    _check(lib().packed_prefill_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseq, int(max_seqlen),
+    _check(lib().packed_prefill_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseq, int(max_seqlen), T,
                                           _ptr(block_tables), block_tables.shape[1], cache.handle, hq,
                                           ctypes.c_float(scale), _ptr(out), _stream()))
     return out

@@ -275,12 +275,15 @@ int paged_decode_attention(const void *q, pkv_cache_t c, const int32_t *block_ta
 }
 
 int packed_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens, int num_seqs,
-                             int max_seqlen, const int32_t *block_tables, int max_blocks_per_seq, pkv_cache_t c,
-                             int num_q_heads, float scale, void *out, void *stream) {
+                             int max_seqlen, int64_t total_tokens, const int32_t *block_tables,
+                             int max_blocks_per_seq, pkv_cache_t c, int num_q_heads, float scale, void *out,
+                             void *stream) {
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
-    if (num_seqs < 0 || max_seqlen < 0 || max_blocks_per_seq < 0) return pkv_fail(PKV_EINVAL, "negative size");
+    if (num_seqs < 0 || max_seqlen < 0 || max_blocks_per_seq < 0 || total_tokens < 0)
+        return pkv_fail(PKV_EINVAL, "negative size");
+    if (total_tokens > 0x7FFFFFFF) return pkv_fail(PKV_EUNSUPPORTED, "more than 2^31 - 1 packed tokens");
     if (c->kv_dtype == PKV_FP8_E4M3) return pkv_fail(PKV_EUNSUPPORTED, "packed prefill writes fp16/bf16 caches only");
-    if (num_seqs == 0 || max_seqlen == 0) return PKV_OK;
+    if (num_seqs == 0 || max_seqlen == 0 || total_tokens == 0) return PKV_OK;
     if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads)
         return pkv_fail(PKV_EINVAL, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
                         c->num_kv_heads);
@@ -300,6 +303,7 @@ int packed_prefill_attention(const void *q, const void *k, const void *v, const 
     p.tables = block_tables;
     p.num_seqs = num_seqs;
     p.max_seqlen = max_seqlen;
+    p.total_tokens = total_tokens;
     p.max_blocks = max_blocks_per_seq;
     p.num_q_heads = num_q_heads;
     p.scale = scale;

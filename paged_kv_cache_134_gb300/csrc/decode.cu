@@ -85,8 +85,10 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
     const int want = ctas_per_sm();
     const size_t budget = (size_t)(233472 / want) - 1024;
     int nst = budget > fixed ? static_cast<int>((budget - fixed) / per_stage) : 0;
+    // a whole number of stages per consumer warp (see the tile-to-warp rule in the kernel)
+    nst -= nst % kConsumerWarps;
     if (nst > 32) nst = 32;
-    if (nst < 2) nst = 2;
+    if (nst < kConsumerWarps) nst = kConsumerWarps;
     a.nstages = nst;
     const size_t smem = smem_bytes(c->head_dim, G, nst, a.tile_bytes, d.num_seqs);
     int per_sm = occ(c->head_dim, G, smem);

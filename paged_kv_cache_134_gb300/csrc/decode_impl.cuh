@@ -20,7 +20,7 @@
 //    counts.  The pool layout [block][K|V][head][offset][dim] makes each tile one contiguous
 //    bs*D*elt-byte run (4 KB for bs=16, D=128, fp16), so one table lookup yields two large
 //    aligned copies.  The copies carry an L2 evict-first hint: KV is streamed once.
-//  * Four consumer warps take the unit's tiles round-robin.  In a warp, D/8 lanes share a
+//  * Four consumer warps take the tiles round-robin by their index in the CTA's tile stream.  In a warp, D/8 lanes share a
 //    token (16-byte vector loads from shared memory, conflict-free), partial dot products are
 //    reduced with xor-shuffles, and an online softmax (running max m, sum l, rescaled
 //    accumulator) runs per 16-token chunk with exp2 on prescaled scores.
@@ -334,7 +334,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
         }
-        for (int i = warp; i < un.ntiles; i += NCW) {
+        // Tile t of the CTA's stream (t counted over all its units) belongs to warp t % NCW and
+        // sits in stage t % NST with NST a multiple of NCW, so a warp's previous tile in any stage
+        // is its own: when it waits for phase k of a stage, phase k-1 has completed, which keeps
+        // the parity wait unambiguous.
+        int i0 = warp - static_cast<int>(tau % NCW);
+        if (i0 < 0) i0 += NCW;
+        for (int i = i0; i < un.ntiles; i += NCW) {
             const uint32_t t = tau + i;
             const uint32_t stage = t % NST;
             if (!mbar_wait(&full[stage], (t / NST) & 1)) {

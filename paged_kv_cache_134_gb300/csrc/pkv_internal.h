@@ -83,6 +83,7 @@ struct PrefillLaunch {
     const int32_t *cu;
     const int32_t *tables;
     int num_seqs, max_seqlen, max_blocks, num_q_heads;
+    int64_t total_tokens;
     float scale;
 };
 cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st);

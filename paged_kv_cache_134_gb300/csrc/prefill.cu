@@ -1,4 +1,433 @@
-// Packed causal prefill (placeholder until the tensor-core kernel lands).
+// Packed causal prefill on the 5th-generation tensor cores, with the paged K/V write fused in.
+//
+// What it computes ("Paged KV Cache 与 Packed Sequence", discosf.com, sections 3.1-3.3, 4.2):
+// sequences packed back to back, sequence i owning rows [cu[i], cu[i+1]); a query at in-sequence
+// position r attends to the keys of its own sequence at positions c <= r (block-diagonal causal
+// mask), out = softmax(scale q.k) v.  Every token's k/v is also written into the paged cache at
+// block_table[i][r / bs], offset r % bs (the prompt-phase write of section 4.2, bounded by the
+// sequence length so a partly filled tail block is never overrun).
+//
+// One CTA = (sequence, 128-query tile, query head).  Warp roles:
+//   warp 0     TMA producer: Q tile once, then K/V tiles of 64 keys into a 2-stage ring (tiled TMA,
+//              128-byte swizzle, out-of-range rows zero-filled);
+//   warp 1     tensor-memory owner and MMA issuer (one thread): S = Q K^T into one of two TMEM S
+//              buffers (M=128, N=64, fp32), then O += P V into the TMEM O accumulator (M=128, N=D);
+//   warps 2-5  softmax, one thread per query row (TMEM lane = row): mask, exp2, row sums, P rounded
+//              to the model dtype and written to shared memory in the 128-byte-swizzled K-major
+//              layout the MMA reads; O in TMEM is rescaled only when a row's running max grows by
+//              more than 2^8 (the exponent base stays fixed otherwise, which is exact algebra);
+//   warps 6-7  paged K/V writer for the tile's rows (only the CTA of the first query head of each
+//              KV group writes, so every (token, KV head) is written once).
+// The diagonal tiles are masked per element; tiles entirely above the diagonal are never issued.
+// Every mbarrier wait is bounded; a timeout sets PKV_DEVERR_TIMEOUT and the CTA winds down.
+#include <mutex>
+
+#include "tcgen05.cuh"
 #include "pkv_internal.h"
 
-cudaError_t launch_prefill(pkv_cache *, const PrefillLaunch &, cudaStream_t) { return cudaErrorNotSupported; }
+namespace pkv_prefill {
+
+constexpr int BM = 128;          // query rows per tile (MMA M)
+constexpr int BN = 64;           // keys per tile (MMA N of Q K^T, K of P V)
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 256; // S0 [0,64) S1 [64,128) O [128, 128+D)
+constexpr float kRescale = 8.0f; // log2 units
+
+struct Args {
+    const char *k, *v;  // packed [T][Hkv][D]
+    void *out;          // packed [T][Hq][D]
+    const int32_t *cu, *tables;
+    char *pool;
+    unsigned int *err;
+    int64_t total_tokens, num_blocks, tile_elems;
+    int num_seqs, max_seqlen, max_blocks, hq, hkv, bs, nqt_max;
+    float scale_log2;
+};
+
+template <int D>
+struct Layout {
+    static constexpr int Q = 0;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int KV_BYTES = BN * D * 2; // one K or V tile
+    static constexpr int K0 = Q + Q_BYTES;
+    static constexpr int V0 = K0 + 2 * KV_BYTES;
+    static constexpr int P = V0 + 2 * KV_BYTES;
+    static constexpr int P_BYTES = BM * BN * 2;
+    static constexpr int BAR = P + P_BYTES;
+    static constexpr int TOTAL = BAR + 256;
+};
+
+// two floats -> packed fp16/bf16 pair (round-to-nearest-even), `lo` in the low half
+PKV_DEV uint32_t pack2(float lo, float hi, int mt) {
+    uint32_t r;
+    if (mt == PKV_BF16)
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <int D, int MT>
+__global__ void __launch_bounds__(kThreads, 2)
+    prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const Args a) {
+    using L = Layout<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+
+    // ---- work item, heaviest query tiles first
+    const int per_qt = a.num_seqs * a.hq;
+    const int rank = blockIdx.x / per_qt;
+    const int qt = a.nqt_max - 1 - rank;
+    const int rem = blockIdx.x - rank * per_qt;
+    const int seq = rem / a.hq, h = rem - seq * a.hq;
+    const int start = a.cu[seq], end = a.cu[seq + 1];
+    const int n = end - start;
+    if (start < 0 || n < 0 || end > a.total_tokens || n > a.max_seqlen) {
+        if (threadIdx.x == 0 && h == 0 && qt == 0) set_error(a.err, PKV_DEVERR_CU_SEQLENS);
+        return;
+    }
+    if (qt * BM >= n) return;
+    if (smem_u32(smem) & 1023u) return; // the swizzled tiles need 1024-byte alignment (always true)
+    const int G = a.hq / a.hkv;
+    const int kvh = h / G;
+    const int q0 = qt * BM;
+    const int qlast = min(q0 + BM, n) - 1;
+    const int nkv = qlast / BN + 1;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR);
+    uint64_t *q_full = bars + 0, *kv_full = bars + 1, *kv_empty = bars + 3, *s_full = bars + 5, *s_free = bars + 7;
+    uint64_t *p_full = bars + 9, *t_full = bars + 10, *fin = bars + 11;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 13);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(kv_full + s, 1);
+            mbar_init(kv_empty + s, 1);
+            mbar_init(s_full + s, 1);
+            mbar_init(s_free + s, 128);
+        }
+        mbar_init(p_full, 128);
+        mbar_init(t_full, 1);
+        mbar_init(fin, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tc::prefetch_tmap(&tq);
+            tc::prefetch_tmap(&tk);
+            tc::prefetch_tmap(&tv);
+            mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+                tc::tma_load_2d(smem + L::Q + c * BM * 128, &tq, h * D + c * 64, start + q0, q_full);
+            int issued = 0;
+            for (int j = 0; j < nkv; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !mbar_wait(kv_empty + st, ((j >> 1) - 1) & 1)) {
+                    set_error(a.err, PKV_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                mbar_arrive_expect_tx(kv_full + st, 2 * L::KV_BYTES);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    tc::tma_load_2d(smem + L::K0 + st * L::KV_BYTES + c * BN * 128, &tk, kvh * D + c * 64,
+                                    start + j * BN, kv_full + st);
+                    tc::tma_load_2d(smem + L::V0 + st * L::KV_BYTES + c * BN * 128, &tv, kvh * D + c * 64,
+                                    start + j * BN, kv_full + st);
+                }
+                issued = j + 1;
+            }
+            // the loads of the last stages must land before this CTA's shared memory goes away
+            for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+                if (!mbar_wait(kv_full + (j & 1), (j >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            if (!mbar_wait(q_full, 0)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IQK = tc::idesc_f16(MT == PKV_BF16 ? 1u : 0u, 0u, BM, BN);
+            constexpr uint32_t IPV = tc::idesc_f16(MT == PKV_BF16 ? 1u : 0u, 1u, BM, D);
+            const uint32_t sQ = smem_u32(smem + L::Q), sK = smem_u32(smem + L::K0), sV = smem_u32(smem + L::V0);
+            const uint32_t sP = smem_u32(smem + L::P);
+            const uint32_t tO = tmem + 128;
+            auto issue_s = [&](int j) {
+                const int st = j & 1;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const int c = k >> 2, kk = k & 3;
+                    const uint64_t ad = tc::smem_desc(sQ + c * BM * 128 + kk * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc(sK + st * L::KV_BYTES + c * BN * 128 + kk * 32, 16, 1024);
+                    tc::mma_f16(tmem + st * BN, ad, bd, IQK, k > 0 ? 1u : 0u);
+                }
+                tc::commit(s_full + st);
+            };
+            bool ok = mbar_wait(q_full, 0) && mbar_wait(kv_full, 0);
+            if (ok) {
+                tc::fence_after_sync();
+                issue_s(0);
+            }
+            for (int j = 0; j < nkv && ok; ++j) {
+                if (j + 1 < nkv) {
+                    const int b = (j + 1) & 1;
+                    ok = mbar_wait(kv_full + b, ((j + 1) >> 1) & 1);
+                    if (ok && j + 1 >= 2) ok = mbar_wait(s_free + b, ((j - 1) >> 1) & 1);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    issue_s(j + 1);
+                }
+                ok = mbar_wait(p_full, j & 1);
+                if (!ok) break;
+                tc::fence_after_sync();
+                const int st = j & 1;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    const uint64_t ad = tc::smem_desc(sP + k * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc(sV + st * L::KV_BYTES + k * 2048, BN * 128, 1024);
+                    tc::mma_f16(tO, ad, bd, IPV, (j > 0 || k > 0) ? 1u : 0u);
+                }
+                tc::commit(t_full);
+                tc::commit(kv_empty + st);
+            }
+            if (!ok) {
+                set_error(a.err, PKV_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // every MMA issued by this thread has completed before TMEM is released
+            tc::commit(fin);
+            if (!mbar_wait(fin, 0)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ softmax, one thread per row
+        const int lw = warp & 3;
+        const int r = lw * 32 + lane;
+        const int qpos = q0 + r;
+        const uint32_t lane_off = static_cast<uint32_t>(lw * 32) << 16;
+        float m_use = -INFINITY, l = 0.f;
+        bool ok = true;
+        uint8_t *prow = smem + L::P + (r >> 3) * 1024 + (r & 7) * 128;
+        for (int j = 0; j < nkv && ok; ++j) {
+            const int b = j & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j >> 1) & 1));
+            if (!ok) break;
+            tc::fence_after_sync();
+            uint32_t sr[64];
+            {
+                uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+                uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+                tc::ld32(tmem + lane_off + b * BN, lo);
+                tc::ld32(tmem + lane_off + b * BN + 32, hi);
+            }
+            tc::wait_ld();
+            tc::fence_before_sync();
+            mbar_arrive(s_free + b);
+            const int kbase = j * BN;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BN; ++c) {
+                float x = __uint_as_float(sr[c]) * a.scale_log2;
+                x = (kbase + c > qpos) ? -INFINITY : x;
+                sr[c] = __float_as_uint(x);
+                mx = fmaxf(mx, x);
+            }
+            const bool up = mx > m_use + kRescale;
+            const float m_new = up ? mx : m_use;
+            const float alpha = up ? fast_exp2(m_use - m_new) : 1.f;
+            m_use = m_new;
+            const float base = m_use == -INFINITY ? 0.f : m_use; // a row with no live key yet keeps p = 0
+            float rs = 0.f;
+            uint32_t pk[BN / 2];
+#pragma unroll
+            for (int c = 0; c < BN / 2; ++c) {
+                const float p0 = fast_exp2(__uint_as_float(sr[2 * c]) - base);
+                const float p1 = fast_exp2(__uint_as_float(sr[2 * c + 1]) - base);
+                rs += p0 + p1;
+                pk[c] = pack2(p0, p1, MT);
+            }
+            l = l * alpha + rs;
+            if (j > 0) {
+                // P V of the previous tile has finished: P's buffer is free and O is stable
+                ok = __all_sync(0xffffffffu, mbar_wait(t_full, (j - 1) & 1));
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (__any_sync(0xffffffffu, up)) {
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        tc::ld32(tmem + lane_off + 128 + cc * 32, o);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tc::st32(tmem + lane_off + 128 + cc * 32, o);
+                    }
+                    tc::wait_st();
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < BN / 8; ++c)
+                *reinterpret_cast<uint4 *>(prow + ((c ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(p_full);
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(t_full, (nkv - 1) & 1));
+        if (!ok) {
+            set_error(a.err, PKV_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+        } else {
+            tc::fence_after_sync();
+            const float inv = 1.f / l;
+            using T = typename ModelT<MT>::T;
+            T *orow = static_cast<T *>(a.out) + ((int64_t)(start + qpos) * a.hq + h) * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                tc::ld32(tmem + lane_off + 128 + cc * 32, o);
+                tc::wait_ld();
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv, MT);
+                if (qpos < n) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                }
+            }
+        }
+    } else if (h % G == 0) {
+        // ------------------------------------------------------------ paged K/V write of this tile's rows
+        constexpr int CPR = D / 8; // 16-byte chunks per row
+        const int t = threadIdx.x - 192;
+        const int nrows = qlast - q0 + 1;
+        for (int idx = t; idx < nrows * CPR; idx += 64) {
+            const int rr = idx / CPR, c = idx - rr * CPR;
+            const int p = q0 + rr;
+            const int lb = p / a.bs;
+            const int blk = lb < a.max_blocks ? a.tables[(int64_t)seq * a.max_blocks + lb] : -1;
+            if (blk < 0 || blk >= a.num_blocks) {
+                if (c == 0) set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                continue;
+            }
+            const int off = p - lb * a.bs;
+            const int64_t src = ((int64_t)(start + p) * a.hkv + kvh) * D + c * 8;
+            const int64_t dst = ((int64_t)blk * 2 * a.hkv + kvh) * a.tile_elems + (int64_t)off * D + c * 8;
+            const int64_t vdst = dst + (int64_t)a.hkv * a.tile_elems;
+            *reinterpret_cast<uint4 *>(a.pool + dst * 2) = *reinterpret_cast<const uint4 *>(a.k + src * 2);
+            *reinterpret_cast<uint4 *>(a.pool + vdst * 2) = *reinterpret_cast<const uint4 *>(a.v + src * 2);
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+    static EncodeFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeFn>(p);
+    });
+    return fn;
+}
+
+// 2-D view [rows = tokens][cols = heads * D] of a packed tensor; box = 64 columns x box_rows rows.
+bool make_map(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t cols, int box_rows) {
+    EncodeFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, mt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                           const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, int MT>
+cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const Args &a, int grid,
+                     cudaStream_t st) {
+    auto kern = prefill_kernel<D, MT>;
+    const int smem = Layout<D>::TOTAL;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
+    return cudaGetLastError();
+}
+
+} // namespace pkv_prefill
+
+cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st) {
+    using namespace pkv_prefill;
+    if (p.total_tokens <= 0) return cudaSuccess;
+    const int D = c->head_dim;
+    const int mt = c->model_dtype;
+    Args a;
+    a.k = static_cast<const char *>(p.k);
+    a.v = static_cast<const char *>(p.v);
+    a.out = p.out;
+    a.cu = p.cu;
+    a.tables = p.tables;
+    a.pool = static_cast<char *>(c->pool);
+    a.err = c->err;
+    a.total_tokens = p.total_tokens;
+    a.num_blocks = c->num_blocks;
+    a.tile_elems = (int64_t)c->block_size * D;
+    a.num_seqs = p.num_seqs;
+    a.max_seqlen = p.max_seqlen;
+    a.max_blocks = p.max_blocks;
+    a.hq = p.num_q_heads;
+    a.hkv = c->num_kv_heads;
+    a.bs = c->block_size;
+    a.nqt_max = (p.max_seqlen + BM - 1) / BM;
+    a.scale_log2 = p.scale * 1.4426950408889634f;
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, p.q, mt, p.total_tokens, (int64_t)p.num_q_heads * D, BM) ||
+        !make_map(&tk, p.k, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN) ||
+        !make_map(&tv, p.v, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN))
+        return cudaErrorInvalidValue;
+    const int64_t grid = (int64_t)a.nqt_max * p.num_seqs * p.num_q_heads;
+    if (grid == 0) return cudaSuccess;
+    if (grid > 0x7FFFFFFF) return cudaErrorNotSupported;
+    PkvTimer timer(c, PKV_KIND_PREFILL, st);
+    cudaError_t e;
+    if (D == 128)
+        e = mt == PKV_BF16 ? launch_t<128, PKV_BF16>(tq, tk, tv, a, (int)grid, st)
+                           : launch_t<128, PKV_F16>(tq, tk, tv, a, (int)grid, st);
+    else
+        e = mt == PKV_BF16 ? launch_t<64, PKV_BF16>(tq, tk, tv, a, (int)grid, st)
+                           : launch_t<64, PKV_F16>(tq, tk, tv, a, (int)grid, st);
+    g_pkv_launches++;
+    return e;
+}
