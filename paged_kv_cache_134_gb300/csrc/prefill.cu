@@ -12,9 +12,9 @@
 //              128-byte swizzle, out-of-range rows zero-filled);
 //   warp 1     tensor-memory owner and MMA issuer (one thread): S = Q K^T into one of two TMEM S
 //              buffers (M=128, N=64, fp32), then O += P V into the TMEM O accumulator (M=128, N=D);
-//   warps 2-5  softmax, one thread per query row (TMEM lane = row): mask, exp2, row sums, P rounded
-//              to the model dtype and written to shared memory in the 128-byte-swizzled K-major
-//              layout the MMA reads; O in TMEM is rescaled only when a row's running max grows by
+//   warps 2-5  softmax, one thread per query row (TMEM lane = row): mask, exp2, row sums, P written
+//              to shared memory in the 128-byte-swizzled K-major layout the MMA reads (fp16 P for
+//              fp16 models; for bf16 models P = hi + lo, two bf16 tiles and two accumulating MMAs); O in TMEM is rescaled only when a row's running max grows by
 //              more than 2^8 (the exponent base stays fixed otherwise, which is exact algebra);
 //   warps 6-7  paged K/V writer for the tile's rows (only the CTA of the first query head of each
 //              KV group writes, so every (token, KV head) is written once).
@@ -44,8 +44,12 @@ struct Args {
     float scale_log2;
 };
 
-template <int D>
+// Shared memory.  bf16 models keep P as a hi + lo pair of bf16 tiles (P = hi + lo to ~2^-16
+// relative), because one bf16 rounding of P (2^-9 relative) alone would exceed the accuracy the
+// outputs are held to; fp16 P (2^-12) is used as a single tile.
+template <int D, int MT>
 struct Layout {
+    static constexpr int NP = MT == PKV_BF16 ? 2 : 1;
     static constexpr int Q = 0;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int KV_BYTES = BN * D * 2; // one K or V tile
@@ -53,7 +57,7 @@ struct Layout {
     static constexpr int V0 = K0 + 2 * KV_BYTES;
     static constexpr int P = V0 + 2 * KV_BYTES;
     static constexpr int P_BYTES = BM * BN * 2;
-    static constexpr int BAR = P + P_BYTES;
+    static constexpr int BAR = P + NP * P_BYTES;
     static constexpr int TOTAL = BAR + 256;
 };
 
@@ -67,11 +71,17 @@ PKV_DEV uint32_t pack2(float lo, float hi, int mt) {
     return r;
 }
 
+// two CTAs per SM whenever the shared memory allows it (then at most 128 registers a thread)
 template <int D, int MT>
-__global__ void __launch_bounds__(kThreads, 2)
+constexpr int min_blocks() {
+    return 2 * (Layout<D, MT>::TOTAL + 1024) <= 233472 ? 2 : 1;
+}
+
+template <int D, int MT>
+__global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const Args a) {
-    using L = Layout<D>;
+    using L = Layout<D, MT>;
     extern __shared__ __align__(1024) uint8_t smem[];
 
     // ---- work item, heaviest query tiles first
@@ -196,11 +206,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc::fence_after_sync();
                 const int st = j & 1;
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    const uint64_t ad = tc::smem_desc(sP + k * 32, 16, 1024);
-                    const uint64_t bd = tc::smem_desc(sV + st * L::KV_BYTES + k * 2048, BN * 128, 1024);
-                    tc::mma_f16(tO, ad, bd, IPV, (j > 0 || k > 0) ? 1u : 0u);
-                }
+                for (int part = 0; part < L::NP; ++part)
+#pragma unroll
+                    for (int k = 0; k < BN / 16; ++k) {
+                        const uint64_t ad = tc::smem_desc(sP + part * L::P_BYTES + k * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc(sV + st * L::KV_BYTES + k * 2048, BN * 128, 1024);
+                        tc::mma_f16(tO, ad, bd, IPV, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
+                    }
                 tc::commit(t_full);
                 tc::commit(kv_empty + st);
             }
@@ -251,13 +263,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             m_use = m_new;
             const float base = m_use == -INFINITY ? 0.f : m_use; // a row with no live key yet keeps p = 0
             float rs = 0.f;
-            uint32_t pk[BN / 2];
+            uint32_t phi[BN / 2], plo[L::NP == 2 ? BN / 2 : 1];
 #pragma unroll
             for (int c = 0; c < BN / 2; ++c) {
                 const float p0 = fast_exp2(__uint_as_float(sr[2 * c]) - base);
                 const float p1 = fast_exp2(__uint_as_float(sr[2 * c + 1]) - base);
                 rs += p0 + p1;
-                pk[c] = pack2(p0, p1, MT);
+                phi[c] = pack2(p0, p1, MT);
+                if constexpr (L::NP == 2) // remainders after bf16 rounding, themselves rounded to bf16
+                    plo[c] = pack2(p0 - __uint_as_float(phi[c] << 16), p1 - __uint_as_float(phi[c] & 0xFFFF0000u), MT);
             }
             l = l * alpha + rs;
             if (j > 0) {
@@ -267,21 +281,26 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc::fence_after_sync();
                 if (__any_sync(0xffffffffu, up)) {
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t o[32];
-                        tc::ld32(tmem + lane_off + 128 + cc * 32, o);
+                    for (int cc = 0; cc < D / 16; ++cc) {
+                        uint32_t o[16];
+                        tc::ld16(tmem + lane_off + 128 + cc * 16, o);
                         tc::wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tc::st32(tmem + lane_off + 128 + cc * 32, o);
+                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tc::st16(tmem + lane_off + 128 + cc * 16, o);
                     }
                     tc::wait_st();
                 }
             }
 #pragma unroll
-            for (int c = 0; c < BN / 8; ++c)
-                *reinterpret_cast<uint4 *>(prow + ((c ^ (r & 7)) << 4)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            for (int c = 0; c < BN / 8; ++c) {
+                const int off = (c ^ (r & 7)) << 4;
+                *reinterpret_cast<uint4 *>(prow + off) =
+                    make_uint4(phi[4 * c], phi[4 * c + 1], phi[4 * c + 2], phi[4 * c + 3]);
+                if constexpr (L::NP == 2)
+                    *reinterpret_cast<uint4 *>(prow + L::P_BYTES + off) =
+                        make_uint4(plo[4 * c], plo[4 * c + 1], plo[4 * c + 2], plo[4 * c + 3]);
+            }
             fence_proxy_async_smem();
             tc::fence_before_sync();
             mbar_arrive(p_full);
@@ -296,18 +315,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             using T = typename ModelT<MT>::T;
             T *orow = static_cast<T *>(a.out) + ((int64_t)(start + qpos) * a.hq + h) * D;
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t o[32];
-                tc::ld32(tmem + lane_off + 128 + cc * 32, o);
+            for (int cc = 0; cc < D / 16; ++cc) {
+                uint32_t o[16];
+                tc::ld16(tmem + lane_off + 128 + cc * 16, o);
                 tc::wait_ld();
-                uint32_t w[16];
+                uint32_t w[8];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
+                for (int e = 0; e < 8; ++e)
                     w[e] = pack2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv, MT);
                 if (qpos < n) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 16);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
         }
@@ -379,7 +398,7 @@ template <int D, int MT>
 cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const Args &a, int grid,
                      cudaStream_t st) {
     auto kern = prefill_kernel<D, MT>;
-    const int smem = Layout<D>::TOTAL;
+    const int smem = Layout<D, MT>::TOTAL;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
