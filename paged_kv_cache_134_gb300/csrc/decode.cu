@@ -15,7 +15,7 @@ int env_int(const char *name, int dflt) {
 // target resident CTAs per SM (shared-memory budget per CTA follows from it)
 int ctas_per_sm() { return env_int("PAGEDKV_DECODE_CTAS", 3); }
 
-using DecodeFn = cudaError_t (*)(const pkv_decode::Args &, int, int, int, size_t, cudaStream_t, bool);
+using DecodeFn = cudaError_t (*)(const pkv_decode::Args &, int, int, int, size_t, cudaStream_t);
 using OccFn = int (*)(int, int, size_t);
 
 void pick(const pkv_cache *c, DecodeFn *fn, OccFn *occ) {
@@ -43,10 +43,11 @@ int decode_split_blocks(const pkv_cache *c) {
 }
 
 int64_t decode_workspace_floats(const pkv_cache *c, int num_seqs, int num_q_heads, int max_splits) {
-    // partial o [rows][D] and (m, l) [rows][2], rows = S * Hq * max_splits; only needed when splits > 1
+    // partial o [rows][D], (m, l) [rows][2] with rows = S * Hq * max_splits, then S * Hkv int counters;
+    // only needed when a sequence can have more than one split
     if (max_splits <= 1) return 0;
     const int64_t rows = (int64_t)num_seqs * num_q_heads * max_splits;
-    return rows * (c->head_dim + 2);
+    return rows * (c->head_dim + 2) + (int64_t)num_seqs * c->num_kv_heads;
 }
 
 cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) {
@@ -61,7 +62,9 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
     a.tables = d.tables;
     a.lens = d.lens;
     a.ws_o = d.ws_o;
-    a.ws_ml = d.ws_o ? d.ws_o + (int64_t)d.num_seqs * d.num_q_heads * d.max_splits * c->head_dim : nullptr;
+    const int64_t rows = (int64_t)d.num_seqs * d.num_q_heads * d.max_splits;
+    a.ws_ml = d.ws_o ? d.ws_o + rows * c->head_dim : nullptr;
+    a.counters = d.ws_o ? reinterpret_cast<int *>(a.ws_ml + 2 * rows) : nullptr;
     a.err = c->err;
     a.num_blocks = c->num_blocks;
     a.tile_bytes = static_cast<int>(c->tile_bytes);
@@ -94,14 +97,8 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
     int per_sm = occ(c->head_dim, G, smem);
     if (per_sm < 1) per_sm = 1;
     const int grid = c->num_sms * per_sm;
-    cudaError_t e;
-    {
-        PkvTimer timer(c, PKV_KIND_DECODE, st);
-        e = fn(a, c->head_dim, G, grid, smem, st, false);
-        g_pkv_launches++;
-    }
-    if (e != cudaSuccess) return e;
-    e = fn(a, c->head_dim, G, 0, 0, st, true);
+    PkvTimer timer(c, PKV_KIND_DECODE, st);
+    const cudaError_t e = fn(a, c->head_dim, G, grid, smem, st);
     g_pkv_launches++;
     return e;
 }

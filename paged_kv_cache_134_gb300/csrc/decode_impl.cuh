@@ -26,8 +26,9 @@
 //    accumulator) runs per 16-token chunk with exp2 on prescaled scores.
 //  * At the end of a unit the four warps' (m, l, acc) are merged through shared memory.  A
 //    sequence with one split writes its output row directly; otherwise the unit writes an
-//    fp32 partial (m, l, unnormalised o) and a merge kernel combines the splits in split
-//    order.
+//    fp32 partial (m, l, unnormalised o), fences, and bumps a per-(sequence, KV head) counter;
+//    the CTA that finishes the last split combines all partials in split order and resets the
+//    counter (so the merge order, and every output bit, is independent of which CTA is last).
 //  * Every mbarrier wait is bounded (PKV_WAIT_LIMIT_NS); a timeout sets PKV_DEVERR_TIMEOUT
 //    and the CTA winds down without further waiting on work that will not arrive.
 #pragma once
@@ -47,7 +48,8 @@ struct Args {
     const char *pool;
     const float *k_scale, *v_scale;
     const int32_t *tables, *lens;
-    float *ws_o, *ws_ml;
+    float *ws_o, *ws_ml; // split partials: o [rows][D], (m, l) [rows][2], rows = S * Hq * max_splits
+    int *counters;       // [S * Hkv] finished split units per (sequence, KV head); zero between launches
     unsigned int *err;
     int64_t num_blocks;
     int64_t blk_stride;  // bytes between consecutive physical blocks
@@ -190,6 +192,36 @@ PKV_DEV void process_tile(const char *ks, const char *vs, int bs, int valid, con
     }
 }
 
+// Combine the split partials of (sequence s, KV head kvh) in split order and write the rows of its
+// G query heads.  Partials written by other CTAs are read through L2 (ld.global.cg).
+template <int D, int G, int MT>
+PKV_DEV void merge_splits(const Args &a, int s, int kvh, int nsplit, int tid) {
+    using M = ModelT<MT>;
+    using T = typename M::T;
+    for (int o = tid; o < G * D; o += kConsumerWarps * 32) {
+        const int g = o / D, d = o - g * D;
+        const int h = kvh * G + g;
+        const int64_t base = ((int64_t)s * a.hq + h) * a.max_splits;
+        float Mx = -INFINITY;
+#pragma unroll 4
+        for (int j = 0; j < nsplit; ++j) {
+            const float lj = __ldcg(a.ws_ml + 2 * (base + j) + 1);
+            if (lj > 0.f) Mx = fmaxf(Mx, __ldcg(a.ws_ml + 2 * (base + j)));
+        }
+        float num = 0.f, den = 0.f;
+#pragma unroll 4
+        for (int j = 0; j < nsplit; ++j) {
+            const float lj = __ldcg(a.ws_ml + 2 * (base + j) + 1);
+            if (lj > 0.f) {
+                const float wt = fast_exp2(__ldcg(a.ws_ml + 2 * (base + j)) - Mx);
+                den = fmaf(wt, lj, den);
+                num = fmaf(wt, __ldcg(a.ws_o + (base + j) * D + d), num);
+            }
+        }
+        static_cast<T *>(a.out)[((int64_t)s * a.hq + h) * D + d] = M::from_f(den > 0.f ? num / den : 0.f);
+    }
+}
+
 template <int D, int G, int MT, int KVT>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     using M = ModelT<MT>;
@@ -204,6 +236,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     uint64_t *empty = full + NST;
     int *flags = reinterpret_cast<int *>(empty + NST);
     int *abort_flag = flags + NST;
+    int *last_flag = abort_flag + 1;
     float *mrg = reinterpret_cast<float *>(abort_flag + 4);
     int *pf = reinterpret_cast<int *>(mrg + NCW * G * (D + 2));
     int *pp = pf + (S + 1);
@@ -259,6 +292,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     }
     __syncthreads();
     const int U = (pf[S] + pp[S]) * a.hkv;
+    // rows of sequences with no tokens are zero (no unit covers them)
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < (int64_t)S * a.hq * D;
+         e += (int64_t)gridDim.x * blockDim.x)
+        if (nb[e / ((int64_t)a.hq * D)] == 0) static_cast<T *>(a.out)[e] = M::from_f(0.f);
 
     if (warp == NCW) {
         // ---------------------------------------------------------------- producer warp
@@ -413,49 +450,20 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
                 }
             }
         }
+        if (un.nsplit > 1) {
+            __threadfence();
+            named_barrier_sync(1, NCW * 32);
+            int *cnt = a.counters + (int64_t)un.s * a.hkv + un.kvh;
+            if (tid == 0) *last_flag = (atomicAdd(cnt, 1) == un.nsplit - 1) ? 1 : 0;
+            named_barrier_sync(1, NCW * 32);
+            if (*reinterpret_cast<volatile int *>(last_flag)) {
+                __threadfence();
+                merge_splits<D, G, MT>(a, un.s, un.kvh, un.nsplit, tid);
+                if (tid == 0) *cnt = 0;
+            }
+        }
         named_barrier_sync(1, NCW * 32);
     }
-}
-
-// Merge of the per-split partials of sequences with more than one split; zero rows for
-// L_s == 0.  One warp per (sequence, query head); splits are combined in split order.
-template <int D, int MT>
-__global__ void __launch_bounds__(128) merge_kernel(const Args a) {
-    using M = ModelT<MT>;
-    using T = typename M::T;
-    const int wid = blockIdx.x * 4 + threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (wid >= a.num_seqs * a.hq) return;
-    const int s = wid / a.hq;
-    const int L = a.lens[s];
-    int n = L > 0 ? (L + a.bs - 1) / a.bs : 0;
-    if (n > a.max_blocks) n = a.max_blocks;
-    const int nsplit = n / a.split_blocks + ((n % a.split_blocks) ? 1 : 0);
-    if (nsplit == 1) return;
-    T *o = static_cast<T *>(a.out) + (int64_t)wid * D;
-    constexpr int PER = D / 32;
-    if (nsplit == 0) {
-#pragma unroll
-        for (int e = 0; e < PER; ++e) o[lane * PER + e] = M::from_f(0.f);
-        return;
-    }
-    const int64_t base = (int64_t)wid * a.max_splits;
-    float Mx = -INFINITY;
-    for (int j = 0; j < nsplit; ++j)
-        if (a.ws_ml[2 * (base + j) + 1] > 0.f) Mx = fmaxf(Mx, a.ws_ml[2 * (base + j)]);
-    float num[PER], den = 0.f;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) num[e] = 0.f;
-    for (int j = 0; j < nsplit; ++j) {
-        const float lj = a.ws_ml[2 * (base + j) + 1];
-        if (!(lj > 0.f)) continue;
-        const float wt = fast_exp2(a.ws_ml[2 * (base + j)] - Mx);
-        den = fmaf(wt, lj, den);
-        const float *src = a.ws_o + (base + j) * D + lane * PER;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) num[e] = fmaf(wt, src[e], num[e]);
-    }
-#pragma unroll
-    for (int e = 0; e < PER; ++e) o[lane * PER + e] = M::from_f(den > 0.f ? num[e] / den : 0.f);
 }
 
 inline size_t smem_bytes(int D, int G, int nst, int tile_bytes, int S) {
@@ -472,19 +480,11 @@ cudaError_t launch_t(const Args &a, int grid, size_t smem, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <int D, int MT>
-cudaError_t launch_merge_t(const Args &a, cudaStream_t st) {
-    const int rows = a.num_seqs * a.hq;
-    if (rows == 0) return cudaSuccess;
-    merge_kernel<D, MT><<<(rows + 3) / 4, 128, 0, st>>>(a);
-    return cudaGetLastError();
-}
-
 // Dispatch over head_dim and group size for one (model dtype, KV dtype) pair.
 template <int MT, int KVT>
-cudaError_t dispatch(const Args &a, int D, int G, int grid, size_t smem, cudaStream_t st, bool merge) {
+cudaError_t dispatch(const Args &a, int D, int G, int grid, size_t smem, cudaStream_t st) {
 #define PKV_CASE(DD, GG)                                                                                               \
-    if (D == DD && G == GG) return merge ? launch_merge_t<DD, MT>(a, st) : launch_t<DD, GG, MT, KVT>(a, grid, smem, st);
+    if (D == DD && G == GG) return launch_t<DD, GG, MT, KVT>(a, grid, smem, st);
     PKV_CASE(64, 1)
     PKV_CASE(64, 2)
     PKV_CASE(64, 4)
@@ -524,12 +524,10 @@ int occupancy_dispatch(int D, int G, size_t smem) {
 } // namespace pkv_decode
 
 // Per (model dtype, KV dtype) entry points, each compiled in its own translation unit.
-cudaError_t pkv_decode_f16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t, bool merge);
-cudaError_t pkv_decode_bf16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t, bool merge);
-cudaError_t pkv_decode_fp8_f16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t,
-                               bool merge);
-cudaError_t pkv_decode_fp8_bf16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t,
-                                bool merge);
+cudaError_t pkv_decode_f16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t);
+cudaError_t pkv_decode_bf16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t);
+cudaError_t pkv_decode_fp8_f16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t);
+cudaError_t pkv_decode_fp8_bf16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t);
 int pkv_decode_occupancy_f16(int D, int G, size_t smem);
 int pkv_decode_occupancy_bf16(int D, int G, size_t smem);
 int pkv_decode_occupancy_fp8_f16(int D, int G, size_t smem);
