@@ -115,12 +115,23 @@ struct ModelT<PKV_F16> {
     using T = __half;
     static PKV_DEV float to_f(T x) { return __half2float(x); }
     static PKV_DEV T from_f(float x) { return __float2half_rn(x); }
+    // two floats -> one 32-bit word of two fp16 (round-to-nearest-even), `lo` in the low half
+    static PKV_DEV uint32_t pack(float lo, float hi) {
+        uint32_t r;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        return r;
+    }
 };
 template <>
 struct ModelT<PKV_BF16> {
     using T = __nv_bfloat16;
     static PKV_DEV float to_f(T x) { return __bfloat162float(x); }
     static PKV_DEV T from_f(float x) { return __float2bfloat16_rn(x); }
+    static PKV_DEV uint32_t pack(float lo, float hi) {
+        uint32_t r;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        return r;
+    }
 };
 
 // 8 consecutive 16-bit elements (one uint4) -> 8 floats
