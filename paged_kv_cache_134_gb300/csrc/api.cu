@@ -35,7 +35,6 @@ int ensure_workspace(pkv_cache *c, int64_t floats) {
     c->ws = nullptr;
     c->ws_bytes = 0;
     cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&c->ws), (size_t)bytes);
-    if (e == cudaSuccess) e = cudaMemset(c->ws, 0, (size_t)bytes); // the split counters start at zero
     if (e != cudaSuccess) {
         c->ws = nullptr;
         cudaGetLastError();
@@ -206,7 +205,6 @@ int kv_cache_check_error(pkv_cache_t c, int *device_code) {
     if (e == cudaSuccess) e = cudaMemset(c->err, 0, sizeof v);
     if (e != cudaSuccess) return pkv_cuda_fail(e, "reading the device error word");
     if (device_code) *device_code = static_cast<int>(v);
-    if (v && c->ws) cudaMemset(c->ws, 0, (size_t)c->ws_bytes); // a cut-short decode may leave split counters set
     if (v) return pkv_fail(PKV_EDEVICE, "device error bits 0x%x", v);
     return PKV_OK;
 }

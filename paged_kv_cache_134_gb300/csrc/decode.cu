@@ -12,27 +12,41 @@ int env_int(const char *name, int dflt) {
     return x > 0 ? x : dflt;
 }
 
-PkvDecodeFn pick(const pkv_cache *c) {
-    if (c->kv_dtype == PKV_F16) return pkv_decode_f16;
-    if (c->kv_dtype == PKV_BF16) return pkv_decode_bf16;
-    return c->model_dtype == PKV_F16 ? pkv_decode_fp8_f16 : pkv_decode_fp8_bf16;
+// target resident CTAs per SM (shared-memory budget per CTA follows from it)
+int ctas_per_sm() { return env_int("PAGEDKV_DECODE_CTAS", 3); }
+
+using DecodeFn = cudaError_t (*)(const pkv_decode::Args &, int, int, int, size_t, cudaStream_t, bool);
+using OccFn = int (*)(int, int, size_t);
+
+void pick(const pkv_cache *c, DecodeFn *fn, OccFn *occ) {
+    if (c->kv_dtype == PKV_F16) {
+        *fn = pkv_decode_f16;
+        *occ = pkv_decode_occupancy_f16;
+    } else if (c->kv_dtype == PKV_BF16) {
+        *fn = pkv_decode_bf16;
+        *occ = pkv_decode_occupancy_bf16;
+    } else if (c->model_dtype == PKV_F16) {
+        *fn = pkv_decode_fp8_f16;
+        *occ = pkv_decode_occupancy_fp8_f16;
+    } else {
+        *fn = pkv_decode_fp8_bf16;
+        *occ = pkv_decode_occupancy_fp8_bf16;
+    }
 }
 
 } // namespace
 
 int decode_split_blocks(const pkv_cache *c) {
-    // a unit's block ids must fit one per lane of a warp
     const int tokens = env_int("PAGEDKV_SPLIT_TOKENS", 256);
     const int b = tokens / c->block_size;
-    return b < 1 ? 1 : (b > 32 ? 32 : b);
+    return b > 0 ? b : 1;
 }
 
 int64_t decode_workspace_floats(const pkv_cache *c, int num_seqs, int num_q_heads, int max_splits) {
-    // partial o [rows][D], (m, l) [rows][2] with rows = S * Hq * max_splits, then S * Hkv int counters;
-    // only needed when a sequence can have more than one split
+    // partial o [rows][D] and (m, l) [rows][2], rows = S * Hq * max_splits; only needed when splits > 1
     if (max_splits <= 1) return 0;
     const int64_t rows = (int64_t)num_seqs * num_q_heads * max_splits;
-    return rows * (c->head_dim + 2) + (int64_t)num_seqs * c->num_kv_heads;
+    return rows * (c->head_dim + 2);
 }
 
 cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) {
@@ -47,9 +61,7 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
     a.tables = d.tables;
     a.lens = d.lens;
     a.ws_o = d.ws_o;
-    const int64_t rows = (int64_t)d.num_seqs * d.num_q_heads * d.max_splits;
-    a.ws_ml = d.ws_o ? d.ws_o + rows * c->head_dim : nullptr;
-    a.counters = d.ws_o ? reinterpret_cast<int *>(a.ws_ml + 2 * rows) : nullptr;
+    a.ws_ml = d.ws_o ? d.ws_o + (int64_t)d.num_seqs * d.num_q_heads * d.max_splits * c->head_dim : nullptr;
     a.err = c->err;
     a.num_blocks = c->num_blocks;
     a.tile_bytes = static_cast<int>(c->tile_bytes);
@@ -64,22 +76,32 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
     a.max_splits = d.max_splits;
     a.qk_scale_log2 = d.scale * 1.4426950408889634f;
 
-    const PkvDecodeFn fn = pick(c);
-    // per-warp ring: at least 16 KB (2 stages minimum); 4 warps per CTA when a warp's ring is <= 16 KB,
-    // else 2, so that at least 3 CTAs fit an SM's shared memory
-    const int stage = 2 * a.tile_bytes;
-    int nst = env_int("PAGEDKV_DECODE_STAGES", (16384 + stage - 1) / stage);
-    if (nst < 2) nst = 2;
-    if (nst > 16) nst = 16;
+    DecodeFn fn;
+    OccFn occ;
+    pick(c, &fn, &occ);
+    // stages: fill the per-CTA shared-memory budget
+    const size_t fixed = smem_bytes(c->head_dim, G, 0, a.tile_bytes, d.num_seqs);
+    const size_t per_stage = smem_bytes(c->head_dim, G, 1, a.tile_bytes, d.num_seqs) - fixed;
+    const int want = ctas_per_sm();
+    const size_t budget = (size_t)(233472 / want) - 1024;
+    int nst = budget > fixed ? static_cast<int>((budget - fixed) / per_stage) : 0;
+    // a whole number of stages per consumer warp (see the tile-to-warp rule in the kernel)
+    nst -= nst % kConsumerWarps;
+    if (nst > 32) nst = 32;
+    if (nst < kConsumerWarps) nst = kConsumerWarps;
     a.nstages = nst;
-    const int nw = (size_t)nst * stage <= 16384 ? kMaxWarps : 2;
-    const size_t smem = smem_bytes(nw, nst, a.tile_bytes, d.num_seqs);
-    int per_sm = 0;
-    fn(a, c->head_dim, G, 0, nw * 32, smem, st, &per_sm);
+    const size_t smem = smem_bytes(c->head_dim, G, nst, a.tile_bytes, d.num_seqs);
+    int per_sm = occ(c->head_dim, G, smem);
     if (per_sm < 1) per_sm = 1;
     const int grid = c->num_sms * per_sm;
-    PkvTimer timer(c, PKV_KIND_DECODE, st);
-    const cudaError_t e = fn(a, c->head_dim, G, grid, nw * 32, smem, st, nullptr);
+    cudaError_t e;
+    {
+        PkvTimer timer(c, PKV_KIND_DECODE, st);
+        e = fn(a, c->head_dim, G, grid, smem, st, false);
+        g_pkv_launches++;
+    }
+    if (e != cudaSuccess) return e;
+    e = fn(a, c->head_dim, G, 0, 0, st, true);
     g_pkv_launches++;
     return e;
 }

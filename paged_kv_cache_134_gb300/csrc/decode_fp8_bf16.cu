@@ -2,7 +2,9 @@
 // that the instantiations compile in parallel).
 #include "decode_impl.cuh"
 
-cudaError_t pkv_decode_fp8_bf16(const pkv_decode::Args &a, int D, int G, int grid, int threads, size_t smem,
-                          cudaStream_t st, int *occ) {
-    return pkv_decode::dispatch<PKV_BF16, PKV_FP8_E4M3>(a, D, G, grid, threads, smem, st, occ);
+cudaError_t pkv_decode_fp8_bf16(const pkv_decode::Args &a, int D, int G, int grid, size_t smem, cudaStream_t st,
+                          bool merge) {
+    return pkv_decode::dispatch<PKV_BF16, PKV_FP8_E4M3>(a, D, G, grid, smem, st, merge);
 }
+
+int pkv_decode_occupancy_fp8_bf16(int D, int G, size_t smem) { return pkv_decode::occupancy_dispatch<PKV_BF16, PKV_FP8_E4M3>(D, G, smem); }

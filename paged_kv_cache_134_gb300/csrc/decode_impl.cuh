@@ -8,31 +8,28 @@
 // head's tiles serves all G query heads that share it, so every K/V byte is read once.
 //
 // Design (GB300, HBM-bound, ~1 flop per byte for G = 1):
-//  * Work unit = (sequence, KV head, split), a split being up to `split_blocks` (<= 32)
-//    consecutive logical blocks.  Splits are block-aligned and depend only on L_s, so the
-//    arithmetic order of every output is fixed by the lengths alone (placement of physical
-//    blocks, sharing of prefix blocks and the batch composition never change a bit).
-//  * Persistent CTAs (as many as fit per SM); every warp is an independent worker.  Units are
-//    listed full splits first, partial tail splits last, and go round-robin over all warps of
-//    the grid.
-//  * A warp owns a ring of `nstages` shared-memory stages.  Its lane 0 issues one 1-D bulk async
-//    copy (cp.async.bulk, the TMA's linear mode) per (block, K|V, head) tile, completion tracked by
-//    an mbarrier transaction count; it refills a stage right after the warp has consumed it, so the
-//    ring runs `nstages` tiles ahead across unit boundaries and needs no "empty" barrier.  The pool
-//    layout [block][K|V][head][offset][dim] makes each tile one contiguous bs*D*elt-byte run (4 KB
-//    for bs=16, D=128, fp16): one table lookup yields two large aligned copies, issued with an L2
-//    evict-first hint because KV is streamed once.  Block ids for a unit are read once, one per
-//    lane, and moved to lane 0 with a shuffle.
-//  * In a warp, D/8 lanes share a token (16-byte vector loads from shared memory, conflict-free),
-//    partial dot products are reduced with xor-shuffles, and an online softmax (running max m, sum l,
-//    rescaled accumulator) runs per 16-token chunk with exp2 on prescaled scores.
-//  * A sequence with one split writes its output row at the end of its unit.  Otherwise the warp
-//    writes an fp32 partial (m, l, unnormalised o), and its lane 0 fences and bumps a per-(sequence,
-//    KV head) counter; the warp that finishes the last split combines all partials in split order
-//    and resets the counter (so the merge order, and every output bit, does not depend on which warp
-//    is last).  A warp's unit-end work never blocks the other warps.
-//  * Every mbarrier wait is bounded (PKV_WAIT_LIMIT_NS); a timeout sets PKV_DEVERR_TIMEOUT, the warp
-//    waits (bounded) for its own copies in flight and stops.
+//  * Work unit = (sequence, KV head, split), a split being up to `split_blocks` consecutive
+//    logical blocks.  Splits are block-aligned and depend only on L_s, so the arithmetic
+//    order of every output is fixed by the lengths alone (placement of physical blocks,
+//    sharing of prefix blocks and the batch composition never change a bit).
+//  * Persistent CTAs (a whole number of CTAs per SM) walk a unit list that puts full splits
+//    first and partial tail splits last; units go round-robin over CTAs.
+//  * One producer warp per CTA reads block-table entries (32 at a time, coalesced) and issues
+//    one 1-D bulk async copy (cp.async.bulk, the TMA's linear mode) per (block, K|V, head)
+//    tile into a ring of shared-memory stages, completion tracked by mbarrier transaction
+//    counts.  The pool layout [block][K|V][head][offset][dim] makes each tile one contiguous
+//    bs*D*elt-byte run (4 KB for bs=16, D=128, fp16), so one table lookup yields two large
+//    aligned copies.  The copies carry an L2 evict-first hint: KV is streamed once.
+//  * Four consumer warps take the tiles round-robin by their index in the CTA's tile stream.  In a warp, D/8 lanes share a
+//    token (16-byte vector loads from shared memory, conflict-free), partial dot products are
+//    reduced with xor-shuffles, and an online softmax (running max m, sum l, rescaled
+//    accumulator) runs per 16-token chunk with exp2 on prescaled scores.
+//  * At the end of a unit the four warps' (m, l, acc) are merged through shared memory.  A
+//    sequence with one split writes its output row directly; otherwise the unit writes an
+//    fp32 partial (m, l, unnormalised o) and a merge kernel combines the splits in split
+//    order.
+//  * Every mbarrier wait is bounded (PKV_WAIT_LIMIT_NS); a timeout sets PKV_DEVERR_TIMEOUT
+//    and the CTA winds down without further waiting on work that will not arrive.
 #pragma once
 
 #include "device_common.cuh"
@@ -40,7 +37,8 @@
 
 namespace pkv_decode {
 
-constexpr int kMaxWarps = 4;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxSeqs = 1024;
 
 struct Args {
@@ -49,8 +47,7 @@ struct Args {
     const char *pool;
     const float *k_scale, *v_scale;
     const int32_t *tables, *lens;
-    float *ws_o, *ws_ml; // split partials: o [rows][D], (m, l) [rows][2], rows = S * Hq * max_splits
-    int *counters;       // [S * Hkv] finished split units per (sequence, KV head); zero between launches
+    float *ws_o, *ws_ml;
     unsigned int *err;
     int64_t num_blocks;
     int64_t blk_stride;  // bytes between consecutive physical blocks
@@ -193,91 +190,32 @@ PKV_DEV void process_tile(const char *ks, const char *vs, int bs, int valid, con
     }
 }
 
-PKV_DEV float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-PKV_DEV float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// Combine the split partials of (sequence s, KV head kvh) and write the rows of its G query heads,
-// one warp.  The weights exp2(m_j - M) are formed per split; the sums run in a fixed order.
-// Partials written by other warps are read through L2 (ld.global.cg).
-template <int D, int G, int MT>
-PKV_DEV void merge_splits_warp(const Args &a, int s, int kvh, int nsplit, int lane) {
-    using M = ModelT<MT>;
-    using T = typename M::T;
-    constexpr int PER = D / 32;
-#pragma unroll 1
-    for (int g = 0; g < G; ++g) {
-        const int h = kvh * G + g;
-        const int64_t base = ((int64_t)s * a.hq + h) * a.max_splits;
-        float Mx = -INFINITY;
-        for (int j = lane; j < nsplit; j += 32) {
-            const float lj = __ldcg(a.ws_ml + 2 * (base + j) + 1);
-            if (lj > 0.f) Mx = fmaxf(Mx, __ldcg(a.ws_ml + 2 * (base + j)));
-        }
-        Mx = warp_max(Mx);
-        float num[PER], den = 0.f;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) num[e] = 0.f;
-        for (int j0 = 0; j0 < nsplit; j0 += 32) {
-            const int j = j0 + lane;
-            float wj = 0.f, lj = 0.f;
-            if (j < nsplit) {
-                lj = __ldcg(a.ws_ml + 2 * (base + j) + 1);
-                if (lj > 0.f) wj = fast_exp2(__ldcg(a.ws_ml + 2 * (base + j)) - Mx);
-            }
-            den += warp_sum(wj * lj);
-            const int cnt = min(32, nsplit - j0);
-            for (int jj = 0; jj < cnt; ++jj) {
-                const float w = __shfl_sync(0xffffffffu, wj, jj);
-                const float *src = a.ws_o + (base + j0 + jj) * D + lane * PER;
-                if constexpr (PER == 4) {
-                    const float4 o4 = __ldcg(reinterpret_cast<const float4 *>(src));
-                    num[0] = fmaf(w, o4.x, num[0]);
-                    num[1] = fmaf(w, o4.y, num[1]);
-                    num[2] = fmaf(w, o4.z, num[2]);
-                    num[3] = fmaf(w, o4.w, num[3]);
-                } else {
-                    const float2 o2 = __ldcg(reinterpret_cast<const float2 *>(src));
-                    num[0] = fmaf(w, o2.x, num[0]);
-                    num[1] = fmaf(w, o2.y, num[1]);
-                }
-            }
-        }
-        T *orow = static_cast<T *>(a.out) + ((int64_t)s * a.hq + h) * D + lane * PER;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) orow[e] = M::from_f(den > 0.f ? num[e] / den : 0.f);
-    }
-}
-
 template <int D, int G, int MT, int KVT>
-__global__ void __launch_bounds__(kMaxWarps * 32) decode_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     using M = ModelT<MT>;
     using T = typename M::T;
+    constexpr int NCW = kConsumerWarps;
     constexpr int LPT = D / 8;
     extern __shared__ __align__(128) unsigned char smem[];
-    const int NW = blockDim.x >> 5;
     const int NST = a.nstages;
     const int S = a.num_seqs;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const size_t stage_bytes = 2 * (size_t)a.tile_bytes;
-    char *ring = reinterpret_cast<char *>(smem) + (size_t)warp * NST * stage_bytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NW * NST * stage_bytes) + warp * NST;
-    int *flags = reinterpret_cast<int *>(reinterpret_cast<uint64_t *>(smem + (size_t)NW * NST * stage_bytes) +
-                                         NW * NST) + warp * NST;
-    int *pf = reinterpret_cast<int *>(reinterpret_cast<uint64_t *>(smem + (size_t)NW * NST * stage_bytes) + NW * NST) +
-              NW * NST;
+    char *ring = reinterpret_cast<char *>(smem);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NST * 2 * a.tile_bytes);
+    uint64_t *empty = full + NST;
+    int *flags = reinterpret_cast<int *>(empty + NST);
+    int *abort_flag = flags + NST;
+    float *mrg = reinterpret_cast<float *>(abort_flag + 4);
+    int *pf = reinterpret_cast<int *>(mrg + NCW * G * (D + 2));
     int *pp = pf + (S + 1);
     int *nb = pp + (S + 1);
 
-    if (lane == 0) {
-        for (int i = 0; i < NST; ++i) mbar_init(&full[i], 1);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        *abort_flag = 0;
         fence_mbarrier_init();
     }
     // unit list: per sequence, full splits and (0 or 1) partial split
@@ -321,58 +259,60 @@ __global__ void __launch_bounds__(kMaxWarps * 32) decode_kernel(const Args a) {
     }
     __syncthreads();
     const int U = (pf[S] + pp[S]) * a.hkv;
-    // rows of sequences with no tokens are zero (no unit covers them)
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < (int64_t)S * a.hq * D;
-         e += (int64_t)gridDim.x * blockDim.x)
-        if (nb[e / ((int64_t)a.hq * D)] == 0) static_cast<T *>(a.out)[e] = M::from_f(0.f);
 
-    const int gw = blockIdx.x * NW + warp, TW = gridDim.x * NW;
-    const uint64_t policy = l2_policy_evict_first();
-
-    // ---- issue side: runs `NST` tiles ahead of consumption over this warp's unit sequence
-    int iu = gw, it = 0;
-    Unit iun{};
-    int irow = 0; // block id of tile `lane` of unit iu
-    if (iu < U) {
-        iun = unit_info(iu, pf, pp, nb, S, a.hkv, bps);
-        irow = lane < iun.ntiles ? a.tables[(int64_t)iun.s * a.max_blocks + iun.blk0 + lane] : 0;
-    }
-    uint32_t issued = 0, consumed = 0;
-    auto issue_one = [&]() {
-        while (iu < U && it >= iun.ntiles) {
-            iu += TW;
-            it = 0;
-            if (iu < U) {
-                iun = unit_info(iu, pf, pp, nb, S, a.hkv, bps);
-                irow = lane < iun.ntiles ? a.tables[(int64_t)iun.s * a.max_blocks + iun.blk0 + lane] : 0;
+    if (warp == NCW) {
+        // ---------------------------------------------------------------- producer warp
+        const uint64_t policy = l2_policy_evict_first();
+        uint32_t tau = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+            const Unit un = unit_info(u, pf, pp, nb, S, a.hkv, bps);
+            const int32_t *trow = a.tables + (int64_t)un.s * a.max_blocks + un.blk0;
+            const char *head_base = a.pool + (int64_t)un.kvh * a.tile_bytes;
+            for (int i0 = 0; i0 < un.ntiles && ok; i0 += 32) {
+                const int cnt = min(32, un.ntiles - i0);
+                const int myb = lane < cnt ? trow[i0 + lane] : 0;
+                for (int i = 0; i < cnt; ++i) {
+                    const int b = __shfl_sync(0xffffffffu, myb, i);
+                    if (lane == 0) {
+                        const uint32_t stage = tau % NST, round = tau / NST;
+                        if (round > 0 && !mbar_wait(&empty[stage], (round - 1) & 1)) {
+                            // stop issuing; the consumers time out on the stages that never fill
+                            set_error(a.err, PKV_DEVERR_TIMEOUT);
+                            ok = false;
+                        } else if (b >= 0 && b < a.num_blocks) {
+                            flags[stage] = 0;
+                            char *dst = ring + (size_t)stage * 2 * a.tile_bytes;
+                            const char *src = head_base + (int64_t)b * a.blk_stride;
+                            mbar_arrive_expect_tx(&full[stage], 2u * a.tile_bytes);
+                            bulk_g2s_hint(dst, src, a.tile_bytes, &full[stage], policy);
+                            bulk_g2s_hint(dst + a.tile_bytes, src + a.kv_stride, a.tile_bytes, &full[stage], policy);
+                        } else {
+                            flags[stage] = 1;
+                            set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                            mbar_arrive(&full[stage]);
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    ++tau;
+                }
             }
         }
-        if (iu >= U) return;
-        const int b = __shfl_sync(0xffffffffu, irow, it);
+        // drain: the copies of the last stages must land before this CTA's shared memory goes away
         if (lane == 0) {
-            const uint32_t st = issued % NST;
-            char *dst = ring + st * stage_bytes;
-            if (b >= 0 && b < a.num_blocks) {
-                flags[st] = 0;
-                const char *src = a.pool + (int64_t)iun.kvh * a.tile_bytes + (int64_t)b * a.blk_stride;
-                mbar_arrive_expect_tx(&full[st], 2u * a.tile_bytes);
-                bulk_g2s_hint(dst, src, a.tile_bytes, &full[st], policy);
-                bulk_g2s_hint(dst + a.tile_bytes, src + a.kv_stride, a.tile_bytes, &full[st], policy);
-            } else {
-                flags[st] = 1;
-                set_error(a.err, PKV_DEVERR_BLOCK_ID);
-                mbar_arrive(&full[st]);
-            }
+            const uint32_t first = tau > (uint32_t)NST ? tau - NST : 0;
+            for (uint32_t t = first; t < tau; ++t)
+                if (!mbar_wait(&full[t % NST], (t / NST) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
         }
-        ++it;
-        ++issued;
-    };
-    for (int k = 0; k < NST; ++k) issue_one();
+        return;
+    }
 
-    // ---- consume side
+    // -------------------------------------------------------------------- consumer warps
     const int sub = lane % LPT, grp = lane / LPT;
-    bool ok = true;
-    for (int u = gw; u < U && ok; u += TW) {
+    const int tid = threadIdx.x; // 0 .. NCW*32-1
+    uint32_t tau = 0;
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
         const Unit un = unit_info(u, pf, pp, nb, S, a.hkv, bps);
         const int L = a.lens[un.s];
         float qs = a.qk_scale_log2;
@@ -381,7 +321,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) decode_kernel(const Args a) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             const T *qp = static_cast<const T *>(a.q) + ((int64_t)un.s * a.hq + un.kvh * G + g) * D + sub * 8;
-            cvt8<MT>(*reinterpret_cast<const uint4 *>(qp), qf[g]);
+            const uint4 raw = *reinterpret_cast<const uint4 *>(qp);
+            cvt8<MT>(raw, qf[g]);
 #pragma unroll
             for (int e = 0; e < 8; ++e) qf[g][e] *= qs;
         }
@@ -393,23 +334,29 @@ __global__ void __launch_bounds__(kMaxWarps * 32) decode_kernel(const Args a) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
         }
-        for (int i = 0; i < un.ntiles; ++i) {
-            const uint32_t st = consumed % NST;
-            if (!mbar_wait(&full[st], (consumed / NST) & 1)) ok = false;
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
+        // Tile t of the CTA's stream (t counted over all its units) belongs to warp t % NCW and
+        // sits in stage t % NST with NST a multiple of NCW, so a warp's previous tile in any stage
+        // is its own: when it waits for phase k of a stage, phase k-1 has completed, which keeps
+        // the parity wait unambiguous.
+        int i0 = warp - static_cast<int>(tau % NCW);
+        if (i0 < 0) i0 += NCW;
+        for (int i = i0; i < un.ntiles; i += NCW) {
+            const uint32_t t = tau + i;
+            const uint32_t stage = t % NST;
+            if (!mbar_wait(&full[stage], (t / NST) & 1)) {
+                set_error(a.err, PKV_DEVERR_TIMEOUT);
+                *reinterpret_cast<volatile int *>(abort_flag) = 1;
             }
-            if (!flags[st]) {
-                const char *ks = ring + st * stage_bytes;
+            if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+            if (!flags[stage]) {
+                const char *ks = ring + (size_t)stage * 2 * a.tile_bytes;
                 const int valid = min(a.bs, L - (un.blk0 + i) * a.bs);
                 process_tile<D, G, KVT>(ks, ks + a.tile_bytes, a.bs, valid, qf, m, l, acc, lane);
             }
             __syncwarp();
-            ++consumed;
-            issue_one(); // refills the stage just consumed
+            if (lane == 0) mbar_arrive(&empty[stage]);
         }
-        if (!ok) break;
+        tau += un.ntiles;
         // combine the token groups of this warp
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -420,90 +367,146 @@ __global__ void __launch_bounds__(kMaxWarps * 32) decode_kernel(const Args a) {
                 for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
             }
         }
+        if (grp == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float *r = mrg + (warp * G + g) * (D + 2);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) r[sub * 8 + e] = acc[g][e];
+                if (sub == 0) {
+                    r[D] = m[g];
+                    r[D + 1] = l[g];
+                }
+            }
+        }
+        named_barrier_sync(1, NCW * 32);
+        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
         const float vs = (KVT == PKV_FP8_E4M3) ? a.v_scale[un.kvh] : 1.f;
-        if (un.nsplit == 1) {
-            if (grp == 0) {
+        for (int o = tid; o < G * D; o += NCW * 32) {
+            const int g = o / D, d = o - g * D;
+            float Mx = -INFINITY;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float r = l[g] > 0.f ? vs / l[g] : 0.f;
-                    uint32_t w[4];
+            for (int w = 0; w < NCW; ++w) {
+                const float *r = mrg + (w * G + g) * (D + 2);
+                if (r[D + 1] > 0.f) Mx = fmaxf(Mx, r[D]);
+            }
+            float num = 0.f, den = 0.f;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) w[e] = M::pack(acc[g][2 * e] * r, acc[g][2 * e + 1] * r);
-                    T *orow = static_cast<T *>(a.out) + ((int64_t)un.s * a.hq + un.kvh * G + g) * D + sub * 8;
-                    *reinterpret_cast<uint4 *>(orow) = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int w = 0; w < NCW; ++w) {
+                const float *r = mrg + (w * G + g) * (D + 2);
+                if (r[D + 1] > 0.f) {
+                    const float wt = fast_exp2(r[D] - Mx);
+                    num = fmaf(wt, r[d], num);
+                    den = fmaf(wt, r[D + 1], den);
                 }
             }
-        } else {
-            if (grp == 0) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const int64_t idx = ((int64_t)un.s * a.hq + un.kvh * G + g) * a.max_splits + un.j;
-                    float *dst = a.ws_o + idx * D + sub * 8;
-                    reinterpret_cast<float4 *>(dst)[0] =
-                        make_float4(acc[g][0] * vs, acc[g][1] * vs, acc[g][2] * vs, acc[g][3] * vs);
-                    reinterpret_cast<float4 *>(dst)[1] =
-                        make_float4(acc[g][4] * vs, acc[g][5] * vs, acc[g][6] * vs, acc[g][7] * vs);
-                    if (sub == 0) reinterpret_cast<float2 *>(a.ws_ml)[idx] = make_float2(m[g], l[g]);
-                }
-            }
-            __syncwarp();
-            int last = 0;
-            int *cnt = a.counters + (int64_t)un.s * a.hkv + un.kvh;
-            if (lane == 0) {
-                __threadfence();
-                last = (atomicAdd(cnt, 1) == un.nsplit - 1) ? 1 : 0;
-            }
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {
-                __threadfence();
-                merge_splits_warp<D, G, MT>(a, un.s, un.kvh, un.nsplit, lane);
-                if (lane == 0) *cnt = 0;
+            const int h = un.kvh * G + g;
+            if (un.nsplit == 1) {
+                const float y = den > 0.f ? (num / den) * vs : 0.f;
+                static_cast<T *>(a.out)[((int64_t)un.s * a.hq + h) * D + d] = M::from_f(y);
+            } else {
+                const int64_t idx = ((int64_t)un.s * a.hq + h) * a.max_splits + un.j;
+                a.ws_o[idx * D + d] = num * vs;
+                if (d == 0) reinterpret_cast<float2 *>(a.ws_ml)[idx] = make_float2(Mx, den);
             }
         }
-    }
-    if (!ok) {
-        // a wait gave up: record it, let this warp's copies in flight land (bounded), stop
-        if (lane == 0) {
-            set_error(a.err, PKV_DEVERR_TIMEOUT);
-            for (uint32_t t = consumed; t < issued; ++t) mbar_wait(&full[t % NST], (t / NST) & 1);
-        }
+        named_barrier_sync(1, NCW * 32);
     }
 }
 
-// Shared memory of one CTA of `nw` warps with `nst` stages each.
-inline size_t smem_bytes(int nw, int nst, int tile_bytes, int S) {
-    return (size_t)nw * nst * (2 * (size_t)tile_bytes + 8 + 4) + (size_t)(3 * S + 2) * 4;
+// Merge of the per-split partials of sequences with more than one split; zero rows for
+// L_s == 0.  One warp per (sequence, query head): lane j reads split j's (m, l) so the weights
+// exp2(m_j - M) are formed in parallel, then every split's partial o is read as float4/float2
+// vectors (lane = dims) and accumulated in split order.
+template <int D, int MT>
+__global__ void __launch_bounds__(128) merge_kernel(const Args a) {
+    using M = ModelT<MT>;
+    using T = typename M::T;
+    constexpr int PER = D / 32;
+    const int wid = blockIdx.x * 4 + threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (wid >= a.num_seqs * a.hq) return;
+    const int s = wid / a.hq;
+    const int L = a.lens[s];
+    int n = L > 0 ? (L + a.bs - 1) / a.bs : 0;
+    if (n > a.max_blocks) n = a.max_blocks;
+    const int nsplit = n / a.split_blocks + ((n % a.split_blocks) ? 1 : 0);
+    if (nsplit == 1) return;
+    T *o = static_cast<T *>(a.out) + (int64_t)wid * D + lane * PER;
+    if (nsplit == 0) {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) o[e] = M::from_f(0.f);
+        return;
+    }
+    const int64_t base = (int64_t)wid * a.max_splits;
+    const float2 *ml = reinterpret_cast<const float2 *>(a.ws_ml) + base;
+    float Mx = -INFINITY;
+    for (int j = lane; j < nsplit; j += 32) {
+        const float2 v = ml[j];
+        if (v.y > 0.f) Mx = fmaxf(Mx, v.x);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
+    float num[PER], den = 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) num[e] = 0.f;
+    for (int j0 = 0; j0 < nsplit; j0 += 32) {
+        float wj = 0.f, lj = 0.f;
+        if (j0 + lane < nsplit) {
+            const float2 v = ml[j0 + lane];
+            lj = v.y;
+            if (lj > 0.f) wj = fast_exp2(v.x - Mx);
+        }
+        const int cnt = min(32, nsplit - j0);
+#pragma unroll 4
+        for (int jj = 0; jj < cnt; ++jj) {
+            const float w = __shfl_sync(0xffffffffu, wj, jj);
+            den = fmaf(w, __shfl_sync(0xffffffffu, lj, jj), den);
+            const float *src = a.ws_o + (base + j0 + jj) * D + lane * PER;
+            if constexpr (PER == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(src);
+                num[0] = fmaf(w, v.x, num[0]);
+                num[1] = fmaf(w, v.y, num[1]);
+                num[2] = fmaf(w, v.z, num[2]);
+                num[3] = fmaf(w, v.w, num[3]);
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(src);
+                num[0] = fmaf(w, v.x, num[0]);
+                num[1] = fmaf(w, v.y, num[1]);
+            }
+        }
+    }
+    const float r = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) o[e] = M::from_f(num[e] * r);
+}
+
+inline size_t smem_bytes(int D, int G, int nst, int tile_bytes, int S) {
+    return (size_t)nst * 2 * tile_bytes + (size_t)nst * (8 + 8 + 4) + 16 + (size_t)kConsumerWarps * G * (D + 2) * 4 +
+           (size_t)(3 * S + 2) * 4;
 }
 
 template <int D, int G, int MT, int KVT>
-cudaError_t launch_t(const Args &a, int grid, int threads, size_t smem, cudaStream_t st) {
+cudaError_t launch_t(const Args &a, int grid, size_t smem, cudaStream_t st) {
     auto kern = decode_kernel<D, G, MT, KVT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, threads, smem, st>>>(a);
+    kern<<<grid, kThreads, smem, st>>>(a);
     return cudaGetLastError();
 }
 
-template <int D, int G, int MT, int KVT>
-int occupancy(int threads, size_t smem) {
-    int n = 0;
-    cudaFuncSetAttribute(decode_kernel<D, G, MT, KVT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, G, MT, KVT>, threads, smem);
-    return n;
+template <int D, int MT>
+cudaError_t launch_merge_t(const Args &a, cudaStream_t st) {
+    const int rows = a.num_seqs * a.hq;
+    if (rows == 0) return cudaSuccess;
+    merge_kernel<D, MT><<<(rows + 3) / 4, 128, 0, st>>>(a);
+    return cudaGetLastError();
 }
 
-// Dispatch over head_dim and group size for one (model dtype, KV dtype) pair: occupancy query
-// when grid == 0, launch otherwise.
+// Dispatch over head_dim and group size for one (model dtype, KV dtype) pair.
 template <int MT, int KVT>
-cudaError_t dispatch(const Args &a, int D, int G, int grid, int threads, size_t smem, cudaStream_t st, int *occ) {
+cudaError_t dispatch(const Args &a, int D, int G, int grid, size_t smem, cudaStream_t st, bool merge) {
 #define PKV_CASE(DD, GG)                                                                                               \
-    if (D == DD && G == GG) {                                                                                          \
-        if (occ) {                                                                                                     \
-            *occ = occupancy<DD, GG, MT, KVT>(threads, smem);                                                          \
-            return cudaSuccess;                                                                                        \
-        }                                                                                                              \
-        return launch_t<DD, GG, MT, KVT>(a, grid, threads, smem, st);                                                  \
-    }
+    if (D == DD && G == GG) return merge ? launch_merge_t<DD, MT>(a, st) : launch_t<DD, GG, MT, KVT>(a, grid, smem, st);
     PKV_CASE(64, 1)
     PKV_CASE(64, 2)
     PKV_CASE(64, 4)
@@ -516,12 +519,40 @@ cudaError_t dispatch(const Args &a, int D, int G, int grid, int threads, size_t 
     return cudaErrorInvalidValue;
 }
 
+template <int D, int G, int MT, int KVT>
+int occupancy(size_t smem) {
+    int n = 0;
+    cudaFuncSetAttribute(decode_kernel<D, G, MT, KVT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, G, MT, KVT>, kThreads, smem);
+    return n;
+}
+
+template <int MT, int KVT>
+int occupancy_dispatch(int D, int G, size_t smem) {
+#define PKV_CASE(DD, GG)                                                                                               \
+    if (D == DD && G == GG) return occupancy<DD, GG, MT, KVT>(smem);
+    PKV_CASE(64, 1)
+    PKV_CASE(64, 2)
+    PKV_CASE(64, 4)
+    PKV_CASE(64, 8)
+    PKV_CASE(128, 1)
+    PKV_CASE(128, 2)
+    PKV_CASE(128, 4)
+    PKV_CASE(128, 8)
+#undef PKV_CASE
+    return 0;
+}
+
 } // namespace pkv_decode
 
 // Per (model dtype, KV dtype) entry points, each compiled in its own translation unit.
-using PkvDecodeFn = cudaError_t (*)(const pkv_decode::Args &, int D, int G, int grid, int threads, size_t smem,
-                                    cudaStream_t, int *occ);
-cudaError_t pkv_decode_f16(const pkv_decode::Args &, int, int, int, int, size_t, cudaStream_t, int *);
-cudaError_t pkv_decode_bf16(const pkv_decode::Args &, int, int, int, int, size_t, cudaStream_t, int *);
-cudaError_t pkv_decode_fp8_f16(const pkv_decode::Args &, int, int, int, int, size_t, cudaStream_t, int *);
-cudaError_t pkv_decode_fp8_bf16(const pkv_decode::Args &, int, int, int, int, size_t, cudaStream_t, int *);
+cudaError_t pkv_decode_f16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t, bool merge);
+cudaError_t pkv_decode_bf16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t, bool merge);
+cudaError_t pkv_decode_fp8_f16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t,
+                               bool merge);
+cudaError_t pkv_decode_fp8_bf16(const pkv_decode::Args &, int D, int G, int grid, size_t smem, cudaStream_t,
+                                bool merge);
+int pkv_decode_occupancy_f16(int D, int G, size_t smem);
+int pkv_decode_occupancy_bf16(int D, int G, size_t smem);
+int pkv_decode_occupancy_fp8_f16(int D, int G, size_t smem);
+int pkv_decode_occupancy_fp8_bf16(int D, int G, size_t smem);
