@@ -116,6 +116,15 @@ int paged_slot_mapping(const int32_t *block_tables, int num_rows, int max_blocks
 int paged_kv_append(pkv_cache_t cache, const void *k, const void *v, const int64_t *slot_mapping,
                     int64_t num_tokens, void *stream);
 
+/* Slot indexing and paged KV append in one launch: for each token j, slot_j is computed as in
+ * paged_slot_mapping from (block_tables, seq_ids[j], positions[j]) and k[j], v[j] are written as in
+ * paged_kv_append.  slot_mapping, when not NULL, receives the int64 slots (the same values
+ * paged_slot_mapping returns).  This is the decode step's "write the new token at its block
+ * offset" (discosf.com section 4.3 steps 1-2) without a separate indexing launch. */
+int paged_kv_append_at(pkv_cache_t cache, const void *k, const void *v, const int32_t *block_tables, int num_rows,
+                       int max_blocks_per_seq, const int32_t *seq_ids, const int32_t *positions, int64_t num_tokens,
+                       int64_t *slot_mapping, void *stream);
+
 /* Paged decode attention (2kiu.com section 2.3: walk the block table, mask the tail
  * block by the true length; section 3.3: prefix blocks are read per sequence):
  *   out[s][h] = sum_{t < L_s} softmax_t(scale * q[s][h] . K_t) V_t,  L_s = context_lens[s],

@@ -52,6 +52,7 @@ def lib() -> ctypes.CDLL:
         L.pkv_last_error.restype = ctypes.c_char_p
         L.paged_slot_mapping.argtypes = [vp, i32, i32, vp, vp, i64, i32, vp, vp]
         L.paged_kv_append.argtypes = [vp, vp, vp, vp, i64, vp]
+        L.paged_kv_append_at.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, i64, vp, vp]
         L.paged_decode_attention.argtypes = [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]
         L.packed_prefill_attention.argtypes = [vp, vp, vp, vp, i32, i32, i64, vp, i32, vp, i32, ctypes.c_float, vp,
                                                vp]
@@ -208,6 +209,30 @@ def paged_kv_append(cache: KVCache, k: torch.Tensor, v: torch.Tensor, slot_mappi
     if slot_mapping.numel() != n:
         raise ValueError("slot_mapping length != number of tokens")
     _check(lib().paged_kv_append(cache.handle, _ptr(k), _ptr(v), _ptr(slot_mapping), n, _stream()))
+
+
+def paged_kv_append_at(cache: KVCache, k: torch.Tensor, v: torch.Tensor, block_tables: torch.Tensor,
+                       seq_ids: torch.Tensor, positions: torch.Tensor,
+                       slot_mapping: Optional[torch.Tensor] = None) -> Optional[torch.Tensor]:
+    """Slot indexing + append in one launch; fills ``slot_mapping`` (int64) when given."""
+    _req(k, "k", cache.torch_dtype, 3)
+    _req(v, "v", cache.torch_dtype, 3)
+    _req(block_tables, "block_tables", torch.int32, 2)
+    _req(seq_ids, "seq_ids", torch.int32, 1)
+    _req(positions, "positions", torch.int32, 1)
+    n = k.shape[0]
+    if tuple(k.shape) != (n, cache.num_kv_heads, cache.head_dim) or k.shape != v.shape:
+        raise ValueError(f"k/v must be [T, {cache.num_kv_heads}, {cache.head_dim}]")
+    if seq_ids.numel() != n or positions.numel() != n:
+        raise ValueError("seq_ids/positions length != number of tokens")
+    if slot_mapping is not None:
+        _req(slot_mapping, "slot_mapping", torch.int64, 1)
+        if slot_mapping.numel() != n:
+            raise ValueError("slot_mapping length != number of tokens")
+    _check(lib().paged_kv_append_at(cache.handle, _ptr(k), _ptr(v), _ptr(block_tables), block_tables.shape[0],
+                                    block_tables.shape[1], _ptr(seq_ids), _ptr(positions), n, _ptr(slot_mapping),
+                                    _stream()))
+    return slot_mapping
 
 
 def paged_decode_attention(q: torch.Tensor, cache: KVCache, block_tables: torch.Tensor,

@@ -236,6 +236,22 @@ int paged_kv_append(pkv_cache_t c, const void *k, const void *v, const int64_t *
     return PKV_OK;
 }
 
+int paged_kv_append_at(pkv_cache_t c, const void *k, const void *v, const int32_t *block_tables, int num_rows,
+                       int max_blocks_per_seq, const int32_t *seq_ids, const int32_t *positions, int64_t num_tokens,
+                       int64_t *slot_mapping, void *stream) {
+    if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
+    if (num_tokens < 0 || num_rows < 0 || max_blocks_per_seq < 0) return pkv_fail(PKV_EINVAL, "negative size");
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !seq_ids || !positions || (!block_tables && num_rows > 0 && max_blocks_per_seq > 0))
+        return pkv_fail(PKV_EINVAL, "NULL pointer");
+    if (!aligned16(k) || !aligned16(v)) return pkv_fail(PKV_EINVAL, "k and v must be 16-byte aligned");
+    if (int r = check_device(c)) return r;
+    cudaError_t e = launch_append_at(c, k, v, block_tables, num_rows, max_blocks_per_seq, seq_ids, positions,
+                                     num_tokens, slot_mapping, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return pkv_cuda_fail(e, "append launch");
+    return PKV_OK;
+}
+
 int paged_decode_attention(const void *q, pkv_cache_t c, const int32_t *block_tables, int max_blocks_per_seq,
                            const int32_t *context_lens, int num_seqs, int num_q_heads, float scale, void *out,
                            void *stream) {

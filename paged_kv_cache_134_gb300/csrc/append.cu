@@ -7,32 +7,39 @@
 //
 // Both are HBM-bound scatter/gather work: 16-byte vector loads and stores, one thread per
 // 16-byte source chunk, consecutive threads on consecutive chunks of a (token, K|V, head)
-// row so that every warp moves whole contiguous 256-byte rows.
+// row so that every warp moves whole contiguous 256-byte rows.  The fused variant computes
+// each token's slot in the same kernel (and still returns the slots), which saves a launch
+// per decode step.  All kernels are launched with programmatic dependent launch: they let the
+// next kernel in the stream start its launch early and wait for their own predecessor before
+// touching global memory.
 #include "device_common.cuh"
 #include "pkv_internal.h"
 
 namespace {
 
+PKV_DEV int64_t slot_of(const int32_t *__restrict__ tables, int rows, int max_blocks, int s, int p, int bs) {
+    if (s < 0 || s >= rows || p < 0) return -1;
+    const int lb = p / bs;
+    if (lb >= max_blocks) return -1;
+    const int b = tables[(int64_t)s * max_blocks + lb];
+    return b < 0 ? -1 : (int64_t)b * bs + p % bs;
+}
+
 __global__ void slot_mapping_kernel(const int32_t *__restrict__ tables, int rows, int max_blocks,
                                     const int32_t *__restrict__ seq_ids, const int32_t *__restrict__ positions,
                                     int64_t n, int bs, int64_t *__restrict__ out) {
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const int s = seq_ids[i], p = positions[i];
-        int64_t slot = -1;
-        if (s >= 0 && s < rows && p >= 0) {
-            const int lb = p / bs;
-            if (lb < max_blocks) {
-                const int b = tables[(int64_t)s * max_blocks + lb];
-                if (b >= 0) slot = (int64_t)b * bs + p % bs;
-            }
-        }
-        out[i] = slot;
-    }
+    pdl_trigger();
+    pdl_wait();
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = slot_of(tables, rows, max_blocks, seq_ids[i], positions[i], bs);
 }
 
 struct AppendArgs {
     const uint4 *k, *v;   // [n][Hkv][D] model dtype, viewed as 16-byte chunks
-    const int64_t *slots;
+    const int64_t *slots; // given slots (plain append) ...
+    const int32_t *tables, *seq_ids, *positions; // ... or computed here (fused append)
+    int64_t *slots_out;
+    int rows, max_blocks;
     char *pool;
     const float *k_scale, *v_scale;
     unsigned int *err;
@@ -42,9 +49,12 @@ struct AppendArgs {
     int d;
 };
 
-// KVT: 0 = 16-bit cache (bit copy), 2 = E4M3 cache; MT = model dtype for the E4M3 path
-template <int KVT, int MT>
+// KVT: 0 = 16-bit cache (bit copy), 2 = E4M3 cache; MT = model dtype for the E4M3 path;
+// FUSED: compute the slot from (table, sequence, position) instead of reading it
+template <int KVT, int MT, bool FUSED>
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t per_token = 2LL * a.hkv * a.chunks_per_row;
     const int64_t total = a.n * per_token;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -54,7 +64,13 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
         const int hc = rem - kv * a.hkv * a.chunks_per_row;
         const int h = hc / a.chunks_per_row;
         const int c = hc - h * a.chunks_per_row;
-        const int64_t slot = a.slots[j];
+        int64_t slot;
+        if constexpr (FUSED) {
+            slot = slot_of(a.tables, a.rows, a.max_blocks, a.seq_ids[j], a.positions[j], a.bs);
+            if (rem == 0 && a.slots_out) a.slots_out[j] = slot;
+        } else {
+            slot = a.slots[j];
+        }
         if (slot < 0) continue;
         if (slot >= a.num_slots) {
             if (rem == 0) set_error(a.err, PKV_DEVERR_SLOT);
@@ -87,27 +103,10 @@ inline int grid_for(int64_t work, int threads, int num_sms) {
     return static_cast<int>(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));
 }
 
-} // namespace
-
-cudaError_t launch_slot_mapping(const int32_t *tables, int rows, int max_blocks, const int32_t *seq_ids,
-                                const int32_t *positions, int64_t n, int bs, int64_t *out, cudaStream_t st) {
-    if (n == 0) return cudaSuccess;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    slot_mapping_kernel<<<grid_for(n, 256, sms), 256, 0, st>>>(tables, rows, max_blocks, seq_ids, positions, n, bs,
-                                                               out);
-    g_pkv_launches++;
-    return cudaGetLastError();
-}
-
-cudaError_t launch_append(pkv_cache *c, const void *k, const void *v, const int64_t *slots, int64_t n,
-                          cudaStream_t st) {
-    if (n == 0) return cudaSuccess;
-    AppendArgs a;
+AppendArgs base_args(pkv_cache *c, const void *k, const void *v, int64_t n) {
+    AppendArgs a{};
     a.k = static_cast<const uint4 *>(k);
     a.v = static_cast<const uint4 *>(v);
-    a.slots = slots;
     a.pool = static_cast<char *>(c->pool);
     a.k_scale = c->k_scale;
     a.v_scale = c->v_scale;
@@ -119,15 +118,57 @@ cudaError_t launch_append(pkv_cache *c, const void *k, const void *v, const int6
     a.chunks_per_row = c->head_dim / 8;
     a.tile_elems = (int64_t)c->block_size * c->head_dim;
     a.d = c->head_dim;
-    const int64_t work = n * 2 * a.hkv * a.chunks_per_row;
-    const int grid = grid_for(work, 256, c->num_sms);
+    return a;
+}
+
+template <bool FUSED>
+cudaError_t launch_append_t(pkv_cache *c, const AppendArgs &a, cudaStream_t st) {
+    const int64_t work = a.n * 2 * a.hkv * a.chunks_per_row;
+    const dim3 grid(grid_for(work, 256, c->num_sms));
     PkvTimer timer(c, PKV_KIND_APPEND, st);
+    cudaError_t e;
     if (c->kv_dtype != PKV_FP8_E4M3)
-        append_kernel<PKV_F16, PKV_F16><<<grid, 256, 0, st>>>(a);
+        e = pdl_launch(append_kernel<PKV_F16, PKV_F16, FUSED>, grid, dim3(256), 0, st, a);
     else if (c->model_dtype == PKV_F16)
-        append_kernel<PKV_FP8_E4M3, PKV_F16><<<grid, 256, 0, st>>>(a);
+        e = pdl_launch(append_kernel<PKV_FP8_E4M3, PKV_F16, FUSED>, grid, dim3(256), 0, st, a);
     else
-        append_kernel<PKV_FP8_E4M3, PKV_BF16><<<grid, 256, 0, st>>>(a);
+        e = pdl_launch(append_kernel<PKV_FP8_E4M3, PKV_BF16, FUSED>, grid, dim3(256), 0, st, a);
     g_pkv_launches++;
-    return cudaGetLastError();
+    return e;
+}
+
+} // namespace
+
+cudaError_t launch_slot_mapping(const int32_t *tables, int rows, int max_blocks, const int32_t *seq_ids,
+                                const int32_t *positions, int64_t n, int bs, int64_t *out, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const cudaError_t e = pdl_launch(slot_mapping_kernel, dim3(grid_for(n, 256, sms)), dim3(256), 0, st, tables, rows,
+                                     max_blocks, seq_ids, positions, n, bs, out);
+    g_pkv_launches++;
+    return e;
+}
+
+cudaError_t launch_append(pkv_cache *c, const void *k, const void *v, const int64_t *slots, int64_t n,
+                          cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    AppendArgs a = base_args(c, k, v, n);
+    a.slots = slots;
+    return launch_append_t<false>(c, a, st);
+}
+
+cudaError_t launch_append_at(pkv_cache *c, const void *k, const void *v, const int32_t *tables, int rows,
+                             int max_blocks, const int32_t *seq_ids, const int32_t *positions, int64_t n,
+                             int64_t *slots_out, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    AppendArgs a = base_args(c, k, v, n);
+    a.tables = tables;
+    a.rows = rows;
+    a.max_blocks = max_blocks;
+    a.seq_ids = seq_ids;
+    a.positions = positions;
+    a.slots_out = slots_out;
+    return launch_append_t<true>(c, a, st);
 }

@@ -13,7 +13,7 @@ int env_int(const char *name, int dflt) {
 }
 
 // target resident CTAs per SM (shared-memory budget per CTA follows from it)
-int ctas_per_sm() { return env_int("PAGEDKV_DECODE_CTAS", 3); }
+int ctas_per_sm() { return env_int("PAGEDKV_DECODE_CTAS", 4); }
 
 using DecodeFn = cudaError_t (*)(const pkv_decode::Args &, int, int, int, size_t, cudaStream_t, bool);
 using OccFn = int (*)(int, int, size_t);
@@ -85,6 +85,7 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
     const int want = ctas_per_sm();
     const size_t budget = (size_t)(233472 / want) - 1024;
     int nst = budget > fixed ? static_cast<int>((budget - fixed) / per_stage) : 0;
+    nst = env_int("PAGEDKV_DECODE_STAGES", nst);
     // a whole number of stages per consumer warp (see the tile-to-warp rule in the kernel)
     nst -= nst % kConsumerWarps;
     if (nst > 32) nst = 32;

@@ -218,6 +218,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
         *abort_flag = 0;
         fence_mbarrier_init();
     }
+    pdl_trigger();
+    pdl_wait(); // the previous kernel (e.g. the append of this step) has finished
     // unit list: per sequence, full splits and (0 or 1) partial split
     const int bps = a.split_blocks;
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
@@ -423,6 +425,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const Args a) {
     using M = ModelT<MT>;
     using T = typename M::T;
     constexpr int PER = D / 32;
+    pdl_trigger();
+    pdl_wait();
     const int wid = blockIdx.x * 4 + threadIdx.x / 32, lane = threadIdx.x % 32;
     if (wid >= a.num_seqs * a.hq) return;
     const int s = wid / a.hq;
@@ -490,16 +494,14 @@ cudaError_t launch_t(const Args &a, int grid, size_t smem, cudaStream_t st) {
     auto kern = decode_kernel<D, G, MT, KVT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return pdl_launch(kern, dim3(grid), dim3(kThreads), smem, st, a);
 }
 
 template <int D, int MT>
 cudaError_t launch_merge_t(const Args &a, cudaStream_t st) {
     const int rows = a.num_seqs * a.hq;
     if (rows == 0) return cudaSuccess;
-    merge_kernel<D, MT><<<(rows + 3) / 4, 128, 0, st>>>(a);
-    return cudaGetLastError();
+    return pdl_launch(merge_kernel<D, MT>, dim3((rows + 3) / 4), dim3(128), 0, st, a);
 }
 
 // Dispatch over head_dim and group size for one (model dtype, KV dtype) pair.

@@ -24,6 +24,12 @@ PKV_DEV uint64_t global_timer_ns() {
     return t;
 }
 
+// Programmatic dependent launch: let the next kernel of the stream begin launching, and wait
+// until the previous kernel has completed and its memory is visible (no-ops when the kernel was
+// launched without the programmatic-serialization attribute).
+PKV_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+PKV_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 PKV_DEV void set_error(unsigned int *err, unsigned int bits) {
     if (err) atomicOr(err, bits);
 }

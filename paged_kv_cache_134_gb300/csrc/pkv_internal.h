@@ -55,11 +55,31 @@ struct PkvTimer {
     ~PkvTimer();
 };
 
+// Launch with the programmatic-stream-serialization attribute (the kernel itself calls
+// pdl_wait() before it touches memory a previous kernel may use).
+template <typename... KArgs, typename... Args>
+cudaError_t pdl_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // launchers (one per translation unit); return cudaError_t of the launch
 cudaError_t launch_slot_mapping(const int32_t *tables, int rows, int max_blocks, const int32_t *seq_ids,
                                 const int32_t *positions, int64_t n, int bs, int64_t *out, cudaStream_t st);
 cudaError_t launch_append(pkv_cache *c, const void *k, const void *v, const int64_t *slots, int64_t n,
                           cudaStream_t st);
+cudaError_t launch_append_at(pkv_cache *c, const void *k, const void *v, const int32_t *tables, int rows,
+                             int max_blocks, const int32_t *seq_ids, const int32_t *positions, int64_t n,
+                             int64_t *slots_out, cudaStream_t st);
 
 struct DecodeLaunch {
     const void *q;

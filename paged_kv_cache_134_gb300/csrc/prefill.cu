@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
     using L = Layout<D, MT>;
     extern __shared__ __align__(1024) uint8_t smem[];
 
+    pdl_trigger();
+    pdl_wait();
     // ---- work item, heaviest query tiles first
     const int per_qt = a.num_seqs * a.hq;
     const int rank = blockIdx.x / per_qt;
@@ -401,8 +403,7 @@ cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
     const int smem = Layout<D, MT>::TOTAL;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
-    return cudaGetLastError();
+    return pdl_launch(kern, dim3(grid), dim3(kThreads), smem, st, tq, tk, tv, a);
 }
 
 } // namespace pkv_prefill

@@ -154,3 +154,13 @@ def test_slot_mapping_matches_oracle_including_invalid():
         pos = rng.integers(-5, 50 * bs + 20, size=10000).astype(np.int32)
         got = P.paged_slot_mapping(dev(tables), dev(seq), dev(pos), bs).cpu().numpy()
         assert np.array_equal(got, oracle.slot_mapping(tables, seq, pos, bs))
+
+
+def test_fused_append_matches_slot_mapping_plus_append():
+    w = W.small_decode("fuse", [0, 15, 16, 33, 500], hq=8, hkv=2, d=128, bs=16, seed=47)
+    a = run_decode(w, fused=True)
+    b = run_decode(w, fused=False)
+    assert a["err"] == 0 and b["err"] == 0
+    assert np.array_equal(a["new_slots"], b["new_slots"])
+    assert np.array_equal(a["pool"], b["pool"])
+    assert np.array_equal(a["out"], b["out"])
