@@ -140,6 +140,25 @@ int paged_decode_attention(const void *q, pkv_cache_t cache, const int32_t *bloc
                            const int32_t *context_lens, int num_seqs, int num_q_heads, float scale, void *out,
                            void *stream);
 
+/* paged_decode_attention without any device-memory allocation.  The pages have no counterpart:
+ * this entry point exists for callers that cannot let a library allocate, e.g. a serving engine
+ * that hands nearly all device memory to its own allocator (its KV pool is sized to fill the GPU)
+ * or that cannot afford the device-wide synchronisation cudaMalloc/cudaFree may cause.
+ * Same arguments, results and errors as paged_decode_attention, but the split-K partials live in
+ * one fixed 16 MiB array compiled into the library (every GPU that loads the library holds it until
+ * the process exits) instead of the cache's workspace; nothing is allocated, by CUDA or otherwise.
+ * A call whose partials do not fit (S x Hq x ceil(max_blocks_per_seq / split blocks) x (D + 2)
+ * floats > 16 MiB; with the default 256-token splits, e.g., 32 sequences x 32 heads x 4096-token
+ * tables need 9 MB) returns PKV_EINVAL with the sizes in pkv_last_error().
+ * The first call on a device looks up the array's device address on that device (one
+ * cudaGetSymbolAddress, made with that device current); make that first call before any stream
+ * capture.  Every call shares the array: calls whose work can overlap on the GPU (different
+ * streams, or different host threads) race on it and must be serialised by the caller.  Nothing
+ * in the array has to start at zero; each call writes every partial before it reads it. */
+int paged_decode_attention_noalloc(const void *q, pkv_cache_t cache, const int32_t *block_tables,
+                                   int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                   int num_q_heads, float scale, void *out, void *stream);
+
 /* Packed causal prefill (discosf.com sections 3.1-3.3 and 4.2): sequences packed back to
  * back, sequence i owning rows [cu_seqlens[i], cu_seqlens[i+1]):
  *   out[cu_i + r][h] = sum_{c <= r} softmax_c(scale * q[cu_i + r][h] . k[cu_i + c][g]) v[cu_i + c][g]

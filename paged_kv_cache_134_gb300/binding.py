@@ -54,6 +54,7 @@ def lib() -> ctypes.CDLL:
         L.paged_kv_append.argtypes = [vp, vp, vp, vp, i64, vp]
         L.paged_kv_append_at.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, i64, vp, vp]
         L.paged_decode_attention.argtypes = [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]
+        L.paged_decode_attention_noalloc.argtypes = [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]
         L.packed_prefill_attention.argtypes = [vp, vp, vp, vp, i32, i32, i64, vp, i32, vp, i32, ctypes.c_float, vp,
                                                vp]
         L.kv_cache_profile_start.argtypes = [vp]
@@ -249,6 +250,26 @@ def paged_decode_attention(q: torch.Tensor, cache: KVCache, block_tables: torch.
     _req(out, "out", cache.torch_dtype, 3)
     _check(lib().paged_decode_attention(_ptr(q), cache.handle, _ptr(block_tables), block_tables.shape[1],
                                         _ptr(context_lens), S, hq, ctypes.c_float(scale), _ptr(out), _stream()))
+    return out
+
+
+def paged_decode_attention_noalloc(q: torch.Tensor, cache: KVCache, block_tables: torch.Tensor,
+                                   context_lens: torch.Tensor, scale: float, out: torch.Tensor) -> torch.Tensor:
+    """paged_decode_attention for callers that must not allocate device memory.
+
+    The library keeps the split-K partials in a fixed 16 MiB array of its own instead of the
+    cache's growable workspace, so this call allocates nothing (the caller provides ``out``).
+    Calls that can overlap on the GPU share that array and must be serialised by the caller."""
+    _req(q, "q", cache.torch_dtype, 3)
+    _req(block_tables, "block_tables", torch.int32, 2)
+    _req(context_lens, "context_lens", torch.int32, 1)
+    _req(out, "out", cache.torch_dtype, 3)
+    S, hq, d = q.shape
+    if d != cache.head_dim or block_tables.shape[0] != S or context_lens.numel() != S or out.shape != q.shape:
+        raise ValueError("shape mismatch between q, out, block_tables and context_lens")
+    _check(lib().paged_decode_attention_noalloc(_ptr(q), cache.handle, _ptr(block_tables), block_tables.shape[1],
+                                                _ptr(context_lens), S, hq, ctypes.c_float(scale), _ptr(out),
+                                                _stream()))
     return out
 
 
