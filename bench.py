@@ -116,6 +116,17 @@ def _reduce_sum(x: float, ws: int) -> float:
     return float(t.item())
 
 
+def aggregate(local_bytes: float, local_seqs: float, local_elapsed_s: float, ws: int):
+    """Weak-scaling totals: (GB/s over all ranks, seqs/s over all ranks, slowest rank's seconds).
+
+    Every rank runs its own batch; the job's throughput is all ranks' work over the slowest rank's
+    time (the only cross-rank traffic is these three reductions, none on the data path)."""
+    elapsed = _reduce_max(local_elapsed_s, ws)
+    total_bytes = _reduce_sum(local_bytes, ws)
+    total_seqs = _reduce_sum(local_seqs, ws)
+    return total_bytes / elapsed / 1e9, total_seqs / elapsed, elapsed
+
+
 def _barrier(ws: int):
     if ws > 1:
         import torch.distributed as dist
@@ -262,10 +273,10 @@ def secondary_append(P, W, gpu_path, peaks, reps=20):
 
 def run_ours(args):
     ws, rank, local = _dist()
+    torch.cuda.set_device(local)
     if ws > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     import paged_kv_cache_134_gb300 as P
     from paged_kv_cache_134_gb300 import workloads as W
     from paged_kv_cache_134_gb300 import runner as G
@@ -302,11 +313,13 @@ def run_ours(args):
     assert cache.check_error() == 0
 
     kv_bytes = w.kv_read_bytes()
-    elapsed_max = _reduce_max(elapsed, ws)
-    total_bytes = _reduce_sum(float(kv_bytes) * args.steps, ws)
-    total_seqs = _reduce_sum(float(w.num_seqs) * args.steps, ws)
-    value = total_bytes / elapsed_max / 1e9
+    value, seqs_per_s, elapsed_max = aggregate(float(kv_bytes) * args.steps, float(w.num_seqs) * args.steps, elapsed,
+                                               ws)
     dec_kernel_s = prof["decode_ms"] / max(1, prof["decode_launches"]) / 1e3
+    breakdown = {"append_at_us": round(prof["append_ms"] / max(1, prof["append_launches"]) * 1e3, 2),
+                 "decode_kernel_us": round(dec_kernel_s * 1e6, 2),
+                 "merge_kernel_us": round(prof["merge_ms"] / max(1, prof["merge_launches"]) * 1e3, 2),
+                 "step_us": round(elapsed / args.steps * 1e6, 2)}
     achieved = kv_bytes / dec_kernel_s / 1e9
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
@@ -358,8 +371,8 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (KV read per step 1.07 GB vs 129 MB L2)",
                        "split_tokens": int(os.environ.get("PAGEDKV_SPLIT_TOKENS", "256")),
                        "parallelism": f"replicas x{ws} (one independent batch per GPU)"},
-            "seqs_per_s": round(total_seqs / elapsed_max, 1),
-            "seqs_per_s_32_layers": round(total_seqs / elapsed_max / 32, 1),
+            "seqs_per_s": round(seqs_per_s, 1),
+            "seqs_per_s_32_layers": round(seqs_per_s / 32, 1),
             "hbm_frac": round(value / peaks[0], 4),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks[0], "unit": "GB/s",
                          "frac": round(achieved / peaks[0], 4), "traffic": None,
@@ -367,6 +380,7 @@ def run_ours(args):
                          "kernel_ms": round(dec_kernel_s * 1e3, 5),
                          "peak_source": f"{peaks[3]} hbm_gbs (MEASURED_PEAKS.json)",
                          "algorithmic_bytes": "KV read: sum(L+1) x Hkv x D x 2 B x 2 (K and V) per launch"},
+            "step_breakdown": breakdown,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
             "gpu_launches": int(launches),

@@ -176,14 +176,14 @@ int packed_prefill_attention(const void *q, const void *k, const void *v, const 
                              void *stream);
 
 /* Profiling.  Between kv_cache_profile_start and kv_cache_profile_read the library records
- * CUDA events around each main kernel it launches for this cache (decode split-K kernel,
- * prefill kernel, append kernel) on the launch stream.  kv_cache_profile_read synchronises
+ * CUDA events around each kernel it launches for this cache (decode split-K kernel, split
+ * merge kernel, prefill kernel, append kernel) on the launch stream.  kv_cache_profile_read synchronises
  * those events and returns the summed device time per kind (milliseconds) and launch
  * counts, then stops recording.  pkv_kernel_launches counts every kernel this library
  * launched in the process (all caches and free functions). */
 typedef struct {
-    int64_t decode_launches, prefill_launches, append_launches;
-    double decode_ms, prefill_ms, append_ms;
+    int64_t decode_launches, prefill_launches, append_launches, merge_launches;
+    double decode_ms, prefill_ms, append_ms, merge_ms;
 } pkv_profile_t;
 int kv_cache_profile_start(pkv_cache_t cache);
 int kv_cache_profile_read(pkv_cache_t cache, pkv_profile_t *out);

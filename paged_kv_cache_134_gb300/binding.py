@@ -66,8 +66,9 @@ def lib() -> ctypes.CDLL:
 
 class _Profile(ctypes.Structure):
     _fields_ = [("decode_launches", ctypes.c_int64), ("prefill_launches", ctypes.c_int64),
-                ("append_launches", ctypes.c_int64), ("decode_ms", ctypes.c_double),
-                ("prefill_ms", ctypes.c_double), ("append_ms", ctypes.c_double)]
+                ("append_launches", ctypes.c_int64), ("merge_launches", ctypes.c_int64),
+                ("decode_ms", ctypes.c_double), ("prefill_ms", ctypes.c_double), ("append_ms", ctypes.c_double),
+                ("merge_ms", ctypes.c_double)]
 
 
 def _check(status: int):

@@ -357,9 +357,12 @@ int kv_cache_profile_read(pkv_cache_t c, pkv_profile_t *out) {
         } else if (ev.kind == PKV_KIND_PREFILL) {
             out->prefill_launches++;
             out->prefill_ms += ms;
-        } else {
+        } else if (ev.kind == PKV_KIND_APPEND) {
             out->append_launches++;
             out->append_ms += ms;
+        } else {
+            out->merge_launches++;
+            out->merge_ms += ms;
         }
         c->event_pool.push_back(ev.a);
         c->event_pool.push_back(ev.b);

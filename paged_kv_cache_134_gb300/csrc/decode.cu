@@ -102,7 +102,10 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
         g_pkv_launches++;
     }
     if (e != cudaSuccess) return e;
-    e = fn(a, c->head_dim, G, 0, 0, st, true);
-    g_pkv_launches++;
+    {
+        PkvTimer timer(c, PKV_KIND_MERGE, st);
+        e = fn(a, c->head_dim, G, 0, 0, st, true);
+        g_pkv_launches++;
+    }
     return e;
 }

@@ -38,7 +38,7 @@ struct pkv_cache {
     std::mutex mu;
 };
 
-enum { PKV_KIND_DECODE = 0, PKV_KIND_PREFILL = 1, PKV_KIND_APPEND = 2 };
+enum { PKV_KIND_DECODE = 0, PKV_KIND_PREFILL = 1, PKV_KIND_APPEND = 2, PKV_KIND_MERGE = 3 };
 
 // status helpers (api.cu)
 int pkv_fail(int status, const char *fmt, ...);

@@ -16,8 +16,9 @@
 //              to shared memory in the 128-byte-swizzled K-major layout the MMA reads (fp16 P for
 //              fp16 models; for bf16 models P = hi + lo, two bf16 tiles and two accumulating MMAs); O in TMEM is rescaled only when a row's running max grows by
 //              more than 2^8 (the exponent base stays fixed otherwise, which is exact algebra);
-//   warps 6-7  paged K/V writer for the tile's rows (only the CTA of the first query head of each
-//              KV group writes, so every (token, KV head) is written once).
+//   warps 6-7  paged K/V writer for the tile's rows, straight from the K/V tiles already in shared
+//              memory (only the CTA of the first query head of each KV group writes, so every
+//              (token, KV head) is written once).
 // The diagonal tiles are masked per element; tiles entirely above the diagonal are never issued.
 // Every mbarrier wait is bounded; a timeout sets PKV_DEVERR_TIMEOUT and the CTA winds down.
 #include <mutex>
@@ -334,24 +335,42 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
         }
     } else if (h % G == 0) {
         // ------------------------------------------------------------ paged K/V write of this tile's rows
-        constexpr int CPR = D / 8; // 16-byte chunks per row
-        const int t = threadIdx.x - 192;
-        const int nrows = qlast - q0 + 1;
-        for (int idx = t; idx < nrows * CPR; idx += 64) {
-            const int rr = idx / CPR, c = idx - rr * CPR;
-            const int p = q0 + rr;
-            const int lb = p / a.bs;
-            const int blk = lb < a.max_blocks ? a.tables[(int64_t)seq * a.max_blocks + lb] : -1;
-            if (blk < 0 || blk >= a.num_blocks) {
-                if (c == 0) set_error(a.err, PKV_DEVERR_BLOCK_ID);
-                continue;
+        // The tile's own rows q0..qlast are the keys of K/V tiles q0/BN .. nkv-1, the last ones the
+        // producer loads; no later tile recycles their stages, so they are copied straight from
+        // shared memory (undoing the 128-byte swizzle) to their slots: no global reads, and each
+        // row leaves as one contiguous D*2-byte store from D/8 lanes.
+        constexpr int CPR = D / 8;   // 16-byte chunks per row
+        constexpr int RPI = 32 / CPR; // rows per warp instruction
+        const int wl = warp - 6;
+        const int cc = lane % CPR, rsub = lane / CPR;
+        const int c2 = cc >> 3, u = cc & 7;
+        for (int j = q0 / BN; j < nkv; ++j) {
+            const int st = j & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(kv_full + st, (j >> 1) & 1))) {
+                if (lane == 0) {
+                    set_error(a.err, PKV_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
             }
-            const int off = p - lb * a.bs;
-            const int64_t src = ((int64_t)(start + p) * a.hkv + kvh) * D + c * 8;
-            const int64_t dst = ((int64_t)blk * 2 * a.hkv + kvh) * a.tile_elems + (int64_t)off * D + c * 8;
-            const int64_t vdst = dst + (int64_t)a.hkv * a.tile_elems;
-            *reinterpret_cast<uint4 *>(a.pool + dst * 2) = *reinterpret_cast<const uint4 *>(a.k + src * 2);
-            *reinterpret_cast<uint4 *>(a.pool + vdst * 2) = *reinterpret_cast<const uint4 *>(a.v + src * 2);
+            const int lo = max(j * BN, q0), hi = min(j * BN + BN - 1, qlast);
+            for (int p0 = lo + wl * RPI; p0 <= hi; p0 += 2 * RPI) {
+                const int p = p0 + rsub;
+                if (p > hi) continue;
+                const int lb = p / a.bs;
+                const int blk = lb < a.max_blocks ? a.tables[(int64_t)seq * a.max_blocks + lb] : -1;
+                if (blk < 0 || blk >= a.num_blocks) {
+                    if (cc == 0) set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                    continue;
+                }
+                const int r = p - j * BN;
+                const int sw = c2 * BN * 128 + (r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4);
+                const uint4 kx = *reinterpret_cast<const uint4 *>(smem + L::K0 + st * L::KV_BYTES + sw);
+                const uint4 vx = *reinterpret_cast<const uint4 *>(smem + L::V0 + st * L::KV_BYTES + sw);
+                const int64_t dst = ((int64_t)blk * 2 * a.hkv + kvh) * a.tile_elems + (int64_t)(p - lb * a.bs) * D + cc * 8;
+                *reinterpret_cast<uint4 *>(a.pool + dst * 2) = kx;
+                *reinterpret_cast<uint4 *>(a.pool + (dst + (int64_t)a.hkv * a.tile_elems) * 2) = vx;
+            }
         }
     }
 
