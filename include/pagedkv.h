@@ -185,7 +185,14 @@ typedef struct {
     int64_t decode_launches, prefill_launches, append_launches, merge_launches;
     double decode_ms, prefill_ms, append_ms, merge_ms;
 } pkv_profile_t;
-int kv_cache_profile_start(pkv_cache_t cache);
+#define PKV_PROFILE_DECODE 1u  /* the split-K decode kernel */
+#define PKV_PROFILE_PREFILL 2u
+#define PKV_PROFILE_APPEND 4u
+#define PKV_PROFILE_MERGE 8u   /* the split merge kernel */
+#define PKV_PROFILE_ALL 15u
+/* kinds: which kernels to bracket (events between two kernels stop their launches from overlapping,
+ * so time only what you need). */
+int kv_cache_profile_start(pkv_cache_t cache, unsigned kinds);
 int kv_cache_profile_read(pkv_cache_t cache, pkv_profile_t *out);
 int64_t pkv_kernel_launches(void);
 

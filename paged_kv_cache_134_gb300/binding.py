@@ -57,7 +57,7 @@ def lib() -> ctypes.CDLL:
         L.paged_decode_attention_noalloc.argtypes = [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]
         L.packed_prefill_attention.argtypes = [vp, vp, vp, vp, i32, i32, i64, vp, i32, vp, i32, ctypes.c_float, vp,
                                                vp]
-        L.kv_cache_profile_start.argtypes = [vp]
+        L.kv_cache_profile_start.argtypes = [vp, ctypes.c_uint]
         L.kv_cache_profile_read.argtypes = [vp, ctypes.c_void_p]
         L.pkv_kernel_launches.restype = i64
         _lib = L
@@ -172,8 +172,14 @@ class KVCache:
             _check(st)
         return int(code.value)
 
-    def profile_start(self):
-        _check(lib().kv_cache_profile_start(self.handle))
+    PROFILE = {"decode": 1, "prefill": 2, "append": 4, "merge": 8}
+
+    def profile_start(self, kinds=("decode", "prefill", "append", "merge")):
+        """Record CUDA events around the named kernels (events between kernels stop their overlap)."""
+        mask = 0
+        for k in kinds:
+            mask |= self.PROFILE[k]
+        _check(lib().kv_cache_profile_start(self.handle, mask))
 
     def profile_read(self) -> dict:
         p = _Profile()

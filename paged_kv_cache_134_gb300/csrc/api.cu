@@ -58,7 +58,7 @@ int pkv_cuda_fail(cudaError_t e, const char *what) {
 }
 
 PkvTimer::PkvTimer(pkv_cache *c_, int kind_, cudaStream_t st_) : c(c_), kind(kind_), st(st_) {
-    if (!c || !c->profiling) return;
+    if (!c || !c->profiling || !(c->profile_kinds & (1u << kind))) return;
     std::lock_guard<std::mutex> lk(c->mu);
     for (cudaEvent_t *ev : {&a, &b}) {
         if (!c->event_pool.empty()) {
@@ -329,8 +329,13 @@ int packed_prefill_attention(const void *q, const void *k, const void *v, const 
     return PKV_OK;
 }
 
-int kv_cache_profile_start(pkv_cache_t c) {
+int kv_cache_profile_start(pkv_cache_t c, unsigned kinds) {
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
+    // PKV_PROFILE_* bits map onto (1 << PKV_KIND_*)
+    c->profile_kinds = ((kinds & PKV_PROFILE_DECODE) ? 1u << PKV_KIND_DECODE : 0u) |
+                       ((kinds & PKV_PROFILE_PREFILL) ? 1u << PKV_KIND_PREFILL : 0u) |
+                       ((kinds & PKV_PROFILE_APPEND) ? 1u << PKV_KIND_APPEND : 0u) |
+                       ((kinds & PKV_PROFILE_MERGE) ? 1u << PKV_KIND_MERGE : 0u);
     std::lock_guard<std::mutex> lk(c->mu);
     for (auto &ev : c->events) {
         c->event_pool.push_back(ev.a);

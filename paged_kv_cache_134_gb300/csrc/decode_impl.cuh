@@ -417,31 +417,32 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
 }
 
 // Merge of the per-split partials of sequences with more than one split; zero rows for
-// L_s == 0.  One warp per (sequence, query head): lane j reads split j's (m, l) so the weights
-// exp2(m_j - M) are formed in parallel, then every split's partial o is read as float4/float2
-// vectors (lane = dims) and accumulated in split order.
+// L_s == 0.  One CTA of four warps per (sequence, query head) row: every warp forms the common
+// max M from all splits' (m, l), then accumulates the splits j = warp, warp + 4, ... (lane = D/32
+// dims, vector loads, loads issued ahead of their use); the four warp sums are added in warp order
+// through shared memory, so the result is deterministic.
 template <int D, int MT>
 __global__ void __launch_bounds__(128) merge_kernel(const Args a) {
     using M = ModelT<MT>;
     using T = typename M::T;
     constexpr int PER = D / 32;
+    __shared__ float s_num[4][D];
+    __shared__ float s_den[4];
     pdl_trigger();
     pdl_wait();
-    const int wid = blockIdx.x * 4 + threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (wid >= a.num_seqs * a.hq) return;
-    const int s = wid / a.hq;
+    const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int s = row / a.hq;
     const int L = a.lens[s];
     int n = L > 0 ? (L + a.bs - 1) / a.bs : 0;
     if (n > a.max_blocks) n = a.max_blocks;
     const int nsplit = n / a.split_blocks + ((n % a.split_blocks) ? 1 : 0);
     if (nsplit == 1) return;
-    T *o = static_cast<T *>(a.out) + (int64_t)wid * D + lane * PER;
+    T *o = static_cast<T *>(a.out) + (int64_t)row * D;
     if (nsplit == 0) {
-#pragma unroll
-        for (int e = 0; e < PER; ++e) o[e] = M::from_f(0.f);
+        for (int e = threadIdx.x; e < D; e += blockDim.x) o[e] = M::from_f(0.f);
         return;
     }
-    const int64_t base = (int64_t)wid * a.max_splits;
+    const int64_t base = (int64_t)row * a.max_splits;
     const float2 *ml = reinterpret_cast<const float2 *>(a.ws_ml) + base;
     float Mx = -INFINITY;
     for (int j = lane; j < nsplit; j += 32) {
@@ -453,35 +454,50 @@ __global__ void __launch_bounds__(128) merge_kernel(const Args a) {
     float num[PER], den = 0.f;
 #pragma unroll
     for (int e = 0; e < PER; ++e) num[e] = 0.f;
-    for (int j0 = 0; j0 < nsplit; j0 += 32) {
-        float wj = 0.f, lj = 0.f;
-        if (j0 + lane < nsplit) {
-            const float2 v = ml[j0 + lane];
-            lj = v.y;
-            if (lj > 0.f) wj = fast_exp2(v.x - Mx);
-        }
-        const int cnt = min(32, nsplit - j0);
-#pragma unroll 4
-        for (int jj = 0; jj < cnt; ++jj) {
-            const float w = __shfl_sync(0xffffffffu, wj, jj);
-            den = fmaf(w, __shfl_sync(0xffffffffu, lj, jj), den);
-            const float *src = a.ws_o + (base + j0 + jj) * D + lane * PER;
-            if constexpr (PER == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(src);
-                num[0] = fmaf(w, v.x, num[0]);
-                num[1] = fmaf(w, v.y, num[1]);
-                num[2] = fmaf(w, v.z, num[2]);
-                num[3] = fmaf(w, v.w, num[3]);
+    constexpr int U = 4;
+    for (int j0 = warp; j0 < nsplit; j0 += 4 * U) {
+        float2 mlj[U];
+        float vj[U][PER];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int j = j0 + 4 * k;
+            if (j < nsplit) {
+                mlj[k] = ml[j];
+                const float *src = a.ws_o + (base + j) * D + lane * PER;
+                if constexpr (PER == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src);
+                    vj[k][0] = v.x;
+                    vj[k][1] = v.y;
+                    vj[k][2] = v.z;
+                    vj[k][3] = v.w;
+                } else {
+                    const float2 v = *reinterpret_cast<const float2 *>(src);
+                    vj[k][0] = v.x;
+                    vj[k][1] = v.y;
+                }
             } else {
-                const float2 v = *reinterpret_cast<const float2 *>(src);
-                num[0] = fmaf(w, v.x, num[0]);
-                num[1] = fmaf(w, v.y, num[1]);
+                mlj[k] = make_float2(0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            if (mlj[k].y > 0.f) {
+                const float w = fast_exp2(mlj[k].x - Mx);
+                den = fmaf(w, mlj[k].y, den);
+#pragma unroll
+                for (int e = 0; e < PER; ++e) num[e] = fmaf(w, vj[k][e], num[e]);
             }
         }
     }
-    const float r = den > 0.f ? 1.f / den : 0.f;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) o[e] = M::from_f(num[e] * r);
+    for (int e = 0; e < PER; ++e) s_num[warp][lane * PER + e] = num[e];
+    if (lane == 0) s_den[warp] = den;
+    __syncthreads();
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        const float tn = ((s_num[0][d] + s_num[1][d]) + s_num[2][d]) + s_num[3][d];
+        const float td = ((s_den[0] + s_den[1]) + s_den[2]) + s_den[3];
+        o[d] = M::from_f(td > 0.f ? tn / td : 0.f);
+    }
 }
 
 inline size_t smem_bytes(int D, int G, int nst, int tile_bytes, int S) {
@@ -501,7 +517,7 @@ template <int D, int MT>
 cudaError_t launch_merge_t(const Args &a, cudaStream_t st) {
     const int rows = a.num_seqs * a.hq;
     if (rows == 0) return cudaSuccess;
-    return pdl_launch(merge_kernel<D, MT>, dim3((rows + 3) / 4), dim3(128), 0, st, a);
+    return pdl_launch(merge_kernel<D, MT>, dim3(rows), dim3(128), 0, st, a);
 }
 
 // Dispatch over head_dim and group size for one (model dtype, KV dtype) pair.

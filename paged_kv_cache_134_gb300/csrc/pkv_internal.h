@@ -29,6 +29,7 @@ struct pkv_cache {
     int num_sms = 0;
     // profiling
     bool profiling = false;
+    unsigned profile_kinds = 0; // bit (1 << PKV_KIND_*)
     struct Ev {
         int kind;
         cudaEvent_t a, b;

@@ -109,9 +109,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR);
     uint64_t *q_full = bars + 0, *kv_full = bars + 1, *kv_empty = bars + 3, *s_full = bars + 5, *s_free = bars + 7;
-    uint64_t *p_full = bars + 9, *t_full = bars + 10, *fin = bars + 11;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 13);
+    uint64_t *p_full = bars + 9, *t_full = bars + 10, *fin = bars + 11, *loaded = bars + 12;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 14);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
         mbar_init(p_full, 128);
         mbar_init(t_full, 1);
         mbar_init(fin, 1);
+        mbar_init(loaded, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -192,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             };
             bool ok = mbar_wait(q_full, 0) && mbar_wait(kv_full, 0);
             if (ok) {
+                if (nkv == 1) mbar_arrive(loaded); // every K/V tile of this CTA has landed
                 tc::fence_after_sync();
                 issue_s(0);
             }
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 if (j + 1 < nkv) {
                     const int b = (j + 1) & 1;
                     ok = mbar_wait(kv_full + b, ((j + 1) >> 1) & 1);
+                    if (ok && j + 2 == nkv) mbar_arrive(loaded);
                     if (ok && j + 1 >= 2) ok = mbar_wait(s_free + b, ((j - 1) >> 1) & 1);
                     if (!ok) break;
                     tc::fence_after_sync();
@@ -344,15 +347,16 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
         const int wl = warp - 6;
         const int cc = lane % CPR, rsub = lane / CPR;
         const int c2 = cc >> 3, u = cc & 7;
-        for (int j = q0 / BN; j < nkv; ++j) {
+        // `loaded` has a single phase (the MMA thread arrives once it has seen the last K/V tile land);
+        // waiting on kv_full here could target a phase two or more ahead, which a parity wait cannot tell
+        // from an already completed one
+        const bool landed = __all_sync(0xffffffffu, mbar_wait(loaded, 0));
+        if (!landed && lane == 0) {
+            set_error(a.err, PKV_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        for (int j = q0 / BN; j < nkv && landed; ++j) {
             const int st = j & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(kv_full + st, (j >> 1) & 1))) {
-                if (lane == 0) {
-                    set_error(a.err, PKV_DEVERR_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                break;
-            }
             const int lo = max(j * BN, q0), hi = min(j * BN + BN - 1, qlast);
             for (int p0 = lo + wl * RPI; p0 <= hi; p0 += 2 * RPI) {
                 const int p = p0 + rsub;
