@@ -218,7 +218,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
         *abort_flag = 0;
         fence_mbarrier_init();
     }
-    pdl_trigger();
     pdl_wait(); // the previous kernel (e.g. the append of this step) has finished
     // unit list: per sequence, full splits and (0 or 1) partial split
     const int bps = a.split_blocks;
@@ -301,6 +300,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
                 }
             }
         }
+        // the next kernel (the split merge) may start launching once every CTA has issued its last load
+        pdl_trigger();
         // drain: the copies of the last stages must land before this CTA's shared memory goes away
         if (lane == 0) {
             const uint32_t first = tau > (uint32_t)NST ? tau - NST : 0;
