@@ -265,6 +265,35 @@ def secondary_prefill(P, W, gpu_path, peaks, reps=20):
             "frac_of_bf16_peak": round(tflops / peaks[1], 4), "device_errors": err}
 
 
+def secondary_decode(P, G, peaks, w, reps=50, unique_bytes=None):
+    """Decode step (append_at + decode + merge) on another configuration; decode kernel timed by events."""
+    cache = G.new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype, w.model_dtype,
+                        w.k_scale, w.v_scale)
+    G.fill_cache(cache, w)
+    x = G.DecodeInputs(w)
+    cache.reserve(w.num_seqs, w.num_q_heads, w.max_blocks)
+    for _ in range(5):
+        G.decode_step(cache, x)
+    torch.cuda.synchronize()
+    cache.profile_start(kinds=("decode",))
+    t = _time_loop(lambda: G.decode_step(cache, x), reps, torch.cuda.current_stream()) / reps
+    prof = cache.profile_read()
+    err = cache.check_error()
+    cache.close()
+    kern = prof["decode_ms"] / max(1, prof["decode_launches"]) / 1e3
+    kv = w.kv_read_bytes()
+    r = {"kv_dtype": w.kv_dtype, "block_size": w.block_size, "num_seqs": w.num_seqs,
+         "heads": f"{w.num_q_heads}/{w.num_kv_heads}", "kv_bytes": kv, "step_us": round(t * 1e6, 2),
+         "decode_kernel_us": round(kern * 1e6, 2), "kv_gbs": round(kv / kern / 1e9, 1),
+         "frac_of_hbm": round(kv / kern / 1e9 / peaks[0], 4), "seqs_per_s": round(w.num_seqs / t, 1),
+         "device_errors": err}
+    if unique_bytes is not None:
+        r["kv_gbs_label"] = "logical (shared prefix re-read per sequence, mostly L2 hits)"
+        r["unique_kv_bytes"] = unique_bytes
+        r["unique_kv_gbs"] = round(unique_bytes / kern / 1e9, 1)
+    return r
+
+
 def secondary_append(P, W, gpu_path, peaks, reps=20):
     """Bulk paged append of 5256 tokens x 32 heads x 128 fp16 (86 MB read + 86 MB written)."""
     w = W.prefill()
@@ -374,6 +403,22 @@ def run_ours(args):
     if rank == 0 and not args.skip_secondary:
         secondary["prefill"] = secondary_prefill(P, W, G, peaks)
         secondary["append"] = secondary_append(P, W, G, peaks)
+        w4 = W.prefix13b()
+        uniq = (w4.shared_prefix_len + int((w4.context_lens - w4.shared_prefix_len + 1).sum())) * \
+            w4.num_kv_heads * w4.head_dim * 2 * 2
+        secondary["prefix13b"] = dict(workload="13B-shape decode, 64 seqs sharing a 4096-token prefix (128 blocks, "
+                                               "ref count 64) + private suffix U{1..512}, 40/40 heads, bs=32, fp16",
+                                      **secondary_decode(P, G, peaks, w4, unique_bytes=uniq))
+        del w4
+        stress = {}
+        for kv in ("bf16", "fp8"):
+            for bs in (8, 16, 32):
+                stress[f"bs{bs}_{kv}"] = secondary_decode(P, G, peaks, W.stress(bs=bs, kv_dtype=kv))
+        for bs in (8, 16, 32):
+            stress[f"bs{bs}_fp8_over_bf16_time"] = round(stress[f"bs{bs}_fp8"]["decode_kernel_us"] /
+                                                         stress[f"bs{bs}_bf16"]["decode_kernel_us"], 3)
+        secondary["stress"] = dict(workload="256 seqs, log-normal lengths (median 500, cap 8192), 32 q / 8 KV heads, "
+                                            "D=128, churned free list; KV bf16 or FP8-E4M3 (per-head scales)", **stress)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.skip_cpu:
