@@ -8,8 +8,9 @@
 // sequence length so a partly filled tail block is never overrun).
 //
 // One CTA = (sequence, 128-query tile, query head).  Warp roles:
-//   warp 0     TMA producer: Q tile once, then K/V tiles of 64 keys into a 2-stage ring (tiled TMA,
-//              128-byte swizzle, out-of-range rows zero-filled);
+//   warp 0     TMA producers: lane 0 loads the Q tile once and K tiles of 64 keys into a 2-stage ring,
+//              lane 1 V tiles into another (tiled TMA, 128-byte swizzle, out-of-range rows zero-filled);
+//              a K stage frees when S = Q K^T of its tile is done, a V stage when P V is done;
 //   warp 1     tensor-memory owner and MMA issuer (one thread): S = Q K^T into one of two TMEM S
 //              buffers (M=128, N=64, fp32), then O += P V into the TMEM O accumulator (M=128, N=D);
 //   warps 2-5  softmax, one thread per query row (TMEM lane = row): mask, exp2, row sums, P written
@@ -108,17 +109,20 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
     const int nkv = qlast / BN + 1;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR);
-    uint64_t *q_full = bars + 0, *kv_full = bars + 1, *kv_empty = bars + 3, *s_full = bars + 5, *s_free = bars + 7;
-    uint64_t *p_full = bars + 9, *t_full = bars + 10, *fin = bars + 11, *loaded = bars + 12;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 14);
+    uint64_t *q_full = bars + 0, *k_full = bars + 1, *v_full = bars + 3, *k_empty = bars + 5, *v_empty = bars + 7;
+    uint64_t *s_full = bars + 9, *s_free = bars + 11, *p_full = bars + 13, *t_full = bars + 14, *fin = bars + 15;
+    uint64_t *loaded = bars + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 18);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(kv_full + s, 1);
-            mbar_init(kv_empty + s, 1);
+            mbar_init(k_full + s, 1);
+            mbar_init(v_full + s, 1);
+            mbar_init(k_empty + s, 1);
+            mbar_init(v_empty + s, 1);
             mbar_init(s_full + s, 1);
             mbar_init(s_free + s, 128);
         }
@@ -139,38 +143,43 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tc::prefetch_tmap(&tq);
-            tc::prefetch_tmap(&tk);
-            tc::prefetch_tmap(&tv);
-            mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+        // ------------------------------------------------------------ TMA producers
+        // K and V have rings of their own: a K stage is free once S = Q K^T of its tile is done, so
+        // K loads run about two tiles ahead of the softmax; a V stage is free once P V is done.
+        // Lane 0 streams Q and K, lane 1 streams V.
+        if (lane < 2) {
+            const bool is_k = lane == 0;
+            const CUtensorMap *map = is_k ? &tk : &tv;
+            uint64_t *full = is_k ? k_full : v_full, *empty = is_k ? k_empty : v_empty;
+            uint8_t *ring = smem + (is_k ? L::K0 : L::V0);
+            tc::prefetch_tmap(map);
+            if (is_k) {
+                tc::prefetch_tmap(&tq);
+                mbar_arrive_expect_tx(q_full, L::Q_BYTES);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                tc::tma_load_2d(smem + L::Q + c * BM * 128, &tq, h * D + c * 64, start + q0, q_full);
+                for (int c = 0; c < D / 64; ++c)
+                    tc::tma_load_2d(smem + L::Q + c * BM * 128, &tq, h * D + c * 64, start + q0, q_full);
+            }
             int issued = 0;
             for (int j = 0; j < nkv; ++j) {
                 const int st = j & 1;
-                if (j >= 2 && !mbar_wait(kv_empty + st, ((j >> 1) - 1) & 1)) {
+                if (j >= 2 && !mbar_wait(empty + st, ((j >> 1) - 1) & 1)) {
                     set_error(a.err, PKV_DEVERR_TIMEOUT);
                     *abort_flag = 1;
                     break;
                 }
                 if (*abort_flag) break;
-                mbar_arrive_expect_tx(kv_full + st, 2 * L::KV_BYTES);
+                mbar_arrive_expect_tx(full + st, L::KV_BYTES);
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    tc::tma_load_2d(smem + L::K0 + st * L::KV_BYTES + c * BN * 128, &tk, kvh * D + c * 64,
-                                    start + j * BN, kv_full + st);
-                    tc::tma_load_2d(smem + L::V0 + st * L::KV_BYTES + c * BN * 128, &tv, kvh * D + c * 64,
-                                    start + j * BN, kv_full + st);
-                }
+                for (int c = 0; c < D / 64; ++c)
+                    tc::tma_load_2d(ring + st * L::KV_BYTES + c * BN * 128, map, kvh * D + c * 64, start + j * BN,
+                                    full + st);
                 issued = j + 1;
             }
             // the loads of the last stages must land before this CTA's shared memory goes away
             for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-                if (!mbar_wait(kv_full + (j & 1), (j >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
-            if (!mbar_wait(q_full, 0)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+                if (!mbar_wait(full + (j & 1), (j >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            if (is_k && !mbar_wait(q_full, 0)) set_error(a.err, PKV_DEVERR_TIMEOUT);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -180,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             const uint32_t sQ = smem_u32(smem + L::Q), sK = smem_u32(smem + L::K0), sV = smem_u32(smem + L::V0);
             const uint32_t sP = smem_u32(smem + L::P);
             const uint32_t tO = tmem + 128;
+            // S_j = Q K_j^T into S buffer j % 2; its K stage is released as soon as S_j is done
             auto issue_s = [&](int j) {
                 const int st = j & 1;
 #pragma unroll
@@ -190,27 +200,27 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                     tc::mma_f16(tmem + st * BN, ad, bd, IQK, k > 0 ? 1u : 0u);
                 }
                 tc::commit(s_full + st);
+                tc::commit(k_empty + st);
             };
-            bool ok = mbar_wait(q_full, 0) && mbar_wait(kv_full, 0);
+            bool ok = mbar_wait(q_full, 0) && mbar_wait(k_full, 0);
             if (ok) {
-                if (nkv == 1) mbar_arrive(loaded); // every K/V tile of this CTA has landed
                 tc::fence_after_sync();
                 issue_s(0);
             }
             for (int j = 0; j < nkv && ok; ++j) {
                 if (j + 1 < nkv) {
                     const int b = (j + 1) & 1;
-                    ok = mbar_wait(kv_full + b, ((j + 1) >> 1) & 1);
-                    if (ok && j + 2 == nkv) mbar_arrive(loaded);
+                    ok = mbar_wait(k_full + b, ((j + 1) >> 1) & 1);
                     if (ok && j + 1 >= 2) ok = mbar_wait(s_free + b, ((j - 1) >> 1) & 1);
                     if (!ok) break;
                     tc::fence_after_sync();
                     issue_s(j + 1);
                 }
-                ok = mbar_wait(p_full, j & 1);
-                if (!ok) break;
-                tc::fence_after_sync();
                 const int st = j & 1;
+                ok = mbar_wait(p_full, j & 1) && mbar_wait(v_full + st, (j >> 1) & 1);
+                if (!ok) break;
+                if (j == nkv - 1) mbar_arrive(loaded); // every K and V tile of this CTA has landed
+                tc::fence_after_sync();
 #pragma unroll
                 for (int part = 0; part < L::NP; ++part)
 #pragma unroll
@@ -220,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                         tc::mma_f16(tO, ad, bd, IPV, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
                     }
                 tc::commit(t_full);
-                tc::commit(kv_empty + st);
+                tc::commit(v_empty + st);
             }
             if (!ok) {
                 set_error(a.err, PKV_DEVERR_TIMEOUT);
@@ -348,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
         const int cc = lane % CPR, rsub = lane / CPR;
         const int c2 = cc >> 3, u = cc & 7;
         // `loaded` has a single phase (the MMA thread arrives once it has seen the last K/V tile land);
-        // waiting on kv_full here could target a phase two or more ahead, which a parity wait cannot tell
+        // waiting on k_full/v_full here could target a phase two or more ahead, which a parity wait cannot tell
         // from an already completed one
         const bool landed = __all_sync(0xffffffffu, mbar_wait(loaded, 0));
         if (!landed && lane == 0) {
