@@ -108,82 +108,96 @@ PKV_DEV Unit unit_info(int u, const int *pf, const int *pp, const int *nb, int S
     return r;
 }
 
-// One tile of `bs` tokens, `valid` of them real, for the G query heads of one KV head.
-template <int D, int G, int KVT>
-PKV_DEV void process_tile(const char *ks, const char *vs, int bs, int valid, const float (&qf)[G][8], float (&m)[G],
-                          float (&l)[G], float (&acc)[G][8], int lane) {
-    constexpr int LPT = D / 8;        // lanes per token
-    constexpr int TPP = 32 / LPT;     // tokens per pass
-    constexpr int MAXP = 16 / TPP;    // passes per 16-token chunk
+// Lane layout of a consumer warp for head_dim D and G query heads per KV head.  A token's row is
+// covered by LT = LH * G lanes: each of the G query heads gets LH lanes, each lane DL consecutive
+// dims of that head (so it keeps q, the accumulator and the scores of one head only).  Lanes of
+// different heads read the same K/V chunk (a shared-memory broadcast).  TPP tokens go in one pass.
+//   G=1, D=128: DL=8,  LH=16, 2 tokens/pass     G=4, D=128: DL=16, LH=8, 1 token/pass
+//   G=1, D=64:  DL=8,  LH=8,  4 tokens/pass     G=8, D=128: DL=32, LH=4, 1 token/pass
+template <int D, int G>
+struct Lanes {
+    static constexpr int DL = (D * G / 32) > 8 ? (D * G / 32) : 8; // dims per lane
+    static constexpr int LH = D / DL;                               // lanes per (token, head)
+    static constexpr int LT = LH * G;                               // lanes per token
+    static constexpr int TPP = 32 / LT;                             // tokens per pass
+    static constexpr int MAXP = 16 / TPP;                           // passes per 16-token chunk
+    static_assert(LT <= 32 && 32 % LT == 0 && D % DL == 0 && DL % 8 == 0, "lane layout");
+};
+
+template <int KVT, int N>
+PKV_DEV void loadN(const char *p, float *f) {
     constexpr int EB = (KVT == PKV_FP8_E4M3) ? 1 : 2;
-    const int sub = lane % LPT, grp = lane / LPT;
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c) load8<KVT>(p + c * 8 * EB, f + 8 * c);
+}
+
+// One tile of `bs` tokens, `valid` of them real, for this lane's query head.
+template <int D, int G, int KVT>
+PKV_DEV void process_tile(const char *ks, const char *vs, int bs, int valid,
+                          const float (&qf)[Lanes<D, G>::DL], float &m, float &l, float (&acc)[Lanes<D, G>::DL],
+                          int lane) {
+    using LY = Lanes<D, G>;
+    constexpr int DL = LY::DL, LH = LY::LH, LT = LY::LT, TPP = LY::TPP, MAXP = LY::MAXP;
+    constexpr int EB = (KVT == PKV_FP8_E4M3) ? 1 : 2;
+    const int sub = lane % LH, tg = lane / LT;
     const int ch = bs < 16 ? bs : 16;
     const int npc = ch / TPP;
     for (int c0 = 0; c0 < bs; c0 += ch) {
         if (c0 >= valid) break;
-        float sc[G][MAXP];
+        float sc[MAXP];
 #pragma unroll
         for (int p = 0; p < MAXP; ++p) {
             if (p < npc) {
-                const int t = c0 + p * TPP + grp;
-                float kf[8];
-                load8<KVT>(ks + (t * D + sub * 8) * EB, kf);
+                const int t = c0 + p * TPP + tg;
+                float kf[DL];
+                loadN<KVT, DL>(ks + (t * D + sub * DL) * EB, kf);
+                float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float d0 = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) d0 = fmaf(qf[g][e], kf[e], d0);
-                    sc[g][p] = d0;
+                for (int e = 0; e < DL; e += 2) {
+                    d0 = fmaf(qf[e], kf[e], d0);
+                    d1 = fmaf(qf[e + 1], kf[e + 1], d1);
                 }
+                sc[p] = d0 + d1;
             }
         }
 #pragma unroll
         for (int p = 0; p < MAXP; ++p) {
             if (p < npc) {
-                const bool live = (c0 + p * TPP + grp) < valid;
+                float v = sc[p];
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float v = sc[g][p];
-#pragma unroll
-                    for (int o = LPT / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                    sc[g][p] = live ? v : -INFINITY;
-                }
+                for (int o = LH / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                sc[p] = (c0 + p * TPP + tg) < valid ? v : -INFINITY;
             }
         }
+        float mx = -INFINITY;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float mx = -INFINITY;
+        for (int p = 0; p < MAXP; ++p)
+            if (p < npc) mx = fmaxf(mx, sc[p]);
 #pragma unroll
-            for (int p = 0; p < MAXP; ++p)
-                if (p < npc) mx = fmaxf(mx, sc[g][p]);
+        for (int o = LT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float mn = fmaxf(m, mx); // finite: the chunk holds at least one live token
+        const float alpha = fast_exp2(m - mn);
+        m = mn;
+        l *= alpha;
 #pragma unroll
-            for (int o = LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float mn = fmaxf(m[g], mx); // finite: the chunk holds at least one live token
-            const float alpha = fast_exp2(m[g] - mn);
-            m[g] = mn;
-            l[g] *= alpha;
+        for (int e = 0; e < DL; ++e) acc[e] *= alpha;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
-#pragma unroll
-            for (int p = 0; p < MAXP; ++p) {
-                if (p < npc) {
-                    const float pr = fast_exp2(sc[g][p] - mn);
-                    sc[g][p] = pr;
-                    l[g] += pr;
-                }
+        for (int p = 0; p < MAXP; ++p) {
+            if (p < npc) {
+                const float pr = fast_exp2(sc[p] - mn);
+                sc[p] = pr;
+                l += pr;
             }
         }
 #pragma unroll
         for (int p = 0; p < MAXP; ++p) {
             if (p < npc) {
-                const int t = c0 + p * TPP + grp;
+                const int t = c0 + p * TPP + tg;
                 if (t < valid) {
-                    float vf[8];
-                    load8<KVT>(vs + (t * D + sub * 8) * EB, vf);
+                    float vf[DL];
+                    loadN<KVT, DL>(vs + (t * D + sub * DL) * EB, vf);
 #pragma unroll
-                    for (int g = 0; g < G; ++g)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(sc[g][p], vf[e], acc[g][e]);
+                    for (int e = 0; e < DL; ++e) acc[e] = fmaf(sc[p], vf[e], acc[e]);
                 }
             }
         }
@@ -195,7 +209,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     using M = ModelT<MT>;
     using T = typename M::T;
     constexpr int NCW = kConsumerWarps;
-    constexpr int LPT = D / 8;
     extern __shared__ __align__(128) unsigned char smem[];
     const int NST = a.nstages;
     const int S = a.num_seqs;
@@ -312,7 +325,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     }
 
     // -------------------------------------------------------------------- consumer warps
-    const int sub = lane % LPT, grp = lane / LPT;
+    using LY = Lanes<D, G>;
+    constexpr int DL = LY::DL, LH = LY::LH, LT = LY::LT;
+    const int sub = lane % LH, gl = (lane / LH) % G, tg = lane / LT;
     const int tid = threadIdx.x; // 0 .. NCW*32-1
     uint32_t tau = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x) {
@@ -320,23 +335,17 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
         const int L = a.lens[un.s];
         float qs = a.qk_scale_log2;
         if constexpr (KVT == PKV_FP8_E4M3) qs *= a.k_scale[un.kvh];
-        float qf[G][8];
+        float qf[DL];
+        {
+            const T *qp = static_cast<const T *>(a.q) + ((int64_t)un.s * a.hq + un.kvh * G + gl) * D + sub * DL;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const T *qp = static_cast<const T *>(a.q) + ((int64_t)un.s * a.hq + un.kvh * G + g) * D + sub * 8;
-            const uint4 raw = *reinterpret_cast<const uint4 *>(qp);
-            cvt8<MT>(raw, qf[g]);
+            for (int c = 0; c < DL / 8; ++c) cvt8<MT>(reinterpret_cast<const uint4 *>(qp)[c], qf + 8 * c);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) qf[g][e] *= qs;
+            for (int e = 0; e < DL; ++e) qf[e] *= qs;
         }
-        float m[G], l[G], acc[G][8];
+        float m = -INFINITY, l = 0.f, acc[DL];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            m[g] = -INFINITY;
-            l[g] = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
-        }
+        for (int e = 0; e < DL; ++e) acc[e] = 0.f;
         // Tile t of the CTA's stream (t counted over all its units) belongs to warp t % NCW and
         // sits in stage t % NST with NST a multiple of NCW, so a warp's previous tile in any stage
         // is its own: when it waits for phase k of a stage, phase k-1 has completed, which keeps
@@ -360,26 +369,20 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
             if (lane == 0) mbar_arrive(&empty[stage]);
         }
         tau += un.ntiles;
-        // combine the token groups of this warp
+        // combine the token groups of this warp (same head, same dims)
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int o = LT; o < 32; o <<= 1) {
+            l += __shfl_xor_sync(0xffffffffu, l, o);
 #pragma unroll
-            for (int o = LPT; o < 32; o <<= 1) {
-                l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
-            }
+            for (int e = 0; e < DL; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
         }
-        if (grp == 0) {
+        if (tg == 0) {
+            float *r = mrg + (warp * G + gl) * (D + 2);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float *r = mrg + (warp * G + g) * (D + 2);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) r[sub * 8 + e] = acc[g][e];
-                if (sub == 0) {
-                    r[D] = m[g];
-                    r[D + 1] = l[g];
-                }
+            for (int e = 0; e < DL; ++e) r[sub * DL + e] = acc[e];
+            if (sub == 0) {
+                r[D] = m;
+                r[D + 1] = l;
             }
         }
         named_barrier_sync(1, NCW * 32);
