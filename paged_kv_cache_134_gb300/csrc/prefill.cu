@@ -22,6 +22,7 @@
 //              (token, KV head) is written once).
 // The diagonal tiles are masked per element; tiles entirely above the diagonal are never issued.
 // Every mbarrier wait is bounded; a timeout sets PKV_DEVERR_TIMEOUT and the CTA winds down.
+#include <algorithm>
 #include <mutex>
 
 #include "tcgen05.cuh"
@@ -88,19 +89,59 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
 
     pdl_trigger();
     pdl_wait();
-    // ---- work item, heaviest query tiles first
-    const int per_qt = a.num_seqs * a.hq;
-    const int rank = blockIdx.x / per_qt;
-    const int qt = a.nqt_max - 1 - rank;
-    const int rem = blockIdx.x - rank * per_qt;
-    const int seq = rem / a.hq, h = rem - seq * a.hq;
-    const int start = a.cu[seq], end = a.cu[seq + 1];
-    const int n = end - start;
-    if (start < 0 || n < 0 || end > a.total_tokens || n > a.max_seqlen) {
-        if (threadIdx.x == 0 && h == 0 && qt == 0) set_error(a.err, PKV_DEVERR_CU_SEQLENS);
-        return;
+    // ---- work item.  Items are (sequence, query tile) pairs, hq CTAs (one per query head) each, in
+    // rank order: rank r holds every sequence's r-th heaviest query tile (its (nq-1-r)-th), so the
+    // longest tiles start first.  The grid is sized from the packed token count (at most
+    // T/BM + num_seqs items), and each CTA finds its item from a histogram of per-sequence tile
+    // counts kept, for this prologue only, in the P buffer's shared memory.
+    int *nq = reinterpret_cast<int *>(smem + L::P);
+    int *hist = nq + a.num_seqs;          // [nqt_max + 1]
+    int *pick = hist + a.nqt_max + 1;     // seq, qt
+    for (int x = threadIdx.x; x <= a.nqt_max; x += blockDim.x) hist[x] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.num_seqs; i += blockDim.x) {
+        const int st = a.cu[i], en = a.cu[i + 1];
+        int c = 0;
+        if (st < 0 || en < st || en > a.total_tokens || en - st > a.max_seqlen) {
+            if (blockIdx.x == 0) set_error(a.err, PKV_DEVERR_CU_SEQLENS);
+        } else {
+            c = (en - st + BM - 1) / BM;
+        }
+        nq[i] = c;
+        atomicAdd(&hist[c], 1);
     }
-    if (qt * BM >= n) return;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        int k = blockIdx.x / a.hq, r = 0, above = a.num_seqs - hist[0]; // above = #{i : nq_i > r}
+        while (r < a.nqt_max && k >= above) {
+            k -= above;
+            ++r;
+            above -= hist[r];
+        }
+        int seq_found = -1;
+        if (r < a.nqt_max) {
+            for (int base = 0; base < a.num_seqs; base += 32) {
+                const int i = base + (int)threadIdx.x;
+                const unsigned bal = __ballot_sync(0xffffffffu, i < a.num_seqs && nq[i] > r);
+                const int cnt = __popc(bal);
+                if (k < cnt) {
+                    seq_found = base + (int)__fns(bal, 0, k + 1);
+                    break;
+                }
+                k -= cnt;
+            }
+        }
+        if (threadIdx.x == 0) {
+            pick[0] = seq_found;
+            pick[1] = seq_found >= 0 ? nq[seq_found] - 1 - r : -1;
+        }
+    }
+    __syncthreads();
+    const int seq = pick[0], qt = pick[1];
+    const int h = blockIdx.x % a.hq;
+    if (seq < 0) return;
+    const int start = a.cu[seq];
+    const int n = a.cu[seq + 1] - start;
     if (smem_u32(smem) & 1023u) return; // the swizzled tiles need 1024-byte alignment (always true)
     const int G = a.hq / a.hkv;
     const int kvh = h / G;
@@ -264,31 +305,39 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             tc::wait_ld();
             tc::fence_before_sync();
             mbar_arrive(s_free + b);
+            // causal mask, only on tiles that reach past this tile's first query row
             const int kbase = j * BN;
-            float mx = -INFINITY;
+            if (kbase + BN - 1 > q0) {
+                const int lim = qpos - kbase + 1; // keys c < lim are at or before this row
 #pragma unroll
-            for (int c = 0; c < BN; ++c) {
-                float x = __uint_as_float(sr[c]) * a.scale_log2;
-                x = (kbase + c > qpos) ? -INFINITY : x;
-                sr[c] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
+                for (int c = 0; c < BN; ++c)
+                    if (c >= lim) sr[c] = 0xFF800000u; // -inf
             }
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BN; c += 2) {
+                mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+                mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+            }
+            const float mx = fmaxf(mx0, mx1) * a.scale_log2; // scale > 0 keeps the order
             const bool up = mx > m_use + kRescale;
             const float m_new = up ? mx : m_use;
             const float alpha = up ? fast_exp2(m_use - m_new) : 1.f;
             m_use = m_new;
-            const float base = m_use == -INFINITY ? 0.f : m_use; // a row with no live key yet keeps p = 0
-            float rs = 0.f;
+            const float nbase = m_use == -INFINITY ? 0.f : -m_use; // a row with no live key yet keeps p = 0
+            float rs0 = 0.f, rs1 = 0.f;
             uint32_t phi[BN / 2], plo[L::NP == 2 ? BN / 2 : 1];
 #pragma unroll
             for (int c = 0; c < BN / 2; ++c) {
-                const float p0 = fast_exp2(__uint_as_float(sr[2 * c]) - base);
-                const float p1 = fast_exp2(__uint_as_float(sr[2 * c + 1]) - base);
-                rs += p0 + p1;
+                const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * c]), a.scale_log2, nbase));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * c + 1]), a.scale_log2, nbase));
+                rs0 += p0;
+                rs1 += p1;
                 phi[c] = pack2(p0, p1, MT);
                 if constexpr (L::NP == 2) // remainders after bf16 rounding, themselves rounded to bf16
                     plo[c] = pack2(p0 - __uint_as_float(phi[c] << 16), p1 - __uint_as_float(phi[c] & 0xFFFF0000u), MT);
             }
+            const float rs = rs0 + rs1;
             l = l * alpha + rs;
             if (j > 0) {
                 // P V of the previous tile has finished: P's buffer is free and O is stable
@@ -465,12 +514,16 @@ cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st
     a.bs = c->block_size;
     a.nqt_max = (p.max_seqlen + BM - 1) / BM;
     a.scale_log2 = p.scale * 1.4426950408889634f;
+    // the work-item prologue keeps num_seqs + nqt_max + 3 ints in the P buffer
+    if ((int64_t)p.num_seqs + a.nqt_max + 3 > (int64_t)BM * BN * 2 / 4) return cudaErrorNotSupported;
     CUtensorMap tq, tk, tv;
     if (!make_map(&tq, p.q, mt, p.total_tokens, (int64_t)p.num_q_heads * D, BM) ||
         !make_map(&tk, p.k, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN) ||
         !make_map(&tv, p.v, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN))
         return cudaErrorInvalidValue;
-    const int64_t grid = (int64_t)a.nqt_max * p.num_seqs * p.num_q_heads;
+    // (sequence, query tile) items: sum_i ceil(n_i / BM) <= T / BM + num_seqs
+    const int64_t items = std::min<int64_t>((int64_t)a.nqt_max * p.num_seqs, p.total_tokens / BM + p.num_seqs);
+    const int64_t grid = items * p.num_q_heads;
     if (grid == 0) return cudaSuccess;
     if (grid > 0x7FFFFFFF) return cudaErrorNotSupported;
     PkvTimer timer(c, PKV_KIND_PREFILL, st);
