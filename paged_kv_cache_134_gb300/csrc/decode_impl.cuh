@@ -204,6 +204,108 @@ PKV_DEV void process_tile(const char *ks, const char *vs, int bs, int valid,
     }
 }
 
+// Grouped-query heads (G >= 2): token-parallel lanes.  D/8 lanes share a token (8 dims each) and
+// every lane works for all G query heads, so each K/V element is loaded and widened once and
+// feeds G products.  Products and the P.V accumulation use packed fp32 FMAs (two lanes of an
+// IEEE fma each).  The partial dot products of the chunk's passes are summed across the token's
+// lanes by a reduce-scatter: after log2 steps every lane holds the full score of one pass, so the
+// softmax of a head costs one exp2 per lane, and each pass's weight is then fetched back by a
+// shuffle from the lane that owns it.
+template <int D, int G, int KVT>
+PKV_DEV void process_tile_tp(const char *ks, const char *vs, int bs, int valid, const float (&qf)[G][8],
+                             float (&m)[G], float (&l)[G], float (&acc)[G][8], int lane) {
+    constexpr int LPT = D / 8;     // lanes per token
+    constexpr int TPP = 32 / LPT;  // tokens per pass
+    constexpr int MAXP = 16 / TPP; // passes per 16-token chunk (8 for D=128, 4 for D=64)
+    constexpr int EB = (KVT == PKV_FP8_E4M3) ? 1 : 2;
+    // after the reduce-scatter the lane with sub-lane bits s holds pass (s >> DUP) of its token group;
+    // the DUP lowest sub-lane bits only duplicate it
+    constexpr int LOG_LPT = LPT == 16 ? 4 : 3;
+    constexpr int LOG_P = MAXP == 8 ? 3 : (MAXP == 4 ? 2 : 1);
+    constexpr int DUP = LOG_LPT - LOG_P;
+    const int sub = lane % LPT, grp = lane / LPT;
+    const int mypass = sub >> DUP;
+    const bool owner = (sub & ((1 << DUP) - 1)) == 0;
+    const int ch = bs < 16 ? bs : 16;
+    const int npc = ch / TPP;
+    for (int c0 = 0; c0 < bs; c0 += ch) {
+        if (c0 >= valid) break;
+        float part[G][MAXP];
+#pragma unroll
+        for (int p = 0; p < MAXP; ++p) {
+            if (p < npc) {
+                const int t = c0 + p * TPP + grp;
+                float kf[8];
+                load8<KVT>(ks + (t * D + sub * 8) * EB, kf);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) ffma2(d0, d1, qf[g][e], qf[g][e + 1], kf[e], kf[e + 1]);
+                    part[g][p] = d0 + d1;
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < G; ++g) part[g][p] = 0.f;
+            }
+        }
+        // reduce-scatter over the LPT lanes of a token
+        float sc[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+            for (int lv = 0; lv < LOG_P; ++lv) {
+                const int S = LPT >> (lv + 1); // partner distance
+                const int C = MAXP >> lv;      // values still held
+                const bool upper = (sub & S) != 0;
+#pragma unroll
+                for (int i = 0; i < C / 2; ++i) {
+                    const float a = part[g][i], b = part[g][i + C / 2];
+                    const float recv = __shfl_xor_sync(0xffffffffu, upper ? a : b, S);
+                    part[g][i] = (upper ? b : a) + recv;
+                }
+            }
+            float v = part[g][0];
+#pragma unroll
+            for (int o = (1 << DUP) >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            sc[g] = (c0 + mypass * TPP + grp) < valid ? v : -INFINITY;
+        }
+        // online softmax per head; the chunk's scores are spread one per lane
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float mx = sc[g];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float mn = fmaxf(m[g], mx); // finite: the chunk holds at least one live token
+            const float alpha = fast_exp2(m[g] - mn);
+            m[g] = mn;
+            const float pr = fast_exp2(sc[g] - mn);
+            sc[g] = pr;
+            l[g] = l[g] * alpha + (owner ? pr : 0.f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+        }
+#pragma unroll
+        for (int p = 0; p < MAXP; ++p) {
+            if (p < npc) {
+                const int t = c0 + p * TPP + grp;
+                const int src = grp * LPT + (p << DUP);
+                float w[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) w[g] = __shfl_sync(0xffffffffu, sc[g], src);
+                if (t < valid) {
+                    float vf[8];
+                    load8<KVT>(vs + (t * D + sub * 8) * EB, vf);
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) ffma2(acc[g][e], acc[g][e + 1], w[g], w[g], vf[e], vf[e + 1]);
+                }
+            }
+        }
+    }
+}
+
 template <int D, int G, int MT, int KVT>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     using M = ModelT<MT>;
@@ -325,9 +427,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     }
 
     // -------------------------------------------------------------------- consumer warps
+    // G == 1: Lanes<D, 1> layout (D/8 lanes per token, 8 dims each); G >= 2: token-parallel lanes
+    // (process_tile_tp), each lane carrying all G heads.
     using LY = Lanes<D, G>;
-    constexpr int DL = LY::DL, LH = LY::LH, LT = LY::LT;
-    const int sub = lane % LH, gl = (lane / LH) % G, tg = lane / LT;
+    constexpr int DL = (G == 1) ? LY::DL : 8;
+    constexpr int LH = (G == 1) ? LY::LH : D / 8;
+    constexpr int LT = (G == 1) ? LY::LT : D / 8;
+    constexpr int GS = (G == 1) ? 1 : G; // heads a lane carries
+    const int sub = lane % LH, gl = (G == 1) ? 0 : 0, tg = lane / LT;
     const int tid = threadIdx.x; // 0 .. NCW*32-1
     uint32_t tau = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x) {
@@ -335,17 +442,23 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
         const int L = a.lens[un.s];
         float qs = a.qk_scale_log2;
         if constexpr (KVT == PKV_FP8_E4M3) qs *= a.k_scale[un.kvh];
-        float qf[DL];
-        {
-            const T *qp = static_cast<const T *>(a.q) + ((int64_t)un.s * a.hq + un.kvh * G + gl) * D + sub * DL;
+        float qf[GS][DL];
 #pragma unroll
-            for (int c = 0; c < DL / 8; ++c) cvt8<MT>(reinterpret_cast<const uint4 *>(qp)[c], qf + 8 * c);
+        for (int g = 0; g < GS; ++g) {
+            const T *qp = static_cast<const T *>(a.q) + ((int64_t)un.s * a.hq + un.kvh * G + g + gl) * D + sub * DL;
 #pragma unroll
-            for (int e = 0; e < DL; ++e) qf[e] *= qs;
+            for (int c = 0; c < DL / 8; ++c) cvt8<MT>(reinterpret_cast<const uint4 *>(qp)[c], qf[g] + 8 * c);
+#pragma unroll
+            for (int e = 0; e < DL; ++e) qf[g][e] *= qs;
         }
-        float m = -INFINITY, l = 0.f, acc[DL];
+        float m[GS], l[GS], acc[GS][DL];
 #pragma unroll
-        for (int e = 0; e < DL; ++e) acc[e] = 0.f;
+        for (int g = 0; g < GS; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+#pragma unroll
+            for (int e = 0; e < DL; ++e) acc[g][e] = 0.f;
+        }
         // Tile t of the CTA's stream (t counted over all its units) belongs to warp t % NCW and
         // sits in stage t % NST with NST a multiple of NCW, so a warp's previous tile in any stage
         // is its own: when it waits for phase k of a stage, phase k-1 has completed, which keeps
@@ -363,26 +476,41 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
             if (!flags[stage]) {
                 const char *ks = ring + (size_t)stage * 2 * a.tile_bytes;
                 const int valid = min(a.bs, L - (un.blk0 + i) * a.bs);
-                process_tile<D, G, KVT>(ks, ks + a.tile_bytes, a.bs, valid, qf, m, l, acc, lane);
+                if constexpr (G == 1)
+                    process_tile<D, 1, KVT>(ks, ks + a.tile_bytes, a.bs, valid, qf[0], m[0], l[0], acc[0], lane);
+                else
+                    process_tile_tp<D, G, KVT>(ks, ks + a.tile_bytes, a.bs, valid, qf, m, l, acc, lane);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
         }
         tau += un.ntiles;
-        // combine the token groups of this warp (same head, same dims)
+        // combine the token groups of this warp (same heads, same dims); for G >= 2 the row sums are
+        // spread over all lanes
 #pragma unroll
-        for (int o = LT; o < 32; o <<= 1) {
-            l += __shfl_xor_sync(0xffffffffu, l, o);
+        for (int g = 0; g < GS; ++g) {
+            if constexpr (G == 1) {
 #pragma unroll
-            for (int e = 0; e < DL; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+                for (int o = LT; o < 32; o <<= 1) l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
+            } else {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
+            }
+#pragma unroll
+            for (int o = LT; o < 32; o <<= 1)
+#pragma unroll
+                for (int e = 0; e < DL; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
         }
         if (tg == 0) {
-            float *r = mrg + (warp * G + gl) * (D + 2);
 #pragma unroll
-            for (int e = 0; e < DL; ++e) r[sub * DL + e] = acc[e];
-            if (sub == 0) {
-                r[D] = m;
-                r[D + 1] = l;
+            for (int g = 0; g < GS; ++g) {
+                float *r = mrg + (warp * G + g + gl) * (D + 2);
+#pragma unroll
+                for (int e = 0; e < DL; ++e) r[sub * DL + e] = acc[g][e];
+                if (sub == 0) {
+                    r[D] = m[g];
+                    r[D + 1] = l[g];
+                }
             }
         }
         named_barrier_sync(1, NCW * 32);

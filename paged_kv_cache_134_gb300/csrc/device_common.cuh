@@ -112,6 +112,15 @@ PKV_DEV float fast_exp2(float x) {
     return y;
 }
 
+// (a0, a1) += (x0, x1) * (y0, y1) as one packed fp32 FMA; each half is an IEEE fma, round to nearest
+PKV_DEV void ffma2(float &a0, float &a1, float x0, float x1, float y0, float y1) {
+    asm("{\n\t.reg .b64 ra, rx, ry;\n\t"
+        "mov.b64 ra, {%0, %1};\n\tmov.b64 rx, {%2, %3};\n\tmov.b64 ry, {%4, %5};\n\t"
+        "fma.rn.f32x2 ra, rx, ry, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
+
 // ------------------------------------------------------------------ element conversions
 
 template <int DT>
