@@ -82,7 +82,13 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
     // stages: fill the per-CTA shared-memory budget
     const size_t fixed = smem_bytes(c->head_dim, G, 0, a.tile_bytes, d.num_seqs);
     const size_t per_stage = smem_bytes(c->head_dim, G, 1, a.tile_bytes, d.num_seqs) - fixed;
-    const int want = ctas_per_sm();
+    // CTAs per SM: the target, or fewer when registers allow fewer (grouped heads); the stage ring
+    // then takes that many CTAs' share of shared memory, so the bytes in flight per SM stay high
+    int want = ctas_per_sm();
+    {
+        const int fit = occ(c->head_dim, G, smem_bytes(c->head_dim, G, kConsumerWarps, a.tile_bytes, d.num_seqs));
+        if (fit >= 1 && fit < want) want = fit;
+    }
     const size_t budget = (size_t)(233472 / want) - 1024;
     int nst = budget > fixed ? static_cast<int>((budget - fixed) / per_stage) : 0;
     nst = env_int("PAGEDKV_DECODE_STAGES", nst);
