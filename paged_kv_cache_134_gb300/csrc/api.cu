@@ -150,6 +150,7 @@ int kv_cache_destroy(pkv_cache_t c) {
     if (c->k_scale) cudaFree(c->k_scale);
     if (c->v_scale) cudaFree(c->v_scale);
     if (c->ws) cudaFree(c->ws);
+    if (c->plan) cudaFree(c->plan);
     for (auto &ev : c->events) {
         cudaEventDestroy(ev.a);
         cudaEventDestroy(ev.b);

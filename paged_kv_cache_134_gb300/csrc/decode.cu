@@ -79,6 +79,25 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
     DecodeFn fn;
     OccFn occ;
     pick(c, &fn, &occ);
+    cudaError_t e;
+    if (pkv_decode_tc_eligible(c, G, d.num_seqs)) {
+        a.nstages = 0;
+        // longer splits than the CUDA-core kernel's: a unit then spans several 128-token MMA steps,
+        // which spreads the per-unit work (Q load, epilogue, partial write) over more bytes; the
+        // workspace, sized for the default split, only gets more room
+        const int tc_blocks = env_int("PAGEDKV_SPLIT_TOKENS_TC", 512) / c->block_size;
+        if (tc_blocks > a.split_blocks) a.split_blocks = tc_blocks;
+        {
+            PkvTimer timer(c, PKV_KIND_DECODE, st);
+            e = pkv_decode_tc_launch(c, a, d.q, G, st);
+            g_pkv_launches++;
+        }
+        if (e != cudaSuccess) return e;
+        PkvTimer timer(c, PKV_KIND_MERGE, st);
+        e = fn(a, c->head_dim, G, 0, 0, st, true);
+        g_pkv_launches++;
+        return e;
+    }
     // stages: fill the per-CTA shared-memory budget
     const size_t fixed = smem_bytes(c->head_dim, G, 0, a.tile_bytes, d.num_seqs);
     const size_t per_stage = smem_bytes(c->head_dim, G, 1, a.tile_bytes, d.num_seqs) - fixed;
@@ -101,7 +120,6 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
     int per_sm = occ(c->head_dim, G, smem);
     if (per_sm < 1) per_sm = 1;
     const int grid = c->num_sms * per_sm;
-    cudaError_t e;
     {
         PkvTimer timer(c, PKV_KIND_DECODE, st);
         e = fn(a, c->head_dim, G, grid, smem, st, false);

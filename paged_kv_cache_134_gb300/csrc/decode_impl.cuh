@@ -306,36 +306,12 @@ PKV_DEV void process_tile_tp(const char *ks, const char *vs, int bs, int valid, 
     }
 }
 
-template <int D, int G, int MT, int KVT>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
-    using M = ModelT<MT>;
-    using T = typename M::T;
-    constexpr int NCW = kConsumerWarps;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int NST = a.nstages;
-    const int S = a.num_seqs;
-    char *ring = reinterpret_cast<char *>(smem);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NST * 2 * a.tile_bytes);
-    uint64_t *empty = full + NST;
-    int *flags = reinterpret_cast<int *>(empty + NST);
-    int *abort_flag = flags + NST;
-    float *mrg = reinterpret_cast<float *>(abort_flag + 4);
-    int *pf = reinterpret_cast<int *>(mrg + NCW * G * (D + 2));
-    int *pp = pf + (S + 1);
-    int *nb = pp + (S + 1);
-
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
-        }
-        *abort_flag = 0;
-        fence_mbarrier_init();
-    }
-    pdl_wait(); // the previous kernel (e.g. the append of this step) has finished
-    // unit list: per sequence, full splits and (0 or 1) partial split
-    const int bps = a.split_blocks;
+// Unit list, built by the whole CTA into shared memory: per sequence its block count nb[s], and
+// prefix counts of full splits (pf) and of partial tail splits (pp, 0 or 1 per sequence), so that
+// unit u resolves to (sequence, KV head, split) with two binary searches (unit_info).  Sequences
+// longer than the table allows are clamped and reported.
+PKV_DEV void build_unit_list(const Args &a, int *pf, int *pp, int *nb, int warp, int lane) {
+    const int S = a.num_seqs, bps = a.split_blocks;
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
         const int L = a.lens[s];
         int n = L > 0 ? (L + a.bs - 1) / a.bs : 0;
@@ -374,6 +350,38 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
         }
     }
     __syncthreads();
+}
+
+template <int D, int G, int MT, int KVT>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
+    using M = ModelT<MT>;
+    using T = typename M::T;
+    constexpr int NCW = kConsumerWarps;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int NST = a.nstages;
+    const int S = a.num_seqs;
+    char *ring = reinterpret_cast<char *>(smem);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NST * 2 * a.tile_bytes);
+    uint64_t *empty = full + NST;
+    int *flags = reinterpret_cast<int *>(empty + NST);
+    int *abort_flag = flags + NST;
+    float *mrg = reinterpret_cast<float *>(abort_flag + 4);
+    int *pf = reinterpret_cast<int *>(mrg + NCW * G * (D + 2));
+    int *pp = pf + (S + 1);
+    int *nb = pp + (S + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    pdl_wait(); // the previous kernel (e.g. the append of this step) has finished
+    const int bps = a.split_blocks;
+    build_unit_list(a, pf, pp, nb, warp, lane);
     const int U = (pf[S] + pp[S]) * a.hkv;
 
     if (warp == NCW) {

@@ -1,0 +1,498 @@
+// Paged decode attention for grouped-query heads on the 5th-generation tensor cores.
+//
+// What it computes is the decode of "PagedAttention 与前缀缓存" (2kiu.com, section 2.3), the same
+// as decode_impl.cuh: for sequence s and query head h, softmax(scale q.K_t) weighted sum of V_t
+// over the L_s tokens of the sequence, token t in physical block block_table[s][t / bs] at offset
+// t % bs, query head h reading KV head h / G.  With G query heads per KV head every K/V element
+// meets G queries, so the CUDA-core kernel runs out of issue slots long before HBM runs out of
+// bandwidth; here the two contractions go to tcgen05 instead, transposed so that the token axis
+// fills the MMA's M = 128 rows:
+//   S^T [128 tokens x 16] = K [128 tokens x D] . Q^T [D x 16]      (heads padded from G to 16)
+//   O^T [D x 16]         += V^T [D x 128 tokens] . P^T [128 tokens x 16]
+// K and V come straight from the paged pool by tiled TMA (one box of bs rows x 64 dims per block
+// and half of D, 128-byte swizzle), landing in the K-major layout the first MMA reads as A and the
+// MN-major layout the second MMA reads as A.  Q sits in shared memory K-major, P is written there
+// by the softmax threads.  Accumulators live in tensor memory.
+//
+// Work unit = (sequence, KV head, split of up to split_blocks blocks), the same unit list as the
+// CUDA-core kernel (full splits first), round-robin over one persistent CTA per SM.  A unit is
+// processed in steps of 128 tokens.  Roles:
+//   warp 0     loads: block-table entries (one lane per block of the step), Q of the unit, and the
+//              K and V boxes of every block into rings of 3 K and 3 V stages;
+//   warp 1     tensor-memory owner and MMA issuer (one thread);
+//   warps 2-5  one thread per token row of S^T (a TMEM lane): mask, scale, tile max over the 128
+//              rows (shuffles + shared memory), online softmax with a lazily moved base (the base
+//              changes only when a head's max grows by more than 2^8, exact algebra), P written to
+//              shared memory (fp16; bf16 models as hi + lo so that P keeps ~16 bits); rows that are
+//              masked get their V row zeroed so that no NaN from an unused slot reaches the MMA;
+//              at the end of a unit one thread per dimension reads O^T and writes the output row
+//              (one split) or the fp32 partial (m, l, o) for the split merge.
+// Every mbarrier wait is bounded; a timeout sets PKV_DEVERR_TIMEOUT and the CTA winds down.
+#pragma once
+
+#include "decode_impl.cuh"
+#include "tcgen05.cuh"
+
+namespace pkv_decode_tc {
+
+using pkv_decode::Args;
+using pkv_decode::Unit;
+
+constexpr int D = 128;
+constexpr int TOK = 128;             // tokens per step: MMA M of S^T, MMA K of O^T
+constexpr int NQ = 16;               // MMA N: the group's query heads, padded
+constexpr int NS = 3;                // K stages and V stages
+constexpr int kThreads = 192;        // warp 0 loads, warp 1 MMA, warps 2-5 softmax
+constexpr uint32_t kTmemCols = 64;   // S0 [0,16) S1 [16,32) O [32,48)
+constexpr float kRescale = 8.0f;     // log2 units
+
+template <int MT>
+struct Layout {
+    static constexpr int NP = MT == PKV_BF16 ? 2 : 1;      // P tiles (hi, lo for bf16)
+    static constexpr int STAGE = TOK * D * 2;              // [half][128 rows][128 B] = 32 KB
+    static constexpr int K0 = 0;
+    static constexpr int V0 = K0 + NS * STAGE;
+    static constexpr int Q = V0 + NS * STAGE;              // [2 buffers][half][16 rows][128 B]
+    static constexpr int Q_BYTES = NQ * D * 2;
+    static constexpr int P = Q + 2 * Q_BYTES;                  // [buffer][part][64-token chunk][16 rows][128 B]
+    static constexpr int P_BYTES = NQ * TOK * 2;
+    static constexpr int RED = P + 2 * NP * P_BYTES;       // [2][4 warps][NQ] maxima, [4 warps][NQ] sums
+    static constexpr int BAR = RED + (3 * 4 * NQ) * 4;
+    static constexpr int FIXED = BAR + 512;                // + unit tables, 3 (S + 1) ints
+};
+
+inline size_t smem_bytes(int mt, int num_seqs) {
+    const size_t fixed = mt == PKV_BF16 ? Layout<PKV_BF16>::FIXED : Layout<PKV_F16>::FIXED;
+    return fixed + (size_t)3 * (num_seqs + 1) * sizeof(int);
+}
+
+// one packed pair of the model dtype from two floats (round-to-nearest-even), `lo` in the low half
+template <int MT>
+PKV_DEV uint32_t pack2(float lo, float hi) {
+    uint32_t r;
+    if constexpr (MT == PKV_BF16)
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// byte offset of element (row g, token t) in a P tile: K-major, 128-byte swizzle, 64-token chunks
+PKV_DEV int p_offset(int g, int t) {
+    const int e = t & 63;
+    return (t >> 6) * (NQ * 128) + (g >> 3) * 1024 + (g & 7) * 128 + ((((e >> 3) ^ (g & 7))) << 4) + ((e & 7) << 1);
+}
+
+template <int G, int MT>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tq, const Args a) {
+    using LY = Layout<MT>;
+    using M = ModelT<MT>;
+    using T = typename M::T;
+    extern __shared__ __align__(1024) uint8_t smem[];
+
+    const int S = a.num_seqs;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + LY::BAR);
+    uint64_t *k_full = bars, *k_empty = bars + NS, *v_full = bars + 2 * NS, *v_empty = bars + 3 * NS;
+    uint64_t *s_full = bars + 4 * NS, *s_free = s_full + 2, *p_full = s_full + 4, *t_full = s_full + 6;
+    uint64_t *q_full = s_full + 8, *q_empty = s_full + 10, *o_full = s_full + 12, *o_free = s_full + 13;
+    uint64_t *fin = s_full + 14;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(fin + 2);
+    volatile uint32_t *badmask = reinterpret_cast<volatile uint32_t *>(fin + 3); // [NS]
+    float *red_max = reinterpret_cast<float *>(smem + LY::RED);                  // [2][4][NQ]
+    float *red_sum = red_max + 2 * 4 * NQ;                                      // [4][NQ]
+    int *pf = reinterpret_cast<int *>(smem + LY::FIXED);
+    int *pp = pf + (S + 1);
+    int *nb = pp + (S + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(k_full + i, 1);
+            mbar_init(k_empty + i, 1);
+            mbar_init(v_full + i, 1);
+            mbar_init(v_empty + i, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(s_full + b, 1);
+            mbar_init(s_free + b, 128);
+            mbar_init(p_full + b, 128);
+            mbar_init(t_full + b, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(q_full + b, 1);
+            mbar_init(q_empty + b, 1);
+        }
+        mbar_init(o_full, 1);
+        mbar_init(o_free, 128);
+        mbar_init(fin, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    // Q rows past the group stay zero (the MMA's padding heads)
+    for (int i = threadIdx.x; i < 2 * LY::Q_BYTES / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(smem + LY::Q)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait(); // the previous kernel (e.g. the append of this step) has finished
+    const int bps = a.split_blocks;
+    pkv_decode::build_unit_list(a, pf, pp, nb, warp, lane);
+    const int U = (pf[S] + pp[S]) * a.hkv;
+    const int bpstep = TOK / a.bs; // blocks per step
+    auto fail = [&]() {
+        set_error(a.err, PKV_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- loads
+        const uint64_t policy = l2_policy_evict_first();
+        if (lane == 0) {
+            tc::prefetch_tmap(&tkv);
+            tc::prefetch_tmap(&tq);
+        }
+        int64_t gs = 0; // steps issued so far, all units
+        int nu = 0, last_q = -1;
+        bool ok = true;
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
+            const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps);
+            if (lane == 0) {
+                // Q of unit nu goes to buffer nu % 2, free once the last S^T of unit nu - 2 is done
+                const int qb = nu & 1;
+                if (nu >= 2 && !mbar_wait(q_empty + qb, ((nu >> 1) - 1) & 1)) ok = false;
+                if (ok) {
+                    mbar_arrive_expect_tx(q_full + qb, (uint32_t)(G * D * 2));
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tc::tma_load_2d(smem + LY::Q + qb * LY::Q_BYTES + c * NQ * 128, &tq, c * 64,
+                                        un.s * a.hq + un.kvh * G, q_full + qb);
+                    last_q = nu;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            const int32_t *trow = a.tables + (int64_t)un.s * a.max_blocks + un.blk0;
+            const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
+            for (int i = 0; i < nsteps && ok; ++i, ++gs) {
+                const int st = (int)(gs % NS);
+                const int64_t round = gs / NS;
+                const int nblk = min(bpstep, un.ntiles - i * bpstep);
+                const int b = lane < nblk ? trow[i * bpstep + lane] : 0;
+                const bool good = lane < nblk && b >= 0 && b < a.num_blocks;
+                const unsigned goodmask = __ballot_sync(0xffffffffu, good);
+                const unsigned bad = __ballot_sync(0xffffffffu, lane < nblk && !good);
+                const uint32_t bytes = (uint32_t)__popc(goodmask) * (uint32_t)a.bs * (D * 2);
+                if (lane == 0) {
+                    if (bad) set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                    if (round >= 1 && !mbar_wait(k_empty + st, (round - 1) & 1)) ok = false;
+                    if (ok) mbar_arrive_expect_tx(k_full + st, bytes);
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok || *abort_flag) break;
+                // row of (block b, K or V, KV head) in the pool's [rows][D] view
+                const int krow = ((b * 2 + 0) * a.hkv + un.kvh) * a.bs, vrow = ((b * 2 + 1) * a.hkv + un.kvh) * a.bs;
+                if (good) {
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tc::tma_load_2d_hint(smem + LY::K0 + st * LY::STAGE + c * (TOK * 128) + lane * a.bs * 128, &tkv,
+                                             c * 64, krow, k_full + st, policy);
+                }
+                if (lane == 0) {
+                    if (round >= 1 && !mbar_wait(v_empty + st, (round - 1) & 1)) ok = false;
+                    if (ok) {
+                        badmask[st] = bad; // read by the softmax after v_full, freed with v_empty
+                        mbar_arrive_expect_tx(v_full + st, bytes);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                if (good) {
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tc::tma_load_2d_hint(smem + LY::V0 + st * LY::STAGE + c * (TOK * 128) + lane * a.bs * 128, &tkv,
+                                             c * 64, vrow, v_full + st, policy);
+                }
+            }
+        }
+        if (!ok && lane == 0) fail();
+        // the next kernel (the split merge) may start launching once every CTA has issued its last load
+        pdl_trigger();
+        // the copies of the last stages must land before this CTA's shared memory goes away
+        if (lane == 0) {
+            for (int64_t g = gs > NS ? gs - NS : 0; g < gs; ++g) {
+                if (!mbar_wait(k_full + g % NS, (g / NS) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+                if (!mbar_wait(v_full + g % NS, (g / NS) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            }
+            for (int n = last_q > 0 ? last_q - 1 : 0; n <= last_q; ++n)
+                if (!mbar_wait(q_full + (n & 1), (n >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t ab = MT == PKV_BF16 ? 1u : 0u;
+            constexpr uint32_t ISK = tc::idesc_f16_ab(ab, 0u, 0u, TOK, NQ); // A = K (K-major), B = Q (K-major)
+            constexpr uint32_t IPV = tc::idesc_f16_ab(ab, 1u, 0u, D, NQ);   // A = V^T (MN-major), B = P (K-major)
+            const uint32_t sK = smem_u32(smem + LY::K0), sV = smem_u32(smem + LY::V0);
+            const uint32_t sQ = smem_u32(smem + LY::Q), sP = smem_u32(smem + LY::P);
+            const uint32_t tO = tmem + 2 * NQ;
+            bool any_mma = false;
+            // S^T of step g (Q buffer qb) into S buffer g % 2; the K stage is released as soon as S^T is done
+            auto issue_s = [&](int64_t g, int qb) -> bool {
+                const int st = (int)(g % NS), b = (int)(g & 1);
+                if (!mbar_wait(k_full + st, (g / NS) & 1)) return false;
+                if (g >= 2 && !mbar_wait(s_free + b, ((g >> 1) - 1) & 1)) return false;
+                tc::fence_after_sync();
+                any_mma = true;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const int c = k >> 2, kk = k & 3;
+                    const uint64_t ad = tc::smem_desc(sK + st * LY::STAGE + c * (TOK * 128) + kk * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc(sQ + qb * LY::Q_BYTES + c * (NQ * 128) + kk * 32, 16, 1024);
+                    tc::mma_f16(tmem + b * NQ, ad, bd, ISK, k > 0 ? 1u : 0u);
+                }
+                tc::commit(s_full + b);
+                tc::commit(k_empty + st);
+                return true;
+            };
+            bool ok = true;
+            int64_t gs = 0;
+            int nu = 0;
+            for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
+                const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps);
+                const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
+                const int qb = nu & 1;
+                ok = mbar_wait(q_full + qb, (nu >> 1) & 1) && issue_s(gs, qb);
+                for (int i = 0; i < nsteps && ok; ++i) {
+                    const int64_t g = gs + i;
+                    if (i + 1 < nsteps) {
+                        ok = issue_s(g + 1, qb);
+                        if (!ok) break;
+                    } else {
+                        tc::commit(q_empty + qb); // the unit's last S^T has been issued: its Q buffer may be refilled
+                    }
+                    const int st = (int)(g % NS), b = (int)(g & 1);
+                    ok = mbar_wait(p_full + b, (g >> 1) & 1) && mbar_wait(v_full + st, (g / NS) & 1);
+                    // the epilogue of the previous unit has read O^T out of tensor memory
+                    if (ok && i == 0 && nu >= 1) ok = mbar_wait(o_free, (nu - 1) & 1);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int part = 0; part < LY::NP; ++part)
+#pragma unroll
+                        for (int k = 0; k < TOK / 16; ++k) {
+                            const uint64_t ad = tc::smem_desc(sV + st * LY::STAGE + k * 2048, TOK * 128, 1024);
+                            const uint64_t bd = tc::smem_desc(
+                                sP + (b * LY::NP + part) * LY::P_BYTES + (k >> 2) * (NQ * 128) + (k & 3) * 32, 16, 1024);
+                            tc::mma_f16(tO, ad, bd, IPV, (i > 0 || k > 0 || part > 0) ? 1u : 0u);
+                        }
+                    tc::commit(t_full + b);
+                    tc::commit(v_empty + st);
+                    if (i + 1 == nsteps) tc::commit(o_full);
+                }
+                gs += nsteps;
+                if (*abort_flag) break;
+            }
+            if (!ok) fail();
+            // every MMA issued by this thread has completed before tensor memory is released
+            if (any_mma) {
+                tc::commit(fin);
+                if (!mbar_wait(fin, 0)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax and epilogue
+        const int lw = warp & 3;
+        const int r = lw * 32 + lane;                      // token row of S^T, then dimension of O^T
+        const uint32_t lane_off = static_cast<uint32_t>(lw * 32) << 16;
+        bool ok = true;
+        int64_t gs = 0;
+        int nu = 0;
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
+            const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps);
+            const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
+            const int L = a.lens[un.s];
+            const int tok0 = un.blk0 * a.bs;
+            const int tok_end = min(L, (un.blk0 + un.ntiles) * a.bs);
+            float m[G], lp[G]; // base (uniform over the CTA) and this thread's partial row sums
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                m[g] = -INFINITY;
+                lp[g] = 0.f;
+            }
+            // `ok` agreement: the four warps stop together, at a barrier (see named_barrier_and)
+            for (int i = 0; i < nsteps; ++i) {
+                const int64_t g0 = gs + i;
+                const int st = (int)(g0 % NS), b = (int)(g0 & 1);
+                bool mine = ok && *abort_flag == 0;
+                if (mine) mine = __all_sync(0xffffffffu, mbar_wait(s_full + b, (g0 >> 1) & 1) &&
+                                                             mbar_wait(v_full + st, (g0 / NS) & 1));
+                const int step0 = tok0 + i * TOK;
+                bool valid = false, ragged = false;
+                float sc[G];
+                if (mine) {
+                    tc::fence_after_sync();
+                    uint32_t sr[G];
+                    tc::ldn<G>(tmem + lane_off + b * NQ, sr);
+                    tc::wait_ld();
+                    tc::fence_before_sync();
+                    mbar_arrive(s_free + b);
+                    const uint32_t bm = badmask[st];
+                    valid = step0 + r < tok_end && !((bm >> (r / a.bs)) & 1u);
+                    ragged = step0 + TOK > tok_end || bm != 0u;
+                    // tile max per head over the 128 rows: warp shuffles, then the 4 warps via shared memory
+                    float tmx[G];
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        sc[g] = valid ? __uint_as_float(sr[g]) * a.qk_scale_log2 : -INFINITY;
+                        float v = sc[g];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                        tmx[g] = v;
+                    }
+                    if (lane < G) {
+                        float v = tmx[0];
+#pragma unroll
+                        for (int g = 1; g < G; ++g)
+                            if (lane == g) v = tmx[g];
+                        red_max[(int)(g0 & 1) * 4 * NQ + lw * NQ + lane] = v;
+                    }
+                }
+                ok = named_barrier_and(1, 128, mine);
+                if (!ok) break;
+                const float *rm = red_max + (int)(g0 & 1) * 4 * NQ;
+                bool moved = false;
+                float alpha[G], p[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float t = fmaxf(fmaxf(rm[g], rm[NQ + g]), fmaxf(rm[2 * NQ + g], rm[3 * NQ + g]));
+                    const bool up = t > m[g] + kRescale; // false while t = -inf
+                    alpha[g] = up ? fast_exp2(m[g] - t) : 1.f;
+                    if (up) m[g] = t;
+                    moved |= up;
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    p[g] = valid ? fast_exp2(sc[g] - m[g]) : 0.f;
+                    lp[g] = lp[g] * alpha[g] + p[g];
+                }
+                // P buffer b is free once P V of step g0 - 2 is done; O^T is stable once P V of g0 - 1 is
+                if (g0 >= 2) ok = __all_sync(0xffffffffu, mbar_wait(t_full + b, ((g0 >> 1) - 1) & 1));
+                if (ok && moved && i > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(t_full + (b ^ 1), ((g0 - 1) >> 1) & 1));
+                    if (ok) {
+                        tc::fence_after_sync();
+                        uint32_t o[G];
+                        tc::ldn<G>(tmem + lane_off + 2 * NQ, o);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int g = 0; g < G; ++g) o[g] = __float_as_uint(__uint_as_float(o[g]) * alpha[g]);
+                        tc::stn<G>(tmem + lane_off + 2 * NQ, o);
+                        tc::wait_st();
+                    }
+                }
+                // a warp that failed here carries ok = false to the next barrier
+                if (!ok) continue;
+                uint8_t *pb = smem + LY::P + b * LY::NP * LY::P_BYTES;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const int off = p_offset(g, r);
+                    if constexpr (LY::NP == 2) {
+                        const uint32_t hi = pack2<MT>(p[g], 0.f) & 0xFFFFu;
+                        const float rest = p[g] - __uint_as_float(hi << 16);
+                        *reinterpret_cast<uint16_t *>(pb + off) = (uint16_t)hi;
+                        *reinterpret_cast<uint16_t *>(pb + LY::P_BYTES + off) = (uint16_t)(pack2<MT>(rest, 0.f) & 0xFFFFu);
+                    } else {
+                        *reinterpret_cast<uint16_t *>(pb + off) = (uint16_t)(pack2<MT>(p[g], 0.f) & 0xFFFFu);
+                    }
+                }
+                if (ragged && !valid) {
+                    // this row's V is an unused slot (or a stale stage row): zero it for the MMA
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
+                        uint4 *vr = reinterpret_cast<uint4 *>(smem + LY::V0 + st * LY::STAGE + c * (TOK * 128) + r * 128);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) vr[e] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc::fence_before_sync();
+                mbar_arrive(p_full + b);
+            }
+            gs += nsteps;
+            // ---- epilogue: thread r holds dimension r of the G output rows
+            bool mine = ok && *abort_flag == 0;
+            if (mine) mine = __all_sync(0xffffffffu, mbar_wait(o_full, nu & 1));
+            uint32_t o[G];
+            if (mine) {
+                tc::fence_after_sync();
+                tc::ldn<G>(tmem + lane_off + 2 * NQ, o);
+                tc::wait_ld();
+                tc::fence_before_sync();
+                mbar_arrive(o_free); // the next unit's first P V may overwrite O^T
+                float lt[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float v = lp[g];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                    lt[g] = v;
+                }
+                if (lane < G) {
+                    float v = lt[0];
+#pragma unroll
+                    for (int g = 1; g < G; ++g)
+                        if (lane == g) v = lt[g];
+                    red_sum[lw * NQ + lane] = v;
+                }
+            }
+            ok = named_barrier_and(1, 128, mine);
+            if (!ok) break;
+            float lt[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                lt[g] = (red_sum[g] + red_sum[NQ + g]) + (red_sum[2 * NQ + g] + red_sum[3 * NQ + g]);
+            named_barrier_sync(1, 128); // red_sum is rewritten by the next unit
+            const int h0 = un.kvh * G;
+            if (un.nsplit == 1) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float y = lt[g] > 0.f ? __uint_as_float(o[g]) / lt[g] : 0.f;
+                    static_cast<T *>(a.out)[((int64_t)un.s * a.hq + h0 + g) * D + r] = M::from_f(y);
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const int64_t idx = ((int64_t)un.s * a.hq + h0 + g) * a.max_splits + un.j;
+                    a.ws_o[idx * D + r] = __uint_as_float(o[g]);
+                    if (r == 0) reinterpret_cast<float2 *>(a.ws_ml)[idx] = make_float2(m[g], lt[g]);
+                }
+            }
+        }
+        if (!ok) fail();
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int G, int MT>
+cudaError_t launch(const CUtensorMap &tkv, const CUtensorMap &tq, const Args &a, int grid, size_t smem,
+                   cudaStream_t st) {
+    auto kern = decode_tc_kernel<G, MT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return pdl_launch(kern, dim3(grid), dim3(kThreads), smem, st, tkv, tq, a);
+}
+
+} // namespace pkv_decode_tc

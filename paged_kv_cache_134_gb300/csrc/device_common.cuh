@@ -104,6 +104,22 @@ PKV_DEV void named_barrier_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also ANDs a predicate over the participating threads: every thread leaves
+// with the same answer, so a group of warps can agree to stop together (a warp that left on its
+// own would leave the others waiting at the next barrier).
+PKV_DEV bool named_barrier_and(uint32_t id, uint32_t nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // ------------------------------------------------------------------ math
 
 PKV_DEV float fast_exp2(float x) {

@@ -1,6 +1,7 @@
 // Host-side internals shared by the translation units of the library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -26,6 +27,9 @@ struct pkv_cache {
     // split-K workspace of the decode
     float *ws = nullptr;
     int64_t ws_bytes = 0;
+    // work list of the packed prefill (item count, next-item counter, (sequence, query tile) pairs)
+    int *plan = nullptr;
+    int64_t plan_bytes = 0;
     int num_sms = 0;
     // profiling
     bool profiling = false;
@@ -97,6 +101,12 @@ struct DecodeLaunch {
 int64_t decode_workspace_floats(const pkv_cache *c, int num_seqs, int num_q_heads, int max_splits);
 int decode_split_blocks(const pkv_cache *c);
 cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st);
+// tensor-core decode for grouped-query heads (decode_tc.cu)
+namespace pkv_decode {
+struct Args;
+}
+bool pkv_decode_tc_eligible(const pkv_cache *c, int G, int num_seqs);
+cudaError_t pkv_decode_tc_launch(const pkv_cache *c, const pkv_decode::Args &a, const void *q, int G, cudaStream_t st);
 
 struct PrefillLaunch {
     const void *q, *k, *v;
@@ -108,3 +118,7 @@ struct PrefillLaunch {
     float scale;
 };
 cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st);
+
+// Tiled-TMA map of a row-major fp16/bf16 matrix [rows][cols]: box = 64 columns x box_rows rows,
+// 128-byte swizzle, out-of-range elements read as zero (prefill.cu).
+bool pkv_tmap_2d(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t cols, int box_rows);

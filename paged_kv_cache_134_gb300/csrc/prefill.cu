@@ -7,21 +7,30 @@
 // block_table[i][r / bs], offset r % bs (the prompt-phase write of section 4.2, bounded by the
 // sequence length so a partly filled tail block is never overrun).
 //
-// One CTA = (sequence, 128-query tile, query head).  Warp roles:
-//   warp 0     TMA producers: lane 0 loads the Q tile once and K tiles of 64 keys into a 2-stage ring,
-//              lane 1 V tiles into another (tiled TMA, 128-byte swizzle, out-of-range rows zero-filled);
-//              a K stage frees when S = Q K^T of its tile is done, a V stage when P V is done;
+// Work items are (sequence, 128-query tile, query head) triples.  A one-CTA plan kernel lists the
+// (sequence, query tile) pairs heaviest first; a persistent grid (as many CTAs as fit, two per SM
+// for fp16 models at D = 128) then takes items one at a time from an atomic counter, so an SM
+// whose item ends early starts the next one at once instead of waiting for the hardware to
+// dispatch a new CTA.  Warp roles inside a CTA:
+//   warp 0     lane 0: takes the next item and hands it to the other roles through a 2-entry ring
+//              in shared memory, then loads its Q tile and its K tiles of 64 keys into a 2-stage
+//              ring; lane 1 loads the V tiles into another 2-stage ring (tiled TMA, 128-byte
+//              swizzle, out-of-range rows zero-filled); a K stage frees when S = Q K^T of its tile is
+//              done and the writer warps have passed it, a V stage likewise after P V;
 //   warp 1     tensor-memory owner and MMA issuer (one thread): S = Q K^T into one of two TMEM S
 //              buffers (M=128, N=64, fp32), then O += P V into the TMEM O accumulator (M=128, N=D);
 //   warps 2-5  softmax, one thread per query row (TMEM lane = row): mask, exp2, row sums, P written
 //              to shared memory in the 128-byte-swizzled K-major layout the MMA reads (fp16 P for
-//              fp16 models; for bf16 models P = hi + lo, two bf16 tiles and two accumulating MMAs); O in TMEM is rescaled only when a row's running max grows by
-//              more than 2^8 (the exponent base stays fixed otherwise, which is exact algebra);
-//   warps 6-7  paged K/V writer for the tile's rows, straight from the K/V tiles already in shared
-//              memory (only the CTA of the first query head of each KV group writes, so every
-//              (token, KV head) is written once).
-// The diagonal tiles are masked per element; tiles entirely above the diagonal are never issued.
-// Every mbarrier wait is bounded; a timeout sets PKV_DEVERR_TIMEOUT and the CTA winds down.
+//              fp16 models; for bf16 models P = hi + lo, two bf16 tiles and two accumulating MMAs);
+//              O in TMEM is rescaled only when a row's running max grows by more than 2^8 (the
+//              exponent base stays fixed otherwise, which is exact algebra); then the epilogue;
+//   warps 6-7  paged K/V writer for the item's rows, straight from the K/V tiles already in shared
+//              memory as they land (only items of the first query head of each KV group write, so
+//              every (token, KV head) is written once).
+// Every barrier phase is counted across items (a global K/V tile counter, an item counter), so the
+// pipeline runs on from one item into the next.  The diagonal tiles are masked per element; tiles
+// entirely above the diagonal are never issued.  Every mbarrier wait is bounded; a timeout sets
+// PKV_DEVERR_TIMEOUT and the CTA winds down.
 #include <algorithm>
 #include <mutex>
 
@@ -42,6 +51,7 @@ struct Args {
     const int32_t *cu, *tables;
     char *pool;
     unsigned int *err;
+    int *plan;          // [0] item count, [1] next-item counter, [4 + 2i], [5 + 2i] = (sequence, query tile) of item i
     int64_t total_tokens, num_blocks, tile_elems;
     int num_seqs, max_seqlen, max_blocks, hq, hkv, bs, nqt_max;
     float scale_log2;
@@ -61,7 +71,7 @@ struct Layout {
     static constexpr int P = V0 + 2 * KV_BYTES;
     static constexpr int P_BYTES = BM * BN * 2;
     static constexpr int BAR = P + NP * P_BYTES;
-    static constexpr int TOTAL = BAR + 256;
+    static constexpr int TOTAL = BAR + 256; // 26 mbarriers / words + two 16-byte item slots
 };
 
 // two floats -> packed fp16/bf16 pair (round-to-nearest-even), `lo` in the low half
@@ -80,6 +90,111 @@ constexpr int min_blocks() {
     return 2 * (Layout<D, MT>::TOTAL + 1024) <= 233472 ? 2 : 1;
 }
 
+constexpr int kPlanThreads = 1024;
+constexpr int kItemConsumers = 8;  // V loader, MMA issuer, 4 softmax warps, 2 writer warps
+constexpr int kStageReleasers = 3; // a K or V stage frees after the MMA that reads it and both writer warps
+
+// query tiles of sequence i (0 for a malformed cu_seqlens entry, which is reported)
+PKV_DEV int seq_tiles(const Args &a, int i, bool report) {
+    const int st = a.cu[i], en = a.cu[i + 1];
+    if (st < 0 || en < st || en > a.total_tokens || en - st > a.max_seqlen) {
+        if (report) set_error(a.err, PKV_DEVERR_CU_SEQLENS);
+        return 0;
+    }
+    return (en - st + BM - 1) / BM;
+}
+
+// in-place inclusive prefix sum of x[0, n) by the whole CTA (kPlanThreads threads)
+PKV_DEV void cta_inclusive_scan(int *x, int n, int *warp_sums) {
+    const int per = (n + kPlanThreads - 1) / kPlanThreads;
+    const int b = min((int)threadIdx.x * per, n), e = min(b + per, n);
+    int own = 0;
+    for (int i = b; i < e; ++i) own += x[i];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int v = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    if (lane == 31) warp_sums[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        int u = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, u, o);
+            if (lane >= o) u += t;
+        }
+        warp_sums[lane] = u;
+    }
+    __syncthreads();
+    int run = v - own + (w > 0 ? warp_sums[w - 1] : 0);
+    for (int i = b; i < e; ++i) {
+        run += x[i];
+        x[i] = run;
+    }
+    __syncthreads();
+}
+
+// The work list.  Rank r holds every sequence's r-th heaviest query tile (its (nq-1-r)-th): with
+// gt[r] = #{i : nq_i > r} items in rank r, rank r starts at gt[0] + ... + gt[r-1].  Inside a rank
+// the order is whatever the atomics give; it only decides which CTA computes an item, never what
+// the item computes.  Also resets the next-item counter the attention kernel draws from.
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
+    extern __shared__ int sh[];
+    const int R = a.nqt_max + 1;
+    int *hist = sh;          // hist[c] = #{i : nq_i == c}, then rank starts
+    int *cnt = sh + R;       // items placed so far in each rank
+    int *warp_sums = sh + 2 * R;
+    pdl_trigger();
+    pdl_wait();
+    for (int x = threadIdx.x; x < R; x += kPlanThreads) {
+        hist[x] = 0;
+        cnt[x] = 0;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.num_seqs; i += kPlanThreads) atomicAdd(&hist[min(seq_tiles(a, i, true), a.nqt_max)], 1);
+    __syncthreads();
+    cta_inclusive_scan(hist, R, warp_sums);                             // hist[r] = #{i : nq_i <= r}
+    for (int x = threadIdx.x; x < R; x += kPlanThreads) hist[x] = a.num_seqs - hist[x]; // gt[r]
+    __syncthreads();
+    cta_inclusive_scan(hist, R, warp_sums);                             // hist[r] = gt[0] + ... + gt[r]
+    int2 *list = reinterpret_cast<int2 *>(a.plan + 4);
+    for (int i = threadIdx.x; i < a.num_seqs; i += kPlanThreads) {
+        const int nq = min(seq_tiles(a, i, false), a.nqt_max);
+        for (int r = 0; r < nq; ++r) {
+            const int pos = (r > 0 ? hist[r - 1] : 0) + atomicAdd(&cnt[r], 1);
+            list[pos] = make_int2(i, nq - 1 - r);
+        }
+    }
+    if (threadIdx.x == 0) {
+        a.plan[0] = hist[R - 1];
+        a.plan[1] = 0;
+    }
+}
+
+// one item as the roles see it
+struct Item {
+    int seq, qt, h; // seq < 0: no more items
+    int start, n, q0, qlast, nkv;
+};
+
+PKV_DEV Item decode_item(const Args &a, int4 raw) {
+    Item it;
+    it.seq = raw.x;
+    it.qt = raw.y;
+    it.h = raw.z;
+    if (it.seq >= 0) {
+        it.start = a.cu[it.seq];
+        it.n = a.cu[it.seq + 1] - it.start;
+        it.q0 = it.qt * BM;
+        it.qlast = min(it.q0 + BM, it.n) - 1;
+        it.nkv = it.qlast / BN + 1;
+    }
+    return it;
+}
+
 template <int D, int MT>
 __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -88,89 +203,35 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
     extern __shared__ __align__(1024) uint8_t smem[];
 
     pdl_trigger();
-    pdl_wait();
-    // ---- work item.  Items are (sequence, query tile) pairs, hq CTAs (one per query head) each, in
-    // rank order: rank r holds every sequence's r-th heaviest query tile (its (nq-1-r)-th), so the
-    // longest tiles start first.  The grid is sized from the packed token count (at most
-    // T/BM + num_seqs items), and each CTA finds its item from a histogram of per-sequence tile
-    // counts kept, for this prologue only, in the P buffer's shared memory.
-    int *nq = reinterpret_cast<int *>(smem + L::P);
-    int *hist = nq + a.num_seqs;          // [nqt_max + 1]
-    int *pick = hist + a.nqt_max + 1;     // seq, qt
-    for (int x = threadIdx.x; x <= a.nqt_max; x += blockDim.x) hist[x] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < a.num_seqs; i += blockDim.x) {
-        const int st = a.cu[i], en = a.cu[i + 1];
-        int c = 0;
-        if (st < 0 || en < st || en > a.total_tokens || en - st > a.max_seqlen) {
-            if (blockIdx.x == 0) set_error(a.err, PKV_DEVERR_CU_SEQLENS);
-        } else {
-            c = (en - st + BM - 1) / BM;
-        }
-        nq[i] = c;
-        atomicAdd(&hist[c], 1);
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        int k = blockIdx.x / a.hq, r = 0, above = a.num_seqs - hist[0]; // above = #{i : nq_i > r}
-        while (r < a.nqt_max && k >= above) {
-            k -= above;
-            ++r;
-            above -= hist[r];
-        }
-        int seq_found = -1;
-        if (r < a.nqt_max) {
-            for (int base = 0; base < a.num_seqs; base += 32) {
-                const int i = base + (int)threadIdx.x;
-                const unsigned bal = __ballot_sync(0xffffffffu, i < a.num_seqs && nq[i] > r);
-                const int cnt = __popc(bal);
-                if (k < cnt) {
-                    seq_found = base + (int)__fns(bal, 0, k + 1);
-                    break;
-                }
-                k -= cnt;
-            }
-        }
-        if (threadIdx.x == 0) {
-            pick[0] = seq_found;
-            pick[1] = seq_found >= 0 ? nq[seq_found] - 1 - r : -1;
-        }
-    }
-    __syncthreads();
-    const int seq = pick[0], qt = pick[1];
-    const int h = blockIdx.x % a.hq;
-    if (seq < 0) return;
-    const int start = a.cu[seq];
-    const int n = a.cu[seq + 1] - start;
     if (smem_u32(smem) & 1023u) return; // the swizzled tiles need 1024-byte alignment (always true)
-    const int G = a.hq / a.hkv;
-    const int kvh = h / G;
-    const int q0 = qt * BM;
-    const int qlast = min(q0 + BM, n) - 1;
-    const int nkv = qlast / BN + 1;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR);
-    uint64_t *q_full = bars + 0, *k_full = bars + 1, *v_full = bars + 3, *k_empty = bars + 5, *v_empty = bars + 7;
-    uint64_t *s_full = bars + 9, *s_free = bars + 11, *p_full = bars + 13, *t_full = bars + 14, *fin = bars + 15;
-    uint64_t *loaded = bars + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 18);
+    uint64_t *q_full = bars + 0, *q_empty = bars + 1, *k_full = bars + 2, *v_full = bars + 4;
+    uint64_t *k_empty = bars + 6, *v_empty = bars + 8, *s_full = bars + 10, *s_free = bars + 12;
+    uint64_t *p_full = bars + 14, *t_full = bars + 15, *o_free = bars + 16;
+    uint64_t *item_full = bars + 19, *item_empty = bars + 21, *fin = bars + 23;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 24);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 25);
+    volatile int4 *item_slot = reinterpret_cast<volatile int4 *>(bars + 26); // [2]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(k_full + s, 1);
             mbar_init(v_full + s, 1);
-            mbar_init(k_empty + s, 1);
-            mbar_init(v_empty + s, 1);
+            mbar_init(k_empty + s, kStageReleasers);
+            mbar_init(v_empty + s, kStageReleasers);
             mbar_init(s_full + s, 1);
             mbar_init(s_free + s, 128);
+            mbar_init(item_full + s, 1);
+            mbar_init(item_empty + s, kItemConsumers);
         }
         mbar_init(p_full, 128);
         mbar_init(t_full, 1);
+        mbar_init(o_free, 128);
         mbar_init(fin, 1);
-        mbar_init(loaded, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -182,45 +243,119 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // everything above is private to this CTA; from here on global memory written by the previous
+    // kernels on the stream (the work list, the inputs) is read
+    pdl_wait();
+
+    const int G = a.hq / a.hkv;
+    auto fail = [&]() {
+        set_error(a.err, PKV_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+    };
+    // the item in ring slot n % 2, once the scheduler has published it
+    auto take_item = [&](int n, bool &ok) -> Item {
+        Item it;
+        it.seq = -1;
+        ok = mbar_wait(item_full + (n & 1), (n >> 1) & 1);
+        if (!ok) return it;
+        const int4 raw = make_int4(item_slot[n & 1].x, item_slot[n & 1].y, item_slot[n & 1].z, 0);
+        return decode_item(a, raw);
+    };
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producers
-        // K and V have rings of their own: a K stage is free once S = Q K^T of its tile is done, so
-        // K loads run about two tiles ahead of the softmax; a V stage is free once P V is done.
-        // Lane 0 streams Q and K, lane 1 streams V.
-        if (lane < 2) {
-            const bool is_k = lane == 0;
-            const CUtensorMap *map = is_k ? &tk : &tv;
-            uint64_t *full = is_k ? k_full : v_full, *empty = is_k ? k_empty : v_empty;
-            uint8_t *ring = smem + (is_k ? L::K0 : L::V0);
-            tc::prefetch_tmap(map);
-            if (is_k) {
-                tc::prefetch_tmap(&tq);
+        if (lane == 0) {
+            // ------------------------------------------------------------ scheduler, Q and K loads
+            tc::prefetch_tmap(&tq);
+            tc::prefetch_tmap(&tk);
+            const int total = a.plan[0] * a.hq;
+            int n = 0, last_q = -1;
+            int64_t g = 0; // K tiles issued so far (all items)
+            for (;; ++n) {
+                const int s = n & 1;
+                if (n >= 2 && !mbar_wait(item_empty + s, ((n >> 1) - 1) & 1)) {
+                    fail();
+                    break;
+                }
+                const int idx = *abort_flag ? total : atomicAdd(a.plan + 1, 1);
+                int4 raw = make_int4(-1, 0, 0, 0);
+                if (idx < total) {
+                    const int2 sq = reinterpret_cast<const int2 *>(a.plan + 4)[idx / a.hq];
+                    raw = make_int4(sq.x, sq.y, idx % a.hq, 0);
+                }
+                item_slot[s].x = raw.x;
+                item_slot[s].y = raw.y;
+                item_slot[s].z = raw.z;
+                mbar_arrive(item_full + s);
+                if (raw.x < 0) break;
+                const Item it = decode_item(a, raw);
+                const int kvh = it.h / G;
+                if (n >= 1 && !mbar_wait(q_empty, (n - 1) & 1)) {
+                    fail();
+                    break;
+                }
                 mbar_arrive_expect_tx(q_full, L::Q_BYTES);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    tc::tma_load_2d(smem + L::Q + c * BM * 128, &tq, h * D + c * 64, start + q0, q_full);
-            }
-            int issued = 0;
-            for (int j = 0; j < nkv; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !mbar_wait(empty + st, ((j >> 1) - 1) & 1)) {
-                    set_error(a.err, PKV_DEVERR_TIMEOUT);
-                    *abort_flag = 1;
+                    tc::tma_load_2d(smem + L::Q + c * BM * 128, &tq, it.h * D + c * 64, it.start + it.q0, q_full);
+                last_q = n;
+                bool ok = true;
+                int issued = 0;
+                for (int j = 0; j < it.nkv && ok; ++j) {
+                    const int64_t gg = g + j;
+                    const int st = (int)(gg & 1);
+                    if (gg >= 2) ok = mbar_wait(k_empty + st, ((gg >> 1) - 1) & 1);
+                    if (!ok || *abort_flag) break;
+                    mbar_arrive_expect_tx(k_full + st, L::KV_BYTES);
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tc::tma_load_2d(smem + L::K0 + st * L::KV_BYTES + c * BN * 128, &tk, kvh * D + c * 64,
+                                        it.start + j * BN, k_full + st);
+                    issued = j + 1;
+                }
+                g += issued; // tiles issued so far, all items
+                if (!ok) {
+                    fail();
                     break;
                 }
                 if (*abort_flag) break;
-                mbar_arrive_expect_tx(full + st, L::KV_BYTES);
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tc::tma_load_2d(ring + st * L::KV_BYTES + c * BN * 128, map, kvh * D + c * 64, start + j * BN,
-                                    full + st);
-                issued = j + 1;
             }
-            // the loads of the last stages must land before this CTA's shared memory goes away
-            for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-                if (!mbar_wait(full + (j & 1), (j >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
-            if (is_k && !mbar_wait(q_full, 0)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            // the last loads must land before this CTA's shared memory goes away
+            for (int64_t gg = g > 2 ? g - 2 : 0; gg < g; ++gg)
+                if (!mbar_wait(k_full + (gg & 1), (gg >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            if (last_q >= 0 && !mbar_wait(q_full, last_q & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+        } else if (lane == 1) {
+            // ------------------------------------------------------------ V loads
+            tc::prefetch_tmap(&tv);
+            int64_t g = 0;
+            for (int n = 0;; ++n) {
+                bool ok;
+                const Item it = take_item(n, ok);
+                if (!ok) fail();
+                if (!ok || it.seq < 0) break;
+                const int kvh = it.h / G;
+                int issued = 0;
+                for (int j = 0; j < it.nkv && ok; ++j) {
+                    const int64_t gg = g + j;
+                    const int st = (int)(gg & 1);
+                    if (gg >= 2) ok = mbar_wait(v_empty + st, ((gg >> 1) - 1) & 1);
+                    if (!ok || *abort_flag) break;
+                    mbar_arrive_expect_tx(v_full + st, L::KV_BYTES);
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tc::tma_load_2d(smem + L::V0 + st * L::KV_BYTES + c * BN * 128, &tv, kvh * D + c * 64,
+                                        it.start + j * BN, v_full + st);
+                    issued = j + 1;
+                }
+                g += issued; // tiles issued so far, all items
+                mbar_arrive(item_empty + (n & 1));
+                if (!ok) {
+                    fail();
+                    break;
+                }
+                if (*abort_flag) break;
+            }
+            for (int64_t gg = g > 2 ? g - 2 : 0; gg < g; ++gg)
+                if (!mbar_wait(v_full + (gg & 1), (gg >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -230,9 +365,14 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             const uint32_t sQ = smem_u32(smem + L::Q), sK = smem_u32(smem + L::K0), sV = smem_u32(smem + L::V0);
             const uint32_t sP = smem_u32(smem + L::P);
             const uint32_t tO = tmem + 128;
-            // S_j = Q K_j^T into S buffer j % 2; its K stage is released as soon as S_j is done
-            auto issue_s = [&](int j) {
-                const int st = j & 1;
+            bool any_mma = false;
+            // S of global tile gg = Q K^T into S buffer gg % 2; its K stage is released as soon as S is done
+            auto issue_s = [&](int64_t gg) -> bool {
+                const int st = (int)(gg & 1);
+                if (!mbar_wait(k_full + st, (gg >> 1) & 1)) return false;
+                if (gg >= 2 && !mbar_wait(s_free + st, ((gg >> 1) - 1) & 1)) return false;
+                tc::fence_after_sync();
+                any_mma = true;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const int c = k >> 2, kk = k & 3;
@@ -242,143 +382,152 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 }
                 tc::commit(s_full + st);
                 tc::commit(k_empty + st);
+                return true;
             };
-            bool ok = mbar_wait(q_full, 0) && mbar_wait(k_full, 0);
-            if (ok) {
-                tc::fence_after_sync();
-                issue_s(0);
-            }
-            for (int j = 0; j < nkv && ok; ++j) {
-                if (j + 1 < nkv) {
-                    const int b = (j + 1) & 1;
-                    ok = mbar_wait(k_full + b, ((j + 1) >> 1) & 1);
-                    if (ok && j + 1 >= 2) ok = mbar_wait(s_free + b, ((j - 1) >> 1) & 1);
+            bool ok = true;
+            int64_t g = 0;
+            for (int n = 0; ok; ++n) {
+                const Item it = take_item(n, ok);
+                if (!ok || it.seq < 0) break;
+                ok = mbar_wait(q_full, n & 1) && issue_s(g);
+                for (int j = 0; j < it.nkv && ok; ++j) {
+                    const int64_t gg = g + j;
+                    if (j + 1 < it.nkv) {
+                        ok = issue_s(gg + 1);
+                        if (!ok) break;
+                    } else {
+                        tc::commit(q_empty); // the item's last S has been issued: Q may be replaced
+                    }
+                    const int st = (int)(gg & 1);
+                    ok = mbar_wait(p_full, gg & 1) && mbar_wait(v_full + st, (gg >> 1) & 1);
+                    // the epilogue of the previous item has read O out of TMEM
+                    if (ok && j == 0 && n >= 1) ok = mbar_wait(o_free, (n - 1) & 1);
                     if (!ok) break;
                     tc::fence_after_sync();
-                    issue_s(j + 1);
+#pragma unroll
+                    for (int part = 0; part < L::NP; ++part)
+#pragma unroll
+                        for (int k = 0; k < BN / 16; ++k) {
+                            const uint64_t ad = tc::smem_desc(sP + part * L::P_BYTES + k * 32, 16, 1024);
+                            const uint64_t bd = tc::smem_desc(sV + st * L::KV_BYTES + k * 2048, BN * 128, 1024);
+                            tc::mma_f16(tO, ad, bd, IPV, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
+                        }
+                    tc::commit(t_full);
+                    tc::commit(v_empty + st);
                 }
-                const int st = j & 1;
-                ok = mbar_wait(p_full, j & 1) && mbar_wait(v_full + st, (j >> 1) & 1);
-                if (!ok) break;
-                if (j == nkv - 1) mbar_arrive(loaded); // every K and V tile of this CTA has landed
-                tc::fence_after_sync();
-#pragma unroll
-                for (int part = 0; part < L::NP; ++part)
-#pragma unroll
-                    for (int k = 0; k < BN / 16; ++k) {
-                        const uint64_t ad = tc::smem_desc(sP + part * L::P_BYTES + k * 32, 16, 1024);
-                        const uint64_t bd = tc::smem_desc(sV + st * L::KV_BYTES + k * 2048, BN * 128, 1024);
-                        tc::mma_f16(tO, ad, bd, IPV, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
-                    }
-                tc::commit(t_full);
-                tc::commit(v_empty + st);
+                g += it.nkv;
+                mbar_arrive(item_empty + (n & 1));
+                if (*abort_flag) break;
             }
-            if (!ok) {
-                set_error(a.err, PKV_DEVERR_TIMEOUT);
-                *abort_flag = 1;
+            if (!ok) fail();
+            // every MMA issued by this thread has completed before TMEM is released (a CTA that found
+            // no item issued none and has nothing to wait for)
+            if (any_mma) {
+                tc::commit(fin);
+                if (!mbar_wait(fin, 0)) set_error(a.err, PKV_DEVERR_TIMEOUT);
             }
-            // every MMA issued by this thread has completed before TMEM is released
-            tc::commit(fin);
-            if (!mbar_wait(fin, 0)) set_error(a.err, PKV_DEVERR_TIMEOUT);
         }
     } else if (warp < 6) {
         // ------------------------------------------------------------ softmax, one thread per row
         const int lw = warp & 3;
         const int r = lw * 32 + lane;
-        const int qpos = q0 + r;
         const uint32_t lane_off = static_cast<uint32_t>(lw * 32) << 16;
-        float m_use = -INFINITY, l = 0.f;
-        bool ok = true;
         uint8_t *prow = smem + L::P + (r >> 3) * 1024 + (r & 7) * 128;
-        for (int j = 0; j < nkv && ok; ++j) {
-            const int b = j & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j >> 1) & 1));
-            if (!ok) break;
-            tc::fence_after_sync();
-            uint32_t sr[64];
-            {
-                uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-                uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-                tc::ld32(tmem + lane_off + b * BN, lo);
-                tc::ld32(tmem + lane_off + b * BN + 32, hi);
-            }
-            tc::wait_ld();
-            tc::fence_before_sync();
-            mbar_arrive(s_free + b);
-            // causal mask, only on tiles that reach past this tile's first query row
-            const int kbase = j * BN;
-            if (kbase + BN - 1 > q0) {
-                const int lim = qpos - kbase + 1; // keys c < lim are at or before this row
-#pragma unroll
-                for (int c = 0; c < BN; ++c)
-                    if (c >= lim) sr[c] = 0xFF800000u; // -inf
-            }
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < BN; c += 2) {
-                mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-                mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-            }
-            const float mx = fmaxf(mx0, mx1) * a.scale_log2; // scale > 0 keeps the order
-            const bool up = mx > m_use + kRescale;
-            const float m_new = up ? mx : m_use;
-            const float alpha = up ? fast_exp2(m_use - m_new) : 1.f;
-            m_use = m_new;
-            const float nbase = m_use == -INFINITY ? 0.f : -m_use; // a row with no live key yet keeps p = 0
-            float rs0 = 0.f, rs1 = 0.f;
-            uint32_t phi[BN / 2], plo[L::NP == 2 ? BN / 2 : 1];
-#pragma unroll
-            for (int c = 0; c < BN / 2; ++c) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * c]), a.scale_log2, nbase));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * c + 1]), a.scale_log2, nbase));
-                rs0 += p0;
-                rs1 += p1;
-                phi[c] = pack2(p0, p1, MT);
-                if constexpr (L::NP == 2) // remainders after bf16 rounding, themselves rounded to bf16
-                    plo[c] = pack2(p0 - __uint_as_float(phi[c] << 16), p1 - __uint_as_float(phi[c] & 0xFFFF0000u), MT);
-            }
-            const float rs = rs0 + rs1;
-            l = l * alpha + rs;
-            if (j > 0) {
-                // P V of the previous tile has finished: P's buffer is free and O is stable
-                ok = __all_sync(0xffffffffu, mbar_wait(t_full, (j - 1) & 1));
+        bool ok = true;
+        int64_t g = 0;
+        for (int n = 0; ok; ++n) {
+            Item it = take_item(n, ok);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok || it.seq < 0) break;
+            const int q0 = it.q0, qpos = it.q0 + r;
+            float m_use = -INFINITY, l = 0.f;
+            for (int j = 0; j < it.nkv && ok; ++j) {
+                const int64_t gg = g + j;
+                const int b = (int)(gg & 1);
+                ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (gg >> 1) & 1));
                 if (!ok) break;
                 tc::fence_after_sync();
-                if (__any_sync(0xffffffffu, up)) {
-#pragma unroll
-                    for (int cc = 0; cc < D / 16; ++cc) {
-                        uint32_t o[16];
-                        tc::ld16(tmem + lane_off + 128 + cc * 16, o);
-                        tc::wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tc::st16(tmem + lane_off + 128 + cc * 16, o);
-                    }
-                    tc::wait_st();
+                uint32_t sr[64];
+                {
+                    uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+                    uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+                    tc::ld32(tmem + lane_off + b * BN, lo);
+                    tc::ld32(tmem + lane_off + b * BN + 32, hi);
                 }
-            }
+                tc::wait_ld();
+                tc::fence_before_sync();
+                mbar_arrive(s_free + b);
+                // causal mask, only on tiles that reach past the item's first query row
+                const int kbase = j * BN;
+                if (kbase + BN - 1 > q0) {
+                    const int lim = qpos - kbase + 1; // keys c < lim are at or before this row
 #pragma unroll
-            for (int c = 0; c < BN / 8; ++c) {
-                const int off = (c ^ (r & 7)) << 4;
-                *reinterpret_cast<uint4 *>(prow + off) =
-                    make_uint4(phi[4 * c], phi[4 * c + 1], phi[4 * c + 2], phi[4 * c + 3]);
-                if constexpr (L::NP == 2)
-                    *reinterpret_cast<uint4 *>(prow + L::P_BYTES + off) =
-                        make_uint4(plo[4 * c], plo[4 * c + 1], plo[4 * c + 2], plo[4 * c + 3]);
+                    for (int c = 0; c < BN; ++c)
+                        if (c >= lim) sr[c] = 0xFF800000u; // -inf
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < BN; c += 2) {
+                    mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+                    mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+                }
+                const float mx = fmaxf(mx0, mx1) * a.scale_log2; // scale > 0 keeps the order
+                const bool up = mx > m_use + kRescale;
+                const float m_new = up ? mx : m_use;
+                const float alpha = up ? fast_exp2(m_use - m_new) : 1.f;
+                m_use = m_new;
+                const float nbase = m_use == -INFINITY ? 0.f : -m_use; // a row with no live key yet keeps p = 0
+                float rs0 = 0.f, rs1 = 0.f;
+                uint32_t phi[BN / 2], plo[L::NP == 2 ? BN / 2 : 1];
+#pragma unroll
+                for (int c = 0; c < BN / 2; ++c) {
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * c]), a.scale_log2, nbase));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * c + 1]), a.scale_log2, nbase));
+                    rs0 += p0;
+                    rs1 += p1;
+                    phi[c] = pack2(p0, p1, MT);
+                    if constexpr (L::NP == 2) // remainders after bf16 rounding, themselves rounded to bf16
+                        plo[c] = pack2(p0 - __uint_as_float(phi[c] << 16), p1 - __uint_as_float(phi[c] & 0xFFFF0000u), MT);
+                }
+                l = l * alpha + (rs0 + rs1);
+                if (j > 0) {
+                    // P V of the previous tile has finished: P's buffer is free and O is stable
+                    ok = __all_sync(0xffffffffu, mbar_wait(t_full, (gg - 1) & 1));
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    if (__any_sync(0xffffffffu, up)) {
+#pragma unroll
+                        for (int cc = 0; cc < D / 16; ++cc) {
+                            uint32_t o[16];
+                            tc::ld16(tmem + lane_off + 128 + cc * 16, o);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tc::st16(tmem + lane_off + 128 + cc * 16, o);
+                        }
+                        tc::wait_st();
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < BN / 8; ++c) {
+                    const int off = (c ^ (r & 7)) << 4;
+                    *reinterpret_cast<uint4 *>(prow + off) =
+                        make_uint4(phi[4 * c], phi[4 * c + 1], phi[4 * c + 2], phi[4 * c + 3]);
+                    if constexpr (L::NP == 2)
+                        *reinterpret_cast<uint4 *>(prow + L::P_BYTES + off) =
+                            make_uint4(plo[4 * c], plo[4 * c + 1], plo[4 * c + 2], plo[4 * c + 3]);
+                }
+                fence_proxy_async_smem();
+                tc::fence_before_sync();
+                mbar_arrive(p_full);
             }
-            fence_proxy_async_smem();
-            tc::fence_before_sync();
-            mbar_arrive(p_full);
-        }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(t_full, (nkv - 1) & 1));
-        if (!ok) {
-            set_error(a.err, PKV_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-        } else {
+            g += it.nkv;
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(t_full, (g - 1) & 1));
+            if (!ok) break;
             tc::fence_after_sync();
             const float inv = 1.f / l;
             using T = typename ModelT<MT>::T;
-            T *orow = static_cast<T *>(a.out) + ((int64_t)(start + qpos) * a.hq + h) * D;
+            T *orow = static_cast<T *>(a.out) + ((int64_t)(it.start + qpos) * a.hq + it.h) * D;
 #pragma unroll
             for (int cc = 0; cc < D / 16; ++cc) {
                 uint32_t o[16];
@@ -388,53 +537,86 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     w[e] = pack2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv, MT);
-                if (qpos < n) {
+                if (qpos < it.n) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 16);
                     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
                     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
+            tc::fence_before_sync();
+            mbar_arrive(o_free); // O has been read out; the next item's first P V may overwrite it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(item_empty + (n & 1));
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
         }
-    } else if (h % G == 0) {
-        // ------------------------------------------------------------ paged K/V write of this tile's rows
-        // The tile's own rows q0..qlast are the keys of K/V tiles q0/BN .. nkv-1, the last ones the
-        // producer loads; no later tile recycles their stages, so they are copied straight from
-        // shared memory (undoing the 128-byte swizzle) to their slots: no global reads, and each
-        // row leaves as one contiguous D*2-byte store from D/8 lanes.
+        if (!ok) fail();
+    } else {
+        // ------------------------------------------------------------ paged K/V write of the item's rows
+        // The item's own rows q0..qlast are the keys of its last K/V tiles (q0/BN .. nkv-1).  These
+        // warps follow every K/V tile of the ring in order (so a stage's phase is never more than
+        // one ahead of them) and hold each stage until they are done with it: a stage frees only
+        // after the MMA that reads it and both writer warps.  The item's rows are copied straight
+        // from shared memory (undoing the 128-byte swizzle) to their slots as soon as their tiles
+        // land, one contiguous D*2-byte store per row from D/8 lanes; the block-table entries of the
+        // item's rows are read once, at the start of the item, one per lane.
         constexpr int CPR = D / 8;   // 16-byte chunks per row
         constexpr int RPI = 32 / CPR; // rows per warp instruction
         const int wl = warp - 6;
         const int cc = lane % CPR, rsub = lane / CPR;
         const int c2 = cc >> 3, u = cc & 7;
-        // `loaded` has a single phase (the MMA thread arrives once it has seen the last K/V tile land);
-        // waiting on k_full/v_full here could target a phase two or more ahead, which a parity wait cannot tell
-        // from an already completed one
-        const bool landed = __all_sync(0xffffffffu, mbar_wait(loaded, 0));
-        if (!landed && lane == 0) {
-            set_error(a.err, PKV_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-        }
-        for (int j = q0 / BN; j < nkv && landed; ++j) {
-            const int st = j & 1;
-            const int lo = max(j * BN, q0), hi = min(j * BN + BN - 1, qlast);
-            for (int p0 = lo + wl * RPI; p0 <= hi; p0 += 2 * RPI) {
-                const int p = p0 + rsub;
-                if (p > hi) continue;
-                const int lb = p / a.bs;
-                const int blk = lb < a.max_blocks ? a.tables[(int64_t)seq * a.max_blocks + lb] : -1;
-                if (blk < 0 || blk >= a.num_blocks) {
-                    if (cc == 0) set_error(a.err, PKV_DEVERR_BLOCK_ID);
-                    continue;
-                }
-                const int r = p - j * BN;
-                const int sw = c2 * BN * 128 + (r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4);
-                const uint4 kx = *reinterpret_cast<const uint4 *>(smem + L::K0 + st * L::KV_BYTES + sw);
-                const uint4 vx = *reinterpret_cast<const uint4 *>(smem + L::V0 + st * L::KV_BYTES + sw);
-                const int64_t dst = ((int64_t)blk * 2 * a.hkv + kvh) * a.tile_elems + (int64_t)(p - lb * a.bs) * D + cc * 8;
-                *reinterpret_cast<uint4 *>(a.pool + dst * 2) = kx;
-                *reinterpret_cast<uint4 *>(a.pool + (dst + (int64_t)a.hkv * a.tile_elems) * 2) = vx;
+        bool ok = true;
+        int64_t g = 0;
+        for (int n = 0; ok; ++n) {
+            const Item it = take_item(n, ok);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok || it.seq < 0) break;
+            const bool writes = it.h % G == 0;
+            const int kvh = it.h / G, lb0 = it.q0 / a.bs;
+            // lane l: table entry of logical block lb0 + l (at most BM / bs + 1 <= 17 of them)
+            int blkv = -1;
+            {
+                const int lb = lb0 + lane;
+                if (writes && lb * a.bs <= it.qlast && lb < a.max_blocks)
+                    blkv = a.tables[(int64_t)it.seq * a.max_blocks + lb];
             }
+            for (int j = 0; j < it.nkv && ok; ++j) {
+                const int64_t gg = g + j;
+                const int st = (int)(gg & 1);
+                ok = __all_sync(0xffffffffu, mbar_wait(k_full + st, (gg >> 1) & 1) && mbar_wait(v_full + st, (gg >> 1) & 1));
+                if (!ok) break;
+                if (writes && j >= it.q0 / BN) {
+                    const int lo = max(j * BN, it.q0), hi = min(j * BN + BN - 1, it.qlast);
+                    for (int p0 = lo + wl * RPI; p0 <= hi; p0 += 2 * RPI) {
+                        const int p = p0 + rsub;
+                        const int lb = p / a.bs;
+                        const int blk = __shfl_sync(0xffffffffu, blkv, min(lb - lb0, 31));
+                        if (p > hi) continue;
+                        if (blk < 0 || blk >= a.num_blocks) {
+                            if (cc == 0) set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                            continue;
+                        }
+                        const int r = p - j * BN;
+                        const int sw = c2 * BN * 128 + (r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4);
+                        const uint4 kx = *reinterpret_cast<const uint4 *>(smem + L::K0 + st * L::KV_BYTES + sw);
+                        const uint4 vx = *reinterpret_cast<const uint4 *>(smem + L::V0 + st * L::KV_BYTES + sw);
+                        const int64_t dst = ((int64_t)blk * 2 * a.hkv + kvh) * a.tile_elems +
+                                            (int64_t)(p - lb * a.bs) * D + cc * 8;
+                        *reinterpret_cast<uint4 *>(a.pool + dst * 2) = kx;
+                        *reinterpret_cast<uint4 *>(a.pool + (dst + (int64_t)a.hkv * a.tile_elems) * 2) = vx;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(k_empty + st);
+                    mbar_arrive(v_empty + st);
+                }
+            }
+            if (!ok) break;
+            g += it.nkv;
+            if (lane == 0) mbar_arrive(item_empty + (n & 1));
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
         }
+        if (!ok && lane == 0) fail();
     }
 
     tc::fence_before_sync();
@@ -479,16 +661,31 @@ bool make_map(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t co
 }
 
 template <int D, int MT>
-cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const Args &a, int grid,
-                     cudaStream_t st) {
+cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const Args &a,
+                     int64_t max_ctas, int num_sms, cudaStream_t st) {
     auto kern = prefill_kernel<D, MT>;
     const int smem = Layout<D, MT>::TOTAL;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return pdl_launch(kern, dim3(grid), dim3(kThreads), smem, st, tq, tk, tv, a);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = std::min<int64_t>(max_ctas, (int64_t)num_sms * std::max(per_sm, 1));
+    return pdl_launch(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, tq, tk, tv, a);
+}
+
+cudaError_t launch_plan(const Args &a, cudaStream_t st) {
+    const int smem = (2 * (a.nqt_max + 1) + 32) * (int)sizeof(int);
+    cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return pdl_launch(plan_kernel, dim3(1), dim3(kPlanThreads), smem, st, a);
 }
 
 } // namespace pkv_prefill
+
+bool pkv_tmap_2d(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t cols, int box_rows) {
+    return pkv_prefill::make_map(m, base, mt, rows, cols, box_rows);
+}
 
 cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st) {
     using namespace pkv_prefill;
@@ -514,26 +711,41 @@ cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st
     a.bs = c->block_size;
     a.nqt_max = (p.max_seqlen + BM - 1) / BM;
     a.scale_log2 = p.scale * 1.4426950408889634f;
-    // the work-item prologue keeps num_seqs + nqt_max + 3 ints in the P buffer
-    if ((int64_t)p.num_seqs + a.nqt_max + 3 > (int64_t)BM * BN * 2 / 4) return cudaErrorNotSupported;
+    // (sequence, query tile) items: sum_i ceil(n_i / BM) <= T / BM + num_seqs
+    const int64_t items = std::min<int64_t>((int64_t)a.nqt_max * p.num_seqs, p.total_tokens / BM + p.num_seqs);
+    if (items == 0) return cudaSuccess;
+    if (items * p.num_q_heads > 0x7FFFFFFF) return cudaErrorNotSupported;
+    // the plan kernel's two rank arrays live in shared memory
+    if ((2 * ((int64_t)a.nqt_max + 1) + 32) * (int64_t)sizeof(int) > 200 * 1024) return cudaErrorNotSupported;
+    const int64_t plan_bytes = (4 + 2 * items) * (int64_t)sizeof(int);
+    if (plan_bytes > c->plan_bytes) {
+        if (c->plan) cudaFree(c->plan);
+        c->plan = nullptr;
+        c->plan_bytes = 0;
+        cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&c->plan), (size_t)plan_bytes);
+        if (e != cudaSuccess) {
+            c->plan = nullptr;
+            return e;
+        }
+        c->plan_bytes = plan_bytes;
+    }
+    a.plan = c->plan;
     CUtensorMap tq, tk, tv;
     if (!make_map(&tq, p.q, mt, p.total_tokens, (int64_t)p.num_q_heads * D, BM) ||
         !make_map(&tk, p.k, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN) ||
         !make_map(&tv, p.v, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN))
         return cudaErrorInvalidValue;
-    // (sequence, query tile) items: sum_i ceil(n_i / BM) <= T / BM + num_seqs
-    const int64_t items = std::min<int64_t>((int64_t)a.nqt_max * p.num_seqs, p.total_tokens / BM + p.num_seqs);
-    const int64_t grid = items * p.num_q_heads;
-    if (grid == 0) return cudaSuccess;
-    if (grid > 0x7FFFFFFF) return cudaErrorNotSupported;
     PkvTimer timer(c, PKV_KIND_PREFILL, st);
-    cudaError_t e;
+    cudaError_t e = launch_plan(a, st);
+    g_pkv_launches++;
+    if (e != cudaSuccess) return e;
+    const int64_t max_ctas = items * p.num_q_heads;
     if (D == 128)
-        e = mt == PKV_BF16 ? launch_t<128, PKV_BF16>(tq, tk, tv, a, (int)grid, st)
-                           : launch_t<128, PKV_F16>(tq, tk, tv, a, (int)grid, st);
+        e = mt == PKV_BF16 ? launch_t<128, PKV_BF16>(tq, tk, tv, a, max_ctas, c->num_sms, st)
+                           : launch_t<128, PKV_F16>(tq, tk, tv, a, max_ctas, c->num_sms, st);
     else
-        e = mt == PKV_BF16 ? launch_t<64, PKV_BF16>(tq, tk, tv, a, (int)grid, st)
-                           : launch_t<64, PKV_F16>(tq, tk, tv, a, (int)grid, st);
+        e = mt == PKV_BF16 ? launch_t<64, PKV_BF16>(tq, tk, tv, a, max_ctas, c->num_sms, st)
+                           : launch_t<64, PKV_F16>(tq, tk, tv, a, max_ctas, c->num_sms, st);
     g_pkv_launches++;
     return e;
 }

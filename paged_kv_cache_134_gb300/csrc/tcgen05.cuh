@@ -44,6 +44,12 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_bf16, uint32_t b_mn
     return (1u << 4) | (ab_bf16 << 7) | (ab_bf16 << 10) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Same with the A operand's major-ness too: a_mn = 1 reads A MN-major (bit 15).
+__host__ __device__ constexpr uint32_t idesc_f16_ab(uint32_t ab_bf16, uint32_t a_mn, uint32_t b_mn, uint32_t M,
+                                                    uint32_t N) {
+    return idesc_f16(ab_bf16, b_mn, M, N) | (a_mn << 15);
+}
+
 // ---------------------------------------------------------------- MMA
 
 PKV_DEV void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
@@ -103,6 +109,39 @@ PKV_DEV void st16(uint32_t taddr, const uint32_t (&r)[16]) {
         : "memory");
 }
 
+// 32 lanes x N consecutive columns (N = 2, 4 or 8)
+template <int N>
+PKV_DEV void ldn(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 2) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
+    } else if constexpr (N == 4) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(taddr));
+    } else {
+        static_assert(N == 8, "ldn: N in {2, 4, 8}");
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                     : "r"(taddr));
+    }
+}
+template <int N>
+PKV_DEV void stn(uint32_t taddr, const uint32_t (&r)[N]) {
+    if constexpr (N == 2) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(r[0]), "r"(r[1])
+                     : "memory");
+    } else if constexpr (N == 4) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]),
+                     "r"(r[1]), "r"(r[2]), "r"(r[3])
+                     : "memory");
+    } else {
+        static_assert(N == 8, "stn: N in {2, 4, 8}");
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                     : "memory");
+    }
+}
+
 PKV_DEV void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 PKV_DEV void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -114,6 +153,14 @@ PKV_DEV void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64
             "r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+
+// the same with an L2 cache-policy hint (e.g. evict-first for data read once)
+PKV_DEV void tma_load_2d_hint(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar, uint64_t policy) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+                 : "memory");
 }
 
 PKV_DEV void prefetch_tmap(const CUtensorMap *map) {
