@@ -316,6 +316,27 @@ def secondary_append(P, W, gpu_path, peaks, reps=20):
             "gbs": round(nbytes / kern / 1e9, 1), "frac_of_hbm": round(nbytes / kern / 1e9 / peaks[0], 4)}
 
 
+def run_only(case: str):
+    """One secondary case alone (a short run for ncu captures); prints {case: result}."""
+    torch.cuda.set_device(0)
+    import paged_kv_cache_134_gb300 as P
+    from paged_kv_cache_134_gb300 import workloads as W
+    from paged_kv_cache_134_gb300 import runner as G
+    peaks = _peaks()
+    if case == "prefill":
+        r = secondary_prefill(P, W, G, peaks, reps=5)
+    elif case == "append":
+        r = secondary_append(P, W, G, peaks, reps=5)
+    elif case == "prefix13b":
+        r = secondary_decode(P, G, peaks, W.prefix13b(), reps=5)
+    elif case.startswith("stress_bs"):
+        bs, kv = case[len("stress_bs"):].split("_")
+        r = secondary_decode(P, G, peaks, W.stress(bs=int(bs), kv_dtype=kv), reps=5)
+    else:
+        raise SystemExit(f"unknown case {case}")
+    print(json.dumps({case: r}), flush=True)
+
+
 def run_ours(args):
     ws, rank, local = _dist()
     torch.cuda.set_device(local)
@@ -474,11 +495,16 @@ def main():
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--only", default=None,
+                    help="run one secondary case alone and print its JSON (for profiling): prefill, append, "
+                         "prefix13b or stress_bs{8,16,32}_{bf16,fp8}")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args.only)
     else:
         run_ours(args)
 

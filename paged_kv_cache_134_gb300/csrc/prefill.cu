@@ -32,6 +32,7 @@
 // entirely above the diagonal are never issued.  Every mbarrier wait is bounded; a timeout sets
 // PKV_DEVERR_TIMEOUT and the CTA winds down.
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "tcgen05.cuh"
@@ -42,7 +43,7 @@ namespace pkv_prefill {
 constexpr int BM = 128;          // query rows per tile (MMA M)
 constexpr int BN = 64;           // keys per tile (MMA N of Q K^T, K of P V)
 constexpr int kThreads = 256;
-constexpr uint32_t kTmemCols = 256; // S0 [0,64) S1 [64,128) O [128, 128+D)
+constexpr uint32_t kTmemCols = 256; // S [0,64), P buffers [64,128), O [128, 128+D)
 constexpr float kRescale = 8.0f; // log2 units
 
 struct Args {
@@ -53,25 +54,29 @@ struct Args {
     unsigned int *err;
     int *plan;          // [0] item count, [1] next-item counter, [4 + 2i], [5 + 2i] = (sequence, query tile) of item i
     int64_t total_tokens, num_blocks, tile_elems;
-    int num_seqs, max_seqlen, max_blocks, hq, hkv, bs, nqt_max;
+    int num_seqs, max_seqlen, max_blocks, hq, hkv, bs, lg_bs, nqt_max;
     float scale_log2;
 };
 
-// Shared memory.  bf16 models keep P as a hi + lo pair of bf16 tiles (P = hi + lo to ~2^-16
-// relative), because one bf16 rounding of P (2^-9 relative) alone would exceed the accuracy the
-// outputs are held to; fp16 P (2^-12) is used as a single tile.
+constexpr int NKS = 3;           // K stages (a K stage frees as soon as S = Q K^T of its tile is done)
+constexpr int NVS = 2;           // V stages (a V stage frees after P V)
+
+// Shared memory: Q, the K ring and the V ring (P lives in tensor memory).  bf16 models keep P as a
+// hi + lo pair of bf16 halves (P = hi + lo to ~2^-16 relative), because one bf16 rounding of P
+// (2^-9 relative) alone would exceed the accuracy the outputs are held to; fp16 P (2^-12) is one.
 template <int D, int MT>
 struct Layout {
     static constexpr int NP = MT == PKV_BF16 ? 2 : 1;
+    // P buffers in tensor memory (columns [BN, 2 BN)): two fp16 P tiles of BN/2 columns, or one bf16
+    // hi + lo pair; with two, the softmax never waits for P V before writing the next P
+    static constexpr int NPB = NP == 1 ? 2 : 1;
     static constexpr int Q = 0;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int KV_BYTES = BN * D * 2; // one K or V tile
     static constexpr int K0 = Q + Q_BYTES;
-    static constexpr int V0 = K0 + 2 * KV_BYTES;
-    static constexpr int P = V0 + 2 * KV_BYTES;
-    static constexpr int P_BYTES = BM * BN * 2;
-    static constexpr int BAR = P + NP * P_BYTES;
-    static constexpr int TOTAL = BAR + 256; // 26 mbarriers / words + two 16-byte item slots
+    static constexpr int V0 = K0 + NKS * KV_BYTES;
+    static constexpr int BAR = V0 + NVS * KV_BYTES;
+    static constexpr int TOTAL = BAR + 256; // 24 mbarriers, the TMEM slot, a flag, two 16-byte item slots
 };
 
 // two floats -> packed fp16/bf16 pair (round-to-nearest-even), `lo` in the low half
@@ -91,8 +96,8 @@ constexpr int min_blocks() {
 }
 
 constexpr int kPlanThreads = 1024;
-constexpr int kItemConsumers = 8;  // V loader, MMA issuer, 4 softmax warps, 2 writer warps
-constexpr int kStageReleasers = 3; // a K or V stage frees after the MMA that reads it and both writer warps
+constexpr int kItemConsumers = 7;  // V loader, MMA issuer, 4 softmax warps, the writer warp
+constexpr int kStageReleasers = 2; // a K or V stage frees after the MMA that reads it and the writer warp
 
 // query tiles of sequence i (0 for a malformed cu_seqlens entry, which is reported)
 PKV_DEV int seq_tiles(const Args &a, int i, bool report) {
@@ -198,7 +203,7 @@ PKV_DEV Item decode_item(const Args &a, int4 raw) {
 template <int D, int MT>
 __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                   const __grid_constant__ CUtensorMap tv, const Args a) {
+                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tp, const Args a) {
     using L = Layout<D, MT>;
     extern __shared__ __align__(1024) uint8_t smem[];
 
@@ -206,30 +211,42 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
     if (smem_u32(smem) & 1023u) return; // the swizzled tiles need 1024-byte alignment (always true)
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR);
-    uint64_t *q_full = bars + 0, *q_empty = bars + 1, *k_full = bars + 2, *v_full = bars + 4;
-    uint64_t *k_empty = bars + 6, *v_empty = bars + 8, *s_full = bars + 10, *s_free = bars + 12;
-    uint64_t *p_full = bars + 14, *t_full = bars + 15, *o_free = bars + 16;
-    uint64_t *item_full = bars + 19, *item_empty = bars + 21, *fin = bars + 23;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 24);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 25);
-    volatile int4 *item_slot = reinterpret_cast<volatile int4 *>(bars + 26); // [2]
+    uint64_t *q_full = bars + 0, *q_empty = bars + 1;
+    uint64_t *k_full = bars + 2, *k_empty = k_full + NKS;          // [NKS] each
+    uint64_t *v_full = k_empty + NKS, *v_empty = v_full + NVS;     // [NVS] each
+    uint64_t *s_full = v_empty + NVS, *s_free = s_full + 1;        // phase t: S of global tile t
+    // p_full[t % 2] / t_full[t % 2]: P of global tile t written / P V of tile t done (phase t / 2).
+    // Pairs of barriers, so that a parity wait for tile t only needs tile t - 2 to be complete (which
+    // every waiter knows already) while tile t + 2 cannot be: the softmax may run one tile ahead of
+    // the P V issue, never two.
+    uint64_t *p_full = s_full + 2, *t_full = p_full + 2, *o_free = t_full + 2;
+    uint64_t *item_full = o_free + 1, *item_empty = item_full + 2, *fin = item_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(fin + 2);
+    volatile int4 *item_slot = reinterpret_cast<volatile int4 *>(fin + 3); // [2], 16-byte aligned
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NKS; ++s) {
             mbar_init(k_full + s, 1);
-            mbar_init(v_full + s, 1);
             mbar_init(k_empty + s, kStageReleasers);
+        }
+        for (int s = 0; s < NVS; ++s) {
+            mbar_init(v_full + s, 1);
             mbar_init(v_empty + s, kStageReleasers);
-            mbar_init(s_full + s, 1);
-            mbar_init(s_free + s, 128);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 128);
+        for (int s = 0; s < 2; ++s) {
             mbar_init(item_full + s, 1);
             mbar_init(item_empty + s, kItemConsumers);
         }
-        mbar_init(p_full, 128);
-        mbar_init(t_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(p_full + s, 128);
+            mbar_init(t_full + s, 1);
+        }
         mbar_init(o_free, 128);
         mbar_init(fin, 1);
         *abort_flag = 0;
@@ -302,8 +319,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 int issued = 0;
                 for (int j = 0; j < it.nkv && ok; ++j) {
                     const int64_t gg = g + j;
-                    const int st = (int)(gg & 1);
-                    if (gg >= 2) ok = mbar_wait(k_empty + st, ((gg >> 1) - 1) & 1);
+                    const int st = (int)(gg % NKS);
+                    const int64_t round = gg / NKS;
+                    if (round >= 1) ok = mbar_wait(k_empty + st, (round - 1) & 1);
                     if (!ok || *abort_flag) break;
                     mbar_arrive_expect_tx(k_full + st, L::KV_BYTES);
 #pragma unroll
@@ -320,10 +338,14 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 if (*abort_flag) break;
             }
             // the last loads must land before this CTA's shared memory goes away
-            for (int64_t gg = g > 2 ? g - 2 : 0; gg < g; ++gg)
-                if (!mbar_wait(k_full + (gg & 1), (gg >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            for (int64_t gg = g > NKS ? g - NKS : 0; gg < g; ++gg)
+                if (!mbar_wait(k_full + gg % NKS, (gg / NKS) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
             if (last_q >= 0 && !mbar_wait(q_full, last_q & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
-        } else if (lane == 1) {
+        }
+    } else if (warp == 7) {
+        // a warp of its own: sharing one with the K loader, whose lane spins on its own barriers,
+        // held V loads back by thousands of cycles at every item start
+        if (lane == 0) {
             // ------------------------------------------------------------ V loads
             tc::prefetch_tmap(&tv);
             int64_t g = 0;
@@ -336,8 +358,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 int issued = 0;
                 for (int j = 0; j < it.nkv && ok; ++j) {
                     const int64_t gg = g + j;
-                    const int st = (int)(gg & 1);
-                    if (gg >= 2) ok = mbar_wait(v_empty + st, ((gg >> 1) - 1) & 1);
+                    const int st = (int)(gg % NVS);
+                    const int64_t round = gg / NVS;
+                    if (round >= 1) ok = mbar_wait(v_empty + st, (round - 1) & 1);
                     if (!ok || *abort_flag) break;
                     mbar_arrive_expect_tx(v_full + st, L::KV_BYTES);
 #pragma unroll
@@ -354,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 }
                 if (*abort_flag) break;
             }
-            for (int64_t gg = g > 2 ? g - 2 : 0; gg < g; ++gg)
-                if (!mbar_wait(v_full + (gg & 1), (gg >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            for (int64_t gg = g > NVS ? g - NVS : 0; gg < g; ++gg)
+                if (!mbar_wait(v_full + gg % NVS, (gg / NVS) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -363,14 +386,14 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             constexpr uint32_t IQK = tc::idesc_f16(MT == PKV_BF16 ? 1u : 0u, 0u, BM, BN);
             constexpr uint32_t IPV = tc::idesc_f16(MT == PKV_BF16 ? 1u : 0u, 1u, BM, D);
             const uint32_t sQ = smem_u32(smem + L::Q), sK = smem_u32(smem + L::K0), sV = smem_u32(smem + L::V0);
-            const uint32_t sP = smem_u32(smem + L::P);
-            const uint32_t tO = tmem + 128;
+            const uint32_t tO = tmem + 2 * BN;
             bool any_mma = false;
-            // S of global tile gg = Q K^T into S buffer gg % 2; its K stage is released as soon as S is done
+            // S of global tile gg = Q K^T, once the softmax has read S of tile gg - 1 out of the single
+            // S buffer; the K stage is released as soon as S is done
             auto issue_s = [&](int64_t gg) -> bool {
-                const int st = (int)(gg & 1);
-                if (!mbar_wait(k_full + st, (gg >> 1) & 1)) return false;
-                if (gg >= 2 && !mbar_wait(s_free + st, ((gg >> 1) - 1) & 1)) return false;
+                const int st = (int)(gg % NKS);
+                if (!mbar_wait(k_full + st, (gg / NKS) & 1)) return false;
+                if (gg >= 1 && !mbar_wait(s_free, (gg - 1) & 1)) return false;
                 tc::fence_after_sync();
                 any_mma = true;
 #pragma unroll
@@ -378,9 +401,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                     const int c = k >> 2, kk = k & 3;
                     const uint64_t ad = tc::smem_desc(sQ + c * BM * 128 + kk * 32, 16, 1024);
                     const uint64_t bd = tc::smem_desc(sK + st * L::KV_BYTES + c * BN * 128 + kk * 32, 16, 1024);
-                    tc::mma_f16(tmem + st * BN, ad, bd, IQK, k > 0 ? 1u : 0u);
+                    tc::mma_f16(tmem, ad, bd, IQK, k > 0 ? 1u : 0u);
                 }
-                tc::commit(s_full + st);
+                tc::commit(s_full);
                 tc::commit(k_empty + st);
                 return true;
             };
@@ -398,22 +421,23 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                     } else {
                         tc::commit(q_empty); // the item's last S has been issued: Q may be replaced
                     }
-                    const int st = (int)(gg & 1);
-                    ok = mbar_wait(p_full, gg & 1) && mbar_wait(v_full + st, (gg >> 1) & 1);
+                    const int sv = (int)(gg % NVS);
+                    ok = mbar_wait(p_full + (gg & 1), (gg >> 1) & 1) && mbar_wait(v_full + sv, (gg / NVS) & 1);
                     // the epilogue of the previous item has read O out of TMEM
                     if (ok && j == 0 && n >= 1) ok = mbar_wait(o_free, (n - 1) & 1);
                     if (!ok) break;
                     tc::fence_after_sync();
+                    // O += P V, P (A operand) read from tensor memory where the softmax left it
 #pragma unroll
                     for (int part = 0; part < L::NP; ++part)
 #pragma unroll
                         for (int k = 0; k < BN / 16; ++k) {
-                            const uint64_t ad = tc::smem_desc(sP + part * L::P_BYTES + k * 32, 16, 1024);
-                            const uint64_t bd = tc::smem_desc(sV + st * L::KV_BYTES + k * 2048, BN * 128, 1024);
-                            tc::mma_f16(tO, ad, bd, IPV, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
+                            const uint32_t at = tmem + (uint32_t)(BN + (int)(gg % L::NPB) * (BN / 2) + part * (BN / 2) + k * 8);
+                            const uint64_t bd = tc::smem_desc(sV + sv * L::KV_BYTES + k * 2048, BN * 128, 1024);
+                            tc::mma_f16_ts(tO, at, bd, IPV, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
                         }
-                    tc::commit(t_full);
-                    tc::commit(v_empty + st);
+                    tc::commit(t_full + (gg & 1));
+                    tc::commit(v_empty + sv);
                 }
                 g += it.nkv;
                 mbar_arrive(item_empty + (n & 1));
@@ -432,7 +456,6 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
         const int lw = warp & 3;
         const int r = lw * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(lw * 32) << 16;
-        uint8_t *prow = smem + L::P + (r >> 3) * 1024 + (r & 7) * 128;
         bool ok = true;
         int64_t g = 0;
         for (int n = 0; ok; ++n) {
@@ -443,20 +466,19 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             float m_use = -INFINITY, l = 0.f;
             for (int j = 0; j < it.nkv && ok; ++j) {
                 const int64_t gg = g + j;
-                const int b = (int)(gg & 1);
-                ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (gg >> 1) & 1));
+                ok = __all_sync(0xffffffffu, mbar_wait(s_full, gg & 1));
                 if (!ok) break;
                 tc::fence_after_sync();
                 uint32_t sr[64];
                 {
                     uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
                     uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-                    tc::ld32(tmem + lane_off + b * BN, lo);
-                    tc::ld32(tmem + lane_off + b * BN + 32, hi);
+                    tc::ld32(tmem + lane_off, lo);
+                    tc::ld32(tmem + lane_off + 32, hi);
                 }
                 tc::wait_ld();
                 tc::fence_before_sync();
-                mbar_arrive(s_free + b);
+                mbar_arrive(s_free); // the S buffer may take the next tile
                 // causal mask, only on tiles that reach past the item's first query row
                 const int kbase = j * BN;
                 if (kbase + BN - 1 > q0) {
@@ -490,39 +512,40 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                         plo[c] = pack2(p0 - __uint_as_float(phi[c] << 16), p1 - __uint_as_float(phi[c] & 0xFFFF0000u), MT);
                 }
                 l = l * alpha + (rs0 + rs1);
-                if (j > 0) {
-                    // P V of the previous tile has finished: P's buffer is free and O is stable
-                    ok = __all_sync(0xffffffffu, mbar_wait(t_full, (gg - 1) & 1));
+                // P V of the previous tile must have finished when O is rescaled (only when a row's
+                // base moved) and, with a single P buffer, before P is overwritten.  The wait is
+                // unambiguous: S of this tile is done, hence P V of tile gg - 2 (issued before it), and
+                // P V of tile gg + 1 cannot start before this thread's later p_full arrivals.  With two
+                // P buffers, the one of tile gg was last read by P V of tile gg - 2, already done.  At
+                // j = 0 the previous item's epilogue has waited for its last P V.
+                const bool moved = __any_sync(0xffffffffu, up);
+                if (j > 0 && (L::NPB == 1 || moved)) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(t_full + ((gg - 1) & 1), ((gg - 1) >> 1) & 1));
                     if (!ok) break;
                     tc::fence_after_sync();
-                    if (__any_sync(0xffffffffu, up)) {
+                }
+                if (j > 0 && moved) {
 #pragma unroll
-                        for (int cc = 0; cc < D / 16; ++cc) {
-                            uint32_t o[16];
-                            tc::ld16(tmem + lane_off + 128 + cc * 16, o);
-                            tc::wait_ld();
+                    for (int cc = 0; cc < D / 16; ++cc) {
+                        uint32_t o[16];
+                        tc::ld16(tmem + lane_off + 2 * BN + cc * 16, o);
+                        tc::wait_ld();
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tc::st16(tmem + lane_off + 128 + cc * 16, o);
-                        }
-                        tc::wait_st();
+                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tc::st16(tmem + lane_off + 2 * BN + cc * 16, o);
                     }
                 }
-#pragma unroll
-                for (int c = 0; c < BN / 8; ++c) {
-                    const int off = (c ^ (r & 7)) << 4;
-                    *reinterpret_cast<uint4 *>(prow + off) =
-                        make_uint4(phi[4 * c], phi[4 * c + 1], phi[4 * c + 2], phi[4 * c + 3]);
-                    if constexpr (L::NP == 2)
-                        *reinterpret_cast<uint4 *>(prow + L::P_BYTES + off) =
-                            make_uint4(plo[4 * c], plo[4 * c + 1], plo[4 * c + 2], plo[4 * c + 3]);
-                }
-                fence_proxy_async_smem();
+                // P into its tensor-memory buffer: packed pairs, key c in column c / 2
+                const uint32_t pcol = (uint32_t)(BN + (int)(gg % L::NPB) * (BN / 2));
+                tc::st32(tmem + lane_off + pcol, phi);
+                if constexpr (L::NP == 2) tc::st32(tmem + lane_off + pcol + BN / 2, plo);
+                tc::wait_st();
                 tc::fence_before_sync();
-                mbar_arrive(p_full);
+                mbar_arrive(p_full + (gg & 1));
             }
             g += it.nkv;
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(t_full, (g - 1) & 1));
+            // the commit after P V of the item's last tile covers every earlier MMA as well
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(t_full + ((g - 1) & 1), ((g - 1) >> 1) & 1));
             if (!ok) break;
             tc::fence_after_sync();
             const float inv = 1.f / l;
@@ -531,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
 #pragma unroll
             for (int cc = 0; cc < D / 16; ++cc) {
                 uint32_t o[16];
-                tc::ld16(tmem + lane_off + 128 + cc * 16, o);
+                tc::ld16(tmem + lane_off + 2 * BN + cc * 16, o);
                 tc::wait_ld();
                 uint32_t w[8];
 #pragma unroll
@@ -552,18 +575,21 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
         if (!ok) fail();
     } else {
         // ------------------------------------------------------------ paged K/V write of the item's rows
-        // The item's own rows q0..qlast are the keys of its last K/V tiles (q0/BN .. nkv-1).  These
-        // warps follow every K/V tile of the ring in order (so a stage's phase is never more than
-        // one ahead of them) and hold each stage until they are done with it: a stage frees only
-        // after the MMA that reads it and both writer warps.  The item's rows are copied straight
-        // from shared memory (undoing the 128-byte swizzle) to their slots as soon as their tiles
-        // land, one contiguous D*2-byte store per row from D/8 lanes; the block-table entries of the
-        // item's rows are read once, at the start of the item, one per lane.
+        // The item's own rows q0..qlast are the keys of its last K/V tiles (q0/BN .. nkv-1).  This
+        // warp follows every K tile and every V tile of the rings in order (so a stage's phase is
+        // never more than one ahead of it) and holds each stage until it is done with it: a stage
+        // frees only after the MMA that reads it and this warp.  K and V are released independently,
+        // so a K stage never waits for its V tile to land.  Whole blocks of the item's rows leave
+        // shared memory as tiled TMA stores (one lane per block; one box of bs rows x 64 dims per
+        // half of D, the 128-byte swizzle undone by the copy engine) into their (block, K|V, head)
+        // tile of the pool; the rows of a partly filled last block (a sequence whose length is not a
+        // multiple of bs) go out as plain 16-byte stores, so no slot past the sequence is touched.
+        // The block-table entries of the item's rows are read once, at the start of the item.
         constexpr int CPR = D / 8;   // 16-byte chunks per row
         constexpr int RPI = 32 / CPR; // rows per warp instruction
-        const int wl = warp - 6;
         const int cc = lane % CPR, rsub = lane / CPR;
         const int c2 = cc >> 3, u = cc & 7;
+        if (lane == 0) tc::prefetch_tmap(&tp);
         bool ok = true;
         int64_t g = 0;
         for (int n = 0; ok; ++n) {
@@ -571,51 +597,74 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             ok = __all_sync(0xffffffffu, ok);
             if (!ok || it.seq < 0) break;
             const bool writes = it.h % G == 0;
-            const int kvh = it.h / G, lb0 = it.q0 / a.bs;
-            // lane l: table entry of logical block lb0 + l (at most BM / bs + 1 <= 17 of them)
+            const int kvh = it.h / G, lb0 = it.q0 >> a.lg_bs;
+            // lane l: table entry of logical block lb0 + l (at most BM / bs <= 16 of them)
             int blkv = -1;
             {
                 const int lb = lb0 + lane;
-                if (writes && lb * a.bs <= it.qlast && lb < a.max_blocks)
+                if (writes && (lb << a.lg_bs) <= it.qlast && lb < a.max_blocks)
                     blkv = a.tables[(int64_t)it.seq * a.max_blocks + lb];
             }
-            for (int j = 0; j < it.nkv && ok; ++j) {
-                const int64_t gg = g + j;
-                const int st = (int)(gg & 1);
-                ok = __all_sync(0xffffffffu, mbar_wait(k_full + st, (gg >> 1) & 1) && mbar_wait(v_full + st, (gg >> 1) & 1));
-                if (!ok) break;
-                if (writes && j >= it.q0 / BN) {
-                    const int lo = max(j * BN, it.q0), hi = min(j * BN + BN - 1, it.qlast);
-                    for (int p0 = lo + wl * RPI; p0 <= hi; p0 += 2 * RPI) {
-                        const int p = p0 + rsub;
-                        const int lb = p / a.bs;
-                        const int blk = __shfl_sync(0xffffffffu, blkv, min(lb - lb0, 31));
-                        if (p > hi) continue;
+            // the item's rows of tile j, from `src` (a K or a V stage) into the K (kv = 0) or V half
+            auto write_tile = [&](int j, const uint8_t *src, int kv) {
+                const int lo = max(j * BN, it.q0), hi = min(j * BN + BN - 1, it.qlast);
+                if (lo > hi) return;
+                const int bfirst = lo >> a.lg_bs;            // lo is a multiple of bs
+                const int nfull = (hi + 1 - lo) >> a.lg_bs;  // whole blocks among the rows
+                {
+                    const int lb = bfirst + lane;
+                    const int blk = __shfl_sync(0xffffffffu, blkv, min(lb - lb0, 31));
+                    if (lane < nfull) {
                         if (blk < 0 || blk >= a.num_blocks) {
-                            if (cc == 0) set_error(a.err, PKV_DEVERR_BLOCK_ID);
-                            continue;
+                            set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                        } else {
+                            const uint8_t *box = src + ((lb << a.lg_bs) - j * BN) * 128;
+                            const int y = ((blk * 2 + kv) * a.hkv + kvh) << a.lg_bs;
+#pragma unroll
+                            for (int c = 0; c < D / 64; ++c) tc::tma_store_2d(&tp, c * 64, y, box + c * BN * 128);
+                            tc::bulk_commit();
                         }
-                        const int r = p - j * BN;
-                        const int sw = c2 * BN * 128 + (r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4);
-                        const uint4 kx = *reinterpret_cast<const uint4 *>(smem + L::K0 + st * L::KV_BYTES + sw);
-                        const uint4 vx = *reinterpret_cast<const uint4 *>(smem + L::V0 + st * L::KV_BYTES + sw);
-                        const int64_t dst = ((int64_t)blk * 2 * a.hkv + kvh) * a.tile_elems +
-                                            (int64_t)(p - lb * a.bs) * D + cc * 8;
-                        *reinterpret_cast<uint4 *>(a.pool + dst * 2) = kx;
-                        *reinterpret_cast<uint4 *>(a.pool + (dst + (int64_t)a.hkv * a.tile_elems) * 2) = vx;
                     }
                 }
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(k_empty + st);
-                    mbar_arrive(v_empty + st);
+                for (int p0 = lo + (nfull << a.lg_bs); p0 <= hi; p0 += RPI) { // fewer than bs rows
+                    const int p = p0 + rsub;
+                    const int lb = p >> a.lg_bs;
+                    const int blk = __shfl_sync(0xffffffffu, blkv, min(lb - lb0, 31));
+                    if (p > hi) continue;
+                    if (blk < 0 || blk >= a.num_blocks) {
+                        if (cc == 0) set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                        continue;
+                    }
+                    const int r = p - j * BN;
+                    const int sw = c2 * BN * 128 + (r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4);
+                    const uint4 x = *reinterpret_cast<const uint4 *>(src + sw);
+                    const int64_t dst = ((int64_t)(blk * 2 + kv) * a.hkv + kvh) * a.tile_elems +
+                                        (int64_t)(p - (lb << a.lg_bs)) * D + cc * 8;
+                    *reinterpret_cast<uint4 *>(a.pool + dst * 2) = x;
                 }
+                tc::bulk_wait_read_all(); // the stores have read the stage; it may be released
+            };
+            for (int j = 0; j < it.nkv && ok; ++j) {
+                const int64_t gg = g + j;
+                const bool mine = writes && j >= it.q0 / BN;
+                const int sk = (int)(gg % NKS), sv = (int)(gg % NVS);
+                ok = __all_sync(0xffffffffu, mbar_wait(k_full + sk, (gg / NKS) & 1));
+                if (!ok) break;
+                if (mine) write_tile(j, smem + L::K0 + sk * L::KV_BYTES, 0);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(k_empty + sk);
+                ok = __all_sync(0xffffffffu, mbar_wait(v_full + sv, (gg / NVS) & 1));
+                if (!ok) break;
+                if (mine) write_tile(j, smem + L::V0 + sv * L::KV_BYTES, 1);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(v_empty + sv);
             }
             if (!ok) break;
             g += it.nkv;
             if (lane == 0) mbar_arrive(item_empty + (n & 1));
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
         }
+        tc::bulk_wait_all(); // the pool writes have completed before the CTA exits
         if (!ok && lane == 0) fail();
     }
 
@@ -661,17 +710,25 @@ bool make_map(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t co
 }
 
 template <int D, int MT>
-cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const Args &a,
-                     int64_t max_ctas, int num_sms, cudaStream_t st) {
+cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tp,
+                     const Args &a, int64_t max_ctas, int num_sms, cudaStream_t st) {
     auto kern = prefill_kernel<D, MT>;
     const int smem = Layout<D, MT>::TOTAL;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    // all of the unified L1/shared array as shared memory: two CTAs of ~113 KB then fit an SM
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
+    // resident CTAs per SM: what the launch bounds and the shared-memory size were chosen for (the
+    // occupancy query answers 1 here, though two CTAs of this size do run side by side on an SM)
+    int per_sm = min_blocks<D, MT>();
+    if (const char *v = std::getenv("PAGEDKV_PREFILL_CTAS")) {
+        // resident CTAs per SM, for tuning sweeps (persistent CTAs beyond what fits simply run later)
+        const int x = std::atoi(v);
+        if (x > 0 && x <= 4) per_sm = x;
+    }
     const int64_t grid = std::min<int64_t>(max_ctas, (int64_t)num_sms * std::max(per_sm, 1));
-    return pdl_launch(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, tq, tk, tv, a);
+    return pdl_launch(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, tq, tk, tv, tp, a);
 }
 
 cudaError_t launch_plan(const Args &a, cudaStream_t st) {
@@ -709,6 +766,8 @@ cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st
     a.hq = p.num_q_heads;
     a.hkv = c->num_kv_heads;
     a.bs = c->block_size;
+    a.lg_bs = 0;
+    while ((1 << a.lg_bs) < c->block_size) ++a.lg_bs;
     a.nqt_max = (p.max_seqlen + BM - 1) / BM;
     a.scale_log2 = p.scale * 1.4426950408889634f;
     // (sequence, query tile) items: sum_i ceil(n_i / BM) <= T / BM + num_seqs
@@ -730,10 +789,15 @@ cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st
         c->plan_bytes = plan_bytes;
     }
     a.plan = c->plan;
-    CUtensorMap tq, tk, tv;
+    // the pool as rows [(block, K|V, head, slot)][D] for the tiled stores of whole blocks; row
+    // coordinates are 32-bit
+    const int64_t pool_rows = c->num_blocks * 2 * c->num_kv_heads * c->block_size;
+    if (pool_rows > 0x7FFFFFFFLL) return cudaErrorNotSupported;
+    CUtensorMap tq, tk, tv, tp;
     if (!make_map(&tq, p.q, mt, p.total_tokens, (int64_t)p.num_q_heads * D, BM) ||
         !make_map(&tk, p.k, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN) ||
-        !make_map(&tv, p.v, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN))
+        !make_map(&tv, p.v, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN) ||
+        !make_map(&tp, c->pool, mt, pool_rows, D, c->block_size))
         return cudaErrorInvalidValue;
     PkvTimer timer(c, PKV_KIND_PREFILL, st);
     cudaError_t e = launch_plan(a, st);
@@ -741,11 +805,11 @@ cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st
     if (e != cudaSuccess) return e;
     const int64_t max_ctas = items * p.num_q_heads;
     if (D == 128)
-        e = mt == PKV_BF16 ? launch_t<128, PKV_BF16>(tq, tk, tv, a, max_ctas, c->num_sms, st)
-                           : launch_t<128, PKV_F16>(tq, tk, tv, a, max_ctas, c->num_sms, st);
+        e = mt == PKV_BF16 ? launch_t<128, PKV_BF16>(tq, tk, tv, tp, a, max_ctas, c->num_sms, st)
+                           : launch_t<128, PKV_F16>(tq, tk, tv, tp, a, max_ctas, c->num_sms, st);
     else
-        e = mt == PKV_BF16 ? launch_t<64, PKV_BF16>(tq, tk, tv, a, max_ctas, c->num_sms, st)
-                           : launch_t<64, PKV_F16>(tq, tk, tv, a, max_ctas, c->num_sms, st);
+        e = mt == PKV_BF16 ? launch_t<64, PKV_BF16>(tq, tk, tv, tp, a, max_ctas, c->num_sms, st)
+                           : launch_t<64, PKV_F16>(tq, tk, tv, tp, a, max_ctas, c->num_sms, st);
     g_pkv_launches++;
     return e;
 }
