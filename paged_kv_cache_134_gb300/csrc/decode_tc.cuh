@@ -17,8 +17,9 @@
 // Work unit = (sequence, KV head, split of up to split_blocks blocks), the same unit list as the
 // CUDA-core kernel (full splits first), round-robin over one persistent CTA per SM.  A unit is
 // processed in steps of 128 tokens.  Roles:
-//   warp 0     loads: block-table entries (one lane per block of the step), Q of the unit, and the
-//              K and V boxes of every block into rings of 3 K and 3 V stages;
+//   warp 0     loads: block-table entries (one lane per block of the step, read a step ahead), Q of
+//              the unit, and the K boxes of every block into a ring of 3 K stages;
+//   warp 6     the same walk for the V boxes (ring of 3 V stages);
 //   warp 1     tensor-memory owner and MMA issuer (one thread);
 //   warps 2-5  one thread per token row of S^T (a TMEM lane): mask, scale, tile max over the 128
 //              rows (shuffles + shared memory), online softmax with a lazily moved base (the base
@@ -42,21 +43,25 @@ constexpr int D = 128;
 constexpr int TOK = 128;             // tokens per step: MMA M of S^T, MMA K of O^T
 constexpr int NQ = 16;               // MMA N: the group's query heads, padded
 constexpr int NS = 3;                // K stages and V stages
-constexpr int kThreads = 192;        // warp 0 loads, warp 1 MMA, warps 2-5 softmax
-constexpr uint32_t kTmemCols = 64;   // S0 [0,16) S1 [16,32) O [32,48)
+constexpr int kThreads = 224;        // warp 0 Q and K loads, warp 1 MMA, warps 2-5 softmax, warp 6 V loads
+constexpr uint32_t kTmemCols = 64;   // S0 [0,16) S1 [16,32) O^T [32, 32 + 16 NP)
 constexpr float kRescale = 8.0f;     // log2 units
 
 template <int MT>
 struct Layout {
-    static constexpr int NP = MT == PKV_BF16 ? 2 : 1;      // P tiles (hi, lo for bf16)
+    static constexpr int NP = MT == PKV_BF16 ? 2 : 1;      // P parts (hi, lo for bf16)
+    // rows of the P^T operand: the group's heads (padded to NQ), and for bf16 the lo parts as rows
+    // NQ.. 2 NQ - 1, so that one N = 2 NQ MMA per K step covers both parts (the two O^T column
+    // groups are added in the epilogue)
+    static constexpr int NPR = NQ * NP;
     static constexpr int STAGE = TOK * D * 2;              // [half][128 rows][128 B] = 32 KB
     static constexpr int K0 = 0;
     static constexpr int V0 = K0 + NS * STAGE;
     static constexpr int Q = V0 + NS * STAGE;              // [2 buffers][half][16 rows][128 B]
     static constexpr int Q_BYTES = NQ * D * 2;
     static constexpr int P = Q + 2 * Q_BYTES;                  // [buffer][part][64-token chunk][16 rows][128 B]
-    static constexpr int P_BYTES = NQ * TOK * 2;
-    static constexpr int RED = P + 2 * NP * P_BYTES;       // [2][4 warps][NQ] maxima, [4 warps][NQ] sums
+    static constexpr int P_BYTES = NPR * TOK * 2;          // one buffer
+    static constexpr int RED = P + 2 * P_BYTES;            // [2][4 warps][NQ] maxima, [4 warps][NQ] sums
     static constexpr int BAR = RED + (3 * 4 * NQ) * 4;
     static constexpr int FIXED = BAR + 512;                // + unit tables, 3 (S + 1) ints
 };
@@ -77,10 +82,12 @@ PKV_DEV uint32_t pack2(float lo, float hi) {
     return r;
 }
 
-// byte offset of element (row g, token t) in a P tile: K-major, 128-byte swizzle, 64-token chunks
+// byte offset of element (row g, token t) in a P buffer of NPR rows: K-major, 128-byte swizzle,
+// 64-token chunks
+template <int NPR>
 PKV_DEV int p_offset(int g, int t) {
     const int e = t & 63;
-    return (t >> 6) * (NQ * 128) + (g >> 3) * 1024 + (g & 7) * 128 + ((((e >> 3) ^ (g & 7))) << 4) + ((e & 7) << 1);
+    return (t >> 6) * (NPR * 128) + (g >> 3) * 1024 + (g & 7) * 128 + ((((e >> 3) ^ (g & 7))) << 4) + ((e & 7) << 1);
 }
 
 template <int G, int MT>
@@ -152,19 +159,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
     };
 
-    if (warp == 0) {
+    if (warp == 0 || warp == 6) {
         // ---------------------------------------------------------------- loads
+        // Warp 0 loads Q of each unit and the K boxes, warp 6 the V boxes (one warp issuing both
+        // spent most of each step issuing boxes one after another).  Both walk this CTA's steps in
+        // the same order, one lane per block of a step, and read the block-table entries of the
+        // next step before issuing the current one, so the table read latency stays off the path.
+        const bool is_k = warp == 0;
         const uint64_t policy = l2_policy_evict_first();
-        if (lane == 0) {
-            tc::prefetch_tmap(&tkv);
-            tc::prefetch_tmap(&tq);
-        }
+        if (lane == 0) tc::prefetch_tmap(&tkv);
+        if (lane == 0 && is_k) tc::prefetch_tmap(&tq);
+        // table entry of this lane's block in step i of unit `un` (0 for lanes past the step's blocks)
+        auto entry = [&](const Unit &un, int i) -> int {
+            const int nblk = min(bpstep, un.ntiles - i * bpstep);
+            return lane < nblk ? a.tables[(int64_t)un.s * a.max_blocks + un.blk0 + i * bpstep + lane] : 0;
+        };
         int64_t gs = 0; // steps issued so far, all units
         int nu = 0, last_q = -1;
         bool ok = true;
-        for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
-            const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps);
-            if (lane == 0) {
+        int u = blockIdx.x, i = 0, nsteps = 0;
+        Unit un{};
+        if (u < U) {
+            un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps);
+            nsteps = (un.ntiles + bpstep - 1) / bpstep;
+        }
+        int cur = u < U ? entry(un, 0) : 0;
+        while (u < U && ok) {
+            if (i == 0 && is_k && lane == 0) {
                 // Q of unit nu goes to buffer nu % 2, free once the last S^T of unit nu - 2 is done
                 const int qb = nu & 1;
                 if (nu >= 2 && !mbar_wait(q_empty + qb, ((nu >> 1) - 1) & 1)) ok = false;
@@ -178,67 +199,77 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            const int32_t *trow = a.tables + (int64_t)un.s * a.max_blocks + un.blk0;
-            const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
-            for (int i = 0; i < nsteps && ok; ++i, ++gs) {
-                const int st = (int)(gs % NS);
-                const int64_t round = gs / NS;
-                const int nblk = min(bpstep, un.ntiles - i * bpstep);
-                const int b = lane < nblk ? trow[i * bpstep + lane] : 0;
-                const bool good = lane < nblk && b >= 0 && b < a.num_blocks;
-                const unsigned goodmask = __ballot_sync(0xffffffffu, good);
-                const unsigned bad = __ballot_sync(0xffffffffu, lane < nblk && !good);
-                const uint32_t bytes = (uint32_t)__popc(goodmask) * (uint32_t)a.bs * (D * 2);
-                if (lane == 0) {
-                    if (bad) set_error(a.err, PKV_DEVERR_BLOCK_ID);
-                    if (round >= 1 && !mbar_wait(k_empty + st, (round - 1) & 1)) ok = false;
-                    if (ok) mbar_arrive_expect_tx(k_full + st, bytes);
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok || *abort_flag) break;
-                // row of (block b, K or V, KV head) in the pool's [rows][D] view
-                const int krow = ((b * 2 + 0) * a.hkv + un.kvh) * a.bs, vrow = ((b * 2 + 1) * a.hkv + un.kvh) * a.bs;
-                if (good) {
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c)
-                        tc::tma_load_2d_hint(smem + LY::K0 + st * LY::STAGE + c * (TOK * 128) + lane * a.bs * 128, &tkv,
-                                             c * 64, krow, k_full + st, policy);
-                }
-                if (lane == 0) {
-                    if (round >= 1 && !mbar_wait(v_empty + st, (round - 1) & 1)) ok = false;
-                    if (ok) {
-                        badmask[st] = bad; // read by the softmax after v_full, freed with v_empty
-                        mbar_arrive_expect_tx(v_full + st, bytes);
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                if (good) {
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c)
-                        tc::tma_load_2d_hint(smem + LY::V0 + st * LY::STAGE + c * (TOK * 128) + lane * a.bs * 128, &tkv,
-                                             c * 64, vrow, v_full + st, policy);
+            if (!ok) break;
+            // the next step (maybe of the next unit) and its table entries, read ahead
+            int u2 = u, i2 = i + 1, nsteps2 = nsteps;
+            Unit un2 = un;
+            if (i2 >= nsteps) {
+                u2 = u + gridDim.x;
+                i2 = 0;
+                if (u2 < U) {
+                    un2 = pkv_decode::unit_info(u2, pf, pp, nb, S, a.hkv, bps);
+                    nsteps2 = (un2.ntiles + bpstep - 1) / bpstep;
                 }
             }
+            const int nxt = u2 < U ? entry(un2, i2) : 0;
+            // this step
+            const int st = (int)(gs % NS);
+            const int64_t round = gs / NS;
+            const int nblk = min(bpstep, un.ntiles - i * bpstep);
+            const int b = cur;
+            const bool good = lane < nblk && b >= 0 && b < a.num_blocks;
+            const unsigned goodmask = __ballot_sync(0xffffffffu, good);
+            const unsigned bad = __ballot_sync(0xffffffffu, lane < nblk && !good);
+            const uint32_t bytes = (uint32_t)__popc(goodmask) * (uint32_t)a.bs * (D * 2);
+            uint64_t *full = is_k ? k_full + st : v_full + st;
+            uint64_t *empty = is_k ? k_empty + st : v_empty + st;
+            if (lane == 0) {
+                if (round >= 1 && !mbar_wait(empty, (round - 1) & 1)) ok = false;
+                if (ok) {
+                    if (!is_k) {
+                        if (bad) set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                        badmask[st] = bad; // read by the softmax after v_full, freed with v_empty
+                    }
+                    mbar_arrive_expect_tx(full, bytes);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok || *abort_flag) break;
+            // row of (block b, K or V, KV head) in the pool's [rows][D] view
+            const int row = ((b * 2 + (is_k ? 0 : 1)) * a.hkv + un.kvh) * a.bs;
+            uint8_t *dst0 = smem + (is_k ? LY::K0 : LY::V0) + st * LY::STAGE + lane * a.bs * 128;
+            if (good) {
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tc::tma_load_2d_hint(dst0 + c * (TOK * 128), &tkv, c * 64, row, full, policy);
+            }
+            ++gs;
+            cur = nxt;
+            if (i2 == 0) ++nu;
+            u = u2;
+            i = i2;
+            un = un2;
+            nsteps = nsteps2;
         }
         if (!ok && lane == 0) fail();
         // the next kernel (the split merge) may start launching once every CTA has issued its last load
-        pdl_trigger();
+        if (is_k) pdl_trigger();
         // the copies of the last stages must land before this CTA's shared memory goes away
         if (lane == 0) {
-            for (int64_t g = gs > NS ? gs - NS : 0; g < gs; ++g) {
-                if (!mbar_wait(k_full + g % NS, (g / NS) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
-                if (!mbar_wait(v_full + g % NS, (g / NS) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
-            }
-            for (int n = last_q > 0 ? last_q - 1 : 0; n <= last_q; ++n)
-                if (!mbar_wait(q_full + (n & 1), (n >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            for (int64_t g = gs > NS ? gs - NS : 0; g < gs; ++g)
+                if (!mbar_wait((is_k ? k_full : v_full) + g % NS, (g / NS) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            if (is_k)
+                for (int n = last_q > 0 ? last_q - 1 : 0; n <= last_q; ++n)
+                    if (!mbar_wait(q_full + (n & 1), (n >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // the whole warp runs the issue loop in step (waits agreed with __all_sync); one elected lane
+        // issues each MMA and commit
+        {
             constexpr uint32_t ab = MT == PKV_BF16 ? 1u : 0u;
             constexpr uint32_t ISK = tc::idesc_f16_ab(ab, 0u, 0u, TOK, NQ); // A = K (K-major), B = Q (K-major)
-            constexpr uint32_t IPV = tc::idesc_f16_ab(ab, 1u, 0u, D, NQ);   // A = V^T (MN-major), B = P (K-major)
+            constexpr uint32_t IPV = tc::idesc_f16_ab(ab, 1u, 0u, D, LY::NPR); // A = V^T (MN-major), B = P (K-major)
             const uint32_t sK = smem_u32(smem + LY::K0), sV = smem_u32(smem + LY::V0);
             const uint32_t sQ = smem_u32(smem + LY::Q), sP = smem_u32(smem + LY::P);
             const uint32_t tO = tmem + 2 * NQ;
@@ -246,8 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S^T of step g (Q buffer qb) into S buffer g % 2; the K stage is released as soon as S^T is done
             auto issue_s = [&](int64_t g, int qb) -> bool {
                 const int st = (int)(g % NS), b = (int)(g & 1);
-                if (!mbar_wait(k_full + st, (g / NS) & 1)) return false;
-                if (g >= 2 && !mbar_wait(s_free + b, ((g >> 1) - 1) & 1)) return false;
+                if (!__all_sync(0xffffffffu, mbar_wait(k_full + st, (g / NS) & 1))) return false;
+                if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(s_free + b, ((g >> 1) - 1) & 1))) return false;
                 tc::fence_after_sync();
                 any_mma = true;
 #pragma unroll
@@ -255,10 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int c = k >> 2, kk = k & 3;
                     const uint64_t ad = tc::smem_desc(sK + st * LY::STAGE + c * (TOK * 128) + kk * 32, 16, 1024);
                     const uint64_t bd = tc::smem_desc(sQ + qb * LY::Q_BYTES + c * (NQ * 128) + kk * 32, 16, 1024);
-                    tc::mma_f16(tmem + b * NQ, ad, bd, ISK, k > 0 ? 1u : 0u);
+                    tc::mma_f16_warp(tmem + b * NQ, ad, bd, ISK, k > 0 ? 1u : 0u);
                 }
-                tc::commit(s_full + b);
-                tc::commit(k_empty + st);
+                tc::commit_warp(s_full + b);
+                tc::commit_warp(k_empty + st);
                 return true;
             };
             bool ok = true;
@@ -268,42 +299,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps);
                 const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
                 const int qb = nu & 1;
-                ok = mbar_wait(q_full + qb, (nu >> 1) & 1) && issue_s(gs, qb);
+                ok = __all_sync(0xffffffffu, mbar_wait(q_full + qb, (nu >> 1) & 1)) && issue_s(gs, qb);
                 for (int i = 0; i < nsteps && ok; ++i) {
                     const int64_t g = gs + i;
                     if (i + 1 < nsteps) {
                         ok = issue_s(g + 1, qb);
                         if (!ok) break;
                     } else {
-                        tc::commit(q_empty + qb); // the unit's last S^T has been issued: its Q buffer may be refilled
+                        tc::commit_warp(q_empty + qb); // the unit's last S^T has been issued: its Q buffer may be refilled
                     }
                     const int st = (int)(g % NS), b = (int)(g & 1);
-                    ok = mbar_wait(p_full + b, (g >> 1) & 1) && mbar_wait(v_full + st, (g / NS) & 1);
+                    ok = __all_sync(0xffffffffu, mbar_wait(p_full + b, (g >> 1) & 1) && mbar_wait(v_full + st, (g / NS) & 1));
                     // the epilogue of the previous unit has read O^T out of tensor memory
-                    if (ok && i == 0 && nu >= 1) ok = mbar_wait(o_free, (nu - 1) & 1);
+                    if (ok && i == 0 && nu >= 1) ok = __all_sync(0xffffffffu, mbar_wait(o_free, (nu - 1) & 1));
                     if (!ok) break;
                     tc::fence_after_sync();
 #pragma unroll
-                    for (int part = 0; part < LY::NP; ++part)
-#pragma unroll
-                        for (int k = 0; k < TOK / 16; ++k) {
-                            const uint64_t ad = tc::smem_desc(sV + st * LY::STAGE + k * 2048, TOK * 128, 1024);
-                            const uint64_t bd = tc::smem_desc(
-                                sP + (b * LY::NP + part) * LY::P_BYTES + (k >> 2) * (NQ * 128) + (k & 3) * 32, 16, 1024);
-                            tc::mma_f16(tO, ad, bd, IPV, (i > 0 || k > 0 || part > 0) ? 1u : 0u);
-                        }
-                    tc::commit(t_full + b);
-                    tc::commit(v_empty + st);
-                    if (i + 1 == nsteps) tc::commit(o_full);
+                    for (int k = 0; k < TOK / 16; ++k) {
+                        const uint64_t ad = tc::smem_desc(sV + st * LY::STAGE + k * 2048, TOK * 128, 1024);
+                        const uint64_t bd = tc::smem_desc(
+                            sP + b * LY::P_BYTES + (k >> 2) * (LY::NPR * 128) + (k & 3) * 32, 16, 1024);
+                        tc::mma_f16_warp(tO, ad, bd, IPV, (i > 0 || k > 0) ? 1u : 0u);
+                    }
+                    tc::commit_warp(t_full + b);
+                    tc::commit_warp(v_empty + st);
+                    if (i + 1 == nsteps) tc::commit_warp(o_full);
                 }
                 gs += nsteps;
-                if (*abort_flag) break;
+                if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             }
-            if (!ok) fail();
-            // every MMA issued by this thread has completed before tensor memory is released
+            if (!ok && lane == 0) fail();
+            // every MMA issued by the elected lane has completed before tensor memory is released
             if (any_mma) {
-                tc::commit(fin);
-                if (!mbar_wait(fin, 0)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+                tc::commit_warp(fin);
+                if (!__all_sync(0xffffffffu, mbar_wait(fin, 0)) && lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
             }
         }
     } else {
@@ -388,26 +417,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = __all_sync(0xffffffffu, mbar_wait(t_full + (b ^ 1), ((g0 - 1) >> 1) & 1));
                     if (ok) {
                         tc::fence_after_sync();
-                        uint32_t o[G];
-                        tc::ldn<G>(tmem + lane_off + 2 * NQ, o);
-                        tc::wait_ld();
 #pragma unroll
-                        for (int g = 0; g < G; ++g) o[g] = __float_as_uint(__uint_as_float(o[g]) * alpha[g]);
-                        tc::stn<G>(tmem + lane_off + 2 * NQ, o);
+                        for (int part = 0; part < LY::NP; ++part) {
+                            uint32_t o[G];
+                            tc::ldn<G>(tmem + lane_off + 2 * NQ + part * NQ, o);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int g = 0; g < G; ++g) o[g] = __float_as_uint(__uint_as_float(o[g]) * alpha[g]);
+                            tc::stn<G>(tmem + lane_off + 2 * NQ + part * NQ, o);
+                        }
                         tc::wait_st();
                     }
                 }
                 // a warp that failed here carries ok = false to the next barrier
                 if (!ok) continue;
-                uint8_t *pb = smem + LY::P + b * LY::NP * LY::P_BYTES;
+                uint8_t *pb = smem + LY::P + b * LY::P_BYTES;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const int off = p_offset(g, r);
+                    const int off = p_offset<LY::NPR>(g, r);
                     if constexpr (LY::NP == 2) {
                         const uint32_t hi = pack2<MT>(p[g], 0.f) & 0xFFFFu;
                         const float rest = p[g] - __uint_as_float(hi << 16);
                         *reinterpret_cast<uint16_t *>(pb + off) = (uint16_t)hi;
-                        *reinterpret_cast<uint16_t *>(pb + LY::P_BYTES + off) = (uint16_t)(pack2<MT>(rest, 0.f) & 0xFFFFu);
+                        *reinterpret_cast<uint16_t *>(pb + p_offset<LY::NPR>(NQ + g, r)) =
+                            (uint16_t)(pack2<MT>(rest, 0.f) & 0xFFFFu);
                     } else {
                         *reinterpret_cast<uint16_t *>(pb + off) = (uint16_t)(pack2<MT>(p[g], 0.f) & 0xFFFFu);
                     }
@@ -433,6 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (mine) {
                 tc::fence_after_sync();
                 tc::ldn<G>(tmem + lane_off + 2 * NQ, o);
+                if constexpr (LY::NP == 2) {
+                    uint32_t o2[G];
+                    tc::ldn<G>(tmem + lane_off + 3 * NQ, o2);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int g = 0; g < G; ++g) o[g] = __float_as_uint(__uint_as_float(o[g]) + __uint_as_float(o2[g]));
+                }
                 tc::wait_ld();
                 tc::fence_before_sync();
                 mbar_arrive(o_free); // the next unit's first P V may overwrite O^T

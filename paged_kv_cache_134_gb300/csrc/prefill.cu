@@ -382,7 +382,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // the whole warp runs the issue loop in step (waits agreed with __all_sync); one elected lane
+        // issues each MMA and commit
+        {
             constexpr uint32_t IQK = tc::idesc_f16(MT == PKV_BF16 ? 1u : 0u, 0u, BM, BN);
             constexpr uint32_t IPV = tc::idesc_f16(MT == PKV_BF16 ? 1u : 0u, 1u, BM, D);
             const uint32_t sQ = smem_u32(smem + L::Q), sK = smem_u32(smem + L::K0), sV = smem_u32(smem + L::V0);
@@ -392,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             // S buffer; the K stage is released as soon as S is done
             auto issue_s = [&](int64_t gg) -> bool {
                 const int st = (int)(gg % NKS);
-                if (!mbar_wait(k_full + st, (gg / NKS) & 1)) return false;
-                if (gg >= 1 && !mbar_wait(s_free, (gg - 1) & 1)) return false;
+                if (!__all_sync(0xffffffffu, mbar_wait(k_full + st, (gg / NKS) & 1))) return false;
+                if (gg >= 1 && !__all_sync(0xffffffffu, mbar_wait(s_free, (gg - 1) & 1))) return false;
                 tc::fence_after_sync();
                 any_mma = true;
 #pragma unroll
@@ -401,30 +403,31 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                     const int c = k >> 2, kk = k & 3;
                     const uint64_t ad = tc::smem_desc(sQ + c * BM * 128 + kk * 32, 16, 1024);
                     const uint64_t bd = tc::smem_desc(sK + st * L::KV_BYTES + c * BN * 128 + kk * 32, 16, 1024);
-                    tc::mma_f16(tmem, ad, bd, IQK, k > 0 ? 1u : 0u);
+                    tc::mma_f16_warp(tmem, ad, bd, IQK, k > 0 ? 1u : 0u);
                 }
-                tc::commit(s_full);
-                tc::commit(k_empty + st);
+                tc::commit_warp(s_full);
+                tc::commit_warp(k_empty + st);
                 return true;
             };
             bool ok = true;
             int64_t g = 0;
             for (int n = 0; ok; ++n) {
                 const Item it = take_item(n, ok);
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok || it.seq < 0) break;
-                ok = mbar_wait(q_full, n & 1) && issue_s(g);
+                ok = __all_sync(0xffffffffu, mbar_wait(q_full, n & 1)) && issue_s(g);
                 for (int j = 0; j < it.nkv && ok; ++j) {
                     const int64_t gg = g + j;
                     if (j + 1 < it.nkv) {
                         ok = issue_s(gg + 1);
                         if (!ok) break;
                     } else {
-                        tc::commit(q_empty); // the item's last S has been issued: Q may be replaced
+                        tc::commit_warp(q_empty); // the item's last S has been issued: Q may be replaced
                     }
                     const int sv = (int)(gg % NVS);
-                    ok = mbar_wait(p_full + (gg & 1), (gg >> 1) & 1) && mbar_wait(v_full + sv, (gg / NVS) & 1);
+                    ok = __all_sync(0xffffffffu, mbar_wait(p_full + (gg & 1), (gg >> 1) & 1) && mbar_wait(v_full + sv, (gg / NVS) & 1));
                     // the epilogue of the previous item has read O out of TMEM
-                    if (ok && j == 0 && n >= 1) ok = mbar_wait(o_free, (n - 1) & 1);
+                    if (ok && j == 0 && n >= 1) ok = __all_sync(0xffffffffu, mbar_wait(o_free, (n - 1) & 1));
                     if (!ok) break;
                     tc::fence_after_sync();
                     // O += P V, P (A operand) read from tensor memory where the softmax left it
@@ -434,21 +437,21 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                         for (int k = 0; k < BN / 16; ++k) {
                             const uint32_t at = tmem + (uint32_t)(BN + (int)(gg % L::NPB) * (BN / 2) + part * (BN / 2) + k * 8);
                             const uint64_t bd = tc::smem_desc(sV + sv * L::KV_BYTES + k * 2048, BN * 128, 1024);
-                            tc::mma_f16_ts(tO, at, bd, IPV, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
+                            tc::mma_f16_ts_warp(tO, at, bd, IPV, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
                         }
-                    tc::commit(t_full + (gg & 1));
-                    tc::commit(v_empty + sv);
+                    tc::commit_warp(t_full + (gg & 1));
+                    tc::commit_warp(v_empty + sv);
                 }
                 g += it.nkv;
-                mbar_arrive(item_empty + (n & 1));
-                if (*abort_flag) break;
+                if (lane == 0) mbar_arrive(item_empty + (n & 1));
+                if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             }
-            if (!ok) fail();
-            // every MMA issued by this thread has completed before TMEM is released (a CTA that found
+            if (!ok && lane == 0) fail();
+            // every MMA issued by the elected lane has completed before TMEM is released (a CTA that found
             // no item issued none and has nothing to wait for)
             if (any_mma) {
-                tc::commit(fin);
-                if (!mbar_wait(fin, 0)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+                tc::commit_warp(fin);
+                if (!__all_sync(0xffffffffu, mbar_wait(fin, 0)) && lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
             }
         }
     } else if (warp < 6) {
