@@ -175,21 +175,67 @@ int packed_prefill_attention(const void *q, const void *k, const void *v, const 
                              int max_blocks_per_seq, pkv_cache_t cache, int num_q_heads, float scale, void *out,
                              void *stream);
 
+/* Prefill of a prompt's tail over its cached prefix (2kiu.com section 4.3 steps 2-4: the blocks a
+ * prefix-cache hit found are attached to the table, and only the tokens past the hit are prefilled;
+ * section 3.3: the hit saves the prefill of the prefix, its blocks are still read).  Sequence i
+ * already holds context_lens[i] tokens in its blocks; its n_i = cu_seqlens[i+1] - cu_seqlens[i]
+ * new tokens (packed rows [cu_seqlens[i], cu_seqlens[i+1]) of q/k/v) sit at positions
+ * context_lens[i] .. context_lens[i] + n_i - 1.  The call first writes every new token's k/v at
+ * block_tables[i][p / block_size], offset p % block_size (p = its position), then computes
+ *   out[cu_i + r][h] = sum_{c <= ctx_i + r} softmax_c(scale * q[cu_i + r][h] . K_c[g]) V_c[g]
+ * with every key, cached or new, read from the pool through the table (g = h / group).  With all
+ * context_lens 0 it computes what packed_prefill_attention computes.  context_lens: device int32
+ * [num_seqs], each >= 0 with context + n_i <= max_blocks_per_seq * block_size (else the sequence
+ * is skipped and PKV_DEVERR_LENGTH set); the table must name a block for every position below
+ * context + n_i.  Other arguments, shapes and errors as for packed_prefill_attention. */
+int paged_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                            const int32_t *context_lens, int num_seqs, int max_seqlen, int64_t total_tokens,
+                            const int32_t *block_tables, int max_blocks_per_seq, pkv_cache_t cache, int num_q_heads,
+                            float scale, void *out, void *stream);
+
+/* Block copy for copy-on-write (2kiu.com section 2.2: copy-on-write of prefix blocks shared by
+ * beam search or parallel sampling; section 4.3 step 3: a shared block is never rewritten in
+ * place, the diverging path gets its own copy): for i < num_pairs, physical block
+ * dst_blocks[i] := physical block src_blocks[i], the whole block (K and V of every KV head, all
+ * block_size slots).  src_blocks, dst_blocks: device int32 [num_pairs].  The destinations must
+ * be distinct and none may also be a source in the same call (the copies run in parallel, so
+ * overlapping pairs would race).  An id outside [0, num_blocks) skips its pair and sets
+ * PKV_DEVERR_BLOCK_ID.  Exact byte copy. */
+int paged_block_copy(pkv_cache_t cache, const int32_t *src_blocks, const int32_t *dst_blocks, int64_t num_pairs,
+                     void *stream);
+
+/* Swap out (2kiu.com section 2.2: on preemption a request's block contents go to CPU memory;
+ * section 5.2): for i < num_ids, bytes [i*B, (i+1)*B) of dst := physical block block_ids[i],
+ * B = the block size in bytes (kv_cache_view's num_bytes / num_blocks).  dst must be device
+ * accessible: device memory, or page-locked host memory (cudaHostAlloc / cudaHostRegister; with
+ * unified addressing its host pointer is also its device pointer), at least num_ids*B bytes,
+ * 16-byte aligned.  block_ids: device int32 [num_ids].  Bad ids are skipped as above. */
+int paged_block_swap_out(pkv_cache_t cache, const int32_t *block_ids, int64_t num_ids, void *dst, void *stream);
+
+/* Swap in, the inverse: physical block block_ids[i] := bytes [i*B, (i+1)*B) of src (same rules for
+ * src as for dst above; block_ids distinct).  Together with paged_block_swap_out this moves a
+ * preempted request's blocks to CPU memory and back into whatever blocks the allocator hands out
+ * on resumption; the block table is then rewritten by the caller. */
+int paged_block_swap_in(pkv_cache_t cache, const int32_t *block_ids, int64_t num_ids, const void *src, void *stream);
+
 /* Profiling.  Between kv_cache_profile_start and kv_cache_profile_read the library records
  * CUDA events around each kernel it launches for this cache (decode split-K kernel, split
- * merge kernel, prefill kernel, append kernel) on the launch stream.  kv_cache_profile_read synchronises
+ * merge kernel, prefill kernel, append kernel, block copy kernel) on the launch stream.  kv_cache_profile_read synchronises
  * those events and returns the summed device time per kind (milliseconds) and launch
  * counts, then stops recording.  pkv_kernel_launches counts every kernel this library
  * launched in the process (all caches and free functions). */
 typedef struct {
     int64_t decode_launches, prefill_launches, append_launches, merge_launches;
     double decode_ms, prefill_ms, append_ms, merge_ms;
+    int64_t copy_launches; /* block copy / swap kernels */
+    double copy_ms;
 } pkv_profile_t;
 #define PKV_PROFILE_DECODE 1u  /* the split-K decode kernel */
 #define PKV_PROFILE_PREFILL 2u
 #define PKV_PROFILE_APPEND 4u
 #define PKV_PROFILE_MERGE 8u   /* the split merge kernel */
-#define PKV_PROFILE_ALL 15u
+#define PKV_PROFILE_COPY 16u  /* block copy and swap */
+#define PKV_PROFILE_ALL 31u
 /* kinds: which kernels to bracket (events between two kernels stop their launches from overlapping,
  * so time only what you need). */
 int kv_cache_profile_start(pkv_cache_t cache, unsigned kinds);

@@ -76,6 +76,17 @@ def _load():
         lib.orc_packed_prefill.restype = None
         lib.orc_packed_prefill.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int, _i32p, ctypes.c_int64, ctypes.c_int64,
                                            ctypes.c_int64, ctypes.c_int64, ctypes.c_double, _f64p]
+        for name in ("orc_block_copy", "orc_block_swap_out", "orc_block_swap_in"):
+            getattr(lib, name).restype = ctypes.c_int64
+        lib.orc_block_copy.argtypes = [_vp, _i64p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.c_int64, _i32p, _i32p, ctypes.c_int64]
+        lib.orc_block_swap_out.argtypes = [_vp, _i64p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_int64, _i32p, ctypes.c_int64, _vp]
+        lib.orc_block_swap_in.argtypes = list(lib.orc_block_swap_out.argtypes)
+        lib.orc_prefill_ctx.restype = ctypes.c_int64
+        lib.orc_prefill_ctx.argtypes = [_u16p, ctypes.c_int, _vp, _i64p, ctypes.c_int, _f32p, _f32p, ctypes.c_int64,
+                                        _i32p, ctypes.c_int64, _i32p, _i32p, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_double, _f64p]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_init()
         _lib = lib
@@ -199,4 +210,76 @@ def packed_prefill(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, d
     out = np.zeros((T, hq, d), np.float64)
     _load().orc_packed_prefill(_p(q_bits, _u16p), _p(k_bits, _u16p), _p(v_bits, _u16p), DTYPE[dtype], _p(cu, _i32p),
                                len(cu) - 1, hq, hkv, d, float(scale), _p(out, _f64p))
+    return out
+
+
+# ----------------------------------------------------------------------------- whole-block copies
+
+def _block_args(pool, strides, block_size, hkv, d):
+    strides = np.ascontiguousarray(strides, np.int64)
+    return pool.ctypes.data, strides, int(pool.itemsize), int(block_size), int(hkv), int(d)
+
+
+def block_copy(pool: np.ndarray, strides, num_blocks: int, block_size: int, hkv: int, d: int,
+               src_ids: np.ndarray, dst_ids: np.ndarray) -> int:
+    """Copy-on-write (2kiu.com section 2.2, 4.3): block dst_ids[i] := block src_ids[i], in place.
+    Returns the number of pairs skipped for an id outside the pool."""
+    base, st, elt, bs, hkv, d = _block_args(pool, strides, block_size, hkv, d)
+    src = np.ascontiguousarray(src_ids, np.int32)
+    dst = np.ascontiguousarray(dst_ids, np.int32)
+    assert len(src) == len(dst)
+    return int(_load().orc_block_copy(base, _p(st, _i64p), elt, num_blocks, bs, hkv, d, _p(src, _i32p),
+                                      _p(dst, _i32p), len(src)))
+
+
+def block_swap_out(pool: np.ndarray, strides, num_blocks: int, block_size: int, hkv: int, d: int,
+                   ids: np.ndarray):
+    """Swap out (2kiu.com sections 2.2, 5.2): returns (buffer, skipped) with buffer block i = pool
+    block ids[i] in the documented order [K|V][head][slot][dim]; skipped blocks stay zero."""
+    base, st, elt, bs, hkv, d = _block_args(pool, strides, block_size, hkv, d)
+    ids = np.ascontiguousarray(ids, np.int32)
+    buf = np.zeros(len(ids) * 2 * hkv * bs * d, dtype=pool.dtype)
+    bad = _load().orc_block_swap_out(base, _p(st, _i64p), elt, num_blocks, bs, hkv, d, _p(ids, _i32p), len(ids),
+                                     buf.ctypes.data)
+    return buf, int(bad)
+
+
+def block_swap_in(pool: np.ndarray, strides, num_blocks: int, block_size: int, hkv: int, d: int,
+                  ids: np.ndarray, buf: np.ndarray) -> int:
+    """Swap in: pool block ids[i] := buffer block i, in place.  Returns the count of skipped ids."""
+    base, st, elt, bs, hkv, d = _block_args(pool, strides, block_size, hkv, d)
+    ids = np.ascontiguousarray(ids, np.int32)
+    buf = np.ascontiguousarray(buf, pool.dtype)
+    assert buf.size >= len(ids) * 2 * hkv * bs * d
+    return int(_load().orc_block_swap_in(base, _p(st, _i64p), elt, num_blocks, bs, hkv, d, _p(ids, _i32p),
+                                         len(ids), buf.ctypes.data))
+
+
+# ----------------------------------------------------------------------------- prefill on a cached prefix
+
+def prefill_ctx(q_bits: np.ndarray, q_dtype: str, pool: np.ndarray, strides, cache_dtype: str, num_blocks: int,
+                tables: np.ndarray, cu_seqlens: np.ndarray, context_lens: np.ndarray, hkv: int, block_size: int,
+                scale: float, k_scale=None, v_scale=None) -> np.ndarray:
+    """fp64 attention of the tail tokens of each prompt over its cached prefix and itself, every key
+    read from the pool through the table (2kiu.com section 4.3 steps 2-4).  The tail tokens' K/V
+    must already be in the pool.  Returns out [T, Hq, D] float64."""
+    q_bits = np.ascontiguousarray(q_bits, np.uint16)
+    T, hq, d = q_bits.shape
+    tables = np.ascontiguousarray(tables, np.int32)
+    cu = np.ascontiguousarray(cu_seqlens, np.int32)
+    ctx = np.ascontiguousarray(context_lens, np.int32)
+    strides = np.ascontiguousarray(strides, np.int64)
+    out = np.zeros((T, hq, d), np.float64)
+    if cache_dtype == "fp8":
+        ks = np.ascontiguousarray(k_scale, np.float32)
+        vs = np.ascontiguousarray(v_scale, np.float32)
+        ksp, vsp = _p(ks, _f32p), _p(vs, _f32p)
+    else:
+        ksp = vsp = None
+    bad = _load().orc_prefill_ctx(_p(q_bits, _u16p), DTYPE[q_dtype], pool.ctypes.data, _p(strides, _i64p),
+                                  DTYPE[cache_dtype], ksp, vsp, num_blocks, _p(tables, _i32p), tables.shape[1],
+                                  _p(cu, _i32p), _p(ctx, _i32p), len(cu) - 1, hq, hkv, d, block_size, float(scale),
+                                  _p(out, _f64p))
+    if bad:
+        raise ValueError(f"{bad} rows needed a block id outside the pool")
     return out

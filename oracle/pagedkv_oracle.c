@@ -26,6 +26,11 @@
  *    [cu[i], cu[i+1]); a query attends to keys of its own sequence at an
  *    in-sequence position <= its own (block-diagonal causal mask, discosf.com
  *    sections 3.1-3.2).
+ *  - prefill on a cached prefix: the same for the tail tokens of a prompt whose
+ *    first ctx tokens are already in the sequence's blocks (2kiu.com section 4.3
+ *    steps 2-4), every key read through the block table.
+ *  - whole-block copy and swap: copy-on-write of shared blocks and moving block
+ *    contents to CPU memory and back (2kiu.com sections 2.2, 4.3, 5.2).
  *
  * Readings where the pages are silent (all listed with the design notes):
  *  - softmax is the exact real-number definition, evaluated in fp64 with libm exp;
@@ -286,6 +291,148 @@ void orc_packed_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         }
         free(x);
     }
+}
+
+/* ---------------------------------------------------------------- whole-block copies */
+
+/* Copy-on-write of shared blocks and swapping block contents to CPU memory ("PagedAttention 与前缀缓存",
+ * 2kiu.com, section 2.2; section 4.3 step 3: a shared block is never rewritten in place, the
+ * diverging path gets its own copy; section 5.2: preempted requests' blocks go to CPU memory).
+ * A block is every element (K|V, head, slot, dim) of one physical block.  elt = bytes per element.
+ * Pairs whose ids fall outside [0, num_blocks) are skipped and counted. */
+
+static void copy_elem(void *dst, int64_t di, const void *src, int64_t si, int elt) {
+    memcpy((char *)dst + di * elt, (const char *)src + si * elt, (size_t)elt);
+}
+
+/* block dst_ids[i] := block src_ids[i] (the caller keeps destinations distinct from sources). */
+int64_t orc_block_copy(void *pool, const int64_t *st, int elt, int64_t num_blocks, int64_t bs, int64_t hkv, int64_t d,
+                       const int32_t *src_ids, const int32_t *dst_ids, int64_t n) {
+    int64_t bad = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t sb = src_ids[i], db = dst_ids[i];
+        if (sb < 0 || sb >= num_blocks || db < 0 || db >= num_blocks) {
+            ++bad;
+            continue;
+        }
+        for (int kv = 0; kv < 2; ++kv)
+            for (int64_t h = 0; h < hkv; ++h)
+                for (int64_t o = 0; o < bs; ++o)
+                    for (int64_t e = 0; e < d; ++e)
+                        copy_elem(pool, pool_index(st, db, kv, h, o, e), pool, pool_index(st, sb, kv, h, o, e), elt);
+    }
+    return bad;
+}
+
+/* index of element (kv, h, o, e) of block i in a swap buffer: blocks back to back, each in the
+ * documented pool order [K|V][head][slot][dim] */
+static int64_t buf_index(int64_t i, int kv, int64_t h, int64_t o, int64_t e, int64_t bs, int64_t hkv, int64_t d) {
+    return (((i * 2 + kv) * hkv + h) * bs + o) * d + e;
+}
+
+/* swap out: buffer block i := pool block ids[i] */
+int64_t orc_block_swap_out(const void *pool, const int64_t *st, int elt, int64_t num_blocks, int64_t bs, int64_t hkv,
+                           int64_t d, const int32_t *ids, int64_t n, void *buf) {
+    int64_t bad = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t b = ids[i];
+        if (b < 0 || b >= num_blocks) {
+            ++bad;
+            continue;
+        }
+        for (int kv = 0; kv < 2; ++kv)
+            for (int64_t h = 0; h < hkv; ++h)
+                for (int64_t o = 0; o < bs; ++o)
+                    for (int64_t e = 0; e < d; ++e)
+                        copy_elem(buf, buf_index(i, kv, h, o, e, bs, hkv, d), pool, pool_index(st, b, kv, h, o, e), elt);
+    }
+    return bad;
+}
+
+/* swap in: pool block ids[i] := buffer block i */
+int64_t orc_block_swap_in(void *pool, const int64_t *st, int elt, int64_t num_blocks, int64_t bs, int64_t hkv,
+                          int64_t d, const int32_t *ids, int64_t n, const void *buf) {
+    int64_t bad = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t b = ids[i];
+        if (b < 0 || b >= num_blocks) {
+            ++bad;
+            continue;
+        }
+        for (int kv = 0; kv < 2; ++kv)
+            for (int64_t h = 0; h < hkv; ++h)
+                for (int64_t o = 0; o < bs; ++o)
+                    for (int64_t e = 0; e < d; ++e)
+                        copy_elem(pool, pool_index(st, b, kv, h, o, e), buf, buf_index(i, kv, h, o, e, bs, hkv, d), elt);
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------- prefill on a cached prefix */
+
+/* The tail of a prompt after a prefix-cache hit ("PagedAttention 与前缀缓存", 2kiu.com, section 4.3
+ * steps 2-4 and section 3.3: only the tokens past the hit are prefilled, the hit blocks are read):
+ * sequence i already holds ctx[i] tokens in its blocks; its n_i = cu[i+1] - cu[i] new tokens sit
+ * at positions ctx[i] .. ctx[i] + n_i - 1 and their K/V have been written at their slots (append).
+ * New row r attends to every position c <= ctx[i] + r of the sequence, all read from the pool
+ * through the table:
+ *   out[cu[i] + r][h] = sum_{c <= ctx_i + r} softmax_c(scale * q[cu[i] + r][h] . K_c) V_c.
+ * Returns the number of (row, head) outputs that needed a table entry outside [0, num_blocks). */
+int64_t orc_prefill_ctx(const uint16_t *q, int q_dtype, const void *pool, const int64_t *st, int cache_dtype,
+                        const float *k_scale, const float *v_scale, int64_t num_blocks, const int32_t *tables,
+                        int64_t max_blocks, const int32_t *cu, const int32_t *ctx, int64_t num_seqs, int64_t hq,
+                        int64_t hkv, int64_t d, int64_t bs, double scale, double *out) {
+    build_luts();
+    int64_t group = hq / hkv, bad = 0;
+#pragma omp parallel for schedule(dynamic) reduction(+ : bad)
+    for (int64_t ih = 0; ih < num_seqs * hq; ++ih) {
+        int64_t i = ih / hq, h = ih % hq, g = h / group;
+        int64_t start = cu[i], n = (int64_t)cu[i + 1] - cu[i], c0 = ctx[i];
+        if (n <= 0) continue;
+        int64_t total = c0 + n;
+        double *x = (double *)malloc((size_t)total * sizeof(double));
+        int64_t *blk = (int64_t *)malloc((size_t)total * sizeof(int64_t));
+        int ok = 1;
+        for (int64_t c = 0; c < total; ++c) {
+            int64_t lb = c / bs;
+            int32_t b = lb < max_blocks ? tables[i * max_blocks + lb] : -1;
+            if (b < 0 || b >= num_blocks) {
+                ok = 0;
+                break;
+            }
+            blk[c] = b;
+        }
+        for (int64_t r = 0; r < n; ++r) {
+            double *o = out + ((start + r) * hq + h) * d;
+            for (int64_t e = 0; e < d; ++e) o[e] = 0.0;
+            if (!ok) continue;
+            const uint16_t *qr = q + ((start + r) * hq + h) * d;
+            int64_t L = c0 + r + 1;
+            for (int64_t c = 0; c < L; ++c) {
+                double dot = 0.0;
+                for (int64_t e = 0; e < d; ++e)
+                    dot += widen(qr[e], q_dtype) * pool_value(pool, st, cache_dtype, k_scale, blk[c], 0, g, c % bs, e);
+                x[c] = scale * dot;
+            }
+            double m = x[0];
+            for (int64_t c = 1; c < L; ++c)
+                if (x[c] > m) m = x[c];
+            double den = 0.0;
+            for (int64_t c = 0; c < L; ++c) {
+                x[c] = exp(x[c] - m);
+                den += x[c];
+            }
+            for (int64_t c = 0; c < L; ++c) {
+                double p = x[c] / den;
+                for (int64_t e = 0; e < d; ++e)
+                    o[e] += p * pool_value(pool, st, cache_dtype, v_scale, blk[c], 1, g, c % bs, e);
+            }
+        }
+        if (!ok) bad += n;
+        free(x);
+        free(blk);
+    }
+    return bad;
 }
 
 int orc_num_threads(void) {

@@ -57,6 +57,11 @@ def lib() -> ctypes.CDLL:
         L.paged_decode_attention_noalloc.argtypes = [vp, vp, vp, i32, vp, i32, i32, ctypes.c_float, vp, vp]
         L.packed_prefill_attention.argtypes = [vp, vp, vp, vp, i32, i32, i64, vp, i32, vp, i32, ctypes.c_float, vp,
                                                vp]
+        L.paged_prefill_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, vp, i32, vp, i32, ctypes.c_float, vp,
+                                              vp]
+        L.paged_block_copy.argtypes = [vp, vp, vp, i64, vp]
+        L.paged_block_swap_out.argtypes = [vp, vp, i64, vp, vp]
+        L.paged_block_swap_in.argtypes = [vp, vp, i64, vp, vp]
         L.kv_cache_profile_start.argtypes = [vp, ctypes.c_uint]
         L.kv_cache_profile_read.argtypes = [vp, ctypes.c_void_p]
         L.pkv_kernel_launches.restype = i64
@@ -68,7 +73,7 @@ class _Profile(ctypes.Structure):
     _fields_ = [("decode_launches", ctypes.c_int64), ("prefill_launches", ctypes.c_int64),
                 ("append_launches", ctypes.c_int64), ("merge_launches", ctypes.c_int64),
                 ("decode_ms", ctypes.c_double), ("prefill_ms", ctypes.c_double), ("append_ms", ctypes.c_double),
-                ("merge_ms", ctypes.c_double)]
+                ("merge_ms", ctypes.c_double), ("copy_launches", ctypes.c_int64), ("copy_ms", ctypes.c_double)]
 
 
 def _check(status: int):
@@ -172,7 +177,12 @@ class KVCache:
             _check(st)
         return int(code.value)
 
-    PROFILE = {"decode": 1, "prefill": 2, "append": 4, "merge": 8}
+    PROFILE = {"decode": 1, "prefill": 2, "append": 4, "merge": 8, "copy": 16}
+
+    @property
+    def block_bytes(self) -> int:
+        """Bytes of one physical block (K and V of every KV head)."""
+        return 2 * self.num_kv_heads * self.block_size * self.head_dim * (1 if self.kv_dtype == "fp8" else 2)
 
     def profile_start(self, kinds=("decode", "prefill", "append", "merge")):
         """Record CUDA events around the named kernels (events between kernels stop their overlap)."""
@@ -299,4 +309,68 @@ def packed_prefill_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     _check(lib().packed_prefill_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseq, int(max_seqlen), T,
                                           _ptr(block_tables), block_tables.shape[1], cache.handle, hq,
                                           ctypes.c_float(scale), _ptr(out), _stream()))
+    return out
+
+
+def _req_buffer(t: torch.Tensor, name: str, nbytes: int):
+    """A contiguous byte buffer the GPU can reach: a CUDA tensor or page-locked host memory."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, {nbytes} needed")
+
+
+def paged_block_copy(cache: KVCache, src_blocks: torch.Tensor, dst_blocks: torch.Tensor) -> None:
+    """Copy-on-write: block dst_blocks[i] := block src_blocks[i] (whole blocks)."""
+    _req(src_blocks, "src_blocks", torch.int32, 1)
+    _req(dst_blocks, "dst_blocks", torch.int32, 1)
+    if src_blocks.numel() != dst_blocks.numel():
+        raise ValueError("src_blocks and dst_blocks differ in length")
+    _check(lib().paged_block_copy(cache.handle, _ptr(src_blocks), _ptr(dst_blocks), src_blocks.numel(), _stream()))
+
+
+def paged_block_swap_out(cache: KVCache, block_ids: torch.Tensor, dst: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Gather whole blocks into ``dst`` (uint8, CUDA or pinned host; block i at i * block_bytes)."""
+    _req(block_ids, "block_ids", torch.int32, 1)
+    n = block_ids.numel()
+    if dst is None:
+        dst = torch.empty(n * cache.block_bytes, dtype=torch.uint8).pin_memory()
+    _req_buffer(dst, "dst", n * cache.block_bytes)
+    _check(lib().paged_block_swap_out(cache.handle, _ptr(block_ids), n, _ptr(dst), _stream()))
+    return dst
+
+
+def paged_block_swap_in(cache: KVCache, block_ids: torch.Tensor, src: torch.Tensor) -> None:
+    """Scatter whole blocks back: block block_ids[i] := src[i * block_bytes : (i + 1) * block_bytes]."""
+    _req(block_ids, "block_ids", torch.int32, 1)
+    n = block_ids.numel()
+    _req_buffer(src, "src", n * cache.block_bytes)
+    _check(lib().paged_block_swap_in(cache.handle, _ptr(block_ids), n, _ptr(src), _stream()))
+
+
+def paged_prefill_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                            context_lens: torch.Tensor, max_seqlen: int, block_tables: torch.Tensor, cache: KVCache,
+                            scale: float, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Prefill of each prompt's tail over the prefix its blocks already hold (writes the tail's K/V)."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _req(t, name, cache.torch_dtype, 3)
+    _req(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _req(context_lens, "context_lens", torch.int32, 1)
+    _req(block_tables, "block_tables", torch.int32, 2)
+    T, hq, d = q.shape
+    if k.shape != (T, cache.num_kv_heads, d) or v.shape != k.shape or d != cache.head_dim:
+        raise ValueError("q/k/v shape mismatch")
+    nseq = cu_seqlens.numel() - 1
+    if block_tables.shape[0] != nseq or context_lens.numel() != nseq:
+        raise ValueError("one block-table row and one context length per sequence")
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, "out", cache.torch_dtype, 3)
+    _check(lib().paged_prefill_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(context_lens), nseq,
+                                         int(max_seqlen), T, _ptr(block_tables), block_tables.shape[1], cache.handle,
+                                         hq, ctypes.c_float(scale), _ptr(out), _stream()))
     return out

@@ -1,6 +1,6 @@
 // C ABI of the library: handle management, host-side validation, launches, error
 // reporting and profiling.  Every computation happens in the kernels of append.cu,
-// decode*.cu and prefill.cu.
+// decode*.cu, prefill.cu and blocks.cu.
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -291,15 +291,15 @@ int paged_decode_attention(const void *q, pkv_cache_t c, const int32_t *block_ta
     return PKV_OK;
 }
 
-int packed_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens, int num_seqs,
-                             int max_seqlen, int64_t total_tokens, const int32_t *block_tables,
-                             int max_blocks_per_seq, pkv_cache_t c, int num_q_heads, float scale, void *out,
-                             void *stream) {
+static int prefill_entry(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                         const int32_t *context_lens, int num_seqs, int max_seqlen, int64_t total_tokens,
+                         const int32_t *block_tables, int max_blocks_per_seq, pkv_cache_t c, int num_q_heads,
+                         float scale, void *out, void *stream) {
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     if (num_seqs < 0 || max_seqlen < 0 || max_blocks_per_seq < 0 || total_tokens < 0)
         return pkv_fail(PKV_EINVAL, "negative size");
     if (total_tokens > 0x7FFFFFFF) return pkv_fail(PKV_EUNSUPPORTED, "more than 2^31 - 1 packed tokens");
-    if (c->kv_dtype == PKV_FP8_E4M3) return pkv_fail(PKV_EUNSUPPORTED, "packed prefill writes fp16/bf16 caches only");
+    if (c->kv_dtype == PKV_FP8_E4M3) return pkv_fail(PKV_EUNSUPPORTED, "prefill writes fp16/bf16 caches only");
     if (num_seqs == 0 || max_seqlen == 0 || total_tokens == 0) return PKV_OK;
     if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads)
         return pkv_fail(PKV_EINVAL, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
@@ -317,6 +317,7 @@ int packed_prefill_attention(const void *q, const void *k, const void *v, const 
     p.v = v;
     p.out = out;
     p.cu = cu_seqlens;
+    p.ctx = context_lens;
     p.tables = block_tables;
     p.num_seqs = num_seqs;
     p.max_seqlen = max_seqlen;
@@ -330,13 +331,70 @@ int packed_prefill_attention(const void *q, const void *k, const void *v, const 
     return PKV_OK;
 }
 
+int packed_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens, int num_seqs,
+                             int max_seqlen, int64_t total_tokens, const int32_t *block_tables,
+                             int max_blocks_per_seq, pkv_cache_t c, int num_q_heads, float scale, void *out,
+                             void *stream) {
+    return prefill_entry(q, k, v, cu_seqlens, nullptr, num_seqs, max_seqlen, total_tokens, block_tables,
+                         max_blocks_per_seq, c, num_q_heads, scale, out, stream);
+}
+
+int paged_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                            const int32_t *context_lens, int num_seqs, int max_seqlen, int64_t total_tokens,
+                            const int32_t *block_tables, int max_blocks_per_seq, pkv_cache_t c, int num_q_heads,
+                            float scale, void *out, void *stream) {
+    if (!context_lens && num_seqs > 0) return pkv_fail(PKV_EINVAL, "NULL pointer");
+    return prefill_entry(q, k, v, cu_seqlens, context_lens, num_seqs, max_seqlen, total_tokens, block_tables,
+                         max_blocks_per_seq, c, num_q_heads, scale, out, stream);
+}
+
+int paged_block_copy(pkv_cache_t c, const int32_t *src_blocks, const int32_t *dst_blocks, int64_t num_pairs,
+                     void *stream) {
+    if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
+    if (num_pairs < 0) return pkv_fail(PKV_EINVAL, "num_pairs < 0");
+    if (num_pairs == 0) return PKV_OK;
+    if (!src_blocks || !dst_blocks) return pkv_fail(PKV_EINVAL, "NULL pointer");
+    if (int r = check_device(c)) return r;
+    cudaError_t e = launch_copy_blocks(c, c->pool, src_blocks, c->num_blocks, c->pool, dst_blocks, c->num_blocks,
+                                       num_pairs, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return pkv_cuda_fail(e, "block copy launch");
+    return PKV_OK;
+}
+
+int paged_block_swap_out(pkv_cache_t c, const int32_t *block_ids, int64_t num_ids, void *dst, void *stream) {
+    if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
+    if (num_ids < 0) return pkv_fail(PKV_EINVAL, "num_ids < 0");
+    if (num_ids == 0) return PKV_OK;
+    if (!block_ids || !dst) return pkv_fail(PKV_EINVAL, "NULL pointer");
+    if (!aligned16(dst)) return pkv_fail(PKV_EINVAL, "dst must be 16-byte aligned");
+    if (int r = check_device(c)) return r;
+    cudaError_t e = launch_copy_blocks(c, c->pool, block_ids, c->num_blocks, dst, nullptr, num_ids, num_ids,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return pkv_cuda_fail(e, "swap-out launch");
+    return PKV_OK;
+}
+
+int paged_block_swap_in(pkv_cache_t c, const int32_t *block_ids, int64_t num_ids, const void *src, void *stream) {
+    if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
+    if (num_ids < 0) return pkv_fail(PKV_EINVAL, "num_ids < 0");
+    if (num_ids == 0) return PKV_OK;
+    if (!block_ids || !src) return pkv_fail(PKV_EINVAL, "NULL pointer");
+    if (!aligned16(src)) return pkv_fail(PKV_EINVAL, "src must be 16-byte aligned");
+    if (int r = check_device(c)) return r;
+    cudaError_t e = launch_copy_blocks(c, src, nullptr, num_ids, c->pool, block_ids, c->num_blocks, num_ids,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return pkv_cuda_fail(e, "swap-in launch");
+    return PKV_OK;
+}
+
 int kv_cache_profile_start(pkv_cache_t c, unsigned kinds) {
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     // PKV_PROFILE_* bits map onto (1 << PKV_KIND_*)
     c->profile_kinds = ((kinds & PKV_PROFILE_DECODE) ? 1u << PKV_KIND_DECODE : 0u) |
                        ((kinds & PKV_PROFILE_PREFILL) ? 1u << PKV_KIND_PREFILL : 0u) |
                        ((kinds & PKV_PROFILE_APPEND) ? 1u << PKV_KIND_APPEND : 0u) |
-                       ((kinds & PKV_PROFILE_MERGE) ? 1u << PKV_KIND_MERGE : 0u);
+                       ((kinds & PKV_PROFILE_MERGE) ? 1u << PKV_KIND_MERGE : 0u) |
+                       ((kinds & PKV_PROFILE_COPY) ? 1u << PKV_KIND_COPY : 0u);
     std::lock_guard<std::mutex> lk(c->mu);
     for (auto &ev : c->events) {
         c->event_pool.push_back(ev.a);
@@ -366,6 +424,9 @@ int kv_cache_profile_read(pkv_cache_t c, pkv_profile_t *out) {
         } else if (ev.kind == PKV_KIND_APPEND) {
             out->append_launches++;
             out->append_ms += ms;
+        } else if (ev.kind == PKV_KIND_COPY) {
+            out->copy_launches++;
+            out->copy_ms += ms;
         } else {
             out->merge_launches++;
             out->merge_ms += ms;

@@ -38,6 +38,7 @@ struct AppendArgs {
     const uint4 *k, *v;   // [n][Hkv][D] model dtype, viewed as 16-byte chunks
     const int64_t *slots; // given slots (plain append) ...
     const int32_t *tables, *seq_ids, *positions; // ... or computed here (fused append)
+    const int32_t *cu, *ctx; // ... or from packed ranges: token j of [cu[i], cu[i+1]) at position ctx[i] + j - cu[i]
     int64_t *slots_out;
     int rows, max_blocks;
     char *pool;
@@ -50,8 +51,10 @@ struct AppendArgs {
 };
 
 // KVT: 0 = 16-bit cache (bit copy), 2 = E4M3 cache; MT = model dtype for the E4M3 path;
-// FUSED: compute the slot from (table, sequence, position) instead of reading it
-template <int KVT, int MT, bool FUSED>
+// MODE: 0 = slots given, 1 = slot from (table, sequence id, position) per token, 2 = sequence and
+// position from packed ranges (cu_seqlens, context lengths), then the slot as in mode 1
+enum { SLOTS_GIVEN = 0, SLOTS_AT = 1, SLOTS_RANGES = 2 };
+template <int KVT, int MT, int MODE>
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
     pdl_trigger();
     pdl_wait();
@@ -65,8 +68,24 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
         const int h = hc / a.chunks_per_row;
         const int c = hc - h * a.chunks_per_row;
         int64_t slot;
-        if constexpr (FUSED) {
+        if constexpr (MODE == SLOTS_AT) {
             slot = slot_of(a.tables, a.rows, a.max_blocks, a.seq_ids[j], a.positions[j], a.bs);
+            if (rem == 0 && a.slots_out) a.slots_out[j] = slot;
+        } else if constexpr (MODE == SLOTS_RANGES) {
+            // sequence: the largest i with cu[i] <= j (a.rows = number of sequences)
+            int lo = 0, hi = a.rows;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (a.cu[mid] <= j)
+                    lo = mid;
+                else
+                    hi = mid;
+            }
+            const int64_t st = a.cu[lo], en = a.cu[lo + 1];
+            const int64_t pos = (int64_t)a.ctx[lo] + (j - st);
+            slot = (j >= st && j < en && a.ctx[lo] >= 0 && pos <= 0x7FFFFFFF)
+                       ? slot_of(a.tables, a.rows, a.max_blocks, lo, (int)pos, a.bs)
+                       : -1;
             if (rem == 0 && a.slots_out) a.slots_out[j] = slot;
         } else {
             slot = a.slots[j];
@@ -121,18 +140,18 @@ AppendArgs base_args(pkv_cache *c, const void *k, const void *v, int64_t n) {
     return a;
 }
 
-template <bool FUSED>
+template <int MODE>
 cudaError_t launch_append_t(pkv_cache *c, const AppendArgs &a, cudaStream_t st) {
     const int64_t work = a.n * 2 * a.hkv * a.chunks_per_row;
     const dim3 grid(grid_for(work, 256, c->num_sms));
     PkvTimer timer(c, PKV_KIND_APPEND, st);
     cudaError_t e;
     if (c->kv_dtype != PKV_FP8_E4M3)
-        e = pdl_launch(append_kernel<PKV_F16, PKV_F16, FUSED>, grid, dim3(256), 0, st, a);
+        e = pdl_launch(append_kernel<PKV_F16, PKV_F16, MODE>, grid, dim3(256), 0, st, a);
     else if (c->model_dtype == PKV_F16)
-        e = pdl_launch(append_kernel<PKV_FP8_E4M3, PKV_F16, FUSED>, grid, dim3(256), 0, st, a);
+        e = pdl_launch(append_kernel<PKV_FP8_E4M3, PKV_F16, MODE>, grid, dim3(256), 0, st, a);
     else
-        e = pdl_launch(append_kernel<PKV_FP8_E4M3, PKV_BF16, FUSED>, grid, dim3(256), 0, st, a);
+        e = pdl_launch(append_kernel<PKV_FP8_E4M3, PKV_BF16, MODE>, grid, dim3(256), 0, st, a);
     g_pkv_launches++;
     return e;
 }
@@ -156,7 +175,7 @@ cudaError_t launch_append(pkv_cache *c, const void *k, const void *v, const int6
     if (n == 0) return cudaSuccess;
     AppendArgs a = base_args(c, k, v, n);
     a.slots = slots;
-    return launch_append_t<false>(c, a, st);
+    return launch_append_t<SLOTS_GIVEN>(c, a, st);
 }
 
 cudaError_t launch_append_at(pkv_cache *c, const void *k, const void *v, const int32_t *tables, int rows,
@@ -170,5 +189,17 @@ cudaError_t launch_append_at(pkv_cache *c, const void *k, const void *v, const i
     a.seq_ids = seq_ids;
     a.positions = positions;
     a.slots_out = slots_out;
-    return launch_append_t<true>(c, a, st);
+    return launch_append_t<SLOTS_AT>(c, a, st);
+}
+
+cudaError_t launch_append_ranges(pkv_cache *c, const void *k, const void *v, const int32_t *tables, int num_seqs,
+                                 int max_blocks, const int32_t *cu, const int32_t *ctx, int64_t n, cudaStream_t st) {
+    if (n == 0 || num_seqs <= 0) return cudaSuccess;
+    AppendArgs a = base_args(c, k, v, n);
+    a.tables = tables;
+    a.rows = num_seqs;
+    a.max_blocks = max_blocks;
+    a.cu = cu;
+    a.ctx = ctx;
+    return launch_append_t<SLOTS_RANGES>(c, a, st);
 }

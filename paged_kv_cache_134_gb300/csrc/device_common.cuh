@@ -51,6 +51,12 @@ PKV_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
+// raise the transaction count of the current phase without arriving (the arrival comes later)
+PKV_DEV void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
 PKV_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(

@@ -43,7 +43,7 @@ struct pkv_cache {
     std::mutex mu;
 };
 
-enum { PKV_KIND_DECODE = 0, PKV_KIND_PREFILL = 1, PKV_KIND_APPEND = 2, PKV_KIND_MERGE = 3 };
+enum { PKV_KIND_DECODE = 0, PKV_KIND_PREFILL = 1, PKV_KIND_APPEND = 2, PKV_KIND_MERGE = 3, PKV_KIND_COPY = 4 };
 
 // status helpers (api.cu)
 int pkv_fail(int status, const char *fmt, ...);
@@ -86,6 +86,16 @@ cudaError_t launch_append_at(pkv_cache *c, const void *k, const void *v, const i
                              int max_blocks, const int32_t *seq_ids, const int32_t *positions, int64_t n,
                              int64_t *slots_out, cudaStream_t st);
 
+// append of packed token ranges: token j of [cu[i], cu[i+1]) goes to position ctx[i] + j - cu[i]
+// of sequence i (the tail of a prompt after its cached prefix)
+cudaError_t launch_append_ranges(pkv_cache *c, const void *k, const void *v, const int32_t *tables, int num_seqs,
+                                 int max_blocks, const int32_t *cu, const int32_t *ctx, int64_t n, cudaStream_t st);
+
+// whole-block copies (blocks.cu): pair i copies block src_ids[i] (or i) of `src` to block
+// dst_ids[i] (or i) of `dst`; both regions are made of blocks of the cache's block size
+cudaError_t launch_copy_blocks(pkv_cache *c, const void *src, const int32_t *src_ids, int64_t src_blocks, void *dst,
+                               const int32_t *dst_ids, int64_t dst_blocks, int64_t n, cudaStream_t st);
+
 struct DecodeLaunch {
     const void *q;
     void *out;
@@ -112,6 +122,7 @@ struct PrefillLaunch {
     const void *q, *k, *v;
     void *out;
     const int32_t *cu;
+    const int32_t *ctx; // cached tokens per sequence (paged mode: K/V read from the pool), or NULL
     const int32_t *tables;
     int num_seqs, max_seqlen, max_blocks, num_q_heads;
     int64_t total_tokens;

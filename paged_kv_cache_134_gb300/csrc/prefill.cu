@@ -53,6 +53,7 @@ struct Args {
     char *pool;
     unsigned int *err;
     int *plan;          // [0] item count, [1] next-item counter, [4 + 2i], [5 + 2i] = (sequence, query tile) of item i
+    const int32_t *ctx; // paged mode: tokens each sequence already holds in its blocks (else NULL)
     int64_t total_tokens, num_blocks, tile_elems;
     int num_seqs, max_seqlen, max_blocks, hq, hkv, bs, lg_bs, nqt_max;
     float scale_log2;
@@ -105,6 +106,14 @@ PKV_DEV int seq_tiles(const Args &a, int i, bool report) {
     if (st < 0 || en < st || en > a.total_tokens || en - st > a.max_seqlen) {
         if (report) set_error(a.err, PKV_DEVERR_CU_SEQLENS);
         return 0;
+    }
+    if (a.ctx) {
+        // paged mode: the cached tokens plus the new ones must fit the sequence's table
+        const int64_t c0 = a.ctx[i];
+        if (c0 < 0 || c0 + (en - st) > (int64_t)a.max_blocks * a.bs) {
+            if (report) set_error(a.err, PKV_DEVERR_LENGTH);
+            return 0;
+        }
     }
     return (en - st + BM - 1) / BM;
 }
@@ -183,6 +192,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
 struct Item {
     int seq, qt, h; // seq < 0: no more items
     int start, n, q0, qlast, nkv;
+    int c0; // paged mode: cached tokens ahead of the item's sequence rows (absolute position of row 0)
 };
 
 PKV_DEV Item decode_item(const Args &a, int4 raw) {
@@ -195,12 +205,13 @@ PKV_DEV Item decode_item(const Args &a, int4 raw) {
         it.n = a.cu[it.seq + 1] - it.start;
         it.q0 = it.qt * BM;
         it.qlast = min(it.q0 + BM, it.n) - 1;
-        it.nkv = it.qlast / BN + 1;
+        it.c0 = a.ctx ? a.ctx[it.seq] : 0;
+        it.nkv = (it.c0 + it.qlast) / BN + 1; // key tiles up to the item's last row
     }
     return it;
 }
 
-template <int D, int MT>
+template <int D, int MT, bool PAGED>
 __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tp, const Args a) {
@@ -323,11 +334,42 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                     const int64_t round = gg / NKS;
                     if (round >= 1) ok = mbar_wait(k_empty + st, (round - 1) & 1);
                     if (!ok || *abort_flag) break;
-                    mbar_arrive_expect_tx(k_full + st, L::KV_BYTES);
+                    if constexpr (PAGED) {
+                        // the tile's blocks that hold tokens of the sequence, one box of bs rows per
+                        // block and half of D from the pool; rows past the sequence's end are masked
+                        // by the softmax, and unusable block ids (reported by the V loader) are skipped
+                        const int send = it.c0 + it.n, lb0 = (j * BN) >> a.lg_bs, nbt = BN >> a.lg_bs;
+                        int blk[BN / 8];
+                        uint32_t bytes = 0;
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c)
-                        tc::tma_load_2d(smem + L::K0 + st * L::KV_BYTES + c * BN * 128, &tk, kvh * D + c * 64,
-                                        it.start + j * BN, k_full + st);
+                        for (int l = 0; l < BN / 8; ++l) {
+                            blk[l] = -1;
+                            if (l < nbt && ((lb0 + l) << a.lg_bs) < send) {
+                                const int b = a.tables[(int64_t)it.seq * a.max_blocks + lb0 + l];
+                                if (b >= 0 && b < a.num_blocks) {
+                                    blk[l] = b;
+                                    bytes += (uint32_t)(a.bs * D * 2);
+                                }
+                            }
+                        }
+                        mbar_arrive_expect_tx(k_full + st, bytes);
+#pragma unroll
+                        for (int l = 0; l < BN / 8; ++l)
+                            if (blk[l] >= 0) {
+                                const int y = (blk[l] * 2 * a.hkv + kvh) << a.lg_bs;
+#pragma unroll
+                                for (int c = 0; c < D / 64; ++c)
+                                    tc::tma_load_2d(smem + L::K0 + st * L::KV_BYTES + c * BN * 128 +
+                                                        ((l << a.lg_bs) * 128),
+                                                    &tp, c * 64, y, k_full + st);
+                            }
+                    } else {
+                        mbar_arrive_expect_tx(k_full + st, L::KV_BYTES);
+#pragma unroll
+                        for (int c = 0; c < D / 64; ++c)
+                            tc::tma_load_2d(smem + L::K0 + st * L::KV_BYTES + c * BN * 128, &tk, kvh * D + c * 64,
+                                            it.start + j * BN, k_full + st);
+                    }
                     issued = j + 1;
                 }
                 g += issued; // tiles issued so far, all items
@@ -342,6 +384,70 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 if (!mbar_wait(k_full + gg % NKS, (gg / NKS) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
             if (last_q >= 0 && !mbar_wait(q_full, last_q & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
         }
+    } else if (warp == 7 && PAGED) {
+        // ------------------------------------------------------------ V loads from the pool (whole warp)
+        // Lane l handles block l of the tile.  Blocks full of the sequence's tokens arrive as TMA boxes;
+        // every other row of the tile is written with plain stores: the tokens of a partly filled last
+        // block copied from the pool, zeros for slots past the sequence and for unusable block ids.  P
+        // is 0 on those rows, but 0 * NaN is NaN, and the pool's unused slots may hold anything.
+        constexpr int CPR = D / 8;    // 16-byte chunks per row
+        constexpr int RPI = 32 / CPR; // rows per warp instruction (never two blocks: bs >= 8)
+        const int cc = lane % CPR, rsub = lane / CPR, c2 = cc >> 3, u = cc & 7;
+        if (lane == 0) tc::prefetch_tmap(&tp);
+        int64_t g = 0;
+        bool ok = true;
+        for (int n = 0;; ++n) {
+            const Item it = take_item(n, ok);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok || it.seq < 0) break;
+            const int kvh = it.h / G, send = it.c0 + it.n, nbt = BN >> a.lg_bs;
+            int issued = 0;
+            for (int j = 0; j < it.nkv && ok; ++j) {
+                const int64_t gg = g + j;
+                const int st = (int)(gg % NVS);
+                const int64_t round = gg / NVS;
+                if (round >= 1) ok = __all_sync(0xffffffffu, mbar_wait(v_empty + st, (round - 1) & 1));
+                if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) break;
+                const int kbase = j * BN, lb = (kbase >> a.lg_bs) + lane;
+                const bool has = lane < nbt && (lb << a.lg_bs) < send;
+                const int b = has ? a.tables[(int64_t)it.seq * a.max_blocks + lb] : -1;
+                const bool good = has && b >= 0 && b < a.num_blocks;
+                if (has && !good) set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                const bool full = good && ((lb + 1) << a.lg_bs) <= send;
+                const unsigned fullmask = __ballot_sync(0xffffffffu, full);
+                uint8_t *stage = smem + L::V0 + st * L::KV_BYTES;
+                if (lane == 0) mbar_expect_tx(v_full + st, (uint32_t)__popc(fullmask) * (uint32_t)(a.bs * D * 2));
+                __syncwarp();
+                if (full) {
+                    const int y = ((b * 2 + 1) * a.hkv + kvh) << a.lg_bs;
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tc::tma_load_2d(stage + c * BN * 128 + ((lane << a.lg_bs) * 128), &tp, c * 64, y, v_full + st);
+                }
+                for (int r0 = 0; r0 < BN; r0 += RPI) {
+                    const int r = r0 + rsub, l = r >> a.lg_bs;
+                    const int bl = __shfl_sync(0xffffffffu, good ? b : -1, l);
+                    if ((fullmask >> l) & 1u) continue;
+                    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                    if (bl >= 0 && kbase + r < send)
+                        x = *reinterpret_cast<const uint4 *>(
+                            a.pool + ((((int64_t)bl * 2 + 1) * a.hkv + kvh) * a.tile_elems +
+                                      (int64_t)(r - (l << a.lg_bs)) * D + cc * 8) * 2);
+                    *reinterpret_cast<uint4 *>(stage + c2 * BN * 128 + r * 128 + ((u ^ (r & 7)) << 4)) = x;
+                }
+                fence_proxy_async_smem(); // the plain stores are read by the MMA (async proxy)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(v_full + st);
+                issued = j + 1;
+            }
+            g += issued; // tiles issued so far, all items
+            if (lane == 0) mbar_arrive(item_empty + (n & 1));
+            if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) break;
+        }
+        if (!ok && lane == 0) fail();
+        if (lane == 0)
+            for (int64_t gg = g > NVS ? g - NVS : 0; gg < g; ++gg)
+                if (!mbar_wait(v_full + gg % NVS, (gg / NVS) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
     } else if (warp == 7) {
         // a warp of its own: sharing one with the K loader, whose lane spins on its own barriers,
         // held V loads back by thousands of cycles at every item start
@@ -465,7 +571,8 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             Item it = take_item(n, ok);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok || it.seq < 0) break;
-            const int q0 = it.q0, qpos = it.q0 + r;
+            // absolute positions: row r of the item sits at c0 + q0 + r (c0 = 0 without a cached prefix)
+            const int q0 = it.c0 + it.q0, qpos = it.q0 + r;
             float m_use = -INFINITY, l = 0.f;
             for (int j = 0; j < it.nkv && ok; ++j) {
                 const int64_t gg = g + j;
@@ -485,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 // causal mask, only on tiles that reach past the item's first query row
                 const int kbase = j * BN;
                 if (kbase + BN - 1 > q0) {
-                    const int lim = qpos - kbase + 1; // keys c < lim are at or before this row
+                    const int lim = q0 + r - kbase + 1; // keys c < lim are at or before this row
 #pragma unroll
                     for (int c = 0; c < BN; ++c)
                         if (c >= lim) sr[c] = 0xFF800000u; // -inf
@@ -599,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             const Item it = take_item(n, ok);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok || it.seq < 0) break;
-            const bool writes = it.h % G == 0;
+            const bool writes = !PAGED && it.h % G == 0; // paged mode: the K/V were appended before
             const int kvh = it.h / G, lb0 = it.q0 >> a.lg_bs;
             // lane l: table entry of logical block lb0 + l (at most BM / bs <= 16 of them)
             int blkv = -1;
@@ -712,10 +819,10 @@ bool make_map(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t co
     return r == CUDA_SUCCESS;
 }
 
-template <int D, int MT>
+template <int D, int MT, bool PAGED>
 cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tp,
                      const Args &a, int64_t max_ctas, int num_sms, cudaStream_t st) {
-    auto kern = prefill_kernel<D, MT>;
+    auto kern = prefill_kernel<D, MT, PAGED>;
     const int smem = Layout<D, MT>::TOTAL;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -757,6 +864,7 @@ cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st
     a.v = static_cast<const char *>(p.v);
     a.out = p.out;
     a.cu = p.cu;
+    a.ctx = p.ctx;
     a.tables = p.tables;
     a.pool = static_cast<char *>(c->pool);
     a.err = c->err;
@@ -802,17 +910,29 @@ cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st
         !make_map(&tv, p.v, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN) ||
         !make_map(&tp, c->pool, mt, pool_rows, D, c->block_size))
         return cudaErrorInvalidValue;
+    cudaError_t e;
+    if (p.ctx) {
+        // a cached prefix: the new tokens' K/V go to their slots first, then attention reads every
+        // key through the block table
+        e = launch_append_ranges(c, p.k, p.v, p.tables, p.num_seqs, p.max_blocks, p.cu, p.ctx, p.total_tokens, st);
+        if (e != cudaSuccess) return e;
+    }
     PkvTimer timer(c, PKV_KIND_PREFILL, st);
-    cudaError_t e = launch_plan(a, st);
+    e = launch_plan(a, st);
     g_pkv_launches++;
     if (e != cudaSuccess) return e;
     const int64_t max_ctas = items * p.num_q_heads;
-    if (D == 128)
-        e = mt == PKV_BF16 ? launch_t<128, PKV_BF16>(tq, tk, tv, tp, a, max_ctas, c->num_sms, st)
-                           : launch_t<128, PKV_F16>(tq, tk, tv, tp, a, max_ctas, c->num_sms, st);
-    else
-        e = mt == PKV_BF16 ? launch_t<64, PKV_BF16>(tq, tk, tv, tp, a, max_ctas, c->num_sms, st)
-                           : launch_t<64, PKV_F16>(tq, tk, tv, tp, a, max_ctas, c->num_sms, st);
+#define PKV_PREFILL_CASE(DD, MM, PG) \
+    if (D == DD && mt == MM && (p.ctx != nullptr) == PG) e = launch_t<DD, MM, PG>(tq, tk, tv, tp, a, max_ctas, c->num_sms, st);
+    PKV_PREFILL_CASE(128, PKV_F16, false)
+    PKV_PREFILL_CASE(128, PKV_BF16, false)
+    PKV_PREFILL_CASE(64, PKV_F16, false)
+    PKV_PREFILL_CASE(64, PKV_BF16, false)
+    PKV_PREFILL_CASE(128, PKV_F16, true)
+    PKV_PREFILL_CASE(128, PKV_BF16, true)
+    PKV_PREFILL_CASE(64, PKV_F16, true)
+    PKV_PREFILL_CASE(64, PKV_BF16, true)
+#undef PKV_PREFILL_CASE
     g_pkv_launches++;
     return e;
 }

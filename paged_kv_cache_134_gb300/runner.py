@@ -111,3 +111,44 @@ def run_prefill(w, keep_cache=False):
         cache.close()
     return res
 
+
+
+class ContextPrefillInputs:
+    """Device-resident inputs of a prefill over cached prefixes."""
+
+    def __init__(self, w):
+        md = TORCH_DT[w.dtype]
+        self.q, self.k, self.v = dev(w.q, md), dev(w.k, md), dev(w.v, md)
+        self.cu = dev(w.cu_seqlens)
+        self.ctx = dev(w.context_lens.astype(np.int32))
+        self.tables = dev(w.block_tables)
+        self.out = torch.empty_like(self.q)
+        self.max_seqlen = w.max_seqlen
+        self.scale = float(w.scale)
+
+
+def fill_context(cache, w):
+    """Write the cached tokens of a ContextPrefillWorkload (the shared prefix once)."""
+    md = TORCH_DT[w.dtype]
+    if len(w.fill_seq_ids):
+        slots = P.paged_slot_mapping(dev(w.block_tables), dev(w.fill_seq_ids), dev(w.fill_positions), w.block_size)
+        P.paged_kv_append(cache, dev(w.fill_k, md), dev(w.fill_v, md), slots)
+
+
+def context_prefill_step(cache, x: ContextPrefillInputs):
+    return P.paged_prefill_attention(x.q, x.k, x.v, x.cu, x.ctx, x.max_seqlen, x.tables, cache, x.scale, out=x.out)
+
+
+def run_context_prefill(w, keep_cache=False):
+    cache = new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.dtype, w.dtype)
+    fill_context(cache, w)
+    x = ContextPrefillInputs(w)
+    out = context_prefill_step(cache, x)
+    torch.cuda.synchronize()
+    res = dict(out=out.float().cpu().double().numpy(), err=cache.check_error(), strides=cache.view()[1],
+               pool=pool_numpy(cache))
+    if keep_cache:
+        res["cache"], res["inputs"] = cache, x
+    else:
+        cache.close()
+    return res

@@ -21,6 +21,9 @@ decode, packed prefill, prefix sharing and stress sweep are measured on:
 * ``prefix13b`` 13B layer shape: 64 sequences, 40/40 heads, D=128, bs=32,
                 a 4096-token prefix (128 blocks) shared by every table
                 (ref count 64) plus a private suffix U{1..512}.
+* ``prefix_hit_prefill``  16 requests behind one cached 1500-token system prompt (its 93 whole
+                blocks shared by every table), each prefilling the prompt's last 12 tokens
+                plus a tail of U{100..300} tokens; 32/32 heads, D=128, bs=16, fp16.
 * ``stress``    256 sequences, log-normal lengths (median 500, cap 8192),
                 32 query / 8 KV heads, D=128, bs in {8,16,32}, KV bf16 or
                 FP8-E4M3 with a per-KV-head fp32 scale, block ids drawn from
@@ -209,6 +212,111 @@ class PrefillWorkload:
     def flops(self) -> int:
         """Causal attention flops: 2 contractions * 2 flop/MAC * D per (query, key) pair per head."""
         return 4 * self.head_dim * self.num_q_heads * self.causal_pairs()
+
+
+@dataclasses.dataclass
+class ContextPrefillWorkload:
+    """Prefill of each prompt's tail over the prefix its blocks already hold."""
+
+    name: str
+    context_lens: np.ndarray        # int32 [S] tokens already cached (a multiple of bs when shared)
+    new_lens: np.ndarray            # int32 [S] tail tokens to prefill
+    cu_seqlens: np.ndarray          # int32 [S + 1] over the tail tokens
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    dtype: str
+    scale: np.float32
+    block_tables: np.ndarray        # int32 [S, max_blocks] covering context + tail, -1 padded
+    fill_seq_ids: np.ndarray        # int32 [N] table row used to write each cached token
+    fill_positions: np.ndarray      # int32 [N]
+    fill_k: np.ndarray              # uint16 [N, Hkv, D]
+    fill_v: np.ndarray
+    q: np.ndarray                   # uint16 [T, Hq, D] tail tokens, packed
+    k: np.ndarray                   # uint16 [T, Hkv, D]
+    v: np.ndarray
+    ref_count: np.ndarray           # int32 [NB]
+    shared_prefix_len: int = 0      # tokens at the head of every table, stored once
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.new_lens)
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def max_seqlen(self) -> int:
+        return int(self.new_lens.max()) if len(self.new_lens) else 0
+
+    def causal_pairs(self) -> int:
+        """(query, key) pairs: tail row r of sequence i sees context_i + r + 1 keys."""
+        return int(sum(int(n) * int(c) + int(n) * (int(n) + 1) // 2 for c, n in zip(self.context_lens, self.new_lens)))
+
+    def flops(self) -> int:
+        return 4 * self.head_dim * self.num_q_heads * self.causal_pairs()
+
+
+def context_prefill(seed: int = 1006, context_lens=(0, 16, 37, 200), new_lens=(5, 130, 64, 1), shared_prefix: int = 0,
+                    heads: int = 4, kv_heads: Optional[int] = None, d: int = 128, bs: int = 16, dtype: str = F16,
+                    pool_factor: float = 1.25) -> ContextPrefillWorkload:
+    """Sequences holding context_lens[i] cached tokens get new_lens[i] tail tokens.  With shared_prefix
+    > 0 (a multiple of bs) the first shared_prefix tokens of every sequence live once, in blocks every
+    table points at (the prefix-cache hit, 2kiu.com section 4.3 step 3); the rest is private."""
+    rng = np.random.default_rng(seed)
+    prng = np.random.default_rng(seed + 0x9E37)
+    ctx = np.asarray(context_lens, dtype=np.int32)
+    nl = np.asarray(new_lens, dtype=np.int32)
+    S = len(nl)
+    hkv = heads if kv_heads is None else kv_heads
+    assert shared_prefix % bs == 0 and all(int(c) >= shared_prefix for c in ctx)
+    nshared = shared_prefix // bs
+    need = nshared + int(sum(blocks_for(int(c) + int(n), bs) - nshared for c, n in zip(ctx, nl)))
+    nb = max(1, int(math.ceil(pool_factor * need)))
+    alloc = BlockAllocator(nb, prng)
+    shared = alloc.allocate(nshared) if nshared else []
+    tables = []
+    for c, n in zip(ctx, nl):
+        if shared:
+            alloc.share(shared)
+            # the allocator counted the creator's reference already; every table adds one
+        tables.append(list(shared) + alloc.allocate(blocks_for(int(c) + int(n), bs) - nshared))
+    bt = _tables_array(tables)
+    # cached tokens: the shared prefix once (through table 0), every private context token once
+    fill_ids, fill_pos = [], []
+    if S and shared_prefix:
+        fill_ids.append(np.zeros(shared_prefix, np.int32))
+        fill_pos.append(np.arange(shared_prefix, dtype=np.int32))
+    for i, c in enumerate(ctx):
+        fill_ids.append(np.full(int(c) - shared_prefix, i, np.int32))
+        fill_pos.append(np.arange(shared_prefix, int(c), dtype=np.int32))
+    fill_ids = np.concatenate(fill_ids) if fill_ids else np.zeros(0, np.int32)
+    fill_pos = np.concatenate(fill_pos) if fill_pos else np.zeros(0, np.int32)
+    N, T = len(fill_ids), int(nl.sum())
+    cu = np.zeros(S + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(nl)
+    return ContextPrefillWorkload(
+        name=f"context_prefill_T{T}", context_lens=ctx, new_lens=nl, cu_seqlens=cu, num_q_heads=heads,
+        num_kv_heads=hkv, head_dim=d, block_size=bs, num_blocks=nb, dtype=dtype,
+        scale=np.float32(1.0 / math.sqrt(d)), block_tables=bt, fill_seq_ids=fill_ids, fill_positions=fill_pos,
+        fill_k=normal_bits(rng, (N, hkv, d), dtype), fill_v=normal_bits(rng, (N, hkv, d), dtype),
+        q=normal_bits(rng, (T, heads, d), dtype), k=normal_bits(rng, (T, hkv, d), dtype),
+        v=normal_bits(rng, (T, hkv, d), dtype), ref_count=alloc.ref_count.copy(), shared_prefix_len=shared_prefix)
+
+
+def prefix_hit_prefill(seed: int = 1006, num_seqs: int = 16, prompt: int = 1500, tail=(100, 300), heads: int = 32,
+                       d: int = 128, bs: int = 16, dtype: str = F16) -> ContextPrefillWorkload:
+    """A 1500-token system prompt cached once (its whole blocks: 1488 tokens), then per request the
+    prompt's remaining 12 tokens plus a tail of U{100..300} tokens to prefill (the scenario of
+    2kiu.com section 3.3: only the tail after the prefix hit is prefilled)."""
+    rng = np.random.default_rng(seed ^ 0x5EED)
+    hit = (prompt // bs) * bs
+    nl = (prompt - hit) + rng.integers(tail[0], tail[1] + 1, size=num_seqs)
+    return context_prefill(seed=seed, context_lens=[hit] * num_seqs, new_lens=nl, shared_prefix=hit, heads=heads,
+                           d=d, bs=bs, dtype=dtype, pool_factor=1.1)
 
 
 def _tables_array(tables: List[List[int]], max_blocks: Optional[int] = None) -> np.ndarray:
