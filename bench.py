@@ -316,6 +316,66 @@ def secondary_append(P, W, gpu_path, peaks, reps=20):
             "gbs": round(nbytes / kern / 1e9, 1), "frac_of_hbm": round(nbytes / kern / 1e9 / peaks[0], 4)}
 
 
+def secondary_prefix_hit(P, W, G, peaks, reps=20):
+    """Prefill of 16 prompt tails (U{100..300} + 12 tokens) over a cached, shared 1488-token prefix,
+    7B shape (32/32 heads, D=128, fp16, bs=16): ranged append of the tails + attention over the pool."""
+    w = W.prefix_hit_prefill()
+    cache = G.new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.dtype, w.dtype)
+    G.fill_context(cache, w)
+    x = G.ContextPrefillInputs(w)
+    for _ in range(3):
+        G.context_prefill_step(cache, x)
+    torch.cuda.synchronize()
+    cache.profile_start(kinds=("prefill", "append"))
+    dt = _time_loop(lambda: G.context_prefill_step(cache, x), reps, torch.cuda.current_stream()) / reps
+    prof = cache.profile_read()
+    err = cache.check_error()
+    cache.close()
+    kern = prof["prefill_ms"] / max(1, prof["prefill_launches"]) / 1e3
+    app = prof["append_ms"] / max(1, prof["append_launches"]) / 1e3
+    tflops = w.flops() / kern / 1e12
+    return {"workload": "16 prompt tails (12 + U{100..300} tokens) over a cached 1488-token prefix shared by every "
+                        "table, 32/32 heads, D=128, fp16, bs=16", "tail_tokens": w.total_tokens,
+            "tokens_per_s": round(w.total_tokens / dt, 1), "ms": round(dt * 1e3, 4),
+            "attention_kernel_ms": round(kern * 1e3, 4), "append_kernel_ms": round(app * 1e3, 4),
+            "gflop": round(w.flops() / 1e9, 3), "tflops": round(tflops, 2),
+            "frac_of_bf16_peak": round(tflops / peaks[1], 4), "device_errors": err}
+
+
+def secondary_blocks(P, W, G, peaks, reps=20, nblocks=512):
+    """Whole-block copy (copy-on-write), swap-out to and swap-in from page-locked host memory:
+    512 blocks of the 7B layer shape (256 KB each, 128 MB)."""
+    nb = 2 * nblocks + 8
+    cache = P.KVCache(nb, 16, 32, 128, "f16")
+    cache.pool_elems().fill_(1)
+    src = torch.arange(nblocks, dtype=torch.int32, device="cuda")
+    dst = src + nblocks
+    nbytes = nblocks * cache.block_bytes
+    host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    res = {"workload": f"{nblocks} blocks of 16 tokens x 32 KV heads x 128 x fp16 (256 KB each)",
+           "bytes_per_call": nbytes}
+    # copy: HBM read + write; swaps: the bytes that cross to or from host memory
+    for name, fn, moved in (("copy", lambda: P.paged_block_copy(cache, src, dst), 2 * nbytes),
+                            ("swap_out_host", lambda: P.paged_block_swap_out(cache, src, host), nbytes),
+                            ("swap_in_host", lambda: P.paged_block_swap_in(cache, dst, host), nbytes)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        cache.profile_start(kinds=("copy",))
+        _time_loop(fn, reps, torch.cuda.current_stream())
+        prof = cache.profile_read()
+        kern = prof["copy_ms"] / max(1, prof["copy_launches"]) / 1e3
+        gbs = moved / kern / 1e9
+        if name == "copy":
+            res[name] = {"kernel_us": round(kern * 1e6, 2), "gbs_read_plus_write": round(gbs, 1),
+                         "frac_of_hbm": round(gbs / peaks[0], 4)}
+        else:
+            res[name] = {"kernel_us": round(kern * 1e6, 2), "host_gbs": round(gbs, 1)}
+    res["device_errors"] = cache.check_error()
+    cache.close()
+    return res
+
+
 def run_only(case: str):
     """One secondary case alone (a short run for ncu captures); prints {case: result}."""
     torch.cuda.set_device(0)
@@ -329,6 +389,10 @@ def run_only(case: str):
         r = secondary_append(P, W, G, peaks, reps=5)
     elif case == "prefix13b":
         r = secondary_decode(P, G, peaks, W.prefix13b(), reps=5)
+    elif case == "prefix_hit":
+        r = secondary_prefix_hit(P, W, G, peaks, reps=5)
+    elif case == "blocks":
+        r = secondary_blocks(P, W, G, peaks, reps=5)
     elif case.startswith("stress_bs"):
         bs, kv = case[len("stress_bs"):].split("_")
         r = secondary_decode(P, G, peaks, W.stress(bs=int(bs), kv_dtype=kv), reps=5)
@@ -424,6 +488,8 @@ def run_ours(args):
     if rank == 0 and not args.skip_secondary:
         secondary["prefill"] = secondary_prefill(P, W, G, peaks)
         secondary["append"] = secondary_append(P, W, G, peaks)
+        secondary["prefix_hit_prefill"] = secondary_prefix_hit(P, W, G, peaks)
+        secondary["blocks"] = secondary_blocks(P, W, G, peaks)
         w4 = W.prefix13b()
         uniq = (w4.shared_prefix_len + int((w4.context_lens - w4.shared_prefix_len + 1).sum())) * \
             w4.num_kv_heads * w4.head_dim * 2 * 2
@@ -497,7 +563,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--only", default=None,
                     help="run one secondary case alone and print its JSON (for profiling): prefill, append, "
-                         "prefix13b or stress_bs{8,16,32}_{bf16,fp8}")
+                         "prefix13b, prefix_hit, blocks or stress_bs{8,16,32}_{bf16,fp8}")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -328,6 +328,17 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 last_q = n;
                 bool ok = true;
                 int issued = 0;
+                // paged mode: table entries of the blocks of one key tile (-1: no token of the sequence)
+                int ent[BN / 8];
+                auto read_entries = [&](const Item &itm, int jj) {
+                    const int send = itm.c0 + itm.n, lb0 = (jj * BN) >> a.lg_bs, nbt = BN >> a.lg_bs;
+#pragma unroll
+                    for (int l = 0; l < BN / 8; ++l)
+                        ent[l] = (l < nbt && ((lb0 + l) << a.lg_bs) < send)
+                                     ? a.tables[(int64_t)itm.seq * a.max_blocks + lb0 + l]
+                                     : -1;
+                };
+                if constexpr (PAGED) read_entries(it, 0);
                 for (int j = 0; j < it.nkv && ok; ++j) {
                     const int64_t gg = g + j;
                     const int st = (int)(gg % NKS);
@@ -337,21 +348,17 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                     if constexpr (PAGED) {
                         // the tile's blocks that hold tokens of the sequence, one box of bs rows per
                         // block and half of D from the pool; rows past the sequence's end are masked
-                        // by the softmax, and unusable block ids (reported by the V loader) are skipped
-                        const int send = it.c0 + it.n, lb0 = (j * BN) >> a.lg_bs, nbt = BN >> a.lg_bs;
+                        // by the softmax, and unusable block ids (reported by the V loader) are skipped.
+                        // The table entries of tile j + 1 are read now, ahead of their use.
                         int blk[BN / 8];
                         uint32_t bytes = 0;
 #pragma unroll
                         for (int l = 0; l < BN / 8; ++l) {
-                            blk[l] = -1;
-                            if (l < nbt && ((lb0 + l) << a.lg_bs) < send) {
-                                const int b = a.tables[(int64_t)it.seq * a.max_blocks + lb0 + l];
-                                if (b >= 0 && b < a.num_blocks) {
-                                    blk[l] = b;
-                                    bytes += (uint32_t)(a.bs * D * 2);
-                                }
-                            }
+                            blk[l] = ent[l];
+                            if (blk[l] >= a.num_blocks) blk[l] = -1;
+                            if (blk[l] >= 0) bytes += (uint32_t)(a.bs * D * 2);
                         }
+                        if (j + 1 < it.nkv) read_entries(it, j + 1);
                         mbar_arrive_expect_tx(k_full + st, bytes);
 #pragma unroll
                         for (int l = 0; l < BN / 8; ++l)
@@ -401,16 +408,23 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             ok = __all_sync(0xffffffffu, ok);
             if (!ok || it.seq < 0) break;
             const int kvh = it.h / G, send = it.c0 + it.n, nbt = BN >> a.lg_bs;
+            // lane l: table entry of block l of a key tile, read one tile ahead of its use
+            auto entry = [&](int jj) -> int {
+                const int lbl = ((jj * BN) >> a.lg_bs) + lane;
+                return (lane < nbt && (lbl << a.lg_bs) < send) ? a.tables[(int64_t)it.seq * a.max_blocks + lbl] : -1;
+            };
+            int nxt = entry(0);
             int issued = 0;
             for (int j = 0; j < it.nkv && ok; ++j) {
                 const int64_t gg = g + j;
                 const int st = (int)(gg % NVS);
                 const int64_t round = gg / NVS;
+                const int b = nxt;
+                if (j + 1 < it.nkv) nxt = entry(j + 1);
                 if (round >= 1) ok = __all_sync(0xffffffffu, mbar_wait(v_empty + st, (round - 1) & 1));
                 if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) break;
                 const int kbase = j * BN, lb = (kbase >> a.lg_bs) + lane;
                 const bool has = lane < nbt && (lb << a.lg_bs) < send;
-                const int b = has ? a.tables[(int64_t)it.seq * a.max_blocks + lb] : -1;
                 const bool good = has && b >= 0 && b < a.num_blocks;
                 if (has && !good) set_error(a.err, PKV_DEVERR_BLOCK_ID);
                 const bool full = good && ((lb + 1) << a.lg_bs) <= send;
@@ -424,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                     for (int c = 0; c < D / 64; ++c)
                         tc::tma_load_2d(stage + c * BN * 128 + ((lane << a.lg_bs) * 128), &tp, c * 64, y, v_full + st);
                 }
-                for (int r0 = 0; r0 < BN; r0 += RPI) {
+                for (int r0 = 0; fullmask != (1u << nbt) - 1u && r0 < BN; r0 += RPI) {
                     const int r = r0 + rsub, l = r >> a.lg_bs;
                     const int bl = __shfl_sync(0xffffffffu, good ? b : -1, l);
                     if ((fullmask >> l) & 1u) continue;
