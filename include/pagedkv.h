@@ -218,6 +218,54 @@ int paged_block_swap_out(pkv_cache_t cache, const int32_t *block_ids, int64_t nu
  * on resumption; the block table is then rewritten by the caller. */
 int paged_block_swap_in(pkv_cache_t cache, const int32_t *block_ids, int64_t num_ids, const void *src, void *stream);
 
+/* ---------------------------------------------------------------- prefix cache (host work)
+ * The functions below run on the host and take HOST pointers.  They implement the prefix cache
+ * that sits on top of the paged pool (notes "vLLM：PagedAttention 与前缀缓存", sections on chained
+ * hashing, lookup and reuse, reference counts and LRU, boundary conditions; 2kiu.com sections 3.2
+ * and 4.3 steps 2-3).  Thread-safe per cache object. */
+
+/* Chained block hashes: for every FULL block i of tokens[0 .. num_tokens) (num_tokens / block_size
+ * of them; a partial tail block is not hashed),
+ *   hash_i = SHA-256( hash_{i-1} (32 bytes) || tokens of block i as big-endian uint32 || extra )
+ * with hash_{-1} = init (32 bytes) or 32 zero bytes when init is NULL.  extra (extra_bytes bytes,
+ * may be NULL when 0) keys the semantic context: model and tokenizer version, adapter, salt.
+ * hashes: [num_tokens / block_size][32] bytes, written; *num_hashes = their count. */
+int pkv_block_hashes(const int32_t *tokens, int64_t num_tokens, int block_size, const void *extra, int64_t extra_bytes,
+                     const uint8_t *init, uint8_t *hashes, int64_t *num_hashes);
+
+typedef struct pkv_prefix_cache *pkv_prefix_cache_t; /* opaque */
+
+/* A block manager over num_blocks physical block ids with a hash -> block map.  All blocks start
+ * free and unhashed. */
+int pkv_prefix_cache_create(int64_t num_blocks, pkv_prefix_cache_t *out);
+int pkv_prefix_cache_destroy(pkv_prefix_cache_t pc);
+
+/* Lookup: walk hashes[0 .. num_hashes) in order; each hash found in the map attaches its block
+ * (blocks[i] = id, reference count + 1; a cached-free block leaves the LRU queue); the first hash
+ * not found ends the walk.  *num_hit = number of blocks attached (the hit is *num_hit full blocks). */
+int pkv_prefix_cache_match(pkv_prefix_cache_t pc, const uint8_t *hashes, int64_t num_hashes, int32_t *blocks,
+                           int64_t *num_hit);
+
+/* Take n blocks for new tokens (reference count 1): free unhashed blocks first, in the order they
+ * became free, then cached-free blocks in LRU order (least recently released first), whose
+ * mappings are dropped.  Fewer than n available: PKV_ENOMEM ("KV cache block pool exhausted") and
+ * nothing is taken. */
+int pkv_prefix_cache_allocate(pkv_prefix_cache_t pc, int64_t n, int32_t *blocks);
+
+/* Publish full blocks after their prefill: map hashes[i] -> blocks[i].  A hash that already maps to
+ * a block keeps its block.  Every block must be held by a request (EINVAL otherwise; nothing is
+ * changed). */
+int pkv_prefix_cache_insert(pkv_prefix_cache_t pc, const uint8_t *hashes, const int32_t *blocks, int64_t n);
+
+/* A request lets go of its blocks: reference count - 1; at 0 a hashed block keeps its mapping and
+ * joins the LRU queue (most recently released last), an unhashed block returns to the free list.
+ * Releasing a block nobody holds is EINVAL (nothing is changed). */
+int pkv_prefix_cache_release(pkv_prefix_cache_t pc, const int32_t *blocks, int64_t n);
+
+/* out[0] = free unhashed blocks, out[1] = cached-free blocks (LRU queue), out[2] = blocks held by
+ * requests, out[3] = mapped hashes. */
+int pkv_prefix_cache_stats(pkv_prefix_cache_t pc, int64_t out[4]);
+
 /* Profiling.  Between kv_cache_profile_start and kv_cache_profile_read the library records
  * CUDA events around each kernel it launches for this cache (decode split-K kernel, split
  * merge kernel, prefill kernel, append kernel, block copy kernel) on the launch stream.  kv_cache_profile_read synchronises

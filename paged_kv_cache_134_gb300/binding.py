@@ -60,6 +60,14 @@ def lib() -> ctypes.CDLL:
         L.paged_prefill_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, vp, i32, vp, i32, ctypes.c_float, vp,
                                               vp]
         L.paged_block_copy.argtypes = [vp, vp, vp, i64, vp]
+        L.pkv_block_hashes.argtypes = [vp, i64, i32, vp, i64, vp, vp, ctypes.POINTER(i64)]
+        L.pkv_prefix_cache_create.argtypes = [i64, ctypes.POINTER(vp)]
+        L.pkv_prefix_cache_destroy.argtypes = [vp]
+        L.pkv_prefix_cache_match.argtypes = [vp, vp, i64, vp, ctypes.POINTER(i64)]
+        L.pkv_prefix_cache_allocate.argtypes = [vp, i64, vp]
+        L.pkv_prefix_cache_insert.argtypes = [vp, vp, vp, i64]
+        L.pkv_prefix_cache_release.argtypes = [vp, vp, i64]
+        L.pkv_prefix_cache_stats.argtypes = [vp, vp]
         L.paged_block_swap_out.argtypes = [vp, vp, i64, vp, vp]
         L.paged_block_swap_in.argtypes = [vp, vp, i64, vp, vp]
         L.kv_cache_profile_start.argtypes = [vp, ctypes.c_uint]
@@ -374,3 +382,78 @@ def paged_prefill_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, c
                                          int(max_seqlen), T, _ptr(block_tables), block_tables.shape[1], cache.handle,
                                          hq, ctypes.c_float(scale), _ptr(out), _stream()))
     return out
+
+
+# ----------------------------------------------------------------------------- prefix cache (host)
+
+def _np(a, dtype):
+    import numpy as np
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def block_hashes(tokens, block_size: int, extra: bytes = b"", init: Optional[bytes] = None):
+    """Chained SHA-256 hashes of the full blocks of ``tokens`` (host); returns uint8 [n, 32]."""
+    import numpy as np
+    tok = _np(tokens, np.int32)
+    n = len(tok) // int(block_size)
+    out = np.zeros((n, 32), np.uint8)
+    got = ctypes.c_int64(0)
+    ex = ctypes.create_string_buffer(bytes(extra), len(extra)) if extra else None
+    ini = ctypes.create_string_buffer(bytes(init), 32) if init is not None else None
+    _check(lib().pkv_block_hashes(tok.ctypes.data, len(tok), int(block_size), ex, len(extra), ini,
+                                  out.ctypes.data, ctypes.byref(got)))
+    assert got.value == n
+    return out
+
+
+class PrefixCache:
+    """Host prefix cache: hash -> physical block map, reference counts, LRU retention."""
+
+    def __init__(self, num_blocks: int):
+        h = ctypes.c_void_p()
+        _check(lib().pkv_prefix_cache_create(int(num_blocks), ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            lib().pkv_prefix_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def match(self, hashes):
+        """Blocks of the longest cached prefix (attached: reference count + 1)."""
+        import numpy as np
+        hs = _np(hashes, np.uint8).reshape(-1, 32)
+        out = np.zeros(len(hs), np.int32)
+        hit = ctypes.c_int64(0)
+        _check(lib().pkv_prefix_cache_match(self._h, hs.ctypes.data, len(hs), out.ctypes.data, ctypes.byref(hit)))
+        return out[: hit.value]
+
+    def allocate(self, n: int):
+        import numpy as np
+        out = np.zeros(int(n), np.int32)
+        _check(lib().pkv_prefix_cache_allocate(self._h, int(n), out.ctypes.data))
+        return out
+
+    def insert(self, hashes, blocks):
+        import numpy as np
+        hs = _np(hashes, np.uint8).reshape(-1, 32)
+        bl = _np(blocks, np.int32)
+        assert len(hs) == len(bl)
+        _check(lib().pkv_prefix_cache_insert(self._h, hs.ctypes.data, bl.ctypes.data, len(bl)))
+
+    def release(self, blocks):
+        import numpy as np
+        bl = _np(blocks, np.int32)
+        _check(lib().pkv_prefix_cache_release(self._h, bl.ctypes.data, len(bl)))
+
+    def stats(self) -> dict:
+        import numpy as np
+        out = np.zeros(4, np.int64)
+        _check(lib().pkv_prefix_cache_stats(self._h, out.ctypes.data))
+        return dict(free=int(out[0]), cached_free=int(out[1]), in_use=int(out[2]), hashed=int(out[3]))

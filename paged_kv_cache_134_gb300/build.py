@@ -17,7 +17,8 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libpagedkv.so")
 
 SOURCES = ["api.cu", "append.cu", "decode.cu", "decode_f16.cu", "decode_bf16.cu", "decode_fp8_f16.cu",
-           "decode_fp8_bf16.cu", "decode_tc.cu", "prefill.cu", "noalloc.cu", "blocks.cu"]
+           "decode_fp8_bf16.cu", "decode_tc.cu", "prefill.cu", "noalloc.cu", "blocks.cu",
+           "prefix_cache.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
@@ -48,7 +49,7 @@ def build(verbose: bool = False, extra_flags=None) -> str:
     extra = list(extra_flags or [])
     if os.environ.get("PAGEDKV_PTXAS_VERBOSE"):
         extra += ["-Xptxas", "-v"]
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
+    objs = [os.path.join(BUILD, os.path.splitext(s)[0] + ".o") for s in SOURCES]
     todo = [(s, o) for s, o in zip(SOURCES, objs) if _stale(o, deps) or extra]
 
     def compile_one(so):
