@@ -265,22 +265,26 @@ def secondary_prefill(P, W, gpu_path, peaks, reps=20):
             "frac_of_bf16_peak": round(tflops / peaks[1], 4), "device_errors": err}
 
 
-def secondary_decode(P, G, peaks, w, reps=50, unique_bytes=None):
-    """Decode step (append_at + decode + merge) on another configuration; decode kernel timed by events."""
+def secondary_decode(P, G, peaks, w, reps=50, unique_bytes=None, cascade=0):
+    """Decode step (append_at + decode + merge) on another configuration; decode kernel timed by events.
+    cascade > 0: the tables share that many tokens and the step runs the cascade decode (prefix phase
+    on the tensor cores + suffix split-K decode + merge); its kernels are summed."""
     cache = G.new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype, w.model_dtype,
                         w.k_scale, w.v_scale)
     G.fill_cache(cache, w)
     x = G.DecodeInputs(w)
     cache.reserve(w.num_seqs, w.num_q_heads, w.max_blocks)
     for _ in range(5):
-        G.decode_step(cache, x)
+        G.decode_step(cache, x, cascade_prefix=cascade)
     torch.cuda.synchronize()
-    cache.profile_start(kinds=("decode",))
-    t = _time_loop(lambda: G.decode_step(cache, x), reps, torch.cuda.current_stream()) / reps
+    cache.profile_start(kinds=("decode", "prefill") if cascade else ("decode",))
+    t = _time_loop(lambda: G.decode_step(cache, x, cascade_prefix=cascade), reps, torch.cuda.current_stream()) / reps
     prof = cache.profile_read()
     err = cache.check_error()
     cache.close()
     kern = prof["decode_ms"] / max(1, prof["decode_launches"]) / 1e3
+    if cascade:   # prefix phase (recorded as the prefill kind) + suffix decode kernel
+        kern += prof["prefill_ms"] / max(1, prof["prefill_launches"]) / 1e3
     kv = w.kv_read_bytes()
     r = {"kv_dtype": w.kv_dtype, "block_size": w.block_size, "num_seqs": w.num_seqs,
          "heads": f"{w.num_q_heads}/{w.num_kv_heads}", "kv_bytes": kv, "step_us": round(t * 1e6, 2),
@@ -291,6 +295,7 @@ def secondary_decode(P, G, peaks, w, reps=50, unique_bytes=None):
         r["kv_gbs_label"] = "logical (shared prefix re-read per sequence, mostly L2 hits)"
         r["unique_kv_bytes"] = unique_bytes
         r["unique_kv_gbs"] = round(unique_bytes / kern / 1e9, 1)
+        r["unique_frac_of_hbm"] = round(unique_bytes / kern / 1e9 / peaks[0], 4)
     return r
 
 
@@ -419,6 +424,9 @@ def run_only(case: str):
         r = secondary_append(P, W, G, peaks, reps=5)
     elif case == "prefix13b":
         r = secondary_decode(P, G, peaks, W.prefix13b(), reps=5)
+    elif case == "prefix13b_cascade":
+        w4 = W.prefix13b()
+        r = secondary_decode(P, G, peaks, w4, reps=5, cascade=w4.shared_prefix_len)
     elif case == "prefix_hit":
         r = secondary_prefix_hit(P, W, G, peaks, reps=5)
     elif case == "blocks":
@@ -529,6 +537,10 @@ def run_ours(args):
         secondary["prefix13b"] = dict(workload="13B-shape decode, 64 seqs sharing a 4096-token prefix (128 blocks, "
                                                "ref count 64) + private suffix U{1..512}, 40/40 heads, bs=32, fp16",
                                       **secondary_decode(P, G, peaks, w4, unique_bytes=uniq))
+        secondary["prefix13b_cascade"] = dict(
+            workload="the same 13B-shape batch, cascade decode: the 4096-token shared prefix read once per "
+                     "(head, 512-key split) for all 64 sequences on the tensor cores, suffixes by split-K decode",
+            **secondary_decode(P, G, peaks, w4, unique_bytes=uniq, cascade=w4.shared_prefix_len))
         del w4
         stress = {}
         for kv in ("bf16", "fp8"):
@@ -596,7 +608,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--only", default=None,
                     help="run one secondary case alone and print its JSON (for profiling): prefill, append, "
-                         "prefix13b, prefix_hit, blocks or stress_bs{8,16,32}_{bf16,fp8}")
+                         "prefix13b, prefix13b_cascade, prefix_hit, blocks, prefix_cache or stress_bs{8,16,32}_{bf16,fp8}")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

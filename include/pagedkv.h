@@ -159,6 +159,21 @@ int paged_decode_attention_noalloc(const void *q, pkv_cache_t cache, const int32
                                    int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                                    int num_q_heads, float scale, void *out, void *stream);
 
+/* Cascade decode for a batch that shares a prefix (2kiu.com section 3.3: with a prefix cache many
+ * requests share prefix blocks, and decode still reads them; section 6.4: decode-bound batches with
+ * a high hit rate): same result as paged_decode_attention, but the first shared_prefix_len tokens,
+ * which every table must name with the same blocks (those of table row 0), are read once per
+ * (query head, 512-key split) for the whole batch instead of once per sequence.  Their attention
+ * runs on the tensor cores as a matrix product of all the batch's queries with the prefix keys; the
+ * tokens past the prefix go through the split-K decode; one merge combines both.  shared_prefix_len:
+ * a multiple of block_size, at most max_blocks_per_seq * block_size, and at most every context
+ * length (a shorter sequence sets PKV_DEVERR_LENGTH); 0 makes this paged_decode_attention.
+ * fp16/bf16 caches (EUNSUPPORTED for FP8).  The prefix's split partials are rounded like any split
+ * (fp32), so outputs agree with paged_decode_attention to the decode tolerance, not bit for bit. */
+int paged_decode_attention_cascade(const void *q, pkv_cache_t cache, const int32_t *block_tables,
+                                   int max_blocks_per_seq, const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                   int shared_prefix_len, float scale, void *out, void *stream);
+
 /* Packed causal prefill (discosf.com sections 3.1-3.3 and 4.2): sequences packed back to
  * back, sequence i owning rows [cu_seqlens[i], cu_seqlens[i+1]):
  *   out[cu_i + r][h] = sum_{c <= r} softmax_c(scale * q[cu_i + r][h] . k[cu_i + c][g]) v[cu_i + c][g]

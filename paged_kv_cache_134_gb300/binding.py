@@ -60,6 +60,7 @@ def lib() -> ctypes.CDLL:
         L.paged_prefill_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, vp, i32, vp, i32, ctypes.c_float, vp,
                                               vp]
         L.paged_block_copy.argtypes = [vp, vp, vp, i64, vp]
+        L.paged_decode_attention_cascade.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp, vp]
         L.pkv_block_hashes.argtypes = [vp, i64, i32, vp, i64, vp, vp, ctypes.POINTER(i64)]
         L.pkv_prefix_cache_create.argtypes = [i64, ctypes.POINTER(vp)]
         L.pkv_prefix_cache_destroy.argtypes = [vp]
@@ -275,6 +276,25 @@ def paged_decode_attention(q: torch.Tensor, cache: KVCache, block_tables: torch.
     _req(out, "out", cache.torch_dtype, 3)
     _check(lib().paged_decode_attention(_ptr(q), cache.handle, _ptr(block_tables), block_tables.shape[1],
                                         _ptr(context_lens), S, hq, ctypes.c_float(scale), _ptr(out), _stream()))
+    return out
+
+
+def paged_decode_attention_cascade(q: torch.Tensor, cache: KVCache, block_tables: torch.Tensor,
+                                   context_lens: torch.Tensor, shared_prefix_len: int, scale: float,
+                                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """paged_decode_attention for a batch whose tables share their first ``shared_prefix_len`` tokens."""
+    _req(q, "q", cache.torch_dtype, 3)
+    _req(block_tables, "block_tables", torch.int32, 2)
+    _req(context_lens, "context_lens", torch.int32, 1)
+    S, hq, d = q.shape
+    if d != cache.head_dim or block_tables.shape[0] != S or context_lens.numel() != S:
+        raise ValueError("shape mismatch between q, block_tables and context_lens")
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, "out", cache.torch_dtype, 3)
+    _check(lib().paged_decode_attention_cascade(_ptr(q), cache.handle, _ptr(block_tables), block_tables.shape[1],
+                                                _ptr(context_lens), S, hq, int(shared_prefix_len),
+                                                ctypes.c_float(scale), _ptr(out), _stream()))
     return out
 
 

@@ -331,6 +331,78 @@ static int prefill_entry(const void *q, const void *k, const void *v, const int3
     return PKV_OK;
 }
 
+int paged_decode_attention_cascade(const void *q, pkv_cache_t c, const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *context_lens, int num_seqs, int num_q_heads, int shared_prefix_len,
+                                   float scale, void *out, void *stream) {
+    if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
+    if (shared_prefix_len < 0 || shared_prefix_len % c->block_size)
+        return pkv_fail(PKV_EINVAL, "shared_prefix_len %d is not a non-negative multiple of block_size %d",
+                        shared_prefix_len, c->block_size);
+    if (shared_prefix_len == 0)
+        return paged_decode_attention(q, c, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                                      scale, out, stream);
+    if (num_seqs < 0 || max_blocks_per_seq < 0) return pkv_fail(PKV_EINVAL, "negative size");
+    if (num_seqs == 0) return PKV_OK;
+    if (num_seqs > 1024) return pkv_fail(PKV_EUNSUPPORTED, "num_seqs %d > 1024 per call", num_seqs);
+    if ((int64_t)shared_prefix_len > (int64_t)max_blocks_per_seq * c->block_size)
+        return pkv_fail(PKV_EINVAL, "shared prefix longer than the tables");
+    if (c->kv_dtype == PKV_FP8_E4M3)
+        return pkv_fail(PKV_EUNSUPPORTED, "cascade decode reads fp16/bf16 caches only");
+    if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads)
+        return pkv_fail(PKV_EINVAL, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                        c->num_kv_heads);
+    if (!supported_group(num_q_heads / c->num_kv_heads))
+        return pkv_fail(PKV_EUNSUPPORTED, "num_q_heads / num_kv_heads = %d not in {1, 2, 4, 8}",
+                        num_q_heads / c->num_kv_heads);
+    if (!q || !out || !context_lens || !block_tables) return pkv_fail(PKV_EINVAL, "NULL pointer");
+    if (!aligned16(q) || !aligned16(out)) return pkv_fail(PKV_EINVAL, "q and out must be 16-byte aligned");
+    if (!(scale == scale)) return pkv_fail(PKV_EINVAL, "scale is NaN");
+    if (int r = check_device(c)) return r;
+    const int split_tokens = 512; // keys per prefix split: a multiple of the 64-key tiles
+    const int nps = (shared_prefix_len + split_tokens - 1) / split_tokens;
+    const int pb = shared_prefix_len / c->block_size;
+    DecodeLaunch d;
+    d.q = q;
+    d.out = out;
+    d.tables = block_tables;
+    d.lens = context_lens;
+    d.max_blocks = max_blocks_per_seq;
+    d.num_seqs = num_seqs;
+    d.num_q_heads = num_q_heads;
+    d.scale = scale;
+    d.split_blocks = decode_split_blocks(c);
+    d.max_splits = nps + (max_blocks_per_seq - pb + d.split_blocks - 1) / d.split_blocks;
+    d.start_block = pb;
+    d.slot0 = nps;
+    const int64_t rows = (int64_t)num_seqs * num_q_heads * d.max_splits;
+    if (int r = ensure_workspace(c, rows * (c->head_dim + 2))) return r;
+    d.ws_o = c->ws;
+    d.ws_ml = nullptr;
+    CascadePrefixLaunch p;
+    p.q = q;
+    p.tables = block_tables;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.prefix_tokens = shared_prefix_len;
+    p.split_tokens = split_tokens;
+    p.max_splits = d.max_splits;
+    p.scale = scale;
+    p.ws_o = c->ws;
+    p.ws_ml = c->ws + rows * c->head_dim;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    {
+        PkvTimer timer(c, PKV_KIND_PREFILL, st);
+        e = launch_cascade_prefix(c, p, st);
+    }
+    if (e == cudaErrorNotSupported) return pkv_fail(PKV_EUNSUPPORTED, "cascade shape not supported");
+    if (e != cudaSuccess) return pkv_cuda_fail(e, "cascade prefix launch");
+    e = launch_decode(c, d, st);
+    if (e != cudaSuccess) return pkv_cuda_fail(e, "decode launch");
+    return PKV_OK;
+}
+
 int packed_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens, int num_seqs,
                              int max_seqlen, int64_t total_tokens, const int32_t *block_tables,
                              int max_blocks_per_seq, pkv_cache_t c, int num_q_heads, float scale, void *out,

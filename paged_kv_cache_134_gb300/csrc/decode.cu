@@ -75,6 +75,8 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
     a.split_blocks = d.split_blocks;
     a.max_splits = d.max_splits;
     a.qk_scale_log2 = d.scale * 1.4426950408889634f;
+    a.start_block = d.start_block;
+    a.slot0 = d.slot0;
 
     DecodeFn fn;
     OccFn occ;

@@ -56,6 +56,10 @@ struct Args {
     int max_blocks, num_seqs, hq, hkv, bs;
     int split_blocks, max_splits, nstages;
     float qk_scale_log2; // scale * log2(e)
+    // cascade decode: the first start_block blocks of every table are a shared prefix whose
+    // attention another kernel computed into workspace slots [0, slot0); this kernel then covers the
+    // blocks from start_block on and writes its splits from slot slot0 on (both 0 otherwise)
+    int start_block = 0, slot0 = 0;
 };
 
 template <int KVT>
@@ -85,7 +89,7 @@ PKV_DEV int find_row(const int *pref, int n, int k) {
     return lo;
 }
 
-PKV_DEV Unit unit_info(int u, const int *pf, const int *pp, const int *nb, int S, int hkv, int bps) {
+PKV_DEV Unit unit_info(int u, const int *pf, const int *pp, const int *nb, int S, int hkv, int bps, int sb = 0) {
     Unit r;
     const int nfull_units = pf[S] * hkv;
     if (u < nfull_units) {
@@ -93,7 +97,7 @@ PKV_DEV Unit unit_info(int u, const int *pf, const int *pp, const int *nb, int S
         r.kvh = u - k * hkv;
         r.s = find_row(pf, S, k);
         r.j = k - pf[r.s];
-        r.blk0 = r.j * bps;
+        r.blk0 = sb + r.j * bps;
         r.ntiles = bps;
     } else {
         const int u2 = u - nfull_units;
@@ -101,7 +105,7 @@ PKV_DEV Unit unit_info(int u, const int *pf, const int *pp, const int *nb, int S
         r.kvh = u2 - k * hkv;
         r.s = find_row(pp, S, k);
         r.j = pf[r.s + 1] - pf[r.s];
-        r.blk0 = r.j * bps;
+        r.blk0 = sb + r.j * bps;
         r.ntiles = nb[r.s] - r.blk0;
     }
     r.nsplit = (pf[r.s + 1] - pf[r.s]) + (pp[r.s + 1] - pp[r.s]);
@@ -320,8 +324,9 @@ PKV_DEV void build_unit_list(const Args &a, int *pf, int *pp, int *nb, int warp,
             n = a.max_blocks;
         }
         nb[s] = n;
-        pf[s + 1] = n / bps;
-        pp[s + 1] = (n % bps) ? 1 : 0;
+        const int m = n > a.start_block ? n - a.start_block : 0; // blocks this kernel covers
+        pf[s + 1] = m / bps;
+        pp[s + 1] = (m % bps) ? 1 : 0;
     }
     __syncthreads();
     if (warp == 0) {
@@ -390,7 +395,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
         uint32_t tau = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-            const Unit un = unit_info(u, pf, pp, nb, S, a.hkv, bps);
+            const Unit un = unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
             const int32_t *trow = a.tables + (int64_t)un.s * a.max_blocks + un.blk0;
             const char *head_base = a.pool + (int64_t)un.kvh * a.tile_bytes;
             for (int i0 = 0; i0 < un.ntiles && ok; i0 += 32) {
@@ -446,7 +451,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     const int tid = threadIdx.x; // 0 .. NCW*32-1
     uint32_t tau = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        const Unit un = unit_info(u, pf, pp, nb, S, a.hkv, bps);
+        const Unit un = unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
         const int L = a.lens[un.s];
         float qs = a.qk_scale_log2;
         if constexpr (KVT == PKV_FP8_E4M3) qs *= a.k_scale[un.kvh];
@@ -543,11 +548,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
                 }
             }
             const int h = un.kvh * G + g;
-            if (un.nsplit == 1) {
+            if (un.nsplit == 1 && a.slot0 == 0) {
                 const float y = den > 0.f ? (num / den) * vs : 0.f;
                 static_cast<T *>(a.out)[((int64_t)un.s * a.hq + h) * D + d] = M::from_f(y);
             } else {
-                const int64_t idx = ((int64_t)un.s * a.hq + h) * a.max_splits + un.j;
+                const int64_t idx = ((int64_t)un.s * a.hq + h) * a.max_splits + a.slot0 + un.j;
                 a.ws_o[idx * D + d] = num * vs;
                 if (d == 0) reinterpret_cast<float2 *>(a.ws_ml)[idx] = make_float2(Mx, den);
             }
@@ -575,8 +580,13 @@ __global__ void __launch_bounds__(128) merge_kernel(const Args a) {
     const int L = a.lens[s];
     int n = L > 0 ? (L + a.bs - 1) / a.bs : 0;
     if (n > a.max_blocks) n = a.max_blocks;
-    const int nsplit = n / a.split_blocks + ((n % a.split_blocks) ? 1 : 0);
-    if (nsplit == 1) return;
+    if (a.slot0 > 0 && L < a.start_block * a.bs) {
+        // cascade: a sequence shorter than the shared prefix it claims
+        if (threadIdx.x == 0 && row % a.hq == 0) set_error(a.err, PKV_DEVERR_LENGTH);
+    }
+    const int m = n > a.start_block ? n - a.start_block : 0;
+    const int nsplit = a.slot0 + m / a.split_blocks + ((m % a.split_blocks) ? 1 : 0);
+    if (nsplit == 1 && a.slot0 == 0) return;
     T *o = static_cast<T *>(a.out) + (int64_t)row * D;
     if (nsplit == 0) {
         for (int e = threadIdx.x; e < D; e += blockDim.x) o[e] = M::from_f(0.f);

@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int u = blockIdx.x, i = 0, nsteps = 0;
         Unit un{};
         if (u < U) {
-            un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps);
+            un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
             nsteps = (un.ntiles + bpstep - 1) / bpstep;
         }
         int cur = u < U ? entry(un, 0) : 0;
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 u2 = u + gridDim.x;
                 i2 = 0;
                 if (u2 < U) {
-                    un2 = pkv_decode::unit_info(u2, pf, pp, nb, S, a.hkv, bps);
+                    un2 = pkv_decode::unit_info(u2, pf, pp, nb, S, a.hkv, bps, a.start_block);
                     nsteps2 = (un2.ntiles + bpstep - 1) / bpstep;
                 }
             }
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t gs = 0;
             int nu = 0;
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
-                const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps);
+                const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
                 const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
                 const int qb = nu & 1;
                 ok = __all_sync(0xffffffffu, mbar_wait(q_full + qb, (nu >> 1) & 1)) && issue_s(gs, qb);
@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t gs = 0;
         int nu = 0;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
-            const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps);
+            const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
             const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
             const int L = a.lens[un.s];
             const int tok0 = un.blk0 * a.bs;
@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lt[g] = (red_sum[g] + red_sum[NQ + g]) + (red_sum[2 * NQ + g] + red_sum[3 * NQ + g]);
             named_barrier_sync(1, 128); // red_sum is rewritten by the next unit
             const int h0 = un.kvh * G;
-            if (un.nsplit == 1) {
+            if (un.nsplit == 1 && a.slot0 == 0) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const float y = lt[g] > 0.f ? __uint_as_float(o[g]) / lt[g] : 0.f;
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const int64_t idx = ((int64_t)un.s * a.hq + h0 + g) * a.max_splits + un.j;
+                    const int64_t idx = ((int64_t)un.s * a.hq + h0 + g) * a.max_splits + a.slot0 + un.j;
                     a.ws_o[idx * D + r] = __uint_as_float(o[g]);
                     if (r == 0) reinterpret_cast<float2 *>(a.ws_ml)[idx] = make_float2(m[g], lt[g]);
                 }

@@ -107,7 +107,22 @@ struct DecodeLaunch {
     int max_splits;
     float *ws_o;      // [S*Hq*max_splits][D]
     float *ws_ml;     // [S*Hq*max_splits][2]
+    // cascade decode: blocks of the shared prefix (covered by launch_cascade_prefix) and the workspace
+    // slot of the first suffix split; 0 and 0 for a plain decode
+    int start_block = 0, slot0 = 0;
 };
+
+// The prefix phase of a cascade decode (prefill.cu): the decode queries of every sequence against the
+// first prefix_tokens tokens of table row 0, cut into splits of split_tokens keys (a multiple of 64);
+// split p of (sequence s, query head h) goes to workspace slot p of row s * Hq + h.
+struct CascadePrefixLaunch {
+    const void *q; // [S][Hq][D]
+    const int32_t *tables;
+    int max_blocks, num_seqs, num_q_heads, prefix_tokens, split_tokens, max_splits;
+    float scale;
+    float *ws_o, *ws_ml;
+};
+cudaError_t launch_cascade_prefix(pkv_cache *c, const CascadePrefixLaunch &p, cudaStream_t st);
 int64_t decode_workspace_floats(const pkv_cache *c, int num_seqs, int num_q_heads, int max_splits);
 int decode_split_blocks(const pkv_cache *c);
 cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st);

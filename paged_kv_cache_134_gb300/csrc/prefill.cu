@@ -57,7 +57,14 @@ struct Args {
     int64_t total_tokens, num_blocks, tile_elems;
     int num_seqs, max_seqlen, max_blocks, hq, hkv, bs, lg_bs, nqt_max;
     float scale_log2;
+    // cascade mode: the decode queries of num_seqs sequences against a shared prefix of
+    // prefix_tokens tokens (table row 0), cut into nps splits of split_tokens keys; each (sequence,
+    // query head, split) leaves an fp32 partial (m, l, unnormalised o) in workspace slot split
+    float *ws_o = nullptr, *ws_ml = nullptr;
+    int max_splits = 0, prefix_tokens = 0, split_tokens = 0, nps = 0;
 };
+
+enum { MODE_PACKED = 0, MODE_PAGED = 1, MODE_CASCADE = 2 };
 
 constexpr int NKS = 3;           // K stages (a K stage frees as soon as S = Q K^T of its tile is done)
 constexpr int NVS = 2;           // V stages (a V stage frees after P V)
@@ -163,6 +170,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     int *warp_sums = sh + 2 * R;
     pdl_trigger();
     pdl_wait();
+    if (a.nps > 0) {
+        // cascade: the items are the (tile of query rows, prefix split) pairs, taken in order
+        if (threadIdx.x == 0) {
+            a.plan[0] = ((a.num_seqs + BM - 1) / BM) * a.nps;
+            a.plan[1] = 0;
+        }
+        return;
+    }
     for (int x = threadIdx.x; x < R; x += kPlanThreads) {
         hist[x] = 0;
         cnt[x] = 0;
@@ -192,7 +207,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
 struct Item {
     int seq, qt, h; // seq < 0: no more items
     int start, n, q0, qlast, nkv;
-    int c0; // paged mode: cached tokens ahead of the item's sequence rows (absolute position of row 0)
+    int c0;   // paged mode: cached tokens ahead of the item's sequence rows (absolute position of row 0)
+    int k0;   // absolute position of the item's first key (cascade: its split's start; else 0)
+    int kend; // keys at or past kend hold no token of the sequence (or of the prefix)
+    int trow; // block-table row of the item's keys
 };
 
 PKV_DEV Item decode_item(const Args &a, int4 raw) {
@@ -200,6 +218,19 @@ PKV_DEV Item decode_item(const Args &a, int4 raw) {
     it.seq = raw.x;
     it.qt = raw.y;
     it.h = raw.z;
+    if (it.seq >= 0 && a.nps > 0) {
+        // cascade: seq = tile of 128 query rows (sequences), qt = prefix split
+        it.start = it.seq * BM;
+        it.n = min(BM, a.num_seqs - it.start);
+        it.q0 = 0;
+        it.qlast = it.n - 1;
+        it.c0 = 0;
+        it.k0 = it.qt * a.split_tokens;
+        it.kend = min(it.k0 + a.split_tokens, a.prefix_tokens);
+        it.nkv = (it.kend - it.k0 + BN - 1) / BN;
+        it.trow = 0;
+        return it;
+    }
     if (it.seq >= 0) {
         it.start = a.cu[it.seq];
         it.n = a.cu[it.seq + 1] - it.start;
@@ -207,15 +238,20 @@ PKV_DEV Item decode_item(const Args &a, int4 raw) {
         it.qlast = min(it.q0 + BM, it.n) - 1;
         it.c0 = a.ctx ? a.ctx[it.seq] : 0;
         it.nkv = (it.c0 + it.qlast) / BN + 1; // key tiles up to the item's last row
+        it.k0 = 0;
+        it.kend = it.c0 + it.n;
+        it.trow = it.seq;
     }
     return it;
 }
 
-template <int D, int MT, bool PAGED>
+template <int D, int MT, int MODE>
 __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tp, const Args a) {
     using L = Layout<D, MT>;
+    constexpr bool PAGED = MODE != MODE_PACKED;     // keys from the pool through the block table
+    constexpr bool CASCADE = MODE == MODE_CASCADE;  // no causal mask, fp32 split partials out
     extern __shared__ __align__(1024) uint8_t smem[];
 
     pdl_trigger();
@@ -307,8 +343,13 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 const int idx = *abort_flag ? total : atomicAdd(a.plan + 1, 1);
                 int4 raw = make_int4(-1, 0, 0, 0);
                 if (idx < total) {
-                    const int2 sq = reinterpret_cast<const int2 *>(a.plan + 4)[idx / a.hq];
-                    raw = make_int4(sq.x, sq.y, idx % a.hq, 0);
+                    if constexpr (CASCADE) {
+                        const int pair = idx / a.hq; // (tile of query rows, prefix split)
+                        raw = make_int4(pair / a.nps, pair % a.nps, idx % a.hq, 0);
+                    } else {
+                        const int2 sq = reinterpret_cast<const int2 *>(a.plan + 4)[idx / a.hq];
+                        raw = make_int4(sq.x, sq.y, idx % a.hq, 0);
+                    }
                 }
                 item_slot[s].x = raw.x;
                 item_slot[s].y = raw.y;
@@ -331,11 +372,11 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 // paged mode: table entries of the blocks of one key tile (-1: no token of the sequence)
                 int ent[BN / 8];
                 auto read_entries = [&](const Item &itm, int jj) {
-                    const int send = itm.c0 + itm.n, lb0 = (jj * BN) >> a.lg_bs, nbt = BN >> a.lg_bs;
+                    const int lb0 = (itm.k0 + jj * BN) >> a.lg_bs, nbt = BN >> a.lg_bs;
 #pragma unroll
                     for (int l = 0; l < BN / 8; ++l)
-                        ent[l] = (l < nbt && ((lb0 + l) << a.lg_bs) < send)
-                                     ? a.tables[(int64_t)itm.seq * a.max_blocks + lb0 + l]
+                        ent[l] = (l < nbt && ((lb0 + l) << a.lg_bs) < itm.kend)
+                                     ? a.tables[(int64_t)itm.trow * a.max_blocks + lb0 + l]
                                      : -1;
                 };
                 if constexpr (PAGED) read_entries(it, 0);
@@ -407,11 +448,11 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             const Item it = take_item(n, ok);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok || it.seq < 0) break;
-            const int kvh = it.h / G, send = it.c0 + it.n, nbt = BN >> a.lg_bs;
+            const int kvh = it.h / G, send = it.kend, nbt = BN >> a.lg_bs;
             // lane l: table entry of block l of a key tile, read one tile ahead of its use
             auto entry = [&](int jj) -> int {
-                const int lbl = ((jj * BN) >> a.lg_bs) + lane;
-                return (lane < nbt && (lbl << a.lg_bs) < send) ? a.tables[(int64_t)it.seq * a.max_blocks + lbl] : -1;
+                const int lbl = ((it.k0 + jj * BN) >> a.lg_bs) + lane;
+                return (lane < nbt && (lbl << a.lg_bs) < send) ? a.tables[(int64_t)it.trow * a.max_blocks + lbl] : -1;
             };
             int nxt = entry(0);
             int issued = 0;
@@ -423,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 if (j + 1 < it.nkv) nxt = entry(j + 1);
                 if (round >= 1) ok = __all_sync(0xffffffffu, mbar_wait(v_empty + st, (round - 1) & 1));
                 if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) break;
-                const int kbase = j * BN, lb = (kbase >> a.lg_bs) + lane;
+                const int kbase = it.k0 + j * BN, lb = (kbase >> a.lg_bs) + lane;
                 const bool has = lane < nbt && (lb << a.lg_bs) < send;
                 const bool good = has && b >= 0 && b < a.num_blocks;
                 if (has && !good) set_error(a.err, PKV_DEVERR_BLOCK_ID);
@@ -603,9 +644,17 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 tc::wait_ld();
                 tc::fence_before_sync();
                 mbar_arrive(s_free); // the S buffer may take the next tile
-                // causal mask, only on tiles that reach past the item's first query row
-                const int kbase = j * BN;
-                if (kbase + BN - 1 > q0) {
+                const int kbase = it.k0 + j * BN;
+                if constexpr (CASCADE) {
+                    // every query sees the whole prefix: only keys past its end are masked
+                    if (kbase + BN > it.kend) {
+                        const int lim = it.kend - kbase;
+#pragma unroll
+                        for (int c = 0; c < BN; ++c)
+                            if (c >= lim) sr[c] = 0xFF800000u; // -inf
+                    }
+                } else if (kbase + BN - 1 > q0) {
+                    // causal mask, only on tiles that reach past the item's first query row
                     const int lim = q0 + r - kbase + 1; // keys c < lim are at or before this row
 #pragma unroll
                     for (int c = 0; c < BN; ++c)
@@ -674,20 +723,41 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
             tc::fence_after_sync();
             const float inv = 1.f / l;
             using T = typename ModelT<MT>::T;
-            T *orow = static_cast<T *>(a.out) + ((int64_t)(it.start + qpos) * a.hq + it.h) * D;
+            if constexpr (CASCADE) {
+                // fp32 partial of (sequence it.start + qpos, head it.h, split it.qt): unnormalised o and
+                // (m, l) with m the row's exponent base in log2 units, as the split merge expects
+                const int64_t idx = ((int64_t)(it.start + qpos) * a.hq + it.h) * a.max_splits + it.qt;
+                float *wo = a.ws_o + idx * D;
 #pragma unroll
-            for (int cc = 0; cc < D / 16; ++cc) {
-                uint32_t o[16];
-                tc::ld16(tmem + lane_off + 2 * BN + cc * 16, o);
-                tc::wait_ld();
-                uint32_t w[8];
+                for (int cc = 0; cc < D / 16; ++cc) {
+                    uint32_t o[16];
+                    tc::ld16(tmem + lane_off + 2 * BN + cc * 16, o);
+                    tc::wait_ld();
+                    if (qpos < it.n) {
+                        float4 *dst = reinterpret_cast<float4 *>(wo + cc * 16);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    w[e] = pack2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv, MT);
-                if (qpos < it.n) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 16);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                                 __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                    }
+                }
+                if (qpos < it.n) reinterpret_cast<float2 *>(a.ws_ml)[idx] = make_float2(m_use, l);
+            } else {
+                T *orow = static_cast<T *>(a.out) + ((int64_t)(it.start + qpos) * a.hq + it.h) * D;
+#pragma unroll
+                for (int cc = 0; cc < D / 16; ++cc) {
+                    uint32_t o[16];
+                    tc::ld16(tmem + lane_off + 2 * BN + cc * 16, o);
+                    tc::wait_ld();
+                    uint32_t w[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        w[e] = pack2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv, MT);
+                    if (qpos < it.n) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 16);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
                 }
             }
             tc::fence_before_sync();
@@ -833,10 +903,10 @@ bool make_map(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t co
     return r == CUDA_SUCCESS;
 }
 
-template <int D, int MT, bool PAGED>
+template <int D, int MT, int MODE>
 cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tp,
                      const Args &a, int64_t max_ctas, int num_sms, cudaStream_t st) {
-    auto kern = prefill_kernel<D, MT, PAGED>;
+    auto kern = prefill_kernel<D, MT, MODE>;
     const int smem = Layout<D, MT>::TOTAL;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -936,17 +1006,83 @@ cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st
     g_pkv_launches++;
     if (e != cudaSuccess) return e;
     const int64_t max_ctas = items * p.num_q_heads;
-#define PKV_PREFILL_CASE(DD, MM, PG) \
-    if (D == DD && mt == MM && (p.ctx != nullptr) == PG) e = launch_t<DD, MM, PG>(tq, tk, tv, tp, a, max_ctas, c->num_sms, st);
-    PKV_PREFILL_CASE(128, PKV_F16, false)
-    PKV_PREFILL_CASE(128, PKV_BF16, false)
-    PKV_PREFILL_CASE(64, PKV_F16, false)
-    PKV_PREFILL_CASE(64, PKV_BF16, false)
-    PKV_PREFILL_CASE(128, PKV_F16, true)
-    PKV_PREFILL_CASE(128, PKV_BF16, true)
-    PKV_PREFILL_CASE(64, PKV_F16, true)
-    PKV_PREFILL_CASE(64, PKV_BF16, true)
+    const int mode = p.ctx != nullptr ? MODE_PAGED : MODE_PACKED;
+    e = cudaErrorInvalidValue;
+#define PKV_PREFILL_CASE(DD, MM, MO) \
+    if (D == DD && mt == MM && mode == MO) e = launch_t<DD, MM, MO>(tq, tk, tv, tp, a, max_ctas, c->num_sms, st);
+    PKV_PREFILL_CASE(128, PKV_F16, MODE_PACKED)
+    PKV_PREFILL_CASE(128, PKV_BF16, MODE_PACKED)
+    PKV_PREFILL_CASE(64, PKV_F16, MODE_PACKED)
+    PKV_PREFILL_CASE(64, PKV_BF16, MODE_PACKED)
+    PKV_PREFILL_CASE(128, PKV_F16, MODE_PAGED)
+    PKV_PREFILL_CASE(128, PKV_BF16, MODE_PAGED)
+    PKV_PREFILL_CASE(64, PKV_F16, MODE_PAGED)
+    PKV_PREFILL_CASE(64, PKV_BF16, MODE_PAGED)
 #undef PKV_PREFILL_CASE
+    g_pkv_launches++;
+    return e;
+}
+
+cudaError_t launch_cascade_prefix(pkv_cache *c, const CascadePrefixLaunch &p, cudaStream_t st) {
+    using namespace pkv_prefill;
+    if (p.num_seqs <= 0 || p.prefix_tokens <= 0) return cudaSuccess;
+    const int D = c->head_dim;
+    const int mt = c->model_dtype;
+    Args a;
+    a.k = a.v = nullptr;
+    a.out = nullptr;
+    a.cu = nullptr;
+    a.ctx = nullptr;
+    a.tables = p.tables;
+    a.pool = static_cast<char *>(c->pool);
+    a.err = c->err;
+    a.total_tokens = p.num_seqs;
+    a.num_blocks = c->num_blocks;
+    a.tile_elems = (int64_t)c->block_size * D;
+    a.num_seqs = p.num_seqs;
+    a.max_seqlen = 0;
+    a.max_blocks = p.max_blocks;
+    a.hq = p.num_q_heads;
+    a.hkv = c->num_kv_heads;
+    a.bs = c->block_size;
+    a.lg_bs = 0;
+    while ((1 << a.lg_bs) < c->block_size) ++a.lg_bs;
+    a.nqt_max = 0;
+    a.scale_log2 = p.scale * 1.4426950408889634f;
+    a.ws_o = p.ws_o;
+    a.ws_ml = p.ws_ml;
+    a.max_splits = p.max_splits;
+    a.prefix_tokens = p.prefix_tokens;
+    a.split_tokens = p.split_tokens;
+    a.nps = (p.prefix_tokens + p.split_tokens - 1) / p.split_tokens;
+    const int64_t pairs = (int64_t)((p.num_seqs + BM - 1) / BM) * a.nps;
+    if (pairs * p.num_q_heads > 0x7FFFFFFF) return cudaErrorNotSupported;
+    if (c->plan_bytes < 16) {
+        if (c->plan) cudaFree(c->plan);
+        c->plan = nullptr;
+        c->plan_bytes = 0;
+        cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&c->plan), 64);
+        if (e != cudaSuccess) return e;
+        c->plan_bytes = 64;
+    }
+    a.plan = c->plan;
+    const int64_t pool_rows = c->num_blocks * 2 * c->num_kv_heads * c->block_size;
+    if (pool_rows > 0x7FFFFFFFLL) return cudaErrorNotSupported;
+    // q [S][Hq][D] as rows of sequences: a box of 128 sequences x 64 dims of one head
+    CUtensorMap tq, tp;
+    if (!make_map(&tq, p.q, mt, p.num_seqs, (int64_t)p.num_q_heads * D, BM) ||
+        !make_map(&tp, c->pool, mt, pool_rows, D, c->block_size))
+        return cudaErrorInvalidValue;
+    cudaError_t e = launch_plan(a, st);
+    g_pkv_launches++;
+    if (e != cudaSuccess) return e;
+    e = cudaErrorInvalidValue;
+    if (D == 128)
+        e = mt == PKV_BF16 ? launch_t<128, PKV_BF16, MODE_CASCADE>(tq, tp, tp, tp, a, pairs * p.num_q_heads, c->num_sms, st)
+                           : launch_t<128, PKV_F16, MODE_CASCADE>(tq, tp, tp, tp, a, pairs * p.num_q_heads, c->num_sms, st);
+    else
+        e = mt == PKV_BF16 ? launch_t<64, PKV_BF16, MODE_CASCADE>(tq, tp, tp, tp, a, pairs * p.num_q_heads, c->num_sms, st)
+                           : launch_t<64, PKV_F16, MODE_CASCADE>(tq, tp, tp, tp, a, pairs * p.num_q_heads, c->num_sms, st);
     g_pkv_launches++;
     return e;
 }

@@ -65,26 +65,31 @@ class DecodeInputs:
         self.block_size = w.block_size
 
 
-def decode_step(cache, x: DecodeInputs, fused: bool = True):
+def decode_step(cache, x: DecodeInputs, fused: bool = True, cascade_prefix: int = 0):
     """One decode step: slot indexing -> append of the new token -> paged decode attention.
 
     ``fused`` computes the slots inside the append launch (paged_kv_append_at); otherwise slot
-    indexing and append are two launches.  Both write the same slots and the same bytes."""
+    indexing and append are two launches.  Both write the same slots and the same bytes.
+    ``cascade_prefix`` > 0: the tables share their first that many tokens, and the attention runs
+    as a cascade decode (the shared prefix read once for the batch)."""
     if fused:
         P.paged_kv_append_at(cache, x.new_k, x.new_v, x.tables, x.seq_ids, x.positions, x.slots)
     else:
         P.paged_slot_mapping(x.tables, x.seq_ids, x.positions, x.block_size, out=x.slots)
         P.paged_kv_append(cache, x.new_k, x.new_v, x.slots)
-    P.paged_decode_attention(x.q, cache, x.tables, x.lens, x.scale, out=x.out)
+    if cascade_prefix:
+        P.paged_decode_attention_cascade(x.q, cache, x.tables, x.lens, cascade_prefix, x.scale, out=x.out)
+    else:
+        P.paged_decode_attention(x.q, cache, x.tables, x.lens, x.scale, out=x.out)
     return x.out
 
 
-def run_decode(w, keep_cache=False, fused=True):
+def run_decode(w, keep_cache=False, fused=True, cascade_prefix=0):
     cache = new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype, w.model_dtype,
                       w.k_scale, w.v_scale)
     fill_slots = fill_cache(cache, w)
     x = DecodeInputs(w)
-    out = decode_step(cache, x, fused=fused)
+    out = decode_step(cache, x, fused=fused, cascade_prefix=cascade_prefix)
     torch.cuda.synchronize()
     res = dict(fill_slots=fill_slots.cpu().numpy(), new_slots=x.slots.cpu().numpy(),
                out=out.float().cpu().double().numpy(), err=cache.check_error(),

@@ -435,7 +435,8 @@ def prefill(seed: int = 1003, lengths=PACKED_LENGTHS, heads: int = 32, kv_heads:
 
 
 def prefix13b(seed: int = 1004, num_seqs: int = 64, prefix_tokens: int = 4096, max_suffix: int = 512,
-              heads: int = 40, d: int = 128, bs: int = 32, private_prefix: bool = False) -> DecodeWorkload:
+              heads: int = 40, d: int = 128, bs: int = 32, private_prefix: bool = False,
+              kv_heads: Optional[int] = None, dtype: str = F16) -> DecodeWorkload:
     """Shared-prefix decode.  ``private_prefix`` gives every sequence its own copy of the prefix
     blocks (same values, different physical blocks) for the shared-vs-private equality check."""
     rng = np.random.default_rng(seed)
@@ -446,13 +447,14 @@ def prefix13b(seed: int = 1004, num_seqs: int = 64, prefix_tokens: int = 4096, m
     need = pblk * (num_seqs if private_prefix else 1) + sum(blocks_for(s + 1, bs) for s in suffix)
     nb = int(math.ceil(1.1 * need))
     alloc = BlockAllocator(nb, np.random.default_rng(seed + 77))
-    pk = normal_bits(rng, (prefix_tokens, heads, d), F16)
-    pv = normal_bits(rng, (prefix_tokens, heads, d), F16)
-    sk = [normal_bits(rng, (int(s), heads, d), F16) for s in suffix]
-    sv = [normal_bits(rng, (int(s), heads, d), F16) for s in suffix]
-    q = normal_bits(rng, (num_seqs, heads, d), F16)
-    new_k = normal_bits(rng, (num_seqs, heads, d), F16)
-    new_v = normal_bits(rng, (num_seqs, heads, d), F16)
+    hkv = heads if kv_heads is None else kv_heads
+    pk = normal_bits(rng, (prefix_tokens, hkv, d), dtype)
+    pv = normal_bits(rng, (prefix_tokens, hkv, d), dtype)
+    sk = [normal_bits(rng, (int(s), hkv, d), dtype) for s in suffix]
+    sv = [normal_bits(rng, (int(s), hkv, d), dtype) for s in suffix]
+    q = normal_bits(rng, (num_seqs, heads, d), dtype)
+    new_k = normal_bits(rng, (num_seqs, hkv, d), dtype)
+    new_v = normal_bits(rng, (num_seqs, hkv, d), dtype)
     tables = []
     fill_tables = []
     ids, pos, fk, fv = [], [], [], []
@@ -483,7 +485,7 @@ def prefix13b(seed: int = 1004, num_seqs: int = 64, prefix_tokens: int = 4096, m
     mb = max(len(t) for t in fill_tables)
     return DecodeWorkload(
         name="prefix13b" + ("_private" if private_prefix else ""), num_seqs=num_seqs, num_q_heads=heads,
-        num_kv_heads=heads, head_dim=d, block_size=bs, num_blocks=nb, kv_dtype=F16, model_dtype=F16,
+        num_kv_heads=hkv, head_dim=d, block_size=bs, num_blocks=nb, kv_dtype=dtype, model_dtype=dtype,
         scale=np.float32(1.0 / math.sqrt(d)), context_lens=lens, block_tables=_tables_array(tables, mb),
         fill_tables=_tables_array(fill_tables, mb), fill_seq_ids=np.concatenate(ids),
         fill_positions=np.concatenate(pos), fill_k=np.concatenate(fk), fill_v=np.concatenate(fv),
