@@ -43,8 +43,8 @@ constexpr int D = 128;
 constexpr int TOK = 128;             // tokens per step: MMA M of S^T, MMA K of O^T
 constexpr int NQ = 16;               // MMA N: the group's query heads, padded
 constexpr int NS = 3;                // K stages and V stages
-constexpr int kThreads = 224;        // warp 0 Q and K loads, warp 1 MMA, warps 2-5 softmax, warp 6 V loads
-constexpr uint32_t kTmemCols = 64;   // S0 [0,16) S1 [16,32) O^T [32, 32 + 16 NP)
+constexpr int kThreads = 352;        // warp 0 Q and K loads, 1 MMA, 2-5 softmax, 6 V loads, 7-10 epilogue
+constexpr uint32_t kTmemCols = 128;  // S0 [0,16) S1 [16,32) O^T of even units [32,64), of odd units [64,96)
 constexpr float kRescale = 8.0f;     // log2 units
 
 template <int MT>
@@ -61,8 +61,8 @@ struct Layout {
     static constexpr int Q_BYTES = NQ * D * 2;
     static constexpr int P = Q + 2 * Q_BYTES;                  // [buffer][part][64-token chunk][16 rows][128 B]
     static constexpr int P_BYTES = NPR * TOK * 2;          // one buffer
-    static constexpr int RED = P + 2 * P_BYTES;            // [2][4 warps][NQ] maxima, [4 warps][NQ] sums
-    static constexpr int BAR = RED + (3 * 4 * NQ) * 4;
+    static constexpr int RED = P + 2 * P_BYTES;            // [2][4 warps][NQ] maxima, [2][4 warps][NQ] sums,
+    static constexpr int BAR = RED + (4 * 4 * NQ + 2 * NQ) * 4; // [2][NQ] bases (sums and bases per unit parity)
     static constexpr int FIXED = BAR + 512;                // + unit tables, 3 (S + 1) ints
 };
 
@@ -102,13 +102,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + LY::BAR);
     uint64_t *k_full = bars, *k_empty = bars + NS, *v_full = bars + 2 * NS, *v_empty = bars + 3 * NS;
     uint64_t *s_full = bars + 4 * NS, *s_free = s_full + 2, *p_full = s_full + 4, *t_full = s_full + 6;
-    uint64_t *q_full = s_full + 8, *q_empty = s_full + 10, *o_full = s_full + 12, *o_free = s_full + 13;
-    uint64_t *fin = s_full + 14;
+    uint64_t *q_full = s_full + 8, *q_empty = s_full + 10;
+    // per unit parity: O^T complete / read out of tensor memory; row sums and bases published / read
+    uint64_t *o_full = s_full + 12, *o_free = s_full + 14, *l_ready = s_full + 16, *l_free = s_full + 18;
+    uint64_t *fin = s_full + 20;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(fin + 2);
     volatile uint32_t *badmask = reinterpret_cast<volatile uint32_t *>(fin + 3); // [NS]
     float *red_max = reinterpret_cast<float *>(smem + LY::RED);                  // [2][4][NQ]
-    float *red_sum = red_max + 2 * 4 * NQ;                                      // [4][NQ]
+    float *red_sum = red_max + 2 * 4 * NQ;                                      // [2][4][NQ]
+    float *m_base = red_sum + 2 * 4 * NQ;                                       // [2][NQ]
     int *pf = reinterpret_cast<int *>(smem + LY::FIXED);
     int *pp = pf + (S + 1);
     int *nb = pp + (S + 1);
@@ -131,8 +134,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(q_full + b, 1);
             mbar_init(q_empty + b, 1);
         }
-        mbar_init(o_full, 1);
-        mbar_init(o_free, 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(o_full + b, 1);
+            mbar_init(o_free + b, 128);
+            mbar_init(l_ready + b, 128);
+            mbar_init(l_free + b, 128);
+        }
         mbar_init(fin, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -272,7 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t IPV = tc::idesc_f16_ab(ab, 1u, 0u, D, LY::NPR); // A = V^T (MN-major), B = P (K-major)
             const uint32_t sK = smem_u32(smem + LY::K0), sV = smem_u32(smem + LY::V0);
             const uint32_t sQ = smem_u32(smem + LY::Q), sP = smem_u32(smem + LY::P);
-            const uint32_t tO = tmem + 2 * NQ;
             bool any_mma = false;
             // S^T of step g (Q buffer qb) into S buffer g % 2; the K stage is released as soon as S^T is done
             auto issue_s = [&](int64_t g, int qb) -> bool {
@@ -310,9 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int st = (int)(g % NS), b = (int)(g & 1);
                     ok = __all_sync(0xffffffffu, mbar_wait(p_full + b, (g >> 1) & 1) && mbar_wait(v_full + st, (g / NS) & 1));
-                    // the epilogue of the previous unit has read O^T out of tensor memory
-                    if (ok && i == 0 && nu >= 1) ok = __all_sync(0xffffffffu, mbar_wait(o_free, (nu - 1) & 1));
+                    // O^T of this unit's parity was read out by the epilogue warps for unit nu - 2
+                    if (ok && i == 0 && nu >= 2)
+                        ok = __all_sync(0xffffffffu, mbar_wait(o_free + (nu & 1), ((nu >> 1) - 1) & 1));
                     if (!ok) break;
+                    const uint32_t tO = tmem + 2 * NQ + (uint32_t)((nu & 1) * 32);
                     tc::fence_after_sync();
 #pragma unroll
                     for (int k = 0; k < TOK / 16; ++k) {
@@ -323,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc::commit_warp(t_full + b);
                     tc::commit_warp(v_empty + st);
-                    if (i + 1 == nsteps) tc::commit_warp(o_full);
+                    if (i + 1 == nsteps) tc::commit_warp(o_full + (nu & 1));
                 }
                 gs += nsteps;
                 if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
@@ -335,8 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!__all_sync(0xffffffffu, mbar_wait(fin, 0)) && lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
             }
         }
-    } else {
-        // ---------------------------------------------------------------- softmax and epilogue
+    } else if (warp < 6) {
+        // ---------------------------------------------------------------- softmax
         const int lw = warp & 3;
         const int r = lw * 32 + lane;                      // token row of S^T, then dimension of O^T
         const uint32_t lane_off = static_cast<uint32_t>(lw * 32) << 16;
@@ -420,11 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int part = 0; part < LY::NP; ++part) {
                             uint32_t o[G];
-                            tc::ldn<G>(tmem + lane_off + 2 * NQ + part * NQ, o);
+                            tc::ldn<G>(tmem + lane_off + 2 * NQ + (nu & 1) * 32 + part * NQ, o);
                             tc::wait_ld();
 #pragma unroll
                             for (int g = 0; g < G; ++g) o[g] = __float_as_uint(__uint_as_float(o[g]) * alpha[g]);
-                            tc::stn<G>(tmem + lane_off + 2 * NQ + part * NQ, o);
+                            tc::stn<G>(tmem + lane_off + 2 * NQ + (nu & 1) * 32 + part * NQ, o);
                         }
                         tc::wait_st();
                     }
@@ -459,46 +467,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(p_full + b);
             }
             gs += nsteps;
-            // ---- epilogue: thread r holds dimension r of the G output rows
-            bool mine = ok && *abort_flag == 0;
-            if (mine) mine = __all_sync(0xffffffffu, mbar_wait(o_full, nu & 1));
-            uint32_t o[G];
-            if (mine) {
-                tc::fence_after_sync();
-                tc::ldn<G>(tmem + lane_off + 2 * NQ, o);
-                if constexpr (LY::NP == 2) {
-                    uint32_t o2[G];
-                    tc::ldn<G>(tmem + lane_off + 3 * NQ, o2);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int g = 0; g < G; ++g) o[g] = __float_as_uint(__uint_as_float(o[g]) + __uint_as_float(o2[g]));
-                }
-                tc::wait_ld();
-                tc::fence_before_sync();
-                mbar_arrive(o_free); // the next unit's first P V may overwrite O^T
-                float lt[G];
+            // ---- hand the unit's row sums and bases to the epilogue warps (buffer nu % 2)
+            const int eb = nu & 1;
+            if (ok && nu >= 2) ok = __all_sync(0xffffffffu, mbar_wait(l_free + eb, ((nu >> 1) - 1) & 1));
+            if (ok) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     float v = lp[g];
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                    lt[g] = v;
+                    if (lane == g) red_sum[(eb * 4 + lw) * NQ + g] = v;
+                    if (r == 0) m_base[eb * NQ + g] = m[g];
                 }
-                if (lane < G) {
-                    float v = lt[0];
-#pragma unroll
-                    for (int g = 1; g < G; ++g)
-                        if (lane == g) v = lt[g];
-                    red_sum[lw * NQ + lane] = v;
-                }
+                mbar_arrive(l_ready + eb);
             }
-            ok = named_barrier_and(1, 128, mine);
+            // the four warps leave the unit loop together or not at all (a warp that left alone would
+            // leave the others waiting at the next named barrier)
+            ok = named_barrier_and(1, 128, ok);
             if (!ok) break;
-            float lt[G];
+        }
+        if (!ok) fail();
+    } else {
+        // ---------------------------------------------------------------- epilogue (warps 7-10)
+        // Thread r holds dimension r of the unit's G output rows: O^T from tensor memory (its lane
+        // quadrant), the row sums of the four softmax warps and the bases from shared memory.  The
+        // softmax warps go on with the next unit meanwhile; O^T and the sums are double-buffered.
+        const int lw = warp & 3;
+        const int r = lw * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(lw * 32) << 16;
+        bool ok = true;
+        int nu = 0;
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
+            const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
+            const int eb = nu & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(o_full + eb, (nu >> 1) & 1) && mbar_wait(l_ready + eb, (nu >> 1) & 1));
+            if (!ok) break;
+            tc::fence_after_sync();
+            uint32_t o[G];
+            tc::ldn<G>(tmem + lane_off + 2 * NQ + eb * 32, o);
+            if constexpr (LY::NP == 2) {
+                uint32_t o2[G];
+                tc::ldn<G>(tmem + lane_off + 3 * NQ + eb * 32, o2);
+                tc::wait_ld();
 #pragma unroll
-            for (int g = 0; g < G; ++g)
-                lt[g] = (red_sum[g] + red_sum[NQ + g]) + (red_sum[2 * NQ + g] + red_sum[3 * NQ + g]);
-            named_barrier_sync(1, 128); // red_sum is rewritten by the next unit
+                for (int g = 0; g < G; ++g) o[g] = __float_as_uint(__uint_as_float(o[g]) + __uint_as_float(o2[g]));
+            }
+            tc::wait_ld();
+            tc::fence_before_sync();
+            mbar_arrive(o_free + eb); // unit nu + 2's first P V may overwrite this O^T
+            float lt[G], mb[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float *rs = red_sum + eb * 4 * NQ + g;
+                lt[g] = (rs[0] + rs[NQ]) + (rs[2 * NQ] + rs[3 * NQ]);
+                mb[g] = m_base[eb * NQ + g];
+            }
+            mbar_arrive(l_free + eb); // the softmax may publish unit nu + 2's sums here
             const int h0 = un.kvh * G;
             if (un.nsplit == 1 && a.slot0 == 0) {
 #pragma unroll
@@ -511,11 +535,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int g = 0; g < G; ++g) {
                     const int64_t idx = ((int64_t)un.s * a.hq + h0 + g) * a.max_splits + a.slot0 + un.j;
                     a.ws_o[idx * D + r] = __uint_as_float(o[g]);
-                    if (r == 0) reinterpret_cast<float2 *>(a.ws_ml)[idx] = make_float2(m[g], lt[g]);
+                    if (r == 0) reinterpret_cast<float2 *>(a.ws_ml)[idx] = make_float2(mb[g], lt[g]);
                 }
             }
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
         }
-        if (!ok) fail();
+        if (!ok && lane == 0) fail();
     }
 
     tc::fence_before_sync();
