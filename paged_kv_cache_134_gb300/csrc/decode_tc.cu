@@ -11,17 +11,22 @@ bool tc_enabled() {
     return !(v && v[0] == '0');
 }
 
+// the MMAs' operand type: the model dtype, or fp16 for E4M3 caches (widened in shared memory)
+int operand_dtype(const pkv_cache *c) {
+    return c->kv_dtype == PKV_FP8_E4M3 ? (int)PKV_F16 : c->model_dtype;
+}
+
 } // namespace
 
 bool pkv_decode_tc_eligible(const pkv_cache *c, int G, int num_seqs) {
     using namespace pkv_decode_tc;
     if (!tc_enabled()) return false;
-    if (c->kv_dtype == PKV_FP8_E4M3 || c->head_dim != D) return false;
+    if (c->head_dim != D) return false;
     if (G != 2 && G != 4 && G != 8) return false;
     // TMA row coordinates are 32-bit
     if ((int64_t)c->num_blocks * 2 * c->num_kv_heads * c->block_size > 0x7FFFFFFFLL) return false;
     if ((int64_t)num_seqs * 16 > 0x7FFFFFFFLL) return false;
-    return smem_bytes(c->model_dtype, num_seqs) <= 232448;
+    return smem_bytes(operand_dtype(c), num_seqs) <= 232448;
 }
 
 cudaError_t pkv_decode_tc_launch(const pkv_cache *c, const pkv_decode::Args &a, const void *q, int G,
@@ -29,15 +34,23 @@ cudaError_t pkv_decode_tc_launch(const pkv_cache *c, const pkv_decode::Args &a, 
     using namespace pkv_decode_tc;
     CUtensorMap tkv, tq;
     const int mt = c->model_dtype;
-    if (!pkv_tmap_2d(&tkv, c->pool, mt, (int64_t)c->num_blocks * 2 * c->num_kv_heads * c->block_size, D,
-                     c->block_size) ||
-        !pkv_tmap_2d(&tq, q, mt, (int64_t)a.num_seqs * a.hq, D, G))
+    const bool f8 = c->kv_dtype == PKV_FP8_E4M3;
+    if (!pkv_tmap_2d(&tq, q, mt, (int64_t)a.num_seqs * a.hq, D, G)) return cudaErrorInvalidValue;
+    if (f8)
+        tkv = tq; // E4M3 tiles go by 1-D bulk copies; the kernel never reads this map
+    else if (!pkv_tmap_2d(&tkv, c->pool, mt, (int64_t)c->num_blocks * 2 * c->num_kv_heads * c->block_size, D,
+                          c->block_size))
         return cudaErrorInvalidValue;
-    const size_t smem = smem_bytes(mt, a.num_seqs);
+    const size_t smem = smem_bytes(operand_dtype(c), a.num_seqs);
     const int grid = c->num_sms;
 #define PKV_TC_CASE(GG)                                                                                                \
-    if (G == GG) return mt == PKV_BF16 ? launch<GG, PKV_BF16>(tkv, tq, a, grid, smem, st)                              \
-                                       : launch<GG, PKV_F16>(tkv, tq, a, grid, smem, st);
+    if (G == GG) {                                                                                                     \
+        if (f8)                                                                                                        \
+            return mt == PKV_BF16 ? launch<GG, PKV_BF16, PKV_FP8_E4M3>(tkv, tq, a, grid, smem, st)                     \
+                                  : launch<GG, PKV_F16, PKV_FP8_E4M3>(tkv, tq, a, grid, smem, st);                     \
+        return mt == PKV_BF16 ? launch<GG, PKV_BF16, PKV_BF16>(tkv, tq, a, grid, smem, st)                             \
+                              : launch<GG, PKV_F16, PKV_F16>(tkv, tq, a, grid, smem, st);                              \
+    }
     PKV_TC_CASE(2)
     PKV_TC_CASE(4)
     PKV_TC_CASE(8)

@@ -43,7 +43,11 @@ constexpr int D = 128;
 constexpr int TOK = 128;             // tokens per step: MMA M of S^T, MMA K of O^T
 constexpr int NQ = 16;               // MMA N: the group's query heads, padded
 constexpr int NS = 3;                // K stages and V stages
-constexpr int kThreads = 352;        // warp 0 Q and K loads, 1 MMA, 2-5 softmax, 6 V loads, 7-10 epilogue
+// warp 0 Q and K loads, 1 MMA, 2-5 softmax, 6 V loads, 7-10 epilogue; FP8 caches: 11-14 converters
+template <bool F8>
+__host__ __device__ constexpr int threads_for() {
+    return F8 ? 480 : 352;
+}
 constexpr uint32_t kTmemCols = 128;  // S0 [0,16) S1 [16,32) O^T of even units [32,64), of odd units [64,96)
 constexpr float kRescale = 8.0f;     // log2 units
 
@@ -90,10 +94,16 @@ PKV_DEV int p_offset(int g, int t) {
     return (t >> 6) * (NPR * 128) + (g >> 3) * 1024 + (g & 7) * 128 + ((((e >> 3) ^ (g & 7))) << 4) + ((e & 7) << 1);
 }
 
-template <int G, int MT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int G, int MT, int KVT>
+__global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tq, const Args a) {
-    using LY = Layout<MT>;
+    // FP8 caches: the MMAs run on fp16 operands (K and V widened exactly from E4M3, q converted
+    // with a power-of-two scale, P in fp16); the per-head K and V scales fold into the softmax
+    // scale and the epilogue
+    constexpr bool F8 = KVT == PKV_FP8_E4M3;
+    constexpr int OT = F8 ? (int)PKV_F16 : MT; // operand dtype of the MMAs
+    constexpr int kThreads = threads_for<F8>();
+    using LY = Layout<OT>;
     using M = ModelT<MT>;
     using T = typename M::T;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -109,6 +119,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(fin + 2);
     volatile uint32_t *badmask = reinterpret_cast<volatile uint32_t *>(fin + 3); // [NS]
+    // FP8 caches: the exponent of unit nu's q scale in slot nu % 8 (the converters run at most a few
+    // units ahead of the softmax, which reads it after its first v_full wait of the unit: the
+    // converters arrive on v_full themselves), the converters' partial maxima, and barriers for
+    // "E4M3 tile landed" (k8/v8_full, before the in-place widening) and "Q converted"
+    volatile int *qexp = reinterpret_cast<volatile int *>(fin + 5);              // [8]
+    volatile float *qred = reinterpret_cast<volatile float *>(fin + 9);          // [2 unit parities][4 warps]
+    uint64_t *k8_full = fin + 13, *v8_full = fin + 13 + NS, *q_ready = fin + 13 + 2 * NS;
     float *red_max = reinterpret_cast<float *>(smem + LY::RED);                  // [2][4][NQ]
     float *red_sum = red_max + 2 * 4 * NQ;                                      // [2][4][NQ]
     float *m_base = red_sum + 2 * 4 * NQ;                                       // [2][NQ]
@@ -119,11 +136,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(k_full + i, 1);
+            mbar_init(k_full + i, F8 ? 128 : 1); // FP8: the 128 converter threads, else the TMA arrival
             mbar_init(k_empty + i, 1);
-            mbar_init(v_full + i, 1);
+            mbar_init(v_full + i, F8 ? 128 : 1);
             mbar_init(v_empty + i, 1);
+            if constexpr (F8) {
+                mbar_init(k8_full + i, 1);
+                mbar_init(v8_full + i, 1);
+            }
         }
+        if constexpr (F8)
+            for (int b = 0; b < 2; ++b) mbar_init(q_ready + b, 128);
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full + b, 1);
             mbar_init(s_free + b, 128);
@@ -227,8 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool good = lane < nblk && b >= 0 && b < a.num_blocks;
             const unsigned goodmask = __ballot_sync(0xffffffffu, good);
             const unsigned bad = __ballot_sync(0xffffffffu, lane < nblk && !good);
-            const uint32_t bytes = (uint32_t)__popc(goodmask) * (uint32_t)a.bs * (D * 2);
-            uint64_t *full = is_k ? k_full + st : v_full + st;
+            const uint32_t bytes = (uint32_t)__popc(goodmask) * (uint32_t)a.bs * (uint32_t)(F8 ? D : D * 2);
+            // FP8: the E4M3 tiles land in the upper half of the stage (k8/v8_full); the converters widen
+            // them in place and arrive on k/v_full
+            uint64_t *full = F8 ? (is_k ? k8_full + st : v8_full + st) : (is_k ? k_full + st : v_full + st);
             uint64_t *empty = is_k ? k_empty + st : v_empty + st;
             if (lane == 0) {
                 if (round >= 1 && !mbar_wait(empty, (round - 1) & 1)) ok = false;
@@ -246,9 +271,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = ((b * 2 + (is_k ? 0 : 1)) * a.hkv + un.kvh) * a.bs;
             uint8_t *dst0 = smem + (is_k ? LY::K0 : LY::V0) + st * LY::STAGE + lane * a.bs * 128;
             if (good) {
+                if constexpr (F8) {
+                    // one (block, K|V, head) tile of bs rows x 128 one-byte dims is contiguous in the pool
+                    const char *src = a.pool + (int64_t)row / a.bs * a.tile_bytes;
+                    bulk_g2s_hint(smem + (is_k ? LY::K0 : LY::V0) + st * LY::STAGE + TOK * 128 + lane * a.bs * 128, src,
+                                  (uint32_t)a.tile_bytes, full, policy);
+                } else {
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tc::tma_load_2d_hint(dst0 + c * (TOK * 128), &tkv, c * 64, row, full, policy);
+                    for (int c = 0; c < D / 64; ++c)
+                        tc::tma_load_2d_hint(dst0 + c * (TOK * 128), &tkv, c * 64, row, full, policy);
+                }
             }
             ++gs;
             cur = nxt;
@@ -264,7 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the copies of the last stages must land before this CTA's shared memory goes away
         if (lane == 0) {
             for (int64_t g = gs > NS ? gs - NS : 0; g < gs; ++g)
-                if (!mbar_wait((is_k ? k_full : v_full) + g % NS, (g / NS) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+                if (!mbar_wait((F8 ? (is_k ? k8_full : v8_full) : (is_k ? k_full : v_full)) + g % NS, (g / NS) & 1))
+                    set_error(a.err, PKV_DEVERR_TIMEOUT);
             if (is_k)
                 for (int n = last_q > 0 ? last_q - 1 : 0; n <= last_q; ++n)
                     if (!mbar_wait(q_full + (n & 1), (n >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
@@ -274,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the whole warp runs the issue loop in step (waits agreed with __all_sync); one elected lane
         // issues each MMA and commit
         {
-            constexpr uint32_t ab = MT == PKV_BF16 ? 1u : 0u;
+            constexpr uint32_t ab = OT == PKV_BF16 ? 1u : 0u;
             constexpr uint32_t ISK = tc::idesc_f16_ab(ab, 0u, 0u, TOK, NQ); // A = K (K-major), B = Q (K-major)
             constexpr uint32_t IPV = tc::idesc_f16_ab(ab, 1u, 0u, D, LY::NPR); // A = V^T (MN-major), B = P (K-major)
             const uint32_t sK = smem_u32(smem + LY::K0), sV = smem_u32(smem + LY::V0);
@@ -305,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
                 const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
                 const int qb = nu & 1;
-                ok = __all_sync(0xffffffffu, mbar_wait(q_full + qb, (nu >> 1) & 1)) && issue_s(gs, qb);
+                ok = __all_sync(0xffffffffu, mbar_wait((F8 ? q_ready : q_full) + qb, (nu >> 1) & 1)) && issue_s(gs, qb);
                 for (int i = 0; i < nsteps && ok; ++i) {
                     const int64_t g = gs + i;
                     if (i + 1 < nsteps) {
@@ -357,6 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int L = a.lens[un.s];
             const int tok0 = un.blk0 * a.bs;
             const int tok_end = min(L, (un.blk0 + un.ntiles) * a.bs);
+            // scores in log2 units: scale * log2(e), times the K scale of the head and the power of two
+            // taken out of q by the converters (FP8 caches)
+            float qsc = a.qk_scale_log2;
             float m[G], lp[G]; // base (uniform over the CTA) and this thread's partial row sums
 #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -373,6 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int step0 = tok0 + i * TOK;
                 bool valid = false, ragged = false;
                 float sc[G];
+                if constexpr (F8)
+                    if (mine && i == 0) qsc = a.qk_scale_log2 * a.k_scale[un.kvh] * exp2f((float)qexp[nu & 7]);
                 if (mine) {
                     tc::fence_after_sync();
                     uint32_t sr[G];
@@ -387,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float tmx[G];
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
-                        sc[g] = valid ? __uint_as_float(sr[g]) * a.qk_scale_log2 : -INFINITY;
+                        sc[g] = valid ? __uint_as_float(sr[g]) * qsc : -INFINITY;
                         float v = sc[g];
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -444,13 +482,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int g = 0; g < G; ++g) {
                     const int off = p_offset<LY::NPR>(g, r);
                     if constexpr (LY::NP == 2) {
-                        const uint32_t hi = pack2<MT>(p[g], 0.f) & 0xFFFFu;
+                        const uint32_t hi = pack2<OT>(p[g], 0.f) & 0xFFFFu;
                         const float rest = p[g] - __uint_as_float(hi << 16);
                         *reinterpret_cast<uint16_t *>(pb + off) = (uint16_t)hi;
                         *reinterpret_cast<uint16_t *>(pb + p_offset<LY::NPR>(NQ + g, r)) =
-                            (uint16_t)(pack2<MT>(rest, 0.f) & 0xFFFFu);
+                            (uint16_t)(pack2<OT>(rest, 0.f) & 0xFFFFu);
                     } else {
-                        *reinterpret_cast<uint16_t *>(pb + off) = (uint16_t)(pack2<MT>(p[g], 0.f) & 0xFFFFu);
+                        *reinterpret_cast<uint16_t *>(pb + off) = (uint16_t)(pack2<OT>(p[g], 0.f) & 0xFFFFu);
                     }
                 }
                 if (ragged && !valid) {
@@ -487,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
         }
         if (!ok) fail();
-    } else {
+    } else if (warp < 11) {
         // ---------------------------------------------------------------- epilogue (warps 7-10)
         // Thread r holds dimension r of the unit's G output rows: O^T from tensor memory (its lane
         // quadrant), the row sums of the four softmax warps and the bases from shared memory.  The
@@ -524,6 +562,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_arrive(l_free + eb); // the softmax may publish unit nu + 2's sums here
             const int h0 = un.kvh * G;
+            if constexpr (F8) {
+                const float vs = a.v_scale[un.kvh]; // V codes were widened without their scale
+#pragma unroll
+                for (int g = 0; g < G; ++g) o[g] = __float_as_uint(__uint_as_float(o[g]) * vs);
+            }
             if (un.nsplit == 1 && a.slot0 == 0) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
@@ -541,6 +584,99 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
         }
         if (!ok && lane == 0) fail();
+    } else if constexpr (F8) {
+        // ---------------------------------------------------------------- E4M3 -> fp16 (warps 11-14)
+        // Thread r owns row r of every K and V stage (token r of the step) and dimension r of Q.
+        // A stage's E4M3 tile (128 rows of 128 bytes) sits in the stage's upper half; row r is read
+        // into registers whole before its two fp16 halves are written (the second one over the
+        // E4M3 row itself), so the widening runs in place.  E4M3 values are exact in fp16.
+        const int cw = warp - 11, r = cw * 32 + lane;
+        auto widen_row = [&](uint8_t *stage) {
+            const uint8_t *src = stage + TOK * 128 + r * 128;
+            uint4 w[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) w[c] = *reinterpret_cast<const uint4 *>(src + (((c + lane) & 7) << 4));
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int ch = (c + lane) & 7; // 16 dims: 16 ch .. 16 ch + 15
+                const uint32_t in[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+                uint32_t o[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const unsigned short lo = (unsigned short)(in[e] & 0xFFFFu), hi = (unsigned short)(in[e] >> 16);
+                    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o[2 * e]) : "h"(lo));
+                    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o[2 * e + 1]) : "h"(hi));
+                }
+                uint8_t *row = stage + (ch >> 2) * (TOK * 128) + r * 128;
+                const int u0 = (ch & 3) * 2;
+                *reinterpret_cast<uint4 *>(row + ((u0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4 *>(row + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+        };
+        // byte offset of (head g, dimension r) in a K-major, 128-byte-swizzled Q tile
+        auto qoff = [&](int g) {
+            const int e = r & 63;
+            return (r >> 6) * (NQ * 128) + g * 128 + (((e >> 3) ^ (g & 7)) << 4) + (e & 7) * 2;
+        };
+        bool ok = true;
+        int64_t gs = 0;
+        int nu = 0;
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
+            const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
+            const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
+            const int qb = nu & 1;
+            // ---- q of the unit in fp16, scaled by 2^-e so that its largest magnitude lies in [2^14, 2^15)
+            bool mine = ok && *abort_flag == 0;
+            if (mine) mine = __all_sync(0xffffffffu, mbar_wait(q_full + qb, (nu >> 1) & 1));
+            uint8_t *qt = smem + LY::Q + qb * LY::Q_BYTES;
+            float x[G], mx = 0.f;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                x[g] = 0.f;
+                if (mine) {
+                    const uint16_t bits = *reinterpret_cast<const uint16_t *>(qt + qoff(g));
+                    x[g] = MT == PKV_BF16 ? __uint_as_float((uint32_t)bits << 16) : __half2float(__ushort_as_half(bits));
+                    mx = fmaxf(mx, fabsf(x[g]));
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            if (lane == 0) qred[qb * 4 + cw] = mx;
+            ok = named_barrier_and(2, 128, mine);
+            if (!ok) break;
+            const float qm = fmaxf(fmaxf(qred[qb * 4], qred[qb * 4 + 1]), fmaxf(qred[qb * 4 + 2], qred[qb * 4 + 3]));
+            int e = 0;
+            if (qm > 0.f) {
+                int ex;
+                frexpf(qm, &ex);
+                e = min(max(ex - 15, -100), 100);
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) *reinterpret_cast<__half *>(qt + qoff(g)) = __float2half_rn(ldexpf(x[g], -e));
+            if (r == 0) qexp[nu & 7] = e; // read by the softmax after this unit's first v_full
+            fence_proxy_async_smem();    // Q is read by the MMA
+            mbar_arrive(q_ready + qb);
+            // ---- the unit's K and V stages
+            for (int i = 0; i < nsteps && ok; ++i) {
+                const int64_t g = gs + i;
+                const int st = (int)(g % NS);
+                ok = __all_sync(0xffffffffu, mbar_wait(k8_full + st, (g / NS) & 1));
+                if (!ok) break;
+                widen_row(smem + LY::K0 + st * LY::STAGE);
+                fence_proxy_async_smem();
+                mbar_arrive(k_full + st);
+                ok = __all_sync(0xffffffffu, mbar_wait(v8_full + st, (g / NS) & 1));
+                if (!ok) break;
+                widen_row(smem + LY::V0 + st * LY::STAGE);
+                fence_proxy_async_smem();
+                mbar_arrive(v_full + st);
+            }
+            gs += nsteps;
+            // the four warps leave together (the next unit's barrier would wait for a warp gone)
+            ok = named_barrier_and(2, 128, ok && *abort_flag == 0);
+            if (!ok) break;
+        }
+        if (!ok && lane == 0) fail();
     }
 
     tc::fence_before_sync();
@@ -551,10 +687,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int G, int MT>
+template <int G, int MT, int KVT>
 cudaError_t launch(const CUtensorMap &tkv, const CUtensorMap &tq, const Args &a, int grid, size_t smem,
                    cudaStream_t st) {
-    auto kern = decode_tc_kernel<G, MT>;
+    auto kern = decode_tc_kernel<G, MT, KVT>;
+    constexpr int kThreads = threads_for<KVT == PKV_FP8_E4M3>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return pdl_launch(kern, dim3(grid), dim3(kThreads), smem, st, tkv, tq, a);
