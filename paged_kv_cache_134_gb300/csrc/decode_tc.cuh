@@ -50,6 +50,21 @@ __host__ __device__ constexpr int threads_for() {
 }
 constexpr uint32_t kTmemCols = 128;  // S0 [0,16) S1 [16,32) O^T of even units [32,64), of odd units [64,96)
 constexpr float kRescale = 8.0f;     // log2 units
+constexpr int kUnitRing = 16;        // unit records published by the K loader (see UnitRec)
+
+// One work unit as the K loader publishes it for the other roles, which would otherwise each
+// repeat the (sequence, head, split) lookup at every unit boundary on their critical paths.  The
+// loader publishes unit n once it has issued the K loads of unit n - 1; the last of those waited
+// for the S^T four steps back, which waited for the softmax to release the scores six steps back,
+// so the softmax warps are within six units and the other roles within a few more (the epilogue
+// two units behind the softmax): a ring of 16 is never overwritten before it is read.
+struct UnitRec {
+    int s, kvh, j, blk0, ntiles, nsplit;
+    int tok_end; // first token past the unit: min(sequence length, end of its last block)
+    float ksc;   // the KV head's K scale (FP8 caches)
+    int tag;     // the unit's index in this CTA's order, written last
+    int pad[7];
+};
 
 template <int MT>
 struct Layout {
@@ -67,7 +82,8 @@ struct Layout {
     static constexpr int P_BYTES = NPR * TOK * 2;          // one buffer
     static constexpr int RED = P + 2 * P_BYTES;            // [2][4 warps][NQ] maxima, [2][4 warps][NQ] sums,
     static constexpr int BAR = RED + (4 * 4 * NQ + 2 * NQ) * 4; // [2][NQ] bases (sums and bases per unit parity)
-    static constexpr int FIXED = BAR + 512;                // + unit tables, 3 (S + 1) ints
+    static constexpr int UNITS = BAR + 512;                // ring of kUnitRing unit records
+    static constexpr int FIXED = UNITS + kUnitRing * 64;   // + unit tables, 3 (S + 1) ints
 };
 
 inline size_t smem_bytes(int mt, int num_seqs) {
@@ -83,6 +99,46 @@ PKV_DEV uint32_t pack2(float lo, float hi) {
         asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     else
         asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The unit lookup of the CUDA-core kernel, done by a whole warp: each search round tests 32 rows
+// at once and keeps the bracket of the last row whose prefix is <= k, so a few hundred sequences
+// take two rounds of independent shared-memory reads instead of a chain of dependent ones.  All
+// 32 lanes call it with the same arguments.
+PKV_DEV int find_row_warp(const int *pref, int n, int k, int lane) {
+    // largest i in [0, n) with pref[i] <= k (pref non-decreasing, pref[0] = 0 <= k)
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) >> 5;
+        const int i = lo + lane * step;
+        const unsigned le = __ballot_sync(0xffffffffu, i < hi && pref[i] <= k);
+        lo += (31 - __clz(le)) * step; // lane 0 always passes: pref[lo] <= k
+        hi = min(hi, lo + step);
+    }
+    return lo;
+}
+
+PKV_DEV Unit unit_info_warp(int u, const int *pf, const int *pp, const int *nb, int S, int hkv, int bps, int sb,
+                            int lane) {
+    Unit r;
+    const int nfull_units = pf[S] * hkv;
+    if (u < nfull_units) {
+        const int k = u / hkv;
+        r.kvh = u - k * hkv;
+        r.s = find_row_warp(pf, S, k, lane);
+        r.j = k - pf[r.s];
+        r.blk0 = sb + r.j * bps;
+        r.ntiles = bps;
+    } else {
+        const int k = (u - nfull_units) / hkv;
+        r.kvh = (u - nfull_units) - k * hkv;
+        r.s = find_row_warp(pp, S, k, lane);
+        r.j = pf[r.s + 1] - pf[r.s];
+        r.blk0 = sb + r.j * bps;
+        r.ntiles = nb[r.s] - r.blk0;
+    }
+    r.nsplit = (pf[r.s + 1] - pf[r.s]) + (pp[r.s + 1] - pp[r.s]);
     return r;
 }
 
@@ -118,14 +174,13 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
     uint64_t *fin = s_full + 20;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(fin + 2);
-    volatile uint32_t *badmask = reinterpret_cast<volatile uint32_t *>(fin + 3); // [NS]
-    // FP8 caches: the exponent of unit nu's q scale in slot nu % 8 (the converters run at most a few
-    // units ahead of the softmax, which reads it after its first v_full wait of the unit: the
-    // converters arrive on v_full themselves), the converters' partial maxima, and barriers for
-    // "E4M3 tile landed" (k8/v8_full, before the in-place widening) and "Q converted"
+    // FP8 caches: the exponent of unit nu's q scale in slot nu % 8, published with "Q converted"
+    // (q_ready, a ring of 8: unit nu + 8's Q cannot be loaded before the softmax has read the scores
+    // of unit nu + 4, so the MMA and the softmax, which wait for unit nu, never see a later phase),
+    // the converters' partial maxima, and "E4M3 tile landed" (k8/v8_full, before the widening)
     volatile int *qexp = reinterpret_cast<volatile int *>(fin + 5);              // [8]
     volatile float *qred = reinterpret_cast<volatile float *>(fin + 9);          // [2 unit parities][4 warps]
-    uint64_t *k8_full = fin + 13, *v8_full = fin + 13 + NS, *q_ready = fin + 13 + 2 * NS;
+    uint64_t *k8_full = fin + 13, *v8_full = fin + 13 + NS, *q_ready = fin + 13 + 2 * NS; // q_ready [8]
     float *red_max = reinterpret_cast<float *>(smem + LY::RED);                  // [2][4][NQ]
     float *red_sum = red_max + 2 * 4 * NQ;                                      // [2][4][NQ]
     float *m_base = red_sum + 2 * 4 * NQ;                                       // [2][NQ]
@@ -146,7 +201,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             }
         }
         if constexpr (F8)
-            for (int b = 0; b < 2; ++b) mbar_init(q_ready + b, 128);
+            for (int b = 0; b < 8; ++b) mbar_init(q_ready + b, 128);
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full + b, 1);
             mbar_init(s_free + b, 128);
@@ -167,6 +222,8 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         *abort_flag = 0;
         fence_mbarrier_init();
     }
+    UnitRec *ring = reinterpret_cast<UnitRec *>(smem + LY::UNITS);
+    for (int k = threadIdx.x; k < kUnitRing; k += kThreads) ring[k].tag = -1;
     // Q rows past the group stay zero (the MMA's padding heads)
     for (int i = threadIdx.x; i < 2 * LY::Q_BYTES / 16; i += kThreads)
         reinterpret_cast<uint4 *>(smem + LY::Q)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -188,6 +245,48 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         set_error(a.err, PKV_DEVERR_TIMEOUT);
         *abort_flag = 1;
     };
+    // (sequence, KV head, split) of unit u; every lane of the calling warp takes part
+    auto unit_at = [&](int u) { return unit_info_warp(u, pf, pp, nb, S, a.hkv, bps, a.start_block, lane); };
+    // publish this CTA's n-th unit (one thread of the K loader)
+    auto write_rec = [&](int n, const Unit &x, int L, float ks) {
+        UnitRec *r = ring + (n % kUnitRing);
+        r->s = x.s;
+        r->kvh = x.kvh;
+        r->j = x.j;
+        r->blk0 = x.blk0;
+        r->ntiles = x.ntiles;
+        r->nsplit = x.nsplit;
+        r->tok_end = min(L, (x.blk0 + x.ntiles) * a.bs);
+        r->ksc = ks;
+        __threadfence_block();
+        *reinterpret_cast<volatile int *>(&r->tag) = n;
+    };
+    // read this CTA's n-th unit once published (every lane waits for the tag itself); false after
+    // the wait limit, agreed over the warp
+    auto read_rec = [&](int n, Unit &x, int &tok_end, float &ks) -> bool {
+        const UnitRec *r = ring + (n % kUnitRing);
+        const volatile int *tag = &r->tag;
+        bool okr = true;
+        if (*tag != n) {
+            const uint64_t t0 = global_timer_ns();
+            while (*tag != n)
+                if (global_timer_ns() - t0 > PKV_WAIT_LIMIT_NS) {
+                    okr = false;
+                    break;
+                }
+        }
+        okr = __all_sync(0xffffffffu, okr);
+        __threadfence_block();
+        x.s = r->s;
+        x.kvh = r->kvh;
+        x.j = r->j;
+        x.blk0 = r->blk0;
+        x.ntiles = r->ntiles;
+        x.nsplit = r->nsplit;
+        tok_end = r->tok_end;
+        ks = r->ksc;
+        return okr;
+    };
 
     if (warp == 0 || warp == 6) {
         // ---------------------------------------------------------------- loads
@@ -205,28 +304,59 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             return lane < nblk ? a.tables[(int64_t)un.s * a.max_blocks + un.blk0 + i * bpstep + lane] : 0;
         };
         int64_t gs = 0; // steps issued so far, all units
-        int nu = 0, last_q = -1;
+        int nu = 0, q_next = 0; // q_next: this CTA's next unit (in its order) whose Q is still to load
+        // Q of this CTA's k-th unit `uq` into buffer k % 2 (free once the last S^T of unit k - 2 is issued)
+        auto issue_q = [&](int k, const Unit &uq) {
+            const int qb = k & 1;
+            mbar_arrive_expect_tx(q_full + qb, (uint32_t)(G * D * 2));
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+                tc::tma_load_2d(smem + LY::Q + qb * LY::Q_BYTES + c * NQ * 128, &tq, c * 64, uq.s * a.hq + uq.kvh * G,
+                                q_full + qb);
+        };
         bool ok = true;
         int u = blockIdx.x, i = 0, nsteps = 0;
-        Unit un{};
+        // un: the current unit; nx (K loader): the one after it, looked up when `un` starts, with its
+        // length and K scale, which are published a unit later (their loads have landed by then)
+        Unit un{}, nx{};
+        int nx_len = 0;
+        float nx_ks = 1.f;
+        auto look_ahead = [&](int uu) {
+            if (uu < U) {
+                nx = unit_at(uu);
+                nx_len = a.lens[nx.s];
+                if constexpr (F8) nx_ks = a.k_scale[nx.kvh];
+            }
+        };
         if (u < U) {
-            un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
+            if (is_k) {
+                un = unit_at(u);
+                if (lane == 0) write_rec(0, un, a.lens[un.s], F8 ? a.k_scale[un.kvh] : 1.f);
+                look_ahead(u + (int)gridDim.x);
+            } else {
+                int te;
+                float ks;
+                ok = read_rec(0, un, te, ks);
+            }
             nsteps = (un.ntiles + bpstep - 1) / bpstep;
         }
-        int cur = u < U ? entry(un, 0) : 0;
+        int cur = u < U && ok ? entry(un, 0) : 0;
         while (u < U && ok) {
-            if (i == 0 && is_k && lane == 0) {
-                // Q of unit nu goes to buffer nu % 2, free once the last S^T of unit nu - 2 is done
-                const int qb = nu & 1;
-                if (nu >= 2 && !mbar_wait(q_empty + qb, ((nu >> 1) - 1) & 1)) ok = false;
-                if (ok) {
-                    mbar_arrive_expect_tx(q_full + qb, (uint32_t)(G * D * 2));
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c)
-                        tc::tma_load_2d(smem + LY::Q + qb * LY::Q_BYTES + c * NQ * 128, &tq, c * 64,
-                                        un.s * a.hq + un.kvh * G, q_full + qb);
-                    last_q = nu;
+            if (is_k) {
+                // this unit's Q is loaded by its first step at the latest (waiting for its buffer); the
+                // next unit's goes as soon as its buffer is free, tested at every step without waiting
+                const bool first = i == 0 && q_next == nu;
+                const bool early = q_next == nu + 1 && u + (int)gridDim.x < U;
+                if (lane == 0) {
+                    if (first) {
+                        if (nu >= 2 && !mbar_wait_sleep(q_empty + (nu & 1), ((nu >> 1) - 1) & 1)) ok = false;
+                        if (ok) issue_q(q_next++, un);
+                    } else if (early &&
+                               (q_next < 2 || mbar_test_wait(q_empty + (q_next & 1), ((q_next >> 1) - 1) & 1))) {
+                        issue_q(q_next++, nx);
+                    }
                 }
+                q_next = __shfl_sync(0xffffffffu, q_next, 0);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
@@ -237,7 +367,16 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 u2 = u + gridDim.x;
                 i2 = 0;
                 if (u2 < U) {
-                    un2 = pkv_decode::unit_info(u2, pf, pp, nb, S, a.hkv, bps, a.start_block);
+                    if (is_k) {
+                        un2 = nx;
+                    } else {
+                        int te;
+                        float ks;
+                        if (!read_rec(nu + 1, un2, te, ks)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                     nsteps2 = (un2.ntiles + bpstep - 1) / bpstep;
                 }
             }
@@ -256,12 +395,9 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             uint64_t *full = F8 ? (is_k ? k8_full + st : v8_full + st) : (is_k ? k_full + st : v_full + st);
             uint64_t *empty = is_k ? k_empty + st : v_empty + st;
             if (lane == 0) {
-                if (round >= 1 && !mbar_wait(empty, (round - 1) & 1)) ok = false;
+                if (round >= 1 && !mbar_wait_sleep(empty, (round - 1) & 1)) ok = false;
                 if (ok) {
-                    if (!is_k) {
-                        if (bad) set_error(a.err, PKV_DEVERR_BLOCK_ID);
-                        badmask[st] = bad; // read by the softmax after v_full, freed with v_empty
-                    }
+                    if (!is_k && bad) set_error(a.err, PKV_DEVERR_BLOCK_ID);
                     mbar_arrive_expect_tx(full, bytes);
                 }
             }
@@ -284,7 +420,14 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             }
             ++gs;
             cur = nxt;
-            if (i2 == 0) ++nu;
+            if (i2 == 0) {
+                ++nu;
+                if (is_k && u2 < U) {
+                    // entering unit nu (its Q may still be loading): publish it, look up the next one
+                    if (lane == 0) write_rec(nu, un2, nx_len, nx_ks);
+                    look_ahead(u2 + (int)gridDim.x);
+                }
+            }
             u = u2;
             i = i2;
             un = un2;
@@ -296,11 +439,12 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         // the copies of the last stages must land before this CTA's shared memory goes away
         if (lane == 0) {
             for (int64_t g = gs > NS ? gs - NS : 0; g < gs; ++g)
-                if (!mbar_wait((F8 ? (is_k ? k8_full : v8_full) : (is_k ? k_full : v_full)) + g % NS, (g / NS) & 1))
+                if (!mbar_wait_sleep((F8 ? (is_k ? k8_full : v8_full) : (is_k ? k_full : v_full)) + g % NS, (g / NS) & 1))
                     set_error(a.err, PKV_DEVERR_TIMEOUT);
+            const int last_q = q_next - 1;
             if (is_k)
                 for (int n = last_q > 0 ? last_q - 1 : 0; n <= last_q; ++n)
-                    if (!mbar_wait(q_full + (n & 1), (n >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+                    if (!mbar_wait_sleep(q_full + (n & 1), (n >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -316,8 +460,8 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             // S^T of step g (Q buffer qb) into S buffer g % 2; the K stage is released as soon as S^T is done
             auto issue_s = [&](int64_t g, int qb) -> bool {
                 const int st = (int)(g % NS), b = (int)(g & 1);
-                if (!__all_sync(0xffffffffu, mbar_wait(k_full + st, (g / NS) & 1))) return false;
-                if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(s_free + b, ((g >> 1) - 1) & 1))) return false;
+                if (!__all_sync(0xffffffffu, mbar_wait_sleep(k_full + st, (g / NS) & 1))) return false;
+                if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait_sleep(s_free + b, ((g >> 1) - 1) & 1))) return false;
                 tc::fence_after_sync();
                 any_mma = true;
 #pragma unroll
@@ -331,14 +475,24 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 tc::commit_warp(k_empty + st);
                 return true;
             };
-            bool ok = true;
+            // Q of unit n in place: loaded (q_full), or for FP8 caches converted (q_ready, ring of 8)
+            auto q_bar = [&](int n) { return F8 ? q_ready + (n & 7) : q_full + (n & 1); };
+            auto q_par = [&](int n) -> uint32_t { return F8 ? (uint32_t)(n >> 3) & 1u : (uint32_t)(n >> 1) & 1u; };
+            bool ok = true, ahead = false; // ahead: the unit's first S^T went out during the previous unit
             int64_t gs = 0;
             int nu = 0;
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
-                const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
+                Unit un;
+                int te;
+                float ks;
+                if (!read_rec(nu, un, te, ks)) {
+                    ok = false;
+                    break;
+                }
                 const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
                 const int qb = nu & 1;
-                ok = __all_sync(0xffffffffu, mbar_wait((F8 ? q_ready : q_full) + qb, (nu >> 1) & 1)) && issue_s(gs, qb);
+                if (!ahead) ok = __all_sync(0xffffffffu, mbar_wait_sleep(q_bar(nu), q_par(nu))) && issue_s(gs, qb);
+                ahead = false;
                 for (int i = 0; i < nsteps && ok; ++i) {
                     const int64_t g = gs + i;
                     if (i + 1 < nsteps) {
@@ -346,12 +500,19 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                         if (!ok) break;
                     } else {
                         tc::commit_warp(q_empty + qb); // the unit's last S^T has been issued: its Q buffer may be refilled
+                        // the next unit's first S^T goes ahead of this P V when its Q is already in place, so
+                        // the softmax warps find it ready when they start that unit
+                        if (u + (int)gridDim.x < U && __all_sync(0xffffffffu, mbar_test_wait(q_bar(nu + 1), q_par(nu + 1)))) {
+                            ok = issue_s(g + 1, (nu + 1) & 1);
+                            if (!ok) break;
+                            ahead = true;
+                        }
                     }
                     const int st = (int)(g % NS), b = (int)(g & 1);
-                    ok = __all_sync(0xffffffffu, mbar_wait(p_full + b, (g >> 1) & 1) && mbar_wait(v_full + st, (g / NS) & 1));
+                    ok = __all_sync(0xffffffffu, mbar_wait_sleep(p_full + b, (g >> 1) & 1) && mbar_wait_sleep(v_full + st, (g / NS) & 1));
                     // O^T of this unit's parity was read out by the epilogue warps for unit nu - 2
                     if (ok && i == 0 && nu >= 2)
-                        ok = __all_sync(0xffffffffu, mbar_wait(o_free + (nu & 1), ((nu >> 1) - 1) & 1));
+                        ok = __all_sync(0xffffffffu, mbar_wait_sleep(o_free + (nu & 1), ((nu >> 1) - 1) & 1));
                     if (!ok) break;
                     const uint32_t tO = tmem + 2 * NQ + (uint32_t)((nu & 1) * 32);
                     tc::fence_after_sync();
@@ -373,7 +534,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             // every MMA issued by the elected lane has completed before tensor memory is released
             if (any_mma) {
                 tc::commit_warp(fin);
-                if (!__all_sync(0xffffffffu, mbar_wait(fin, 0)) && lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
+                if (!__all_sync(0xffffffffu, mbar_wait_sleep(fin, 0)) && lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
             }
         }
     } else if (warp < 6) {
@@ -384,12 +545,28 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         bool ok = true;
         int64_t gs = 0;
         int nu = 0;
-        for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
-            const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
+        // table entry of this thread's block (row r of the step) in step i of unit un; -1 past the unit
+        const int jb = r / a.bs;
+        auto blk_entry = [&](const Unit &x, int i) -> int {
+            return i * bpstep + jb < x.ntiles ? a.tables[(int64_t)x.s * a.max_blocks + x.blk0 + i * bpstep + jb] : -1;
+        };
+        // the units come from the K loader's records: the next one is read at the last step of the
+        // current one, with the table entry of its first step; entries are read a step ahead
+        int u = blockIdx.x;
+        Unit un{};
+        int tok_end = 0, ent = -1;
+        float ksc = 1.f;
+        if (u < U) {
+            ok = read_rec(0, un, tok_end, ksc);
+            if (ok) ent = blk_entry(un, 0);
+        }
+        for (; u < U && ok; u += gridDim.x, ++nu) {
             const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
-            const int L = a.lens[un.s];
+            const int u2 = u + (int)gridDim.x;
+            Unit un2{};
+            int tok_end2 = 0;
+            float ksc2 = 1.f;
             const int tok0 = un.blk0 * a.bs;
-            const int tok_end = min(L, (un.blk0 + un.ntiles) * a.bs);
             // scores in log2 units: scale * log2(e), times the K scale of the head and the power of two
             // taken out of q by the converters (FP8 caches)
             float qsc = a.qk_scale_log2;
@@ -403,14 +580,25 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             for (int i = 0; i < nsteps; ++i) {
                 const int64_t g0 = gs + i;
                 const int st = (int)(g0 % NS), b = (int)(g0 & 1);
-                bool mine = ok && *abort_flag == 0;
-                if (mine) mine = __all_sync(0xffffffffu, mbar_wait(s_full + b, (g0 >> 1) & 1) &&
-                                                             mbar_wait(v_full + st, (g0 / NS) & 1));
+                // the next step's table entry (the next unit's first one after the last step)
+                bool rec_ok = true;
+                if (i + 1 == nsteps && u2 < U) rec_ok = read_rec(nu + 1, un2, tok_end2, ksc2);
+                const int ent_nx = i + 1 < nsteps ? blk_entry(un, i + 1) : (u2 < U && rec_ok ? blk_entry(un2, 0) : -1);
+                bool mine = ok && rec_ok && *abort_flag == 0;
+                if constexpr (F8) {
+                    // the unit's q exponent, published with its "Q converted" barrier
+                    if (mine && i == 0) {
+                        mine = __all_sync(0xffffffffu, mbar_wait_sleep(q_ready + (nu & 7), (uint32_t)(nu >> 3) & 1u));
+                        qsc = a.qk_scale_log2 * ksc * exp2f((float)qexp[nu & 7]);
+                    }
+                }
+                if (mine) mine = __all_sync(0xffffffffu, mbar_wait_sleep(s_full + b, (g0 >> 1) & 1));
                 const int step0 = tok0 + i * TOK;
-                bool valid = false, ragged = false;
+                // a row holds a token of the unit if it lies before the unit's end and in a block whose
+                // table entry names a block of the pool (the loaders skip the others)
+                const bool valid = step0 + r < tok_end && ent >= 0 && ent < a.num_blocks;
+                ent = ent_nx;
                 float sc[G];
-                if constexpr (F8)
-                    if (mine && i == 0) qsc = a.qk_scale_log2 * a.k_scale[un.kvh] * exp2f((float)qexp[nu & 7]);
                 if (mine) {
                     tc::fence_after_sync();
                     uint32_t sr[G];
@@ -418,9 +606,6 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                     tc::wait_ld();
                     tc::fence_before_sync();
                     mbar_arrive(s_free + b);
-                    const uint32_t bm = badmask[st];
-                    valid = step0 + r < tok_end && !((bm >> (r / a.bs)) & 1u);
-                    ragged = step0 + TOK > tok_end || bm != 0u;
                     // tile max per head over the 128 rows: warp shuffles, then the 4 warps via shared memory
                     float tmx[G];
 #pragma unroll
@@ -458,9 +643,9 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                     lp[g] = lp[g] * alpha[g] + p[g];
                 }
                 // P buffer b is free once P V of step g0 - 2 is done; O^T is stable once P V of g0 - 1 is
-                if (g0 >= 2) ok = __all_sync(0xffffffffu, mbar_wait(t_full + b, ((g0 >> 1) - 1) & 1));
+                if (g0 >= 2) ok = __all_sync(0xffffffffu, mbar_wait_sleep(t_full + b, ((g0 >> 1) - 1) & 1));
                 if (ok && moved && i > 0) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(t_full + (b ^ 1), ((g0 - 1) >> 1) & 1));
+                    ok = __all_sync(0xffffffffu, mbar_wait_sleep(t_full + (b ^ 1), ((g0 - 1) >> 1) & 1));
                     if (ok) {
                         tc::fence_after_sync();
 #pragma unroll
@@ -491,13 +676,21 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                         *reinterpret_cast<uint16_t *>(pb + off) = (uint16_t)(pack2<OT>(p[g], 0.f) & 0xFFFFu);
                     }
                 }
-                if (ragged && !valid) {
-                    // this row's V is an unused slot (or a stale stage row): zero it for the MMA
+                if (__any_sync(0xffffffffu, !valid)) {
+                    // a row without a token holds an unused slot, a skipped block's stale row or (FP8)
+                    // widened garbage: zero its V once the stage has landed, so that no NaN reaches the
+                    // MMA (only these steps wait for V here; P V waits for it in the MMA warp)
+                    if (!__all_sync(0xffffffffu, mbar_wait_sleep(v_full + st, (g0 / NS) & 1))) {
+                        ok = false;
+                        continue; // carried to the next barrier
+                    }
+                    if (!valid) {
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
-                        uint4 *vr = reinterpret_cast<uint4 *>(smem + LY::V0 + st * LY::STAGE + c * (TOK * 128) + r * 128);
+                        for (int c = 0; c < D / 64; ++c) {
+                            uint4 *vr = reinterpret_cast<uint4 *>(smem + LY::V0 + st * LY::STAGE + c * (TOK * 128) + r * 128);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) vr[e] = make_uint4(0u, 0u, 0u, 0u);
+                            for (int e = 0; e < 8; ++e) vr[e] = make_uint4(0u, 0u, 0u, 0u);
+                        }
                     }
                 }
                 fence_proxy_async_smem();
@@ -507,7 +700,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             gs += nsteps;
             // ---- hand the unit's row sums and bases to the epilogue warps (buffer nu % 2)
             const int eb = nu & 1;
-            if (ok && nu >= 2) ok = __all_sync(0xffffffffu, mbar_wait(l_free + eb, ((nu >> 1) - 1) & 1));
+            if (ok && nu >= 2) ok = __all_sync(0xffffffffu, mbar_wait_sleep(l_free + eb, ((nu >> 1) - 1) & 1));
             if (ok) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
@@ -523,6 +716,9 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             // leave the others waiting at the next named barrier)
             ok = named_barrier_and(1, 128, ok);
             if (!ok) break;
+            un = un2;
+            tok_end = tok_end2;
+            ksc = ksc2;
         }
         if (!ok) fail();
     } else if (warp < 11) {
@@ -536,9 +732,15 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         bool ok = true;
         int nu = 0;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
-            const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
+            Unit un;
+            int te;
+            float ks;
+            if (!read_rec(nu, un, te, ks)) {
+                ok = false;
+                break;
+            }
             const int eb = nu & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(o_full + eb, (nu >> 1) & 1) && mbar_wait(l_ready + eb, (nu >> 1) & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait_sleep(o_full + eb, (nu >> 1) & 1) && mbar_wait_sleep(l_ready + eb, (nu >> 1) & 1));
             if (!ok) break;
             tc::fence_after_sync();
             uint32_t o[G];
@@ -622,12 +824,18 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         int64_t gs = 0;
         int nu = 0;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
-            const Unit un = pkv_decode::unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
+            Unit un;
+            int te;
+            float ks;
+            if (!read_rec(nu, un, te, ks)) {
+                ok = false;
+                break;
+            }
             const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
             const int qb = nu & 1;
             // ---- q of the unit in fp16, scaled by 2^-e so that its largest magnitude lies in [2^14, 2^15)
             bool mine = ok && *abort_flag == 0;
-            if (mine) mine = __all_sync(0xffffffffu, mbar_wait(q_full + qb, (nu >> 1) & 1));
+            if (mine) mine = __all_sync(0xffffffffu, mbar_wait_sleep(q_full + qb, (nu >> 1) & 1));
             uint8_t *qt = smem + LY::Q + qb * LY::Q_BYTES;
             float x[G], mx = 0.f;
 #pragma unroll
@@ -653,19 +861,19 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             }
 #pragma unroll
             for (int g = 0; g < G; ++g) *reinterpret_cast<__half *>(qt + qoff(g)) = __float2half_rn(ldexpf(x[g], -e));
-            if (r == 0) qexp[nu & 7] = e; // read by the softmax after this unit's first v_full
+            if (r == 0) qexp[nu & 7] = e; // read by the softmax after q_ready
             fence_proxy_async_smem();    // Q is read by the MMA
-            mbar_arrive(q_ready + qb);
+            mbar_arrive(q_ready + (nu & 7));
             // ---- the unit's K and V stages
             for (int i = 0; i < nsteps && ok; ++i) {
                 const int64_t g = gs + i;
                 const int st = (int)(g % NS);
-                ok = __all_sync(0xffffffffu, mbar_wait(k8_full + st, (g / NS) & 1));
+                ok = __all_sync(0xffffffffu, mbar_wait_sleep(k8_full + st, (g / NS) & 1));
                 if (!ok) break;
                 widen_row(smem + LY::K0 + st * LY::STAGE);
                 fence_proxy_async_smem();
                 mbar_arrive(k_full + st);
-                ok = __all_sync(0xffffffffu, mbar_wait(v8_full + st, (g / NS) & 1));
+                ok = __all_sync(0xffffffffu, mbar_wait_sleep(v8_full + st, (g / NS) & 1));
                 if (!ok) break;
                 widen_row(smem + LY::V0 + st * LY::STAGE);
                 fence_proxy_async_smem();

@@ -69,6 +69,19 @@ PKV_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// non-blocking test: has the phase of `parity` completed?
+PKV_DEV bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false after
 // PKV_WAIT_LIMIT_NS without completion.
 PKV_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) {
@@ -77,6 +90,25 @@ PKV_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) {
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0u && global_timer_ns() - t0 > PKV_WAIT_LIMIT_NS) return false;
+    }
+}
+
+// The same bounded wait with a suspend-time hint: a warp whose phase has not completed sleeps in
+// the barrier until it completes (or the hint runs out) instead of re-testing it, which leaves the
+// shared-memory pipe to the warps doing the work in kernels where many warps wait at once.
+PKV_DEV bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+            : "memory");
+        if (ok) return true;
+        if (global_timer_ns() - t0 > PKV_WAIT_LIMIT_NS) return false;
     }
 }
 
