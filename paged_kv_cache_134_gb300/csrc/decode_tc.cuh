@@ -599,6 +599,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 const bool valid = step0 + r < tok_end && ent >= 0 && ent < a.num_blocks;
                 ent = ent_nx;
                 float sc[G];
+                bool need = !mine; // a failed wait takes the exchange path, where `ok` is agreed
                 if (mine) {
                     tc::fence_after_sync();
                     uint32_t sr[G];
@@ -606,36 +607,49 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                     tc::wait_ld();
                     tc::fence_before_sync();
                     mbar_arrive(s_free + b);
-                    // tile max per head over the 128 rows: warp shuffles, then the 4 warps via shared memory
-                    float tmx[G];
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         sc[g] = valid ? __uint_as_float(sr[g]) * qsc : -INFINITY;
-                        float v = sc[g];
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                        tmx[g] = v;
-                    }
-                    if (lane < G) {
-                        float v = tmx[0];
-#pragma unroll
-                        for (int g = 1; g < G; ++g)
-                            if (lane == g) v = tmx[g];
-                        red_max[(int)(g0 & 1) * 4 * NQ + lw * NQ + lane] = v;
+                        need |= sc[g] > m[g] + kRescale; // false while sc = -inf
                     }
                 }
-                ok = named_barrier_and(1, 128, mine);
-                if (!ok) break;
-                const float *rm = red_max + (int)(g0 & 1) * 4 * NQ;
+                // The base moves only where a score passes it by more than kRescale.  The four warps
+                // first agree whether any score does (one barrier); only then do they exchange the tile
+                // maxima per head (warp shuffles, shared memory, a second barrier).  After a unit's
+                // first step that is rare, so most steps pay one barrier.
                 bool moved = false;
                 float alpha[G], p[G];
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float t = fmaxf(fmaxf(rm[g], rm[NQ + g]), fmaxf(rm[2 * NQ + g], rm[3 * NQ + g]));
-                    const bool up = t > m[g] + kRescale; // false while t = -inf
-                    alpha[g] = up ? fast_exp2(m[g] - t) : 1.f;
-                    if (up) m[g] = t;
-                    moved |= up;
+                for (int g = 0; g < G; ++g) alpha[g] = 1.f;
+                if (named_barrier_or(1, 128, need)) {
+                    if (mine) {
+                        float tmx[G];
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            float v = sc[g];
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                            tmx[g] = v;
+                        }
+                        if (lane < G) {
+                            float v = tmx[0];
+#pragma unroll
+                            for (int g = 1; g < G; ++g)
+                                if (lane == g) v = tmx[g];
+                            red_max[(int)(g0 & 1) * 4 * NQ + lw * NQ + lane] = v;
+                        }
+                    }
+                    ok = named_barrier_and(1, 128, mine);
+                    if (!ok) break;
+                    const float *rm = red_max + (int)(g0 & 1) * 4 * NQ;
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float t = fmaxf(fmaxf(rm[g], rm[NQ + g]), fmaxf(rm[2 * NQ + g], rm[3 * NQ + g]));
+                        const bool up = t > m[g] + kRescale; // false while t = -inf
+                        alpha[g] = up ? fast_exp2(m[g] - t) : 1.f;
+                        if (up) m[g] = t;
+                        moved |= up;
+                    }
                 }
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
@@ -820,22 +834,11 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             const int e = r & 63;
             return (r >> 6) * (NQ * 128) + g * 128 + (((e >> 3) ^ (g & 7)) << 4) + (e & 7) * 2;
         };
-        bool ok = true;
-        int64_t gs = 0;
-        int nu = 0;
-        for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
-            Unit un;
-            int te;
-            float ks;
-            if (!read_rec(nu, un, te, ks)) {
-                ok = false;
-                break;
-            }
-            const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
-            const int qb = nu & 1;
-            // ---- q of the unit in fp16, scaled by 2^-e so that its largest magnitude lies in [2^14, 2^15)
-            bool mine = ok && *abort_flag == 0;
-            if (mine) mine = __all_sync(0xffffffffu, mbar_wait_sleep(q_full + qb, (nu >> 1) & 1));
+        // q of this CTA's n-th unit in fp16, scaled by 2^-e so that its largest magnitude lies in
+        // [2^14, 2^15); false, agreed by the four warps at their barrier, after a failed wait
+        auto convert_q = [&](int n, bool mine) -> bool {
+            const int qb = n & 1;
+            if (mine) mine = __all_sync(0xffffffffu, mbar_wait_sleep(q_full + qb, (n >> 1) & 1));
             uint8_t *qt = smem + LY::Q + qb * LY::Q_BYTES;
             float x[G], mx = 0.f;
 #pragma unroll
@@ -850,8 +853,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
             if (lane == 0) qred[qb * 4 + cw] = mx;
-            ok = named_barrier_and(2, 128, mine);
-            if (!ok) break;
+            if (!named_barrier_and(2, 128, mine)) return false;
             const float qm = fmaxf(fmaxf(qred[qb * 4], qred[qb * 4 + 1]), fmaxf(qred[qb * 4 + 2], qred[qb * 4 + 3]));
             int e = 0;
             if (qm > 0.f) {
@@ -861,9 +863,25 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             }
 #pragma unroll
             for (int g = 0; g < G; ++g) *reinterpret_cast<__half *>(qt + qoff(g)) = __float2half_rn(ldexpf(x[g], -e));
-            if (r == 0) qexp[nu & 7] = e; // read by the softmax after q_ready
-            fence_proxy_async_smem();    // Q is read by the MMA
-            mbar_arrive(q_ready + (nu & 7));
+            if (r == 0) qexp[n & 7] = e; // read by the softmax after q_ready
+            fence_proxy_async_smem();   // Q is read by the MMA
+            mbar_arrive(q_ready + (n & 7));
+            return true;
+        };
+        // unit 0's q first; each later unit's as soon as the previous unit's last K tile is widened,
+        // so that its first S^T does not wait for the previous unit's last V tile
+        bool ok = (int)blockIdx.x < U ? convert_q(0, *abort_flag == 0) : true;
+        int64_t gs = 0;
+        int nu = 0;
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
+            Unit un;
+            int te;
+            float ks;
+            if (!read_rec(nu, un, te, ks)) {
+                ok = false;
+                break;
+            }
+            const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
             // ---- the unit's K and V stages
             for (int i = 0; i < nsteps && ok; ++i) {
                 const int64_t g = gs + i;
@@ -873,6 +891,10 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 widen_row(smem + LY::K0 + st * LY::STAGE);
                 fence_proxy_async_smem();
                 mbar_arrive(k_full + st);
+                if (i + 1 == nsteps && u + (int)gridDim.x < U) {
+                    ok = convert_q(nu + 1, *abort_flag == 0);
+                    if (!ok) break;
+                }
                 ok = __all_sync(0xffffffffu, mbar_wait_sleep(v8_full + st, (g / NS) & 1));
                 if (!ok) break;
                 widen_row(smem + LY::V0 + st * LY::STAGE);

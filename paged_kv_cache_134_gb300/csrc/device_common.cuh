@@ -158,6 +158,20 @@ PKV_DEV bool named_barrier_and(uint32_t id, uint32_t nthreads, bool v) {
     return r != 0;
 }
 
+// The same barrier reducing with OR: true on every thread if any of the nthreads passed true.
+PKV_DEV bool named_barrier_or(uint32_t id, uint32_t nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // ------------------------------------------------------------------ math
 
 PKV_DEV float fast_exp2(float x) {
