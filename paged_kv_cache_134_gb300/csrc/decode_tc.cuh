@@ -119,7 +119,7 @@ PKV_DEV int find_row_warp(const int *pref, int n, int k, int lane) {
     return lo;
 }
 
-PKV_DEV Unit unit_info_warp(int u, const int *pf, const int *pp, const int *nb, int S, int hkv, int bps, int sb,
+static __device__ __noinline__ Unit unit_info_warp(int u, const int *pf, const int *pp, const int *nb, int S, int hkv, int bps, int sb,
                             int lane) {
     Unit r;
     const int nfull_units = pf[S] * hkv;
@@ -140,6 +140,14 @@ PKV_DEV Unit unit_info_warp(int u, const int *pf, const int *pp, const int *nb, 
     }
     r.nsplit = (pf[r.s + 1] - pf[r.s]) + (pp[r.s + 1] - pp[r.s]);
     return r;
+}
+
+// wait (bounded) until a unit record's tag reads n
+static __device__ __noinline__ bool wait_tag(const volatile int *tag, int n) {
+    const uint64_t t0 = global_timer_ns();
+    while (*tag != n)
+        if (global_timer_ns() - t0 > PKV_WAIT_LIMIT_NS) return false;
+    return true;
 }
 
 // byte offset of element (row g, token t) in a P buffer of NPR rows: K-major, 128-byte swizzle,
@@ -266,16 +274,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
     auto read_rec = [&](int n, Unit &x, int &tok_end, float &ks) -> bool {
         const UnitRec *r = ring + (n % kUnitRing);
         const volatile int *tag = &r->tag;
-        bool okr = true;
-        if (*tag != n) {
-            const uint64_t t0 = global_timer_ns();
-            while (*tag != n)
-                if (global_timer_ns() - t0 > PKV_WAIT_LIMIT_NS) {
-                    okr = false;
-                    break;
-                }
-        }
-        okr = __all_sync(0xffffffffu, okr);
+        const bool okr = __all_sync(0xffffffffu, *tag == n || wait_tag(tag, n));
         __threadfence_block();
         x.s = r->s;
         x.kvh = r->kvh;
@@ -454,8 +453,13 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             constexpr uint32_t ab = OT == PKV_BF16 ? 1u : 0u;
             constexpr uint32_t ISK = tc::idesc_f16_ab(ab, 0u, 0u, TOK, NQ); // A = K (K-major), B = Q (K-major)
             constexpr uint32_t IPV = tc::idesc_f16_ab(ab, 1u, 0u, D, LY::NPR); // A = V^T (MN-major), B = P (K-major)
-            const uint32_t sK = smem_u32(smem + LY::K0), sV = smem_u32(smem + LY::V0);
-            const uint32_t sQ = smem_u32(smem + LY::Q), sP = smem_u32(smem + LY::P);
+            // one descriptor per operand layout; the address field counts 16-byte units, so a tile at
+            // byte offset `off` from the base is the base descriptor plus off / 16 (shared memory stays
+            // below the field's 256 KB): each MMA adds a constant instead of rebuilding its descriptors
+            const uint64_t dK = tc::smem_desc(smem_u32(smem + LY::K0), 16, 1024);
+            const uint64_t dQ = tc::smem_desc(smem_u32(smem + LY::Q), 16, 1024);
+            const uint64_t dV = tc::smem_desc(smem_u32(smem + LY::V0), TOK * 128, 1024);
+            const uint64_t dP = tc::smem_desc(smem_u32(smem + LY::P), 16, 1024);
             bool any_mma = false;
             // S^T of step g (Q buffer qb) into S buffer g % 2; the K stage is released as soon as S^T is done
             auto issue_s = [&](int64_t g, int qb) -> bool {
@@ -464,12 +468,12 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait_sleep(s_free + b, ((g >> 1) - 1) & 1))) return false;
                 tc::fence_after_sync();
                 any_mma = true;
+                const uint64_t a0 = dK + (uint64_t)((st * LY::STAGE) >> 4), b0 = dQ + (uint64_t)((qb * LY::Q_BYTES) >> 4);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const int c = k >> 2, kk = k & 3;
-                    const uint64_t ad = tc::smem_desc(sK + st * LY::STAGE + c * (TOK * 128) + kk * 32, 16, 1024);
-                    const uint64_t bd = tc::smem_desc(sQ + qb * LY::Q_BYTES + c * (NQ * 128) + kk * 32, 16, 1024);
-                    tc::mma_f16_warp(tmem + b * NQ, ad, bd, ISK, k > 0 ? 1u : 0u);
+                    tc::mma_f16_warp(tmem + b * NQ, a0 + (uint64_t)((c * (TOK * 128) + kk * 32) >> 4),
+                                     b0 + (uint64_t)((c * (NQ * 128) + kk * 32) >> 4), ISK, k > 0 ? 1u : 0u);
                 }
                 tc::commit_warp(s_full + b);
                 tc::commit_warp(k_empty + st);
@@ -495,18 +499,21 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 ahead = false;
                 for (int i = 0; i < nsteps && ok; ++i) {
                     const int64_t g = gs + i;
-                    if (i + 1 < nsteps) {
-                        ok = issue_s(g + 1, qb);
-                        if (!ok) break;
-                    } else {
+                    // the next S^T (Q buffer qn) goes out before this step's P V
+                    int qn = qb;
+                    if (i + 1 == nsteps) {
                         tc::commit_warp(q_empty + qb); // the unit's last S^T has been issued: its Q buffer may be refilled
                         // the next unit's first S^T goes ahead of this P V when its Q is already in place, so
                         // the softmax warps find it ready when they start that unit
+                        qn = -1;
                         if (u + (int)gridDim.x < U && __all_sync(0xffffffffu, mbar_test_wait(q_bar(nu + 1), q_par(nu + 1)))) {
-                            ok = issue_s(g + 1, (nu + 1) & 1);
-                            if (!ok) break;
+                            qn = (nu + 1) & 1;
                             ahead = true;
                         }
+                    }
+                    if (qn >= 0) {
+                        ok = issue_s(g + 1, qn);
+                        if (!ok) break;
                     }
                     const int st = (int)(g % NS), b = (int)(g & 1);
                     ok = __all_sync(0xffffffffu, mbar_wait_sleep(p_full + b, (g >> 1) & 1) && mbar_wait_sleep(v_full + st, (g / NS) & 1));
@@ -516,13 +523,12 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                     if (!ok) break;
                     const uint32_t tO = tmem + 2 * NQ + (uint32_t)((nu & 1) * 32);
                     tc::fence_after_sync();
+                    const uint64_t a0 = dV + (uint64_t)((st * LY::STAGE) >> 4), b0 = dP + (uint64_t)((b * LY::P_BYTES) >> 4);
 #pragma unroll
-                    for (int k = 0; k < TOK / 16; ++k) {
-                        const uint64_t ad = tc::smem_desc(sV + st * LY::STAGE + k * 2048, TOK * 128, 1024);
-                        const uint64_t bd = tc::smem_desc(
-                            sP + b * LY::P_BYTES + (k >> 2) * (LY::NPR * 128) + (k & 3) * 32, 16, 1024);
-                        tc::mma_f16_warp(tO, ad, bd, IPV, (i > 0 || k > 0) ? 1u : 0u);
-                    }
+                    for (int k = 0; k < TOK / 16; ++k)
+                        tc::mma_f16_warp(tO, a0 + (uint64_t)((k * 2048) >> 4),
+                                         b0 + (uint64_t)(((k >> 2) * (LY::NPR * 128) + (k & 3) * 32) >> 4), IPV,
+                                         (i > 0 || k > 0) ? 1u : 0u);
                     tc::commit_warp(t_full + b);
                     tc::commit_warp(v_empty + st);
                     if (i + 1 == nsteps) tc::commit_warp(o_full + (nu & 1));

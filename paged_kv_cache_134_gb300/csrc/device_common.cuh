@@ -95,21 +95,32 @@ PKV_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) {
 
 // The same bounded wait with a suspend-time hint: a warp whose phase has not completed sleeps in
 // the barrier until it completes (or the hint runs out) instead of re-testing it, which leaves the
-// shared-memory pipe to the warps doing the work in kernels where many warps wait at once.
-PKV_DEV bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
+// shared-memory pipe to the warps doing the work in kernels where many warps wait at once.  The
+// first test is inline; the loop that keeps time for the wait limit is one out-of-line copy, so
+// that the many wait sites of a large kernel stay small in the instruction cache.
+PKV_DEV bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+
+static __device__ __noinline__ bool mbar_wait_sleep_slow(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
-            : "memory");
-        if (ok) return true;
+        if (mbar_try_wait_sleep(bar, parity)) return true;
         if (global_timer_ns() - t0 > PKV_WAIT_LIMIT_NS) return false;
     }
+}
+
+PKV_DEV bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
+    const uint32_t b = smem_u32(bar);
+    return mbar_try_wait_sleep(b, parity) || mbar_wait_sleep_slow(b, parity);
 }
 
 // ------------------------------------------------------------------ bulk async copy (1-D TMA)
