@@ -54,64 +54,97 @@ struct AppendArgs {
 // MODE: 0 = slots given, 1 = slot from (table, sequence id, position) per token, 2 = sequence and
 // position from packed ranges (cu_seqlens, context lengths), then the slot as in mode 1
 enum { SLOTS_GIVEN = 0, SLOTS_AT = 1, SLOTS_RANGES = 2 };
+constexpr int kAppendThreads = 256;
+constexpr int kAppendUnroll = 4; // chunks a thread loads before it stores any
+
+// The slot of token j (mode-specific), or -1 for "skip".
+template <int MODE>
+PKV_DEV int64_t append_slot(const AppendArgs &a, int64_t j) {
+    if constexpr (MODE == SLOTS_AT) {
+        return slot_of(a.tables, a.rows, a.max_blocks, a.seq_ids[j], a.positions[j], a.bs);
+    } else if constexpr (MODE == SLOTS_RANGES) {
+        // sequence: the largest i with cu[i] <= j (a.rows = number of sequences)
+        int lo = 0, hi = a.rows;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (a.cu[mid] <= j)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int64_t st = a.cu[lo], en = a.cu[lo + 1];
+        const int64_t pos = (int64_t)a.ctx[lo] + (j - st);
+        return (j >= st && j < en && a.ctx[lo] >= 0 && pos <= 0x7FFFFFFF)
+                   ? slot_of(a.tables, a.rows, a.max_blocks, lo, (int)pos, a.bs)
+                   : -1;
+    } else {
+        return a.slots[j];
+    }
+}
+
+// Token-major: a pass of the CTA covers whole tokens, tpg = max(1, threads / chunks per token) of
+// them, so a token's slot is found once per thread rather than once per 16-byte chunk, and each
+// thread issues the loads of up to kAppendUnroll chunks before it stores any of them.
 template <int KVT, int MT, int MODE>
-__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
     pdl_trigger();
     pdl_wait();
-    const int64_t per_token = 2LL * a.hkv * a.chunks_per_row;
-    const int64_t total = a.n * per_token;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t j = i / per_token;
-        const int rem = static_cast<int>(i - j * per_token);
-        const int kv = rem / (a.hkv * a.chunks_per_row);
-        const int hc = rem - kv * a.hkv * a.chunks_per_row;
-        const int h = hc / a.chunks_per_row;
-        const int c = hc - h * a.chunks_per_row;
-        int64_t slot;
-        if constexpr (MODE == SLOTS_AT) {
-            slot = slot_of(a.tables, a.rows, a.max_blocks, a.seq_ids[j], a.positions[j], a.bs);
-            if (rem == 0 && a.slots_out) a.slots_out[j] = slot;
-        } else if constexpr (MODE == SLOTS_RANGES) {
-            // sequence: the largest i with cu[i] <= j (a.rows = number of sequences)
-            int lo = 0, hi = a.rows;
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (a.cu[mid] <= j)
-                    lo = mid;
-                else
-                    hi = mid;
-            }
-            const int64_t st = a.cu[lo], en = a.cu[lo + 1];
-            const int64_t pos = (int64_t)a.ctx[lo] + (j - st);
-            slot = (j >= st && j < en && a.ctx[lo] >= 0 && pos <= 0x7FFFFFFF)
-                       ? slot_of(a.tables, a.rows, a.max_blocks, lo, (int)pos, a.bs)
-                       : -1;
-            if (rem == 0 && a.slots_out) a.slots_out[j] = slot;
-        } else {
-            slot = a.slots[j];
-        }
+    const int row_chunks = a.hkv * a.chunks_per_row; // one (token, K|V) row over all heads
+    const int per_token = 2 * row_chunks;
+    const int tpg = per_token >= kAppendThreads ? 1 : kAppendThreads / per_token;
+    const int lt = tpg > 1 ? (int)threadIdx.x / per_token : 0; // this thread's token in the pass
+    const int r0 = tpg > 1 ? (int)threadIdx.x - lt * per_token : (int)threadIdx.x;
+    const int rstep = tpg > 1 ? per_token : kAppendThreads;
+    if (lt >= tpg) return; // threads past the last whole token of a pass
+    for (int64_t j = (int64_t)blockIdx.x * tpg + lt; j < a.n; j += (int64_t)gridDim.x * tpg) {
+        const int64_t slot = append_slot<MODE>(a, j);
+        if (MODE != SLOTS_GIVEN && r0 == 0 && a.slots_out) a.slots_out[j] = slot;
         if (slot < 0) continue;
         if (slot >= a.num_slots) {
-            if (rem == 0) set_error(a.err, PKV_DEVERR_SLOT);
+            if (r0 == 0) set_error(a.err, PKV_DEVERR_SLOT);
             continue;
         }
         const int64_t blk = slot / a.bs;
         const int off = static_cast<int>(slot - blk * a.bs);
-        // element index of (blk, kv, h, off, c*8) in the [NB][2][Hkv][bs][D] pool
-        const int64_t e = ((blk * 2 + kv) * a.hkv + h) * a.tile_elems + (int64_t)off * a.d + c * 8;
-        const uint4 src = (kv ? a.v : a.k)[j * a.hkv * a.chunks_per_row + hc];
-        if constexpr (KVT != PKV_FP8_E4M3) {
-            reinterpret_cast<uint4 *>(a.pool)[e / 8] = src;
-        } else {
-            float f[8];
-            cvt8<MT>(src, f);
-            const float s = (kv ? a.v_scale : a.k_scale)[h];
-            uint2 o;
-            o.x = e4m3x2_from_f32(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
-                  (e4m3x2_from_f32(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
-            o.y = e4m3x2_from_f32(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s)) |
-                  (e4m3x2_from_f32(__fdiv_rn(f[6], s), __fdiv_rn(f[7], s)) << 16);
-            reinterpret_cast<uint2 *>(a.pool)[e / 8] = o;
+        // element index of (blk, kv = 0, h = 0, off, 0) in the [NB][2][Hkv][bs][D] pool
+        const int64_t e0 = blk * 2 * a.hkv * a.tile_elems + (int64_t)off * a.d;
+        const uint4 *ksrc = a.k + j * row_chunks, *vsrc = a.v + j * row_chunks;
+        for (int rb = r0; rb < per_token; rb += kAppendUnroll * rstep) {
+            uint4 src[kAppendUnroll];
+            int64_t dst[kAppendUnroll];
+            int kvs[kAppendUnroll], hs[kAppendUnroll];
+#pragma unroll
+            for (int u = 0; u < kAppendUnroll; ++u) {
+                const int r = rb + u * rstep;
+                dst[u] = -1;
+                if (r < per_token) {
+                    const int kv = r >= row_chunks ? 1 : 0;
+                    const int hc = r - kv * row_chunks;
+                    const int h = hc / a.chunks_per_row;
+                    const int c = hc - h * a.chunks_per_row;
+                    src[u] = (kv ? vsrc : ksrc)[hc];
+                    dst[u] = e0 + (int64_t)(kv * a.hkv + h) * a.tile_elems + c * 8;
+                    kvs[u] = kv;
+                    hs[u] = h;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kAppendUnroll; ++u) {
+                if (dst[u] < 0) continue;
+                if constexpr (KVT != PKV_FP8_E4M3) {
+                    reinterpret_cast<uint4 *>(a.pool)[dst[u] / 8] = src[u];
+                } else {
+                    float f[8];
+                    cvt8<MT>(src[u], f);
+                    const float sc = (kvs[u] ? a.v_scale : a.k_scale)[hs[u]];
+                    uint2 o;
+                    o.x = e4m3x2_from_f32(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)) |
+                          (e4m3x2_from_f32(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc)) << 16);
+                    o.y = e4m3x2_from_f32(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc)) |
+                          (e4m3x2_from_f32(__fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc)) << 16);
+                    reinterpret_cast<uint2 *>(a.pool)[dst[u] / 8] = o;
+                }
+            }
         }
     }
 }
@@ -142,16 +175,20 @@ AppendArgs base_args(pkv_cache *c, const void *k, const void *v, int64_t n) {
 
 template <int MODE>
 cudaError_t launch_append_t(pkv_cache *c, const AppendArgs &a, cudaStream_t st) {
-    const int64_t work = a.n * 2 * a.hkv * a.chunks_per_row;
-    const dim3 grid(grid_for(work, 256, c->num_sms));
+    // one CTA pass per tpg tokens (see append_kernel), up to 8 resident CTAs per SM
+    const int per_token = 2 * a.hkv * a.chunks_per_row;
+    const int tpg = per_token >= kAppendThreads ? 1 : kAppendThreads / per_token;
+    const int64_t passes = (a.n + tpg - 1) / tpg;
+    const int64_t cap = (int64_t)c->num_sms * 8;
+    const dim3 grid((unsigned)(passes < 1 ? 1 : (passes > cap ? cap : passes)));
     PkvTimer timer(c, PKV_KIND_APPEND, st);
     cudaError_t e;
     if (c->kv_dtype != PKV_FP8_E4M3)
-        e = pdl_launch(append_kernel<PKV_F16, PKV_F16, MODE>, grid, dim3(256), 0, st, a);
+        e = pdl_launch(append_kernel<PKV_F16, PKV_F16, MODE>, grid, dim3(kAppendThreads), 0, st, a);
     else if (c->model_dtype == PKV_F16)
-        e = pdl_launch(append_kernel<PKV_FP8_E4M3, PKV_F16, MODE>, grid, dim3(256), 0, st, a);
+        e = pdl_launch(append_kernel<PKV_FP8_E4M3, PKV_F16, MODE>, grid, dim3(kAppendThreads), 0, st, a);
     else
-        e = pdl_launch(append_kernel<PKV_FP8_E4M3, PKV_BF16, MODE>, grid, dim3(256), 0, st, a);
+        e = pdl_launch(append_kernel<PKV_FP8_E4M3, PKV_BF16, MODE>, grid, dim3(kAppendThreads), 0, st, a);
     g_pkv_launches++;
     return e;
 }
