@@ -548,23 +548,29 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
         {
             constexpr uint32_t IQK = tc::idesc_f16(MT == PKV_BF16 ? 1u : 0u, 0u, BM, BN);
             constexpr uint32_t IPV = tc::idesc_f16(MT == PKV_BF16 ? 1u : 0u, 1u, BM, D);
-            const uint32_t sQ = smem_u32(smem + L::Q), sK = smem_u32(smem + L::K0), sV = smem_u32(smem + L::V0);
             const uint32_t tO = tmem + 2 * BN;
+            // one descriptor per operand layout; the address field counts 16-byte units, so a tile at
+            // byte offset `off` from the base is the base descriptor plus off / 16 (shared memory stays
+            // below the field's 256 KB): each MMA adds a constant instead of rebuilding its descriptors
+            const uint64_t dQ = tc::smem_desc(smem_u32(smem + L::Q), 16, 1024);
+            const uint64_t dK = tc::smem_desc(smem_u32(smem + L::K0), 16, 1024);
+            const uint64_t dV = tc::smem_desc(smem_u32(smem + L::V0), BN * 128, 1024);
             bool any_mma = false;
             // S of global tile gg = Q K^T, once the softmax has read S of tile gg - 1 out of the single
             // S buffer; the K stage is released as soon as S is done
             auto issue_s = [&](int64_t gg) -> bool {
                 const int st = (int)(gg % NKS);
-                if (!__all_sync(0xffffffffu, mbar_wait(k_full + st, (gg / NKS) & 1))) return false;
-                if (gg >= 1 && !__all_sync(0xffffffffu, mbar_wait(s_free, (gg - 1) & 1))) return false;
+                if (!__all_sync(0xffffffffu, mbar_wait(k_full + st, (gg / NKS) & 1) &&
+                                                 (gg < 1 || mbar_wait(s_free, (gg - 1) & 1))))
+                    return false;
                 tc::fence_after_sync();
                 any_mma = true;
+                const uint64_t b0 = dK + (uint64_t)((st * L::KV_BYTES) >> 4);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const int c = k >> 2, kk = k & 3;
-                    const uint64_t ad = tc::smem_desc(sQ + c * BM * 128 + kk * 32, 16, 1024);
-                    const uint64_t bd = tc::smem_desc(sK + st * L::KV_BYTES + c * BN * 128 + kk * 32, 16, 1024);
-                    tc::mma_f16_warp(tmem, ad, bd, IQK, k > 0 ? 1u : 0u);
+                    tc::mma_f16_warp(tmem, dQ + (uint64_t)((c * BM * 128 + kk * 32) >> 4),
+                                     b0 + (uint64_t)((c * BN * 128 + kk * 32) >> 4), IQK, k > 0 ? 1u : 0u);
                 }
                 tc::commit_warp(s_full);
                 tc::commit_warp(k_empty + st);
@@ -592,14 +598,14 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                     if (!ok) break;
                     tc::fence_after_sync();
                     // O += P V, P (A operand) read from tensor memory where the softmax left it
+                    const uint32_t a0 = tmem + (uint32_t)(BN + (int)(gg % L::NPB) * (BN / 2));
+                    const uint64_t b0 = dV + (uint64_t)((sv * L::KV_BYTES) >> 4);
 #pragma unroll
                     for (int part = 0; part < L::NP; ++part)
 #pragma unroll
-                        for (int k = 0; k < BN / 16; ++k) {
-                            const uint32_t at = tmem + (uint32_t)(BN + (int)(gg % L::NPB) * (BN / 2) + part * (BN / 2) + k * 8);
-                            const uint64_t bd = tc::smem_desc(sV + sv * L::KV_BYTES + k * 2048, BN * 128, 1024);
-                            tc::mma_f16_ts_warp(tO, at, bd, IPV, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
-                        }
+                        for (int k = 0; k < BN / 16; ++k)
+                            tc::mma_f16_ts_warp(tO, a0 + (uint32_t)(part * (BN / 2) + k * 8), b0 + (uint64_t)((k * 2048) >> 4),
+                                                IPV, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
                     tc::commit_warp(t_full + (gg & 1));
                     tc::commit_warp(v_empty + sv);
                 }
