@@ -48,7 +48,7 @@ template <bool F8>
 __host__ __device__ constexpr int threads_for() {
     return F8 ? 480 : 352;
 }
-constexpr uint32_t kTmemCols = 128;  // S0 [0,16) S1 [16,32) O^T of even units [32,64), of odd units [64,96)
+constexpr uint32_t kTmemCols = 128;  // two S^T buffers, then O^T of even and odd units (see NSC, OB)
 constexpr float kRescale = 8.0f;     // log2 units
 constexpr int kUnitRing = 16;        // unit records published by the K loader (see UnitRec)
 
@@ -161,13 +161,17 @@ PKV_DEV int p_offset(int g, int t) {
 template <int G, int MT, int KVT>
 __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tq, const Args a) {
-    // FP8 caches: the MMAs run on fp16 operands (K and V widened exactly from E4M3, q converted
-    // with a power-of-two scale, P in fp16); the per-head K and V scales fold into the softmax
-    // scale and the epilogue
+    // FP8 caches: S^T = K q^T is an E4M3 x E4M3 MMA (K as stored, q as three E4M3 terms with a
+    // power-of-two scale); P V runs on fp16 operands (V widened exactly from E4M3, P in fp16); the
+    // per-head K and V scales fold into the softmax scale and the epilogue
     constexpr bool F8 = KVT == PKV_FP8_E4M3;
     constexpr int OT = F8 ? (int)PKV_F16 : MT; // operand dtype of the MMAs
     constexpr int kThreads = threads_for<F8>();
     using LY = Layout<OT>;
+    // tensor-memory columns: two S^T buffers of NSC columns (FP8: q as three E4M3 terms of 8 heads
+    // each, N = 32), then O^T of even units at OB and of odd units at OB + 32
+    constexpr int NSC = F8 ? 32 : NQ;
+    constexpr uint32_t OB = 2 * NSC;
     using M = ModelT<MT>;
     using T = typename M::T;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -185,10 +189,10 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
     // FP8 caches: the exponent of unit nu's q scale in slot nu % 8, published with "Q converted"
     // (q_ready, a ring of 8: unit nu + 8's Q cannot be loaded before the softmax has read the scores
     // of unit nu + 4, so the MMA and the softmax, which wait for unit nu, never see a later phase),
-    // the converters' partial maxima, and "E4M3 tile landed" (k8/v8_full, before the widening)
+    // the converters' partial maxima, and "E4M3 V tile landed" (v8_full, before the widening)
     volatile int *qexp = reinterpret_cast<volatile int *>(fin + 5);              // [8]
     volatile float *qred = reinterpret_cast<volatile float *>(fin + 9);          // [2 unit parities][4 warps]
-    uint64_t *k8_full = fin + 13, *v8_full = fin + 13 + NS, *q_ready = fin + 13 + 2 * NS; // q_ready [8]
+    uint64_t *v8_full = fin + 13 + NS, *q_ready = fin + 13 + 2 * NS; // q_ready [8]
     float *red_max = reinterpret_cast<float *>(smem + LY::RED);                  // [2][4][NQ]
     float *red_sum = red_max + 2 * 4 * NQ;                                      // [2][4][NQ]
     float *m_base = red_sum + 2 * 4 * NQ;                                       // [2][NQ]
@@ -199,14 +203,11 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(k_full + i, F8 ? 128 : 1); // FP8: the 128 converter threads, else the TMA arrival
+            mbar_init(k_full + i, 1);             // the TMA arrival (E4M3 K is read by the MMA as is)
             mbar_init(k_empty + i, 1);
             mbar_init(v_full + i, F8 ? 128 : 1);
             mbar_init(v_empty + i, 1);
-            if constexpr (F8) {
-                mbar_init(k8_full + i, 1);
-                mbar_init(v8_full + i, 1);
-            }
+            if constexpr (F8) mbar_init(v8_full + i, 1);
         }
         if constexpr (F8)
             for (int b = 0; b < 8; ++b) mbar_init(q_ready + b, 128);
@@ -389,9 +390,9 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             const unsigned goodmask = __ballot_sync(0xffffffffu, good);
             const unsigned bad = __ballot_sync(0xffffffffu, lane < nblk && !good);
             const uint32_t bytes = (uint32_t)__popc(goodmask) * (uint32_t)a.bs * (uint32_t)(F8 ? D : D * 2);
-            // FP8: the E4M3 tiles land in the upper half of the stage (k8/v8_full); the converters widen
-            // them in place and arrive on k/v_full
-            uint64_t *full = F8 ? (is_k ? k8_full + st : v8_full + st) : (is_k ? k_full + st : v_full + st);
+            // FP8: the E4M3 K tile lands as it is (the MMA reads E4M3); the E4M3 V tile lands in the
+            // upper half of the stage (v8_full) and the converters widen it in place, then arrive on v_full
+            uint64_t *full = is_k ? k_full + st : (F8 ? v8_full + st : v_full + st);
             uint64_t *empty = is_k ? k_empty + st : v_empty + st;
             if (lane == 0) {
                 if (round >= 1 && !mbar_wait_sleep(empty, (round - 1) & 1)) ok = false;
@@ -406,10 +407,13 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             const int row = ((b * 2 + (is_k ? 0 : 1)) * a.hkv + un.kvh) * a.bs;
             uint8_t *dst0 = smem + (is_k ? LY::K0 : LY::V0) + st * LY::STAGE + lane * a.bs * 128;
             if (good) {
-                if constexpr (F8) {
-                    // one (block, K|V, head) tile of bs rows x 128 one-byte dims is contiguous in the pool
+                if (F8 && is_k) {
+                    // the block's bs rows of 128 E4M3 codes, 128-byte swizzled: the MMA's K-major layout
+                    tc::tma_load_2d_hint(dst0, &tkv, 0, row, full, policy);
+                } else if constexpr (F8) {
+                    // one (block, V, head) tile of bs rows x 128 one-byte dims is contiguous in the pool
                     const char *src = a.pool + (int64_t)row / a.bs * a.tile_bytes;
-                    bulk_g2s_hint(smem + (is_k ? LY::K0 : LY::V0) + st * LY::STAGE + TOK * 128 + lane * a.bs * 128, src,
+                    bulk_g2s_hint(smem + LY::V0 + st * LY::STAGE + TOK * 128 + lane * a.bs * 128, src,
                                   (uint32_t)a.tile_bytes, full, policy);
                 } else {
 #pragma unroll
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         // the copies of the last stages must land before this CTA's shared memory goes away
         if (lane == 0) {
             for (int64_t g = gs > NS ? gs - NS : 0; g < gs; ++g)
-                if (!mbar_wait_sleep((F8 ? (is_k ? k8_full : v8_full) : (is_k ? k_full : v_full)) + g % NS, (g / NS) & 1))
+                if (!mbar_wait_sleep((is_k ? k_full : (F8 ? v8_full : v_full)) + g % NS, (g / NS) & 1))
                     set_error(a.err, PKV_DEVERR_TIMEOUT);
             const int last_q = q_next - 1;
             if (is_k)
@@ -451,7 +455,8 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         // issues each MMA and commit
         {
             constexpr uint32_t ab = OT == PKV_BF16 ? 1u : 0u;
-            constexpr uint32_t ISK = tc::idesc_f16_ab(ab, 0u, 0u, TOK, NQ); // A = K (K-major), B = Q (K-major)
+            // A = K (K-major), B = Q (K-major); FP8: E4M3 x E4M3 (type fields 0) with N = 32
+            constexpr uint32_t ISK = tc::idesc_f16_ab(F8 ? 0u : ab, 0u, 0u, TOK, NSC);
             constexpr uint32_t IPV = tc::idesc_f16_ab(ab, 1u, 0u, D, LY::NPR); // A = V^T (MN-major), B = P (K-major)
             // one descriptor per operand layout; the address field counts 16-byte units, so a tile at
             // byte offset `off` from the base is the base descriptor plus off / 16 (shared memory stays
@@ -469,11 +474,19 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 tc::fence_after_sync();
                 any_mma = true;
                 const uint64_t a0 = dK + (uint64_t)((st * LY::STAGE) >> 4), b0 = dQ + (uint64_t)((qb * LY::Q_BYTES) >> 4);
+                if constexpr (F8) {
+                    // E4M3 K rows of 128 codes (one swizzle row each) against the q terms, 32 codes a step
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const int c = k >> 2, kk = k & 3;
-                    tc::mma_f16_warp(tmem + b * NQ, a0 + (uint64_t)((c * (TOK * 128) + kk * 32) >> 4),
-                                     b0 + (uint64_t)((c * (NQ * 128) + kk * 32) >> 4), ISK, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < D / 32; ++k)
+                        tc::mma_f8_warp(tmem + b * NSC, a0 + (uint64_t)((k * 32) >> 4), b0 + (uint64_t)((k * 32) >> 4), ISK,
+                                        k > 0 ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const int c = k >> 2, kk = k & 3;
+                        tc::mma_f16_warp(tmem + b * NSC, a0 + (uint64_t)((c * (TOK * 128) + kk * 32) >> 4),
+                                         b0 + (uint64_t)((c * (NQ * 128) + kk * 32) >> 4), ISK, k > 0 ? 1u : 0u);
+                    }
                 }
                 tc::commit_warp(s_full + b);
                 tc::commit_warp(k_empty + st);
@@ -521,7 +534,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                     if (ok && i == 0 && nu >= 2)
                         ok = __all_sync(0xffffffffu, mbar_wait_sleep(o_free + (nu & 1), ((nu >> 1) - 1) & 1));
                     if (!ok) break;
-                    const uint32_t tO = tmem + 2 * NQ + (uint32_t)((nu & 1) * 32);
+                    const uint32_t tO = tmem + OB + (uint32_t)((nu & 1) * 32);
                     tc::fence_after_sync();
                     const uint64_t a0 = dV + (uint64_t)((st * LY::STAGE) >> 4), b0 = dP + (uint64_t)((b * LY::P_BYTES) >> 4);
 #pragma unroll
@@ -609,7 +622,17 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 if (mine) {
                     tc::fence_after_sync();
                     uint32_t sr[G];
-                    tc::ldn<G>(tmem + lane_off + b * NQ, sr);
+                    tc::ldn<G>(tmem + lane_off + b * NSC, sr);
+                    if constexpr (F8) {
+                        // S^T of the three E4M3 terms of q (columns 0, 8, 16 of the buffer)
+                        uint32_t s1[G], s2[G];
+                        tc::ldn<G>(tmem + lane_off + b * NSC + 8, s1);
+                        tc::ldn<G>(tmem + lane_off + b * NSC + 16, s2);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int g = 0; g < G; ++g)
+                            sr[g] = __float_as_uint((__uint_as_float(sr[g]) + __uint_as_float(s1[g])) + __uint_as_float(s2[g]));
+                    }
                     tc::wait_ld();
                     tc::fence_before_sync();
                     mbar_arrive(s_free + b);
@@ -671,11 +694,11 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
 #pragma unroll
                         for (int part = 0; part < LY::NP; ++part) {
                             uint32_t o[G];
-                            tc::ldn<G>(tmem + lane_off + 2 * NQ + (nu & 1) * 32 + part * NQ, o);
+                            tc::ldn<G>(tmem + lane_off + OB + (nu & 1) * 32 + part * NQ, o);
                             tc::wait_ld();
 #pragma unroll
                             for (int g = 0; g < G; ++g) o[g] = __float_as_uint(__uint_as_float(o[g]) * alpha[g]);
-                            tc::stn<G>(tmem + lane_off + 2 * NQ + (nu & 1) * 32 + part * NQ, o);
+                            tc::stn<G>(tmem + lane_off + OB + (nu & 1) * 32 + part * NQ, o);
                         }
                         tc::wait_st();
                     }
@@ -764,10 +787,10 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             if (!ok) break;
             tc::fence_after_sync();
             uint32_t o[G];
-            tc::ldn<G>(tmem + lane_off + 2 * NQ + eb * 32, o);
+            tc::ldn<G>(tmem + lane_off + OB + eb * 32, o);
             if constexpr (LY::NP == 2) {
                 uint32_t o2[G];
-                tc::ldn<G>(tmem + lane_off + 3 * NQ + eb * 32, o2);
+                tc::ldn<G>(tmem + lane_off + OB + NQ + eb * 32, o2);
                 tc::wait_ld();
 #pragma unroll
                 for (int g = 0; g < G; ++g) o[g] = __float_as_uint(__uint_as_float(o[g]) + __uint_as_float(o2[g]));
@@ -807,11 +830,12 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         }
         if (!ok && lane == 0) fail();
     } else if constexpr (F8) {
-        // ---------------------------------------------------------------- E4M3 -> fp16 (warps 11-14)
-        // Thread r owns row r of every K and V stage (token r of the step) and dimension r of Q.
-        // A stage's E4M3 tile (128 rows of 128 bytes) sits in the stage's upper half; row r is read
-        // into registers whole before its two fp16 halves are written (the second one over the
-        // E4M3 row itself), so the widening runs in place.  E4M3 values are exact in fp16.
+        // ---------------------------------------------------------------- E4M3 V -> fp16, q -> E4M3 (warps 11-14)
+        // Thread r owns row r of every V stage (token r of the step) and dimension r of q.  A V
+        // stage's E4M3 tile (128 rows of 128 bytes) sits in the stage's upper half; row r is read into
+        // registers whole before its two fp16 halves are written (the second one over the E4M3 row
+        // itself), so the widening runs in place.  E4M3 values are exact in fp16.  K stays E4M3: the
+        // S^T MMA reads it as it landed.
         const int cw = warp - 11, r = cw * 32 + lane;
         auto widen_row = [&](uint8_t *stage) {
             const uint8_t *src = stage + TOK * 128 + r * 128;
@@ -835,13 +859,22 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 *reinterpret_cast<uint4 *>(row + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
             }
         };
-        // byte offset of (head g, dimension r) in a K-major, 128-byte-swizzled Q tile
+        // byte offset of (head g, dimension r) in the loaded Q tile (model dtype, K-major, 128-byte swizzle)
         auto qoff = [&](int g) {
             const int e = r & 63;
             return (r >> 6) * (NQ * 128) + g * 128 + (((e >> 3) ^ (g & 7)) << 4) + (e & 7) * 2;
         };
-        // q of this CTA's n-th unit in fp16, scaled by 2^-e so that its largest magnitude lies in
-        // [2^14, 2^15); false, agreed by the four warps at their barrier, after a failed wait
+        auto e4m3_value = [](uint32_t code) -> float {
+            uint32_t h2;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)code));
+            return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+        };
+        // q of this CTA's n-th unit as three E4M3 terms, q = 2^e (t0 + t1 + t2): the largest |q| is
+        // scaled into [2^7, 2^8), each term codes what the earlier ones left (about 4 more significant
+        // bits a term, so ~12 in all, like fp16's 11).  The MMA operand is 32 rows of 128 codes, K-major
+        // and 128-byte swizzled, written over the loaded tile (same 4 KB, every thread has read its
+        // values before the barrier): row 8 t + g holds term t of head g, other rows are zero.  False,
+        // agreed by the four warps at their barrier, after a failed wait.
         auto convert_q = [&](int n, bool mine) -> bool {
             const int qb = n & 1;
             if (mine) mine = __all_sync(0xffffffffu, mbar_wait_sleep(q_full + qb, (n >> 1) & 1));
@@ -865,17 +898,36 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             if (qm > 0.f) {
                 int ex;
                 frexpf(qm, &ex);
-                e = min(max(ex - 15, -100), 100);
+                e = min(max(ex - 8, -100), 100);
+            }
+            uint32_t code[3][G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float y = ldexpf(x[g], -e);
+#pragma unroll
+                for (int t = 0; t < 3; ++t) {
+                    code[t][g] = e4m3x2_from_f32(y, 0.f) & 0xFFu;
+                    y -= e4m3_value(code[t][g]);
+                }
             }
 #pragma unroll
-            for (int g = 0; g < G; ++g) *reinterpret_cast<__half *>(qt + qoff(g)) = __float2half_rn(ldexpf(x[g], -e));
+            for (int row = 0; row < 32; ++row) {
+                const int t = row >> 3, g = row & 7;
+                uint32_t v = 0u;
+#pragma unroll
+                for (int tt = 0; tt < 3; ++tt)
+#pragma unroll
+                    for (int gg = 0; gg < G; ++gg)
+                        if (tt == t && gg == g) v = code[tt][gg];
+                qt[row * 128 + (((r >> 4) ^ (row & 7)) << 4) + (r & 15)] = (uint8_t)v;
+            }
             if (r == 0) qexp[n & 7] = e; // read by the softmax after q_ready
             fence_proxy_async_smem();   // Q is read by the MMA
             mbar_arrive(q_ready + (n & 7));
             return true;
         };
-        // unit 0's q first; each later unit's as soon as the previous unit's last K tile is widened,
-        // so that its first S^T does not wait for the previous unit's last V tile
+        // unit 0's q first; each later unit's at the previous unit's last step, before that step's V
+        // tile (which lands last), so that the unit's first S^T does not wait for it
         bool ok = (int)blockIdx.x < U ? convert_q(0, *abort_flag == 0) : true;
         int64_t gs = 0;
         int nu = 0;
@@ -888,15 +940,10 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 break;
             }
             const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
-            // ---- the unit's K and V stages
+            // ---- the unit's V stages
             for (int i = 0; i < nsteps && ok; ++i) {
                 const int64_t g = gs + i;
                 const int st = (int)(g % NS);
-                ok = __all_sync(0xffffffffu, mbar_wait_sleep(k8_full + st, (g / NS) & 1));
-                if (!ok) break;
-                widen_row(smem + LY::K0 + st * LY::STAGE);
-                fence_proxy_async_smem();
-                mbar_arrive(k_full + st);
                 if (i + 1 == nsteps && u + (int)gridDim.x < U) {
                     ok = convert_q(nu + 1, *abort_flag == 0);
                     if (!ok) break;

@@ -895,14 +895,19 @@ EncodeFn encode_fn() {
 }
 
 // 2-D view [rows = tokens][cols = heads * D] of a packed tensor; box = 64 columns x box_rows rows.
+// mt = PKV_FP8_E4M3: one-byte elements, boxes of 128 columns (one 128-byte swizzle row).
 bool make_map(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t cols, int box_rows) {
     EncodeFn enc = encode_fn();
     if (!enc) return false;
+    const bool bytes = mt == PKV_FP8_E4M3;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * (bytes ? 1 : 2)};
+    const cuuint32_t box[2] = {bytes ? 128u : 64u, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(m, mt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    const CUtensorMapDataType dt = bytes                ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : mt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUresult r = enc(m, dt, 2,
                            const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -91,6 +91,18 @@ PKV_DEV void mma_f16_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uin
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// kind::f8f6f4 with both operands in shared memory (E4M3 A and B: the instruction descriptor's
+// type fields are 0, so idesc_f16(0, ...) describes E4M3 x E4M3 -> fp32 as well); one K step is 32
+// one-byte elements, the same 32 bytes of a 128-byte swizzled row as a 16-element fp16 step.
+PKV_DEV void mma_f8_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 PKV_DEV void mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p, e;\n\t"
