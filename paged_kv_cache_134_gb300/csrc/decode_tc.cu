@@ -26,7 +26,7 @@ bool pkv_decode_tc_eligible(const pkv_cache *c, int G, int num_seqs) {
     // TMA row coordinates are 32-bit
     if ((int64_t)c->num_blocks * 2 * c->num_kv_heads * c->block_size > 0x7FFFFFFFLL) return false;
     if ((int64_t)num_seqs * 16 > 0x7FFFFFFFLL) return false;
-    return smem_bytes(operand_dtype(c), num_seqs) <= 232448;
+    return smem_bytes(operand_dtype(c), c->kv_dtype == PKV_FP8_E4M3, num_seqs) <= 232448;
 }
 
 cudaError_t pkv_decode_tc_launch(const pkv_cache *c, const pkv_decode::Args &a, const void *q, int G,
@@ -41,7 +41,7 @@ cudaError_t pkv_decode_tc_launch(const pkv_cache *c, const pkv_decode::Args &a, 
     if (!pkv_tmap_2d(&tkv, c->pool, f8 ? (int)PKV_FP8_E4M3 : mt,
                      (int64_t)c->num_blocks * 2 * c->num_kv_heads * c->block_size, D, c->block_size))
         return cudaErrorInvalidValue;
-    const size_t smem = smem_bytes(operand_dtype(c), a.num_seqs);
+    const size_t smem = smem_bytes(operand_dtype(c), f8, a.num_seqs);
     const int grid = c->num_sms;
 #define PKV_TC_CASE(GG)                                                                                                \
     if (G == GG) {                                                                                                     \

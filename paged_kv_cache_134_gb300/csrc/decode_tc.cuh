@@ -42,7 +42,6 @@ using pkv_decode::Unit;
 constexpr int D = 128;
 constexpr int TOK = 128;             // tokens per step: MMA M of S^T, MMA K of O^T
 constexpr int NQ = 16;               // MMA N: the group's query heads, padded
-constexpr int NS = 3;                // K stages and V stages
 // warp 0 Q and K loads, 1 MMA, 2-5 softmax, 6 V loads, 7-10 epilogue; FP8 caches: 11-14 converters
 template <bool F8>
 __host__ __device__ constexpr int threads_for() {
@@ -66,28 +65,33 @@ struct UnitRec {
     int pad[7];
 };
 
-template <int MT>
+template <int MT, bool F8 = false>
 struct Layout {
+    // K stages and V stages: an E4M3 K stage (128 rows of 128 codes) takes half the room of a 16-bit
+    // one, which pays for a fourth stage of each ring
+    static constexpr int NS = F8 ? 4 : 3;
     static constexpr int NP = MT == PKV_BF16 ? 2 : 1;      // P parts (hi, lo for bf16)
     // rows of the P^T operand: the group's heads (padded to NQ), and for bf16 the lo parts as rows
     // NQ.. 2 NQ - 1, so that one N = 2 NQ MMA per K step covers both parts (the two O^T column
     // groups are added in the epilogue)
     static constexpr int NPR = NQ * NP;
-    static constexpr int STAGE = TOK * D * 2;              // [half][128 rows][128 B] = 32 KB
+    static constexpr int STAGE = TOK * D * 2;              // V (and 16-bit K): [half][128 rows][128 B] = 32 KB
+    static constexpr int KSTAGE = F8 ? TOK * D : STAGE;    // E4M3 K: [128 rows][128 B] = 16 KB
     static constexpr int K0 = 0;
-    static constexpr int V0 = K0 + NS * STAGE;
+    static constexpr int V0 = K0 + NS * KSTAGE;
     static constexpr int Q = V0 + NS * STAGE;              // [2 buffers][half][16 rows][128 B]
     static constexpr int Q_BYTES = NQ * D * 2;
     static constexpr int P = Q + 2 * Q_BYTES;                  // [buffer][part][64-token chunk][16 rows][128 B]
     static constexpr int P_BYTES = NPR * TOK * 2;          // one buffer
     static constexpr int RED = P + 2 * P_BYTES;            // [2][4 warps][NQ] maxima, [2][4 warps][NQ] sums,
     static constexpr int BAR = RED + (4 * 4 * NQ + 2 * NQ) * 4; // [2][NQ] bases (sums and bases per unit parity)
-    static constexpr int UNITS = BAR + 512;                // ring of kUnitRing unit records
+    static constexpr int UNITS = BAR + 640;                // ring of kUnitRing unit records
     static constexpr int FIXED = UNITS + kUnitRing * 64;   // + unit tables, 3 (S + 1) ints
 };
 
-inline size_t smem_bytes(int mt, int num_seqs) {
-    const size_t fixed = mt == PKV_BF16 ? Layout<PKV_BF16>::FIXED : Layout<PKV_F16>::FIXED;
+inline size_t smem_bytes(int mt, bool f8, int num_seqs) {
+    const size_t fixed = f8 ? Layout<PKV_F16, true>::FIXED
+                            : (mt == PKV_BF16 ? Layout<PKV_BF16>::FIXED : Layout<PKV_F16>::FIXED);
     return fixed + (size_t)3 * (num_seqs + 1) * sizeof(int);
 }
 
@@ -167,7 +171,8 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
     constexpr bool F8 = KVT == PKV_FP8_E4M3;
     constexpr int OT = F8 ? (int)PKV_F16 : MT; // operand dtype of the MMAs
     constexpr int kThreads = threads_for<F8>();
-    using LY = Layout<OT>;
+    using LY = Layout<OT, F8>;
+    constexpr int NS = LY::NS;
     // tensor-memory columns: two S^T buffers of NSC columns (FP8: q as three E4M3 terms of 8 heads
     // each, N = 32), then O^T of even units at OB and of odd units at OB + 32
     constexpr int NSC = F8 ? 32 : NQ;
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             if (!ok || *abort_flag) break;
             // row of (block b, K or V, KV head) in the pool's [rows][D] view
             const int row = ((b * 2 + (is_k ? 0 : 1)) * a.hkv + un.kvh) * a.bs;
-            uint8_t *dst0 = smem + (is_k ? LY::K0 : LY::V0) + st * LY::STAGE + lane * a.bs * 128;
+            uint8_t *dst0 = smem + (is_k ? LY::K0 + st * LY::KSTAGE : LY::V0 + st * LY::STAGE) + lane * a.bs * 128;
             if (good) {
                 if (F8 && is_k) {
                     // the block's bs rows of 128 E4M3 codes, 128-byte swizzled: the MMA's K-major layout
@@ -473,7 +478,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait_sleep(s_free + b, ((g >> 1) - 1) & 1))) return false;
                 tc::fence_after_sync();
                 any_mma = true;
-                const uint64_t a0 = dK + (uint64_t)((st * LY::STAGE) >> 4), b0 = dQ + (uint64_t)((qb * LY::Q_BYTES) >> 4);
+                const uint64_t a0 = dK + (uint64_t)((st * LY::KSTAGE) >> 4), b0 = dQ + (uint64_t)((qb * LY::Q_BYTES) >> 4);
                 if constexpr (F8) {
                     // E4M3 K rows of 128 codes (one swizzle row each) against the q terms, 32 codes a step
 #pragma unroll
