@@ -668,9 +668,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 }
                 float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < BN; c += 2) {
-                    mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-                    mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+                for (int c = 0; c < BN; c += 4) {
+                    mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                    mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
                 }
                 const float mx = fmaxf(mx0, mx1) * a.scale_log2; // scale > 0 keeps the order
                 const bool up = mx > m_use + kRescale;
@@ -678,19 +678,19 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
                 const float alpha = up ? fast_exp2(m_use - m_new) : 1.f;
                 m_use = m_new;
                 const float nbase = m_use == -INFINITY ? 0.f : -m_use; // a row with no live key yet keeps p = 0
-                float rs0 = 0.f, rs1 = 0.f;
+                float2 rs = make_float2(0.f, 0.f);
+                const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nb2 = make_float2(nbase, nbase);
                 uint32_t phi[BN / 2], plo[L::NP == 2 ? BN / 2 : 1];
 #pragma unroll
                 for (int c = 0; c < BN / 2; ++c) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * c]), a.scale_log2, nbase));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * c + 1]), a.scale_log2, nbase));
-                    rs0 += p0;
-                    rs1 += p1;
+                    const float2 x = fma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nb2);
+                    const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                    rs = add2(rs, make_float2(p0, p1));
                     phi[c] = pack2(p0, p1, MT);
                     if constexpr (L::NP == 2) // remainders after bf16 rounding, themselves rounded to bf16
                         plo[c] = pack2(p0 - __uint_as_float(phi[c] << 16), p1 - __uint_as_float(phi[c] & 0xFFFF0000u), MT);
                 }
-                l = l * alpha + (rs0 + rs1);
+                l = l * alpha + (rs.x + rs.y);
                 // P V of the previous tile must have finished when O is rescaled (only when a row's
                 // base moved) and, with a single P buffer, before P is overwritten.  The wait is
                 // unambiguous: S of this tile is done, hence P V of tile gg - 2 (issued before it), and
