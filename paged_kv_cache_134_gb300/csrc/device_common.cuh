@@ -124,6 +124,7 @@ PKV_DEV bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
 }
 
 // two-lane fp32 arithmetic (one instruction for both lanes): a * b + c and a + b; max of three
+// (the softmax of the prefill kernels issues these per key pair instead of two scalar operations)
 PKV_DEV float2 fma2(float2 a, float2 b, float2 c) {
     unsigned long long ra, rb, rc, rd;
     asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));

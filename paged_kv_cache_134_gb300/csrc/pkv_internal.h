@@ -144,9 +144,6 @@ struct PrefillLaunch {
     float scale;
 };
 cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st);
-// packed prefill with two query tiles per CTA (prefill_pair.cu): fp16 models, D 64 or 128, no cached prefix
-bool pkv_prefill_pair_eligible(const pkv_cache *c, const PrefillLaunch &p);
-cudaError_t launch_prefill_pair(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st);
 
 // Tiled-TMA map of a row-major fp16/bf16 matrix [rows][cols]: box = 64 columns x box_rows rows,
 // 128-byte swizzle, out-of-range elements read as zero (prefill.cu).

@@ -952,8 +952,6 @@ bool pkv_tmap_2d(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t
 cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st) {
     using namespace pkv_prefill;
     if (p.total_tokens <= 0) return cudaSuccess;
-    // fp16 packed prefill: two query tiles per CTA (prefill_pair.cu)
-    if (pkv_prefill_pair_eligible(c, p)) return launch_prefill_pair(c, p, st);
     const int D = c->head_dim;
     const int mt = c->model_dtype;
     Args a;

@@ -46,25 +46,17 @@ def test_small_cases(case):
     check_prefill(W.prefill(seed=51, **case), "small")
 
 
-# fp16 packed prefill runs two 128-row query tiles per CTA: lengths around the 256-row pair, odd
-# tile counts (an item without its second tile), up to 32 blocks of bs 8 per item for the writer
-PAIR_CASES = [
+# lengths around 128- and 256-row boundaries, odd tile counts, up to 32 blocks of bs 8 per 256 rows
+BOUNDARY_CASES = [
     dict(lengths=(256, 257, 383, 384, 385), heads=2, kv_heads=2, d=128, bs=8),
     dict(lengths=(640, 1000, 1), heads=4, kv_heads=1, d=64, bs=16),
     dict(lengths=(129, 255, 511), heads=8, kv_heads=2, d=128, bs=32),
 ]
 
 
-@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "_".join(f"{k}{v}" for k, v in c.items()).replace(" ", ""))
-def test_two_tile_kernel_cases(case):
-    check_prefill(W.prefill(seed=53, **case), "pairs")
-
-
-def test_one_tile_kernel_on_fp16(monkeypatch):
-    # the one-tile kernel (kept for bf16, cached-prefix and cascade modes) on the fp16 config too
-    monkeypatch.setenv("PAGEDKV_PREFILL_PAIRS", "0")
-    check_prefill(W.prefill(), "prefill5256 one-tile")
-    check_prefill(W.prefill(seed=54, lengths=(5, 64, 65, 127, 128, 129), heads=2, kv_heads=2, d=128), "small one-tile")
+@pytest.mark.parametrize("case", BOUNDARY_CASES, ids=lambda c: "_".join(f"{k}{v}" for k, v in c.items()).replace(" ", ""))
+def test_tile_boundary_cases(case):
+    check_prefill(W.prefill(seed=53, **case), "boundaries")
 
 
 def test_packed_config_5256_tokens():
