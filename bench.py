@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -467,8 +468,8 @@ def run_ours(args):
     assert cache.check_error() == 0
 
     # ---- timed region: inputs resident in HBM; KV (1.07 GB/step) is larger than L2 (129 MB)
-    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
-        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, f"/tmp/pkv_clocks_{rank}.csv")
+    clock_dir = args.clocks_dir or tempfile.gettempdir()
+    sampler = ClockSampler(local, os.path.join(clock_dir, f"pkv_clocks_rank{rank}.csv"))
     time.sleep(0.2)
     launches0 = P.kernel_launches()
     cache.profile_start(kinds=("decode",))   # events around the decode kernel only
@@ -605,6 +606,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--clocks-dir", default=None,
+                    help="folder for the nvidia-smi clock samples of the timed region (default: the temp dir)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--only", default=None,
                     help="run one secondary case alone and print its JSON (for profiling): prefill, append, "

@@ -358,7 +358,7 @@ int paged_decode_attention_cascade(const void *q, pkv_cache_t c, const int32_t *
     if (!aligned16(q) || !aligned16(out)) return pkv_fail(PKV_EINVAL, "q and out must be 16-byte aligned");
     if (!(scale == scale)) return pkv_fail(PKV_EINVAL, "scale is NaN");
     if (int r = check_device(c)) return r;
-    const int split_tokens = 512; // keys per prefix split: a multiple of the 64-key tiles
+    const int split_tokens = cascade_split_tokens(c, num_seqs, num_q_heads, shared_prefix_len);
     const int nps = (shared_prefix_len + split_tokens - 1) / split_tokens;
     const int pb = shared_prefix_len / c->block_size;
     DecodeLaunch d;

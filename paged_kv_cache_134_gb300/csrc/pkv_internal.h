@@ -123,6 +123,8 @@ struct CascadePrefixLaunch {
     float *ws_o, *ws_ml;
 };
 cudaError_t launch_cascade_prefix(pkv_cache *c, const CascadePrefixLaunch &p, cudaStream_t st);
+// keys per prefix split of the cascade's prefix phase (a multiple of 64)
+int cascade_split_tokens(const pkv_cache *c, int num_seqs, int num_q_heads, int prefix_tokens);
 int64_t decode_workspace_floats(const pkv_cache *c, int num_seqs, int num_q_heads, int max_splits);
 int decode_split_blocks(const pkv_cache *c);
 cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st);

@@ -1034,6 +1034,30 @@ cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st
     return e;
 }
 
+int cascade_split_tokens(const pkv_cache *c, int num_seqs, int num_q_heads, int prefix_tokens) {
+    using namespace pkv_prefill;
+    if (const char *v = std::getenv("PAGEDKV_CASCADE_SPLIT_TOKENS")) {
+        // keys per prefix split, for tuning sweeps (rounded up to whole 64-key tiles)
+        const int x = std::atoi(v);
+        if (x > 0) return (x + 63) / 64 * 64;
+    }
+    // The prefix phase runs as one wave of items where it can: as many splits per (query-row tile,
+    // head) as leave every item a resident CTA (a split past one wave makes the whole phase wait for
+    // a second), each of at least 256 keys so that an item's fixed costs (Q load, epilogue, partial
+    // write) stay small next to its key tiles, in whole 64-key tiles.
+    int per_sm = 1;
+    if (c->head_dim == 128)
+        per_sm = c->model_dtype == PKV_BF16 ? min_blocks<128, PKV_BF16>() : min_blocks<128, PKV_F16>();
+    else
+        per_sm = c->model_dtype == PKV_BF16 ? min_blocks<64, PKV_BF16>() : min_blocks<64, PKV_F16>();
+    const int64_t slots = (int64_t)c->num_sms * per_sm;
+    const int64_t rows = (int64_t)((num_seqs + BM - 1) / BM) * num_q_heads;
+    const int64_t nps = std::max<int64_t>(1, slots / std::max<int64_t>(rows, 1));
+    int64_t split = (prefix_tokens + nps - 1) / nps;
+    split = std::max<int64_t>(split, 256);
+    return (int)((split + 63) / 64 * 64);
+}
+
 cudaError_t launch_cascade_prefix(pkv_cache *c, const CascadePrefixLaunch &p, cudaStream_t st) {
     using namespace pkv_prefill;
     if (p.num_seqs <= 0 || p.prefix_tokens <= 0) return cudaSuccess;

@@ -34,9 +34,9 @@ def check_cascade(w, tag):
 CASES = [
     # prefix not a multiple of the 64-key tile; grouped-query heads; bf16
     dict(num_seqs=5, prefix_tokens=96, max_suffix=40, heads=8, kv_heads=2, d=64, bs=16, dtype="bf16"),
-    # more than 128 sequences (two query-row tiles), two 512-key prefix splits
+    # more than 128 sequences (two query-row tiles), four 256-key prefix splits
     dict(num_seqs=130, prefix_tokens=1024, max_suffix=300, heads=2, d=128, bs=32),
-    # three prefix splits (the last one partial), G = 4 (tensor-core suffix decode), bs 8
+    # five prefix splits (the last one partial), G = 4 (tensor-core suffix decode), bs 8
     dict(num_seqs=9, prefix_tokens=1120, max_suffix=700, heads=8, kv_heads=2, d=128, bs=8, dtype="bf16"),
     # suffixes shorter than a block and longer than a split
     dict(num_seqs=16, prefix_tokens=256, max_suffix=2000, heads=4, d=128, bs=16),
