@@ -540,7 +540,7 @@ def run_ours(args):
                                       **secondary_decode(P, G, peaks, w4, unique_bytes=uniq))
         secondary["prefix13b_cascade"] = dict(
             workload="the same 13B-shape batch, cascade decode: the 4096-token shared prefix read once per "
-                     "(head, 512-key split) for all 64 sequences on the tensor cores, suffixes by split-K decode",
+                     "(head, prefix split) for all 64 sequences on the tensor cores, suffixes by split-K decode",
             **secondary_decode(P, G, peaks, w4, unique_bytes=uniq, cascade=w4.shared_prefix_len))
         del w4
         stress = {}
