@@ -302,6 +302,10 @@ typedef struct {
 /* kinds: which kernels to bracket (events between two kernels stop their launches from overlapping,
  * so time only what you need). */
 int kv_cache_profile_start(pkv_cache_t cache, unsigned kinds);
+/* The same, bracketing only the 1st, (every+1)-th, (2 every+1)-th ... launch of each kind (every >= 1,
+ * else PKV_EINVAL): the kernel times of a long run are sampled while the launches in between keep
+ * their overlap.  kv_cache_profile_start(cache, kinds) is every = 1. */
+int kv_cache_profile_start_sampled(pkv_cache_t cache, unsigned kinds, int every);
 int kv_cache_profile_read(pkv_cache_t cache, pkv_profile_t *out);
 int64_t pkv_kernel_launches(void);
 

@@ -72,6 +72,7 @@ def lib() -> ctypes.CDLL:
         L.paged_block_swap_out.argtypes = [vp, vp, i64, vp, vp]
         L.paged_block_swap_in.argtypes = [vp, vp, i64, vp, vp]
         L.kv_cache_profile_start.argtypes = [vp, ctypes.c_uint]
+        L.kv_cache_profile_start_sampled.argtypes = [vp, ctypes.c_uint, ctypes.c_int]
         L.kv_cache_profile_read.argtypes = [vp, ctypes.c_void_p]
         L.pkv_kernel_launches.restype = i64
         _lib = L
@@ -193,12 +194,13 @@ class KVCache:
         """Bytes of one physical block (K and V of every KV head)."""
         return 2 * self.num_kv_heads * self.block_size * self.head_dim * (1 if self.kv_dtype == "fp8" else 2)
 
-    def profile_start(self, kinds=("decode", "prefill", "append", "merge")):
-        """Record CUDA events around the named kernels (events between kernels stop their overlap)."""
+    def profile_start(self, kinds=("decode", "prefill", "append", "merge"), every: int = 1):
+        """Record CUDA events around the named kernels (events between kernels stop their overlap);
+        with every > 1 only around every n-th launch of each kind."""
         mask = 0
         for k in kinds:
             mask |= self.PROFILE[k]
-        _check(lib().kv_cache_profile_start(self.handle, mask))
+        _check(lib().kv_cache_profile_start_sampled(self.handle, mask, int(every)))
 
     def profile_read(self) -> dict:
         p = _Profile()

@@ -60,6 +60,9 @@ int pkv_cuda_fail(cudaError_t e, const char *what) {
 PkvTimer::PkvTimer(pkv_cache *c_, int kind_, cudaStream_t st_) : c(c_), kind(kind_), st(st_) {
     if (!c || !c->profiling || !(c->profile_kinds & (1u << kind))) return;
     std::lock_guard<std::mutex> lk(c->mu);
+    // sampled profiling: the launches in between run without events, so that their overlap with
+    // the neighbouring kernels (programmatic dependent launch) is left as it is
+    if (c->profile_seen[kind]++ % c->profile_every != 0) return;
     for (cudaEvent_t *ev : {&a, &b}) {
         if (!c->event_pool.empty()) {
             *ev = c->event_pool.back();
@@ -459,8 +462,11 @@ int paged_block_swap_in(pkv_cache_t c, const int32_t *block_ids, int64_t num_ids
     return PKV_OK;
 }
 
-int kv_cache_profile_start(pkv_cache_t c, unsigned kinds) {
+int kv_cache_profile_start(pkv_cache_t c, unsigned kinds) { return kv_cache_profile_start_sampled(c, kinds, 1); }
+
+int kv_cache_profile_start_sampled(pkv_cache_t c, unsigned kinds, int every) {
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
+    if (every < 1) return pkv_fail(PKV_EINVAL, "every must be >= 1, got %d", every);
     // PKV_PROFILE_* bits map onto (1 << PKV_KIND_*)
     c->profile_kinds = ((kinds & PKV_PROFILE_DECODE) ? 1u << PKV_KIND_DECODE : 0u) |
                        ((kinds & PKV_PROFILE_PREFILL) ? 1u << PKV_KIND_PREFILL : 0u) |
@@ -473,6 +479,8 @@ int kv_cache_profile_start(pkv_cache_t c, unsigned kinds) {
         c->event_pool.push_back(ev.b);
     }
     c->events.clear();
+    c->profile_every = every;
+    for (int64_t &n : c->profile_seen) n = 0;
     c->profiling = true;
     return PKV_OK;
 }

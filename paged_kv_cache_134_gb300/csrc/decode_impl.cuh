@@ -573,7 +573,9 @@ __global__ void __launch_bounds__(128) merge_kernel(const Args a) {
     constexpr int PER = D / 32;
     __shared__ float s_num[4][D];
     __shared__ float s_den[4];
-    pdl_trigger();
+    // No early trigger: the kernel after the merge (typically the next decode step's append, then
+    // its decode kernel, whose persistent CTAs fill the SMs) launches when the merge has finished,
+    // rather than taking SM room from the merge's own CTAs while it runs.
     pdl_wait();
     const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int s = row / a.hq;

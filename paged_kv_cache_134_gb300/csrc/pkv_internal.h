@@ -34,6 +34,8 @@ struct pkv_cache {
     // profiling
     bool profiling = false;
     unsigned profile_kinds = 0; // bit (1 << PKV_KIND_*)
+    int profile_every = 1;       // bracket every n-th launch of a kind (see kv_cache_profile_start_sampled)
+    int64_t profile_seen[8] = {}; // launches of each kind since the profile started
     struct Ev {
         int kind;
         cudaEvent_t a, b;
