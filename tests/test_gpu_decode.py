@@ -98,6 +98,27 @@ def test_run_to_run_determinism():
     assert np.array_equal(run_decode(w)["out"], run_decode(w)["out"])
 
 
+def test_sampled_profiling_brackets_every_nth_launch():
+    # 23 decode steps with every = 5: launches 1, 6, 11, 16, 21 are timed (the others run without events)
+    import paged_kv_cache_134_gb300 as P
+    from paged_kv_cache_134_gb300 import runner as G
+    w = W.small_decode("prof", [300, 40, 1], hq=4, hkv=4, d=128, bs=16, seed=46)
+    cache = G.new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype, w.model_dtype)
+    try:
+        G.fill_cache(cache, w)
+        x = G.DecodeInputs(w)
+        cache.profile_start(kinds=("decode", "append"), every=5)
+        for _ in range(23):
+            G.decode_step(cache, x)
+        prof = cache.profile_read()
+        assert prof["decode_launches"] == 5 and prof["append_launches"] == 5, prof
+        assert prof["merge_launches"] == 0 and prof["decode_ms"] > 0.0
+        with pytest.raises(P.PagedKVError):
+            cache.profile_start(kinds=("decode",), every=0)
+    finally:
+        cache.close()
+
+
 def test_invalid_block_id_is_reported_not_fatal():
     w = W.small_decode("bad", [40, 40], hq=2, hkv=2, d=64, bs=16, seed=45)
     w.block_tables = w.block_tables.copy()
