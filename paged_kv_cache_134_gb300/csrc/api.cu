@@ -394,13 +394,11 @@ int paged_decode_attention_cascade(const void *q, pkv_cache_t c, const int32_t *
     p.ws_o = c->ws;
     p.ws_ml = c->ws + rows * c->head_dim;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    {
-        PkvTimer timer(c, PKV_KIND_PREFILL, st);
-        e = launch_cascade_prefix(c, p, st);
-    }
+    // launches: the prefix phase's plan, the suffix decode, the prefix kernel, the merge
+    cudaError_t e = launch_cascade_prefix(c, p, st, 1);
     if (e == cudaErrorNotSupported) return pkv_fail(PKV_EUNSUPPORTED, "cascade shape not supported");
     if (e != cudaSuccess) return pkv_cuda_fail(e, "cascade prefix launch");
+    d.prefix = &p;
     e = launch_decode(c, d, st);
     if (e != cudaSuccess) return pkv_cuda_fail(e, "decode launch");
     return PKV_OK;

@@ -36,6 +36,14 @@ void pick(const pkv_cache *c, DecodeFn *fn, OccFn *occ) {
 
 } // namespace
 
+// cascade decode: the prefix kernel runs between the suffix decode and the merge, overlapping the
+// decode's last units (the decode lets it launch early; it waits for the decode before it exits)
+static cudaError_t launch_prefix_between(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) {
+    if (!d.prefix) return cudaSuccess;
+    PkvTimer timer(c, PKV_KIND_PREFILL, st);
+    return launch_cascade_prefix(c, *d.prefix, st, 2);
+}
+
 int decode_split_blocks(const pkv_cache *c) {
     const int tokens = env_int("PAGEDKV_SPLIT_TOKENS", 256);
     const int b = tokens / c->block_size;
@@ -95,6 +103,7 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
             g_pkv_launches++;
         }
         if (e != cudaSuccess) return e;
+        if ((e = launch_prefix_between(c, d, st)) != cudaSuccess) return e;
         PkvTimer timer(c, PKV_KIND_MERGE, st);
         e = fn(a, c->head_dim, G, 0, 0, st, true);
         g_pkv_launches++;
@@ -128,6 +137,7 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
         g_pkv_launches++;
     }
     if (e != cudaSuccess) return e;
+    if ((e = launch_prefix_between(c, d, st)) != cudaSuccess) return e;
     {
         PkvTimer timer(c, PKV_KIND_MERGE, st);
         e = fn(a, c->head_dim, G, 0, 0, st, true);

@@ -385,6 +385,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
         fence_mbarrier_init();
     }
     pdl_wait(); // the previous kernel (e.g. the append of this step) has finished
+    // cascade decode: the next kernel is the prefix phase, which reads nothing this kernel writes;
+    // it may launch now and take the SMs this grid's CTAs leave
+    if (a.slot0 > 0) pdl_trigger();
     const int bps = a.split_blocks;
     build_unit_list(a, pf, pp, nb, warp, lane);
     const int U = (pf[S] + pp[S]) * a.hkv;

@@ -98,6 +98,7 @@ cudaError_t launch_append_ranges(pkv_cache *c, const void *k, const void *v, con
 cudaError_t launch_copy_blocks(pkv_cache *c, const void *src, const int32_t *src_ids, int64_t src_blocks, void *dst,
                                const int32_t *dst_ids, int64_t dst_blocks, int64_t n, cudaStream_t st);
 
+struct CascadePrefixLaunch;
 struct DecodeLaunch {
     const void *q;
     void *out;
@@ -112,6 +113,9 @@ struct DecodeLaunch {
     // cascade decode: blocks of the shared prefix (covered by launch_cascade_prefix) and the workspace
     // slot of the first suffix split; 0 and 0 for a plain decode
     int start_block = 0, slot0 = 0;
+    // cascade decode: the prefix kernel, launched after the decode kernel and before the merge (its
+    // plan kernel went before the decode)
+    const CascadePrefixLaunch *prefix = nullptr;
 };
 
 // The prefix phase of a cascade decode (prefill.cu): the decode queries of every sequence against the
@@ -124,7 +128,10 @@ struct CascadePrefixLaunch {
     float scale;
     float *ws_o, *ws_ml;
 };
-cudaError_t launch_cascade_prefix(pkv_cache *c, const CascadePrefixLaunch &p, cudaStream_t st);
+// part 1: the plan kernel; part 2: the prefix kernel.  The prefix kernel does not wait for the kernel
+// before it until it exits, so that kernel must be one that lets it launch only after waiting for its
+// own predecessors (the suffix decode, launched between the two parts by launch_decode).
+cudaError_t launch_cascade_prefix(pkv_cache *c, const CascadePrefixLaunch &p, cudaStream_t st, int part);
 // keys per prefix split of the cascade's prefix phase (a multiple of 64)
 int cascade_split_tokens(const pkv_cache *c, int num_seqs, int num_q_heads, int prefix_tokens);
 int64_t decode_workspace_floats(const pkv_cache *c, int num_seqs, int num_q_heads, int max_splits);

@@ -308,8 +308,12 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     // everything above is private to this CTA; from here on global memory written by the previous
-    // kernels on the stream (the work list, the inputs) is read
-    pdl_wait();
+    // kernels on the stream (the work list, the inputs) is read.  Cascade mode runs right after the
+    // suffix decode, which lets it launch once the decode itself has waited for its predecessors
+    // (the plan of this call and everything before it): the prefix phase reads nothing the decode
+    // writes, so it starts at once and fills the SMs the decode's CTAs leave, and waits for the
+    // decode only before it exits (the merge after it then sees both).
+    if constexpr (!CASCADE) pdl_wait();
 
     const int G = a.hq / a.hkv;
     auto fail = [&]() {
@@ -874,6 +878,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<D, MT>())
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
+    if constexpr (CASCADE) pdl_wait(); // the grid completes after the suffix decode (see above)
 }
 
 using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -1058,7 +1063,7 @@ int cascade_split_tokens(const pkv_cache *c, int num_seqs, int num_q_heads, int 
     return (int)((split + 63) / 64 * 64);
 }
 
-cudaError_t launch_cascade_prefix(pkv_cache *c, const CascadePrefixLaunch &p, cudaStream_t st) {
+cudaError_t launch_cascade_prefix(pkv_cache *c, const CascadePrefixLaunch &p, cudaStream_t st, int part) {
     using namespace pkv_prefill;
     if (p.num_seqs <= 0 || p.prefix_tokens <= 0) return cudaSuccess;
     const int D = c->head_dim;
@@ -1108,9 +1113,12 @@ cudaError_t launch_cascade_prefix(pkv_cache *c, const CascadePrefixLaunch &p, cu
     if (!make_map(&tq, p.q, mt, p.num_seqs, (int64_t)p.num_q_heads * D, BM) ||
         !make_map(&tp, c->pool, mt, pool_rows, D, c->block_size))
         return cudaErrorInvalidValue;
-    cudaError_t e = launch_plan(a, st);
-    g_pkv_launches++;
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
+    if (part == 1) {
+        e = launch_plan(a, st);
+        g_pkv_launches++;
+        return e;
+    }
     e = cudaErrorInvalidValue;
     if (D == 128)
         e = mt == PKV_BF16 ? launch_t<128, PKV_BF16, MODE_CASCADE>(tq, tp, tp, tp, a, pairs * p.num_q_heads, c->num_sms, st)
