@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-from gpu_path import assert_close, run_decode  # noqa: E402
+from gpu_path import DecodeInputs, assert_close, decode_step, fill_cache, new_cache, run_decode  # noqa: E402
 
 ATOL, RTOL = 2e-3, 1e-2
 
@@ -66,3 +66,29 @@ def test_cascade_rejects_a_sequence_shorter_than_the_prefix():
     err = cache.check_error()
     cache.close()
     assert err & 4   # PKV_DEVERR_LENGTH
+
+
+@pytest.mark.parametrize("kv_heads", [40, 10], ids=["mha", "gqa4"])
+def test_back_to_back_cascade_steps_agree(kv_heads):
+    # The prefix phase and the suffix decode overlap inside each call, and consecutive calls follow
+    # each other on one stream with no host synchronisation in between; 24 such steps must all give
+    # the first step's output bit for bit, and that output must match the oracle.
+    w = W.prefix13b(seed=93, num_seqs=64, prefix_tokens=2048, max_suffix=400, heads=40, kv_heads=kv_heads,
+                    d=128, bs=32)
+    cache = new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype, w.model_dtype)
+    try:
+        fill_cache(cache, w)
+        x = DecodeInputs(w)
+        outs = []
+        for _ in range(24):
+            decode_step(cache, x, cascade_prefix=w.shared_prefix_len)
+            outs.append(x.out.clone())
+        torch.cuda.synchronize()
+        assert cache.check_error() == 0
+        first = outs[0]
+        for i, o in enumerate(outs[1:], 1):
+            assert torch.equal(o, first), f"step {i} differs from step 0"
+        r = steps.decode_step(w, strides=cache.view()[1], pool_elems=int(cache.pool_elems().numel()))
+        assert_close(first.float().cpu().double().numpy(), r["out"], ATOL, RTOL, "back-to-back cascade")
+    finally:
+        cache.close()
