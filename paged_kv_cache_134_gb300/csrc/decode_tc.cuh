@@ -410,7 +410,9 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             if (!ok || *abort_flag) break;
             // row of (block b, K or V, KV head) in the pool's [rows][D] view
             const int row = ((b * 2 + (is_k ? 0 : 1)) * a.hkv + un.kvh) * a.bs;
-            uint8_t *dst0 = smem + (is_k ? LY::K0 + st * LY::KSTAGE : LY::V0 + st * LY::STAGE) + lane * a.bs * 128;
+            // 16-bit stage layout: [row group of 8][half][8 rows][128 bytes], a block's bs rows at
+            // lane * bs * 256; E4M3 K: [row][128 bytes]
+            uint8_t *dst0 = smem + (is_k ? LY::K0 + st * LY::KSTAGE : LY::V0 + st * LY::STAGE) + lane * a.bs * (F8 ? 128 : 256);
             if (good) {
                 if (F8 && is_k) {
                     // the block's bs rows of 128 E4M3 codes, 128-byte swizzled: the MMA's K-major layout
@@ -421,9 +423,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                     bulk_g2s_hint(smem + LY::V0 + st * LY::STAGE + TOK * 128 + lane * a.bs * 128, src,
                                   (uint32_t)a.tile_bytes, full, policy);
                 } else {
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c)
-                        tc::tma_load_2d_hint(dst0 + c * (TOK * 128), &tkv, c * 64, row, full, policy);
+                    tc::tma_load_4d_hint(dst0, &tkv, 0, 0, 0, row / 8, full, policy);
                 }
             }
             ++gs;
@@ -466,9 +466,14 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             // one descriptor per operand layout; the address field counts 16-byte units, so a tile at
             // byte offset `off` from the base is the base descriptor plus off / 16 (shared memory stays
             // below the field's 256 KB): each MMA adds a constant instead of rebuilding its descriptors
-            const uint64_t dK = tc::smem_desc(smem_u32(smem + LY::K0), 16, 1024);
+            // K: groups of 8 token rows 1024 bytes apart (E4M3) or 2048 (16-bit: the second 64-dim
+            // half of a group sits 1024 bytes after the first)
+            const uint64_t dK = tc::smem_desc(smem_u32(smem + LY::K0), 16, F8 ? 1024 : 2048);
             const uint64_t dQ = tc::smem_desc(smem_u32(smem + LY::Q), 16, 1024);
-            const uint64_t dV = tc::smem_desc(smem_u32(smem + LY::V0), TOK * 128, 1024);
+            // V^T (MN-major): the two 64-dim halves LBO apart, groups of 8 tokens SBO apart
+            const uint64_t dV = F8 ? tc::smem_desc(smem_u32(smem + LY::V0), TOK * 128, 1024)
+                                   : tc::smem_desc(smem_u32(smem + LY::V0), 1024, 2048);
+            constexpr int kVStep = F8 ? 2048 : 4096; // bytes per 16 tokens of V
             const uint64_t dP = tc::smem_desc(smem_u32(smem + LY::P), 16, 1024);
             bool any_mma = false;
             // S^T of step g (Q buffer qb) into S buffer g % 2; the K stage is released as soon as S^T is done
@@ -489,7 +494,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const int c = k >> 2, kk = k & 3;
-                        tc::mma_f16_warp(tmem + b * NSC, a0 + (uint64_t)((c * (TOK * 128) + kk * 32) >> 4),
+                        tc::mma_f16_warp(tmem + b * NSC, a0 + (uint64_t)((c * 1024 + kk * 32) >> 4),
                                          b0 + (uint64_t)((c * (NQ * 128) + kk * 32) >> 4), ISK, k > 0 ? 1u : 0u);
                     }
                 }
@@ -544,7 +549,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                     const uint64_t a0 = dV + (uint64_t)((st * LY::STAGE) >> 4), b0 = dP + (uint64_t)((b * LY::P_BYTES) >> 4);
 #pragma unroll
                     for (int k = 0; k < TOK / 16; ++k)
-                        tc::mma_f16_warp(tO, a0 + (uint64_t)((k * 2048) >> 4),
+                        tc::mma_f16_warp(tO, a0 + (uint64_t)((k * kVStep) >> 4),
                                          b0 + (uint64_t)(((k >> 2) * (LY::NPR * 128) + (k & 3) * 32) >> 4), IPV,
                                          (i > 0 || k > 0) ? 1u : 0u);
                     tc::commit_warp(t_full + b);
@@ -735,7 +740,9 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                     if (!valid) {
 #pragma unroll
                         for (int c = 0; c < D / 64; ++c) {
-                            uint4 *vr = reinterpret_cast<uint4 *>(smem + LY::V0 + st * LY::STAGE + c * (TOK * 128) + r * 128);
+                            uint4 *vr = reinterpret_cast<uint4 *>(
+                                smem + LY::V0 + st * LY::STAGE +
+                                (F8 ? c * (TOK * 128) + r * 128 : (r >> 3) * 2048 + c * 1024 + (r & 7) * 128));
 #pragma unroll
                             for (int e = 0; e < 8; ++e) vr[e] = make_uint4(0u, 0u, 0u, 0u);
                         }

@@ -159,3 +159,7 @@ cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st
 // Tiled-TMA map of a row-major fp16/bf16 matrix [rows][cols]: box = 64 columns x box_rows rows,
 // 128-byte swizzle, out-of-range elements read as zero (prefill.cu).
 bool pkv_tmap_2d(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t cols, int box_rows);
+// rows of 128 16-bit elements (a multiple of 8 of them) as a 4-D map whose box of box_rows rows (a
+// multiple of 8) lands as [row group of 8][64-element half][8 rows][128 bytes], 128-byte swizzled:
+// one copy per block tile where two 2-D boxes (one per half) were needed
+bool pkv_tmap_rows128_grouped(CUtensorMap *m, const void *base, int mt, int64_t rows, int box_rows);

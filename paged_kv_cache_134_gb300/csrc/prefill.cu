@@ -954,6 +954,23 @@ bool pkv_tmap_2d(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t
     return pkv_prefill::make_map(m, base, mt, rows, cols, box_rows);
 }
 
+bool pkv_tmap_rows128_grouped(CUtensorMap *m, const void *base, int mt, int64_t rows, int box_rows) {
+    using namespace pkv_prefill;
+    EncodeFn enc = encode_fn();
+    if (!enc || rows % 8 || box_rows % 8 || box_rows > 256 * 8) return false;
+    // rows of 128 16-bit elements = 256 bytes, seen as (64 elements, row in its group of 8, half, group):
+    // a box of (64, 8, 2, box_rows / 8) lands as [group][half][8 rows][128 bytes]
+    const cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)(rows / 8)};
+    const cuuint64_t strides[3] = {256, 128, 2048};
+    const cuuint32_t box[4] = {64u, 8u, 2u, (cuuint32_t)(box_rows / 8)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType dt = mt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUresult r = enc(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st) {
     using namespace pkv_prefill;
     if (p.total_tokens <= 0) return cudaSuccess;
