@@ -163,9 +163,11 @@ int paged_decode_attention_noalloc(const void *q, pkv_cache_t cache, const int32
  * requests share prefix blocks, and decode still reads them; section 6.4: decode-bound batches with
  * a high hit rate): same result as paged_decode_attention, but the first shared_prefix_len tokens,
  * which every table must name with the same blocks (those of table row 0), are read once per
- * (query head, 512-key split) for the whole batch instead of once per sequence.  Their attention
- * runs on the tensor cores as a matrix product of all the batch's queries with the prefix keys; the
- * tokens past the prefix go through the split-K decode; one merge combines both.  shared_prefix_len:
+ * (query head, prefix split) for the whole batch instead of once per sequence (splits sized so that
+ * the prefix work fits one wave of resident CTAs).  Their attention runs on the tensor cores as a
+ * matrix product of all the batch's queries with the prefix keys; the tokens past the prefix go
+ * through the split-K decode, and the prefix kernel runs alongside that decode's last work units
+ * (it reads nothing the decode writes); one merge combines both.  shared_prefix_len:
  * a multiple of block_size, at most max_blocks_per_seq * block_size, and at most every context
  * length (a shorter sequence sets PKV_DEVERR_LENGTH); 0 makes this paged_decode_attention.
  * fp16/bf16 caches (EUNSUPPORTED for FP8).  The prefix's split partials are rounded like any split
