@@ -234,7 +234,31 @@ def _time_loop(fn, steps, stream):
     return a.elapsed_time(b) / 1e3
 
 
-def secondary_prefill(P, W, gpu_path, peaks, reps=20):
+class L2Flush:
+    """Writes a device buffer of twice the L2 size, so that the next kernel finds none of its inputs
+    in L2.  Called between timed launches, outside the library's events around its kernels."""
+
+    def __init__(self):
+        l2 = int(getattr(torch.cuda.get_device_properties(torch.cuda.current_device()), "L2_cache_size", 0) or
+                 (128 << 20))
+        self.bytes = 2 * l2
+        self.buf = torch.empty(self.bytes // 4, dtype=torch.int32, device="cuda")
+        self.n = 0
+
+    def __call__(self):
+        self.n += 1
+        self.buf.fill_(self.n)
+
+
+def _kernel_loop_flushed(fn, reps, flush):
+    """reps calls of fn, each after an L2 flush (the library's own events time its kernels)."""
+    for _ in range(reps):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+
+
+def secondary_prefill(P, W, gpu_path, peaks, reps=20, flush=None):
     """Packed causal prefill of 5256 tokens (lengths 128..2048), 32 heads, D=128, fp16, bs=16."""
     w = W.prefill()
     md = gpu_path.TORCH_DT[w.dtype]
@@ -253,17 +277,19 @@ def secondary_prefill(P, W, gpu_path, peaks, reps=20):
     except Exception as e:  # reported, not hidden
         cache.close()
         return {"status": f"unavailable: {e}"}
-    cache.profile_start()
-    dt = _time_loop(step, reps, torch.cuda.current_stream()) / reps
+    dt = _time_loop(step, reps, torch.cuda.current_stream()) / reps   # back to back, no events
+    flush = flush or L2Flush()
+    cache.profile_start(kinds=("prefill",))
+    _kernel_loop_flushed(step, reps, flush)
     prof = cache.profile_read()
     err = cache.check_error()
     cache.close()
     kern = prof["prefill_ms"] / max(1, prof["prefill_launches"]) / 1e3
     tflops = w.flops() / kern / 1e12
     return {"workload": "packed causal prefill, lengths 128,200,512,1024,2048,256,64,1024 (5256 tokens), "
-                        "32 heads, D=128, fp16, bs=16", "tokens_per_s": round(w.total_tokens / dt, 1),
-            "ms": round(dt * 1e3, 4), "kernel_ms": round(kern * 1e3, 4), "tflops": round(tflops, 2),
-            "causal_gflop": round(w.flops() / 1e9, 3),
+                        "32 heads, D=128, fp16, bs=16", "tokens_per_s": round(w.total_tokens / kern, 1),
+            "ms_back_to_back": round(dt * 1e3, 4), "kernel_ms": round(kern * 1e3, 4), "tflops": round(tflops, 2),
+            "causal_gflop": round(w.flops() / 1e9, 3), "l2": "flushed before each timed launch",
             "frac_of_bf16_peak": round(tflops / peaks[1], 4), "device_errors": err}
 
 
@@ -304,7 +330,7 @@ def secondary_decode(P, G, peaks, w, reps=50, unique_bytes=None, cascade=0):
     return r
 
 
-def secondary_append(P, W, gpu_path, peaks, reps=20):
+def secondary_append(P, W, gpu_path, peaks, reps=20, flush=None):
     """Bulk paged append of 5256 tokens x 32 heads x 128 fp16 (86 MB read + 86 MB written)."""
     w = W.prefill()
     md = gpu_path.TORCH_DT[w.dtype]
@@ -316,17 +342,19 @@ def secondary_append(P, W, gpu_path, peaks, reps=20):
     for _ in range(3):
         P.paged_kv_append(cache, k, v, slots)
     torch.cuda.synchronize()
-    cache.profile_start()
-    _time_loop(lambda: P.paged_kv_append(cache, k, v, slots), reps, torch.cuda.current_stream())
+    flush = flush or L2Flush()
+    cache.profile_start(kinds=("append",))
+    _kernel_loop_flushed(lambda: P.paged_kv_append(cache, k, v, slots), reps, flush)
     prof = cache.profile_read()
     cache.close()
     kern = prof["append_ms"] / max(1, prof["append_launches"]) / 1e3
     nbytes = 2 * (k.numel() + v.numel()) * 2 + slots.numel() * 8
     return {"workload": "bulk append of 5256 tokens, 32 KV heads, D=128, fp16", "kernel_ms": round(kern * 1e3, 4),
-            "gbs": round(nbytes / kern / 1e9, 1), "frac_of_hbm": round(nbytes / kern / 1e9 / peaks[0], 4)}
+            "gbs": round(nbytes / kern / 1e9, 1), "frac_of_hbm": round(nbytes / kern / 1e9 / peaks[0], 4),
+            "algorithmic_bytes": nbytes, "l2": "flushed before each timed launch"}
 
 
-def secondary_prefix_hit(P, W, G, peaks, reps=20):
+def secondary_prefix_hit(P, W, G, peaks, reps=20, flush=None):
     """Prefill of 16 prompt tails (U{100..300} + 12 tokens) over a cached, shared 1488-token prefix,
     7B shape (32/32 heads, D=128, fp16, bs=16): ranged append of the tails + attention over the pool."""
     w = W.prefix_hit_prefill()
@@ -336,8 +364,10 @@ def secondary_prefix_hit(P, W, G, peaks, reps=20):
     for _ in range(3):
         G.context_prefill_step(cache, x)
     torch.cuda.synchronize()
-    cache.profile_start(kinds=("prefill", "append"))
     dt = _time_loop(lambda: G.context_prefill_step(cache, x), reps, torch.cuda.current_stream()) / reps
+    flush = flush or L2Flush()
+    cache.profile_start(kinds=("prefill", "append"))
+    _kernel_loop_flushed(lambda: G.context_prefill_step(cache, x), reps, flush)
     prof = cache.profile_read()
     err = cache.check_error()
     cache.close()
@@ -346,13 +376,14 @@ def secondary_prefix_hit(P, W, G, peaks, reps=20):
     tflops = w.flops() / kern / 1e12
     return {"workload": "16 prompt tails (12 + U{100..300} tokens) over a cached 1488-token prefix shared by every "
                         "table, 32/32 heads, D=128, fp16, bs=16", "tail_tokens": w.total_tokens,
-            "tokens_per_s": round(w.total_tokens / dt, 1), "ms": round(dt * 1e3, 4),
+            "tokens_per_s": round(w.total_tokens / dt, 1), "ms_back_to_back": round(dt * 1e3, 4),
             "attention_kernel_ms": round(kern * 1e3, 4), "append_kernel_ms": round(app * 1e3, 4),
+            "l2": "flushed before each timed call",
             "gflop": round(w.flops() / 1e9, 3), "tflops": round(tflops, 2),
             "frac_of_bf16_peak": round(tflops / peaks[1], 4), "device_errors": err}
 
 
-def secondary_blocks(P, W, G, peaks, reps=20, nblocks=512):
+def secondary_blocks(P, W, G, peaks, reps=20, nblocks=512, flush=None):
     """Whole-block copy (copy-on-write), swap-out to and swap-in from page-locked host memory:
     512 blocks of the 7B layer shape (256 KB each, 128 MB)."""
     nb = 2 * nblocks + 8
@@ -363,7 +394,7 @@ def secondary_blocks(P, W, G, peaks, reps=20, nblocks=512):
     nbytes = nblocks * cache.block_bytes
     host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
     res = {"workload": f"{nblocks} blocks of 16 tokens x 32 KV heads x 128 x fp16 (256 KB each)",
-           "bytes_per_call": nbytes}
+           "bytes_per_call": nbytes, "l2": "flushed before each timed launch"}
     # copy: HBM read + write; swaps: the bytes that cross to or from host memory
     for name, fn, moved in (("copy", lambda: P.paged_block_copy(cache, src, dst), 2 * nbytes),
                             ("swap_out_host", lambda: P.paged_block_swap_out(cache, src, host), nbytes),
@@ -371,8 +402,9 @@ def secondary_blocks(P, W, G, peaks, reps=20, nblocks=512):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
+        flush = flush or L2Flush()
         cache.profile_start(kinds=("copy",))
-        _time_loop(fn, reps, torch.cuda.current_stream())
+        _kernel_loop_flushed(fn, reps, flush)
         prof = cache.profile_read()
         kern = prof["copy_ms"] / max(1, prof["copy_launches"]) / 1e3
         gbs = moved / kern / 1e9
@@ -414,6 +446,55 @@ def secondary_prefix_cache(P, reps=5):
     return {"workload": "64 prompts of 4096 tokens sharing 4064 (bs 32): hash, lookup, allocate, publish, release",
             "blocks": nblk, "hit_blocks": hits, "ms": round(best * 1e3, 3),
             "blocks_per_s": round(nblk / best, 1), "where": "host (C++), one thread"}
+
+
+def compact_secondary(sec: dict) -> dict:
+    """The secondary figures as they go on the bench line: numbers only, short keys, the kernels
+    furthest from their roofline last (the full records, with workload descriptions, go to
+    --detail-out).  fr = fraction of the measured peak (HBM for decode / append / copy, dense bf16
+    for the prefills); us = mean kernel time; err = device error bits."""
+    if not sec:
+        return {}
+    out = {}
+    if "prefix13b" in sec:
+        d = sec["prefix13b"]
+        out["prefix13b"] = {"us": d["decode_kernel_us"], "gbs_logical": d["kv_gbs"], "gbs_unique": d["unique_kv_gbs"],
+                            "err": d["device_errors"]}
+    if "prefix13b_cascade" in sec:
+        d = sec["prefix13b_cascade"]
+        out["cascade13b"] = {"step_us": d["step_us"], "kernels_us": d["decode_kernel_us"],
+                             "fr_unique": d["unique_frac_of_hbm"], "gbs_unique_step": d["unique_kv_gbs_per_step"],
+                             "err": d["device_errors"]}
+    if "stress" in sec:
+        st = sec["stress"]
+        out["stress"] = {k: {"us": v["decode_kernel_us"], "gbs": v["kv_gbs"], "fr": v["frac_of_hbm"],
+                             "err": v["device_errors"]}
+                         for k, v in st.items() if isinstance(v, dict)}
+        out["stress"]["fp8_over_bf16_time"] = [st[f"bs{b}_fp8_over_bf16_time"] for b in (8, 16, 32)]
+    if "prefix_cache_host" in sec:
+        out["prefix_cache_blocks_per_s"] = sec["prefix_cache_host"]["blocks_per_s"]
+    if "blocks" in sec:
+        b = sec["blocks"]
+        out["blocks"] = {"copy_fr": b["copy"]["frac_of_hbm"], "copy_us": b["copy"]["kernel_us"],
+                         "swap_out_gbs": b["swap_out_host"]["host_gbs"], "swap_in_gbs": b["swap_in_host"]["host_gbs"],
+                         "err": b["device_errors"]}
+    if "prefix_hit_prefill" in sec:
+        d = sec["prefix_hit_prefill"]
+        out["prefix_hit"] = {"attn_us": round(d["attention_kernel_ms"] * 1e3, 2),
+                             "append_us": round(d["append_kernel_ms"] * 1e3, 2), "tflops": d["tflops"],
+                             "fr": d["frac_of_bf16_peak"], "err": d["device_errors"]}
+    if "append" in sec:
+        d = sec["append"]
+        out["append5256"] = {"us": round(d["kernel_ms"] * 1e3, 2), "gbs": d["gbs"], "fr": d["frac_of_hbm"]}
+    if "prefill" in sec:
+        d = sec["prefill"]
+        if "kernel_ms" in d:
+            out["prefill5256"] = {"us": round(d["kernel_ms"] * 1e3, 2), "tflops": d["tflops"],
+                                  "fr": d["frac_of_bf16_peak"], "err": d["device_errors"]}
+        else:
+            out["prefill5256"] = d
+    out["l2"] = "flushed before each timed append / copy / prefill launch; decode inputs exceed L2"
+    return out
 
 
 def run_only(case: str):
@@ -478,7 +559,9 @@ def run_ours(args):
     launches0 = P.kernel_launches()
     # events around every 10th decode kernel only: the kernel's duration is sampled live while the
     # other steps keep the append -> decode -> merge overlap of programmatic dependent launch
-    cache.profile_start(kinds=("decode",), every=10)
+    # (every 10th launch over long runs; at least 10 launches bracketed when the run is short)
+    every = max(1, min(10, args.steps // 10))
+    cache.profile_start(kinds=("decode",), every=every)
     _barrier(ws)
     torch.cuda.synchronize()
     elapsed = _time_loop(step, args.steps, stream)
@@ -596,11 +679,7 @@ def run_ours(args):
 
     secondary = {}
     if rank == 0 and not args.skip_secondary:
-        secondary["prefill"] = secondary_prefill(P, W, G, peaks)
-        secondary["append"] = secondary_append(P, W, G, peaks)
-        secondary["prefix_hit_prefill"] = secondary_prefix_hit(P, W, G, peaks)
-        secondary["blocks"] = secondary_blocks(P, W, G, peaks)
-        secondary["prefix_cache_host"] = secondary_prefix_cache(P)
+        flush = L2Flush()
         w4 = W.prefix13b()
         uniq = (w4.shared_prefix_len + int((w4.context_lens - w4.shared_prefix_len + 1).sum())) * \
             w4.num_kv_heads * w4.head_dim * 2 * 2
@@ -621,6 +700,14 @@ def run_ours(args):
                                                          stress[f"bs{bs}_bf16"]["decode_kernel_us"], 3)
         secondary["stress"] = dict(workload="256 seqs, log-normal lengths (median 500, cap 8192), 32 q / 8 KV heads, "
                                             "D=128, churned free list; KV bf16 or FP8-E4M3 (per-head scales)", **stress)
+        secondary["prefix_cache_host"] = secondary_prefix_cache(P)
+        secondary["blocks"] = secondary_blocks(P, W, G, peaks, flush=flush)
+        secondary["prefix_hit_prefill"] = secondary_prefix_hit(P, W, G, peaks, flush=flush)
+        secondary["append"] = secondary_append(P, W, G, peaks, flush=flush)
+        secondary["prefill"] = secondary_prefill(P, W, G, peaks, flush=flush)
+        if args.detail_out:
+            with open(args.detail_out, "w") as f:
+                json.dump(secondary, f, indent=1)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.skip_cpu:
@@ -650,6 +737,7 @@ def run_ours(args):
                          "traffic_source": "profiles/decode_kernel_decode7b.md (ncu dram__bytes_read+write, one launch)",
                          "kernel": "pkv_decode::decode_kernel<128,1,f16,f16>",
                          "kernel_ms": round(dec_kernel_s * 1e3, 5),
+                         "kernel_ms_samples": int(prof["decode_launches"]),
                          "peak_source": f"{peaks[3]} hbm_gbs (MEASURED_PEAKS.json)",
                          "algorithmic_bytes": "KV read: sum(L+1) x Hkv x D x 2 B x 2 (K and V) per launch"},
             "step_breakdown": breakdown,
@@ -662,7 +750,7 @@ def run_ours(args):
             "gpu_launches": int(launches),
             "clocks": clocks,
             "cpu_baseline": cpu,
-            "secondary": secondary,
+            "secondary": compact_secondary(secondary),
         }
         print(json.dumps(line), flush=True)
     cache.close()
@@ -682,6 +770,8 @@ def main():
     ap.add_argument("--clocks-dir", default=None,
                     help="folder for the nvidia-smi clock samples of the timed region (default: the temp dir)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--detail-out", default=None,
+                    help="file for the full secondary records (workload descriptions included)")
     ap.add_argument("--only", default=None,
                     help="run one secondary case alone and print its JSON (for profiling): prefill, append, "
                          "prefix13b, prefix13b_cascade, prefix_hit, blocks, prefix_cache or stress_bs{8,16,32}_{bf16,fp8}")

@@ -85,12 +85,21 @@ int kv_cache_set_scales(pkv_cache_t cache, const float *k_scale, const float *v_
 int kv_cache_view(pkv_cache_t cache, void **base, int64_t strides_elems[5], int64_t *num_bytes);
 
 /* Pre-size the decode split-K workspace for up to max_seqs x max_q_heads rows and tables
- * of max_blocks_per_seq entries, so that later decode calls allocate nothing. */
+ * of max_blocks_per_seq entries, so that later decode calls allocate nothing (a batch larger
+ * than one launch takes needs only one launch's rows: the launches share the workspace). */
 int kv_cache_reserve(pkv_cache_t cache, int max_seqs, int max_q_heads, int max_blocks_per_seq);
 
 /* Synchronise the device, return the device error word's bits in *device_code and clear
  * it.  Returns PKV_EDEVICE when any bit was set, PKV_OK otherwise. */
 int kv_cache_check_error(pkv_cache_t cache, int *device_code);
+
+/* Self-test of the kernels' bounded waits (discosf.com section 5.1 and 2kiu.com section 6.1: a
+ * failure must degrade, not hang or crash).  Enqueues one small kernel that waits on an mbarrier
+ * nothing ever arrives on, with the same wait routines every kernel uses (spinning and
+ * suspend-hint forms), for limit_ns nanoseconds (1 .. 1e9); both give up and set
+ * PKV_DEVERR_TIMEOUT in the cache's error word, which kv_cache_check_error then reports.  No
+ * memory besides that word is touched, nothing traps, and the cache stays usable. */
+int kv_cache_selftest_wait_timeout(pkv_cache_t cache, uint64_t limit_ns, void *stream);
 
 /* Message for the calling thread's most recent non-OK return ("" if none). */
 const char *pkv_last_error(void);
@@ -132,10 +141,12 @@ int paged_kv_append_at(pkv_cache_t cache, const void *k, const void *v, const in
  * h / (num_q_heads / num_kv_heads).  q, out: [num_seqs][num_q_heads][head_dim] model dtype;
  * block_tables: int32 [num_seqs][max_blocks_per_seq]; entries past ceil(L_s/block_size)
  * are never read.  L_s == 0 gives a zero row.  fp32 accumulation and softmax; the output
- * is rounded to the model dtype (nearest-even).  num_seqs <= 1024.  Runs a split-K pass
- * over block-aligned chunks of each sequence plus a merge; split boundaries depend only on
- * L_s, so results do not depend on block placement.  The workspace grows (cudaMalloc) on
- * demand unless kv_cache_reserve covered the call. */
+ * is rounded to the model dtype (nearest-even).  Runs a split-K pass over block-aligned chunks
+ * of each sequence plus a merge; split boundaries depend only on L_s, so results do not depend
+ * on block placement.  Any num_seqs: a batch larger than one launch takes (1024 sequences, or
+ * fewer for the tensor-core kernel of grouped-query heads, whose shared memory holds fewer) runs
+ * as consecutive launches of that many sequences on the stream, sharing one workspace sized for
+ * a launch.  The workspace grows (cudaMalloc) on demand unless kv_cache_reserve covered the call. */
 int paged_decode_attention(const void *q, pkv_cache_t cache, const int32_t *block_tables, int max_blocks_per_seq,
                            const int32_t *context_lens, int num_seqs, int num_q_heads, float scale, void *out,
                            void *stream);
@@ -145,16 +156,21 @@ int paged_decode_attention(const void *q, pkv_cache_t cache, const int32_t *bloc
  * that hands nearly all device memory to its own allocator (its KV pool is sized to fill the GPU)
  * or that cannot afford the device-wide synchronisation cudaMalloc/cudaFree may cause.
  * Same arguments, results and errors as paged_decode_attention, but the split-K partials live in
- * one fixed 16 MiB array compiled into the library (every GPU that loads the library holds it until
- * the process exits) instead of the cache's workspace; nothing is allocated, by CUDA or otherwise.
- * A call whose partials do not fit (S x Hq x ceil(max_blocks_per_seq / split blocks) x (D + 2)
- * floats > 16 MiB; with the default 256-token splits, e.g., 32 sequences x 32 heads x 4096-token
- * tables need 9 MB) returns PKV_EINVAL with the sizes in pkv_last_error().
- * The first call on a device looks up the array's device address on that device (one
- * cudaGetSymbolAddress, made with that device current); make that first call before any stream
- * capture.  Every call shares the array: calls whose work can overlap on the GPU (different
- * streams, or different host threads) race on it and must be serialised by the caller.  Nothing
- * in the array has to start at zero; each call writes every partial before it reads it. */
+ * one fixed 16 MiB array compiled into the library instead of the cache's workspace; nothing is
+ * allocated, by CUDA or otherwise.  The array becomes resident on a device (and its device address
+ * is looked up, one cudaGetSymbolAddress made with that device current) when kv_cache_create makes
+ * a cache there, so create the cache before handing the rest of the device memory to another
+ * allocator; it then stays until the process exits.  A cudaDeviceReset destroys every cache; the
+ * next kv_cache_create on the device repeats the lookup.  The kernels' own code is loaded by CUDA on
+ * their first launch (lazy module loading), which can allocate a little device memory once: make one
+ * warm-up call (or run with CUDA_MODULE_LOADING=EAGER) before the memory is handed out.
+ * A call whose partials for one launch do not fit (n x Hq x ceil(max_blocks_per_seq / split
+ * blocks) x (D + 2) floats > 16 MiB, n = min(num_seqs, sequences per launch); with the default
+ * 256-token splits, e.g., 32 sequences x 32 heads x 4096-token tables need 9 MB) returns PKV_EINVAL
+ * with the sizes in pkv_last_error().  Every call shares the array: calls whose work can overlap
+ * on the GPU (different streams, or different host threads) race on it and must be serialised by
+ * the caller.  Nothing in the array has to start at zero; each call writes every partial before it
+ * reads it. */
 int paged_decode_attention_noalloc(const void *q, pkv_cache_t cache, const int32_t *block_tables,
                                    int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                                    int num_q_heads, float scale, void *out, void *stream);

@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
         L.kv_cache_profile_start_sampled.argtypes = [vp, ctypes.c_uint, ctypes.c_int]
         L.kv_cache_profile_read.argtypes = [vp, ctypes.c_void_p]
         L.pkv_kernel_launches.restype = i64
+        L.kv_cache_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
         _lib = L
         return L
 
@@ -186,6 +187,11 @@ class KVCache:
         if st not in (0, -5):
             _check(st)
         return int(code.value)
+
+    def selftest_wait_timeout(self, limit_ns: int = 1_000_000):
+        """Enqueue the bounded-wait self-test: a kernel waits on an mbarrier that never completes
+        and gives up after limit_ns, setting the timeout bit that check_error then returns."""
+        _check(lib().kv_cache_selftest_wait_timeout(self.handle, int(limit_ns), _stream()))
 
     PROFILE = {"decode": 1, "prefill": 2, "append": 4, "merge": 8, "copy": 16}
 
@@ -304,9 +310,10 @@ def paged_decode_attention_noalloc(q: torch.Tensor, cache: KVCache, block_tables
                                    context_lens: torch.Tensor, scale: float, out: torch.Tensor) -> torch.Tensor:
     """paged_decode_attention for callers that must not allocate device memory.
 
-    The library keeps the split-K partials in a fixed 16 MiB array of its own instead of the
-    cache's growable workspace, so this call allocates nothing (the caller provides ``out``).
-    Calls that can overlap on the GPU share that array and must be serialised by the caller."""
+    The library keeps the split-K partials in a fixed 16 MiB array of its own (made resident when
+    the cache was created) instead of the cache's growable workspace, so this call allocates
+    nothing (the caller provides ``out``).  Calls that can overlap on the GPU share that array and
+    must be serialised by the caller."""
     _req(q, "q", cache.torch_dtype, 3)
     _req(block_tables, "block_tables", torch.int32, 2)
     _req(context_lens, "context_lens", torch.int32, 1)

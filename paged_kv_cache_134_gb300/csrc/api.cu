@@ -1,6 +1,7 @@
 // C ABI of the library: handle management, host-side validation, launches, error
 // reporting and profiling.  Every computation happens in the kernels of append.cu,
 // decode*.cu, prefill.cu and blocks.cu.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -55,6 +56,40 @@ int pkv_fail(int status, const char *fmt, ...) {
 
 int pkv_cuda_fail(cudaError_t e, const char *what) {
     return pkv_fail(PKV_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+cudaError_t launch_decode_chunked(pkv_cache *c, DecodeLaunch d, cudaStream_t st) {
+    const int G = d.num_q_heads / c->num_kv_heads;
+    const int per = decode_seqs_per_launch(c, G);
+    const int total = d.num_seqs;
+    const int64_t row_bytes = (int64_t)d.num_q_heads * c->head_dim * 2; // q and out rows, 16-bit model dtype
+    const char *q0 = static_cast<const char *>(d.q);
+    char *out0 = static_cast<char *>(d.out);
+    const int32_t *tables0 = d.tables, *lens0 = d.lens;
+    CascadePrefixLaunch p;
+    if (d.prefix) p = *d.prefix;
+    for (int s0 = 0; s0 < total; s0 += per) {
+        const int n = total - s0 < per ? total - s0 : per;
+        d.q = q0 + s0 * row_bytes;
+        d.out = out0 + s0 * row_bytes;
+        d.tables = tables0 ? tables0 + (int64_t)s0 * d.max_blocks : nullptr;
+        d.lens = lens0 + s0;
+        d.num_seqs = n;
+        if (d.prefix) {
+            // the launch's own rows: its queries, its tables (every one names the shared prefix), and the
+            // (m, l) half of the workspace right after its n * Hq * max_splits partial rows
+            p.q = d.q;
+            p.tables = d.tables;
+            p.num_seqs = n;
+            p.ws_ml = p.ws_o + (int64_t)n * d.num_q_heads * d.max_splits * c->head_dim;
+            cudaError_t e = launch_cascade_prefix(c, p, st, 1);
+            if (e != cudaSuccess) return e;
+            d.prefix = &p;
+        }
+        cudaError_t e = launch_decode(c, d, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 PkvTimer::PkvTimer(pkv_cache *c_, int kind_, cudaStream_t st_) : c(c_), kind(kind_), st(st_) {
@@ -122,6 +157,14 @@ int kv_cache_create(int64_t num_blocks, int block_size, int num_kv_heads, int he
     }
     if (e == cudaSuccess) e = cudaMemset(c->pool, 0, (size_t)c->pool_bytes);
     if (e == cudaSuccess) e = cudaMemset(c->err, 0, 16);
+    if (e == cudaSuccess) {
+        // the no-alloc decode's fixed scratch is made resident on this device now, while the cache is
+        // created, so that paged_decode_attention_noalloc never has to bring it in later
+        if (int r = pkv_noalloc_scratch_prepare(c->device)) {
+            kv_cache_destroy(c);
+            return r;
+        }
+    }
     if (e == cudaSuccess && c->k_scale) {
         // default scale 1.0f (0x3F800000)
         float ones[256];
@@ -197,7 +240,11 @@ int kv_cache_reserve(pkv_cache_t c, int max_seqs, int max_q_heads, int max_block
     if (int r = check_device(c)) return r;
     const int bps = decode_split_blocks(c);
     const int max_splits = (max_blocks_per_seq + bps - 1) / bps;
-    return ensure_workspace(c, decode_workspace_floats(c, max_seqs, max_q_heads, max_splits));
+    // consecutive launches of one call share the workspace: one launch's rows are enough
+    int rows = max_seqs;
+    if (max_q_heads > 0 && max_q_heads % c->num_kv_heads == 0 && supported_group(max_q_heads / c->num_kv_heads))
+        rows = std::min(rows, decode_seqs_per_launch(c, max_q_heads / c->num_kv_heads));
+    return ensure_workspace(c, decode_workspace_floats(c, rows, max_q_heads, max_splits));
 }
 
 int kv_cache_check_error(pkv_cache_t c, int *device_code) {
@@ -262,7 +309,6 @@ int paged_decode_attention(const void *q, pkv_cache_t c, const int32_t *block_ta
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     if (num_seqs < 0 || max_blocks_per_seq < 0) return pkv_fail(PKV_EINVAL, "negative size");
     if (num_seqs == 0) return PKV_OK;
-    if (num_seqs > 1024) return pkv_fail(PKV_EUNSUPPORTED, "num_seqs %d > 1024 per call", num_seqs);
     if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads)
         return pkv_fail(PKV_EINVAL, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
                         c->num_kv_heads);
@@ -274,6 +320,8 @@ int paged_decode_attention(const void *q, pkv_cache_t c, const int32_t *block_ta
     if (!aligned16(q) || !aligned16(out)) return pkv_fail(PKV_EINVAL, "q and out must be 16-byte aligned");
     if (!(scale == scale)) return pkv_fail(PKV_EINVAL, "scale is NaN");
     if (int r = check_device(c)) return r;
+    // a batch larger than one launch takes runs in consecutive launches that share the workspace
+    const int per_launch = std::min(num_seqs, decode_seqs_per_launch(c, num_q_heads / c->num_kv_heads));
     DecodeLaunch d;
     d.q = q;
     d.out = out;
@@ -285,11 +333,11 @@ int paged_decode_attention(const void *q, pkv_cache_t c, const int32_t *block_ta
     d.scale = scale;
     d.split_blocks = decode_split_blocks(c);
     d.max_splits = (max_blocks_per_seq + d.split_blocks - 1) / d.split_blocks;
-    const int64_t ws = decode_workspace_floats(c, num_seqs, num_q_heads, d.max_splits);
+    const int64_t ws = decode_workspace_floats(c, per_launch, num_q_heads, d.max_splits);
     if (int r = ensure_workspace(c, ws)) return r;
     d.ws_o = ws ? c->ws : nullptr;
     d.ws_ml = nullptr;
-    cudaError_t e = launch_decode(c, d, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_decode_chunked(c, d, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return pkv_cuda_fail(e, "decode launch");
     return PKV_OK;
 }
@@ -346,7 +394,6 @@ int paged_decode_attention_cascade(const void *q, pkv_cache_t c, const int32_t *
                                       scale, out, stream);
     if (num_seqs < 0 || max_blocks_per_seq < 0) return pkv_fail(PKV_EINVAL, "negative size");
     if (num_seqs == 0) return PKV_OK;
-    if (num_seqs > 1024) return pkv_fail(PKV_EUNSUPPORTED, "num_seqs %d > 1024 per call", num_seqs);
     if ((int64_t)shared_prefix_len > (int64_t)max_blocks_per_seq * c->block_size)
         return pkv_fail(PKV_EINVAL, "shared prefix longer than the tables");
     if (c->kv_dtype == PKV_FP8_E4M3)
@@ -361,7 +408,9 @@ int paged_decode_attention_cascade(const void *q, pkv_cache_t c, const int32_t *
     if (!aligned16(q) || !aligned16(out)) return pkv_fail(PKV_EINVAL, "q and out must be 16-byte aligned");
     if (!(scale == scale)) return pkv_fail(PKV_EINVAL, "scale is NaN");
     if (int r = check_device(c)) return r;
-    const int split_tokens = cascade_split_tokens(c, num_seqs, num_q_heads, shared_prefix_len);
+    // a batch larger than one launch takes runs in consecutive launches (each reads the prefix once)
+    const int per_launch = std::min(num_seqs, decode_seqs_per_launch(c, num_q_heads / c->num_kv_heads));
+    const int split_tokens = cascade_split_tokens(c, per_launch, num_q_heads, shared_prefix_len);
     const int nps = (shared_prefix_len + split_tokens - 1) / split_tokens;
     const int pb = shared_prefix_len / c->block_size;
     DecodeLaunch d;
@@ -377,7 +426,7 @@ int paged_decode_attention_cascade(const void *q, pkv_cache_t c, const int32_t *
     d.max_splits = nps + (max_blocks_per_seq - pb + d.split_blocks - 1) / d.split_blocks;
     d.start_block = pb;
     d.slot0 = nps;
-    const int64_t rows = (int64_t)num_seqs * num_q_heads * d.max_splits;
+    const int64_t rows = (int64_t)per_launch * num_q_heads * d.max_splits;
     if (int r = ensure_workspace(c, rows * (c->head_dim + 2))) return r;
     d.ws_o = c->ws;
     d.ws_ml = nullptr;
@@ -394,13 +443,12 @@ int paged_decode_attention_cascade(const void *q, pkv_cache_t c, const int32_t *
     p.ws_o = c->ws;
     p.ws_ml = c->ws + rows * c->head_dim;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // launches: the prefix phase's plan, the suffix decode, the prefix kernel, the merge
-    cudaError_t e = launch_cascade_prefix(c, p, st, 1);
-    if (e == cudaErrorNotSupported) return pkv_fail(PKV_EUNSUPPORTED, "cascade shape not supported");
-    if (e != cudaSuccess) return pkv_cuda_fail(e, "cascade prefix launch");
+    // launches, per run of sequences: the prefix phase's plan, the suffix decode, the prefix kernel,
+    // the merge
     d.prefix = &p;
-    e = launch_decode(c, d, st);
-    if (e != cudaSuccess) return pkv_cuda_fail(e, "decode launch");
+    cudaError_t e = launch_decode_chunked(c, d, st);
+    if (e == cudaErrorNotSupported) return pkv_fail(PKV_EUNSUPPORTED, "cascade shape not supported");
+    if (e != cudaSuccess) return pkv_cuda_fail(e, "cascade decode launch");
     return PKV_OK;
 }
 

@@ -50,6 +50,16 @@ int decode_split_blocks(const pkv_cache *c) {
     return b > 0 ? b : 1;
 }
 
+int decode_seqs_per_launch(const pkv_cache *c, int G) {
+    // Both decode kernels keep a per-sequence unit table (3 ints a sequence) in shared memory: the
+    // CUDA-core kernel takes up to kMaxSeqs sequences a launch; the tensor-core kernel, whose stage
+    // rings fill nearly all of shared memory, fewer (the largest multiple of 64 that still fits).
+    int n = pkv_decode::kMaxSeqs;
+    if (pkv_decode_tc_eligible(c, G, 64))
+        while (n > 64 && !pkv_decode_tc_eligible(c, G, n)) n -= 64;
+    return n;
+}
+
 int64_t decode_workspace_floats(const pkv_cache *c, int num_seqs, int num_q_heads, int max_splits) {
     // partial o [rows][D] and (m, l) [rows][2], rows = S * Hq * max_splits; only needed when splits > 1
     if (max_splits <= 1) return 0;

@@ -82,16 +82,20 @@ PKV_DEV bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.  Returns false after
-// PKV_WAIT_LIMIT_NS without completion.
-PKV_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Bounded wait for the phase with the given parity to complete.  Returns false after limit_ns
+// without completion (checked every 256 tests), or after 2^31 tests whatever the clock says.
+PKV_DEV bool mbar_wait_for(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
+    for (uint32_t i = 1; i < 0x80000000u; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0u && global_timer_ns() - t0 > PKV_WAIT_LIMIT_NS) return false;
+        if ((i & 255u) == 0u && global_timer_ns() - t0 > limit_ns) return false;
     }
+    return false;
 }
+
+// The kernels' wait: bounded by PKV_WAIT_LIMIT_NS.
+PKV_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) { return mbar_wait_for(bar, parity, PKV_WAIT_LIMIT_NS); }
 
 // The same bounded wait with a suspend-time hint: a warp whose phase has not completed sleeps in
 // the barrier until it completes (or the hint runs out) instead of re-testing it, which leaves the
@@ -110,17 +114,18 @@ PKV_DEV bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-static __device__ __noinline__ bool mbar_wait_sleep_slow(uint32_t bar, uint32_t parity) {
+static __device__ __noinline__ bool mbar_wait_sleep_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = global_timer_ns();
-    for (;;) {
+    for (uint32_t i = 0; i < 0x80000000u; ++i) {
         if (mbar_try_wait_sleep(bar, parity)) return true;
-        if (global_timer_ns() - t0 > PKV_WAIT_LIMIT_NS) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
+    return false;
 }
 
-PKV_DEV bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
+PKV_DEV bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint64_t limit_ns = PKV_WAIT_LIMIT_NS) {
     const uint32_t b = smem_u32(bar);
-    return mbar_try_wait_sleep(b, parity) || mbar_wait_sleep_slow(b, parity);
+    return mbar_try_wait_sleep(b, parity) || mbar_wait_sleep_slow(b, parity, limit_ns);
 }
 
 // two-lane fp32 arithmetic (one instruction for both lanes): a * b + c and a + b; max of three

@@ -135,6 +135,17 @@ cudaError_t launch_cascade_prefix(pkv_cache *c, const CascadePrefixLaunch &p, cu
 // keys per prefix split of the cascade's prefix phase (a multiple of 64)
 int cascade_split_tokens(const pkv_cache *c, int num_seqs, int num_q_heads, int prefix_tokens);
 int64_t decode_workspace_floats(const pkv_cache *c, int num_seqs, int num_q_heads, int max_splits);
+// Sequences one decode launch takes at most (its kernels hold a per-sequence table in shared memory);
+// a call with more runs its sequences in consecutive launches of this many, which reuse one workspace
+// (stream order: each launch waits for the previous launch's merge before it writes partials).
+int decode_seqs_per_launch(const pkv_cache *c, int G);
+// Runs the decode described by d (d.ws_o sized for min(num_seqs, decode_seqs_per_launch) sequences)
+// as consecutive launches of at most decode_seqs_per_launch sequences each (api.cu).
+cudaError_t launch_decode_chunked(pkv_cache *c, DecodeLaunch d, cudaStream_t st);
+// The no-alloc decode's fixed scratch: makes it resident on the current device and records its device
+// address (noalloc.cu); kv_cache_create calls it, so the array is in place before a caller's allocator
+// takes the rest of the device memory.
+int pkv_noalloc_scratch_prepare(int device);
 int decode_split_blocks(const pkv_cache *c);
 cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st);
 // tensor-core decode for grouped-query heads (decode_tc.cu)

@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-from gpu_path import DecodeInputs, assert_close, decode_step, fill_cache, new_cache, run_decode  # noqa: E402
+from gpu_path import OUT_DT, DecodeInputs, assert_close, decode_step, fill_cache, new_cache, run_decode  # noqa: E402
 
 ATOL, RTOL = 2e-3, 1e-2
 
@@ -26,7 +26,7 @@ def check_cascade(w, tag):
     r = steps.decode_step(w, strides=g["strides"], pool_elems=g["pool"].size)
     assert g["err"] == 0, f"device error bits {g['err']}"
     assert np.array_equal(g["new_slots"], r["new_slots"]) and np.array_equal(g["pool"], r["pool"])
-    mx, rel = assert_close(g["out"], r["out"], ATOL, RTOL, tag)
+    mx, rel = assert_close(g["out"], r["out"], ATOL, RTOL, tag, out_dtype=OUT_DT(w))
     print(f"{tag}: max abs {mx:.2e} max rel {rel:.2e}")
     return g
 
@@ -40,6 +40,10 @@ CASES = [
     dict(num_seqs=9, prefix_tokens=1120, max_suffix=700, heads=8, kv_heads=2, d=128, bs=8, dtype="bf16"),
     # suffixes shorter than a block and longer than a split
     dict(num_seqs=16, prefix_tokens=256, max_suffix=2000, heads=4, d=128, bs=16),
+    # more sequences than one launch takes (1024): two runs of launches, each reading the prefix once
+    dict(num_seqs=1100, prefix_tokens=256, max_suffix=60, heads=2, d=128, bs=16),
+    # the same with G = 4 (tensor-core suffix decode, whose launches take fewer sequences)
+    dict(num_seqs=1100, prefix_tokens=192, max_suffix=60, heads=8, kv_heads=2, d=128, bs=16, dtype="bf16"),
 ]
 
 

@@ -32,7 +32,7 @@ def check_decode(w, tag):
     assert np.array_equal(g["fill_slots"], r["fill_slots"]), "fill slots differ"
     assert np.array_equal(g["new_slots"], r["new_slots"]), "new-token slots differ"
     assert np.array_equal(g["pool"], r["pool"]), f"pool bytes differ at {int(np.sum(g['pool'] != r['pool']))} elements"
-    mx, rel = assert_close(g["out"], r["out"], ATOL[w.kv_dtype], RTOL, tag)
+    mx, rel = assert_close(g["out"], r["out"], ATOL[w.kv_dtype], RTOL, tag, out_dtype=w.model_dtype)
     print(f"{tag}: max abs {mx:.2e} max rel {rel:.2e}")
     return g, r
 
@@ -185,3 +185,13 @@ def test_fused_append_matches_slot_mapping_plus_append():
     assert np.array_equal(a["new_slots"], b["new_slots"])
     assert np.array_equal(a["pool"], b["pool"])
     assert np.array_equal(a["out"], b["out"])
+
+
+@pytest.mark.parametrize("hq,hkv,kv", [(8, 8, "f16"), (8, 2, "bf16"), (8, 2, "fp8")], ids=["mha_f16", "gqa4_bf16",
+                                                                                      "gqa4_fp8"])
+def test_more_sequences_than_one_launch(hq, hkv, kv):
+    # 1500 sequences: more than one decode launch takes (1024, fewer for the tensor-core kernel of
+    # grouped-query heads), so the call runs as consecutive launches sharing one workspace
+    lens = np.random.default_rng(71).integers(0, 700, 1500)
+    w = W.small_decode(f"many_{kv}", lens, hq=hq, hkv=hkv, d=128, bs=16, kv_dtype=kv, seed=72)
+    check_decode(w, f"1500 sequences {kv} G={hq // hkv}")

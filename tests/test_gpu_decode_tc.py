@@ -35,7 +35,7 @@ def check(w, tag):
     r = steps.decode_step(w, strides=g["strides"], pool_elems=g["pool"].size)
     assert g["err"] == 0, f"{tag}: device error bits {g['err']}"
     assert np.array_equal(g["pool"], r["pool"]), f"{tag}: pool bytes differ"
-    mx, rel = assert_close(g["out"], r["out"], ATOL[w.kv_dtype], RTOL, tag)
+    mx, rel = assert_close(g["out"], r["out"], ATOL[w.kv_dtype], RTOL, tag, out_dtype=w.model_dtype)
     print(f"{tag}: max abs {mx:.2e} max rel {rel:.2e}")
     return g
 

@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-from gpu_path import assert_close, run_prefill  # noqa: E402
+from gpu_path import OUT_DT, assert_close, run_prefill  # noqa: E402
 
 ATOL, RTOL = 2e-3, 1e-2
 
@@ -25,7 +25,7 @@ def check_prefill(w, tag):
     r = steps.prefill_step(w, strides=g["strides"], pool_elems=g["pool"].size)
     assert g["err"] == 0, f"device error bits {g['err']}"
     assert np.array_equal(g["pool"], r["pool"]), f"pool differs at {int(np.sum(g['pool'] != r['pool']))} elements"
-    mx, rel = assert_close(g["out"], r["out"], ATOL, RTOL, tag)
+    mx, rel = assert_close(g["out"], r["out"], ATOL, RTOL, tag, out_dtype=OUT_DT(w))
     print(f"{tag}: max abs {mx:.2e} max rel {rel:.2e}")
     return g
 

@@ -2,16 +2,21 @@
 
 Such callers (a serving engine whose own allocator owns nearly all of the GPU's memory, or code
 that cannot afford the device-wide synchronisation of cudaMalloc/cudaFree) get the same decode
-with the split-K partials kept in a fixed scratch array inside the library.  This file checks,
-through the C ABI, that two calls in a row (different batches, so the second one runs on the
-first one's leftover scratch contents) agree with paged_decode_attention within the tolerance
-the other decode tests use, and that a call too large for the scratch is refused.  It is named so
-that pytest collects it last.
+with the split-K partials kept in a fixed scratch array inside the library, made resident when the
+cache is created.  Through the C ABI this file checks that:
+  * after one warm-up call (the first launch of a kernel may load its code), a no-alloc call on a
+    fresh cache leaves the device's free memory exactly as it was;
+  * two calls in a row (different batches, so the second runs on the first one's leftover scratch
+    contents) give bit for bit the output of paged_decode_attention, which runs the same kernels
+    with the same split plan, and both match the oracle within the decode tolerance;
+  * a call too large for the scratch is refused.
+It is named so that pytest collects it last.
 """
 import numpy as np
 import pytest
 import torch
 
+from oracle import steps
 from paged_kv_cache_134_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -34,17 +39,30 @@ def _prepared(w):
     return cache, x
 
 
-def test_noalloc_matches_allocating_decode_on_two_calls_in_a_row():
+def test_noalloc_allocates_nothing_and_matches_the_decode_bitwise_on_two_calls_in_a_row():
     batches = [W.decode7b(),  # 32 sequences up to 4097 tokens: most rows have several splits
                W.small_decode("second", [3000, 17, 0, 900, 2500, 64], hq=8, hkv=2, d=128, bs=16, seed=61)]
-    for w in batches:
+    for i, w in enumerate(batches):
         cache, x = _prepared(w)
-        ref = P.paged_decode_attention(x.q, cache, x.tables, x.lens, x.scale)
         got = torch.full_like(x.q, float("nan"))
+        warm = torch.empty_like(x.q)
+        # warm-up: the first launch of a kernel may load its code onto the device
+        P.paged_decode_attention_noalloc(x.q, cache, x.tables, x.lens, x.scale, warm)
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info()
         P.paged_decode_attention_noalloc(x.q, cache, x.tables, x.lens, x.scale, got)
         torch.cuda.synchronize()
+        free1, _ = torch.cuda.mem_get_info()
+        assert free1 == free0, f"batch {i}: device free memory moved by {free0 - free1} bytes"
         assert cache.check_error() == 0
-        assert_close(got.float().cpu().numpy(), ref.float().cpu().numpy(), ATOL, RTOL, w.name)
+        assert torch.equal(got, warm), f"batch {i}: two no-alloc calls differ"
+        # only now the allocating decode (it may grow the cache's workspace): same kernels, same splits
+        ref = P.paged_decode_attention(x.q, cache, x.tables, x.lens, x.scale)
+        torch.cuda.synchronize()
+        assert cache.check_error() == 0
+        assert torch.equal(got, ref), f"batch {i}: no-alloc output differs from paged_decode_attention"
+        r = steps.decode_step(w, strides=cache.view()[1], pool_elems=int(cache.pool_elems().numel()))
+        assert_close(got.float().cpu().numpy(), r["out"], ATOL, RTOL, f"no-alloc {w.name}", out_dtype=w.model_dtype)
         cache.close()
 
 
