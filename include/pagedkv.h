@@ -186,8 +186,11 @@ int paged_decode_attention_noalloc(const void *q, pkv_cache_t cache, const int32
  * (it reads nothing the decode writes); one merge combines both.  shared_prefix_len:
  * a multiple of block_size, at most max_blocks_per_seq * block_size, and at most every context
  * length (a shorter sequence sets PKV_DEVERR_LENGTH); 0 makes this paged_decode_attention.
- * fp16/bf16 caches (EUNSUPPORTED for FP8).  The prefix's split partials are rounded like any split
- * (fp32), so outputs agree with paged_decode_attention to the decode tolerance, not bit for bit. */
+ * fp16/bf16 and FP8 caches (E4M3 prefix codes are widened exactly to the model dtype in shared
+ * memory, the per-head scales fold into the softmax scale and the split partials).  The prefix's
+ * split partials are rounded like any split (fp32), so outputs agree with paged_decode_attention to
+ * the decode tolerance, not bit for bit.  The tensor-core prefix phase takes two prefix splits of
+ * one 128-sequence tile per item. */
 int paged_decode_attention_cascade(const void *q, pkv_cache_t cache, const int32_t *block_tables,
                                    int max_blocks_per_seq, const int32_t *context_lens, int num_seqs, int num_q_heads,
                                    int shared_prefix_len, float scale, void *out, void *stream);
@@ -201,8 +204,12 @@ int paged_decode_attention_cascade(const void *q, pkv_cache_t cache, const int32
  * k, v: [T][num_kv_heads][head_dim] (model dtype), T = total_tokens = cu_seqlens[num_seqs]
  * (passed from the host because the tensor maps of the loads need it); cu_seqlens: int32
  * [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0; max_seqlen >= every length.  A sequence
- * whose bounds break these rules is skipped and sets PKV_DEVERR_CU_SEQLENS.  fp16/bf16 caches only (EUNSUPPORTED for FP8).  Q.K^T and P.V run on the tensor
- * cores (tcgen05, fp32 accumulation in tensor memory); P is rounded to the model dtype for P.V. */
+ * whose bounds break these rules is skipped and sets PKV_DEVERR_CU_SEQLENS.  Q.K^T and P.V run on
+ * the tensor cores (tcgen05, fp32 accumulation in tensor memory), two 128-row query tiles of one
+ * (sequence, head) per work item sharing each 128-key K/V tile; P is rounded to the model dtype for
+ * P.V (bf16: a hi + lo pair).  FP8 caches: the attention reads the packed k, v as given, and the
+ * cache write is paged_kv_append's (E4M3 of fp32(x) / scale[head], the same bytes), issued as a
+ * separate launch before it. */
 int packed_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens, int num_seqs,
                              int max_seqlen, int64_t total_tokens, const int32_t *block_tables,
                              int max_blocks_per_seq, pkv_cache_t cache, int num_q_heads, float scale, void *out,
@@ -220,7 +227,10 @@ int packed_prefill_attention(const void *q, const void *k, const void *v, const 
  * context_lens 0 it computes what packed_prefill_attention computes.  context_lens: device int32
  * [num_seqs], each >= 0 with context + n_i <= max_blocks_per_seq * block_size (else the sequence
  * is skipped and PKV_DEVERR_LENGTH set); the table must name a block for every position below
- * context + n_i.  Other arguments, shapes and errors as for packed_prefill_attention. */
+ * context + n_i.  FP8 caches: the new tokens are written as paged_kv_append writes them, and every
+ * key and value is read as its stored code times the head's scale (codes widened exactly to the
+ * model dtype in shared memory).  Other arguments, shapes and errors as for
+ * packed_prefill_attention. */
 int paged_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
                             const int32_t *context_lens, int num_seqs, int max_seqlen, int64_t total_tokens,
                             const int32_t *block_tables, int max_blocks_per_seq, pkv_cache_t cache, int num_q_heads,

@@ -52,13 +52,13 @@ def prefill_step(w, strides=None, pool_elems=None):
     st = contiguous_strides(w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim) if strides is None \
         else np.asarray(strides, np.int64)
     n_elems = pool_elems if pool_elems is not None else w.num_blocks * 2 * w.num_kv_heads * w.block_size * w.head_dim
-    pool = new_pool(n_elems, w.dtype, _NAN[w.dtype])
+    pool = new_pool(n_elems, w.kv_dtype, _NAN[w.kv_dtype])
     seq_ids = np.repeat(np.arange(len(w.lengths), dtype=np.int32), w.lengths)
     positions = np.concatenate([np.arange(n, dtype=np.int32) for n in w.lengths]) if len(w.lengths) else \
         np.zeros(0, np.int32)
     slots = slot_mapping(w.block_tables, seq_ids, positions, w.block_size)
-    bad = kv_append(pool, st, w.dtype, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.k, w.v, w.dtype,
-                    slots)
+    bad = kv_append(pool, st, w.kv_dtype, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.k, w.v, w.dtype,
+                    slots, w.k_scale, w.v_scale)
     assert bad == 0
     out = packed_prefill(w.q, w.k, w.v, w.dtype, w.cu_seqlens, float(w.scale))
     return dict(slots=slots, pool=pool, out=out)
@@ -69,17 +69,17 @@ def context_prefill_step(w, strides=None, pool_elems=None):
     st = contiguous_strides(w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim) if strides is None \
         else np.asarray(strides, np.int64)
     n_elems = pool_elems if pool_elems is not None else w.num_blocks * 2 * w.num_kv_heads * w.block_size * w.head_dim
-    pool = new_pool(n_elems, w.dtype, _NAN[w.dtype])
+    pool = new_pool(n_elems, w.kv_dtype, _NAN[w.kv_dtype])
     fill_slots = slot_mapping(w.block_tables, w.fill_seq_ids, w.fill_positions, w.block_size)
-    bad = kv_append(pool, st, w.dtype, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.fill_k, w.fill_v,
-                    w.dtype, fill_slots)
+    bad = kv_append(pool, st, w.kv_dtype, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.fill_k, w.fill_v,
+                    w.dtype, fill_slots, w.k_scale, w.v_scale)
     seq_ids = np.repeat(np.arange(w.num_seqs, dtype=np.int32), w.new_lens)
     positions = np.concatenate([c + np.arange(n, dtype=np.int32) for c, n in zip(w.context_lens, w.new_lens)]) \
         if w.total_tokens else np.zeros(0, np.int32)
     new_slots = slot_mapping(w.block_tables, seq_ids, positions, w.block_size)
-    bad += kv_append(pool, st, w.dtype, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.k, w.v, w.dtype,
-                     new_slots)
+    bad += kv_append(pool, st, w.kv_dtype, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.k, w.v, w.dtype,
+                     new_slots, w.k_scale, w.v_scale)
     assert bad == 0, "workload produced slots outside the pool"
-    out = prefill_ctx(w.q, w.dtype, pool, st, w.dtype, w.num_blocks, w.block_tables, w.cu_seqlens, w.context_lens,
-                      w.num_kv_heads, w.block_size, float(w.scale))
+    out = prefill_ctx(w.q, w.dtype, pool, st, w.kv_dtype, w.num_blocks, w.block_tables, w.cu_seqlens, w.context_lens,
+                      w.num_kv_heads, w.block_size, float(w.scale), w.k_scale, w.v_scale)
     return dict(fill_slots=fill_slots, new_slots=new_slots, pool=pool, out=out)

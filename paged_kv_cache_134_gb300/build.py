@@ -17,7 +17,8 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libpagedkv.so")
 
 SOURCES = ["api.cu", "append.cu", "decode.cu", "decode_f16.cu", "decode_bf16.cu", "decode_fp8_f16.cu",
-           "decode_fp8_bf16.cu", "decode_tc.cu", "prefill.cu", "noalloc.cu", "blocks.cu", "selftest.cu",
+           "decode_fp8_bf16.cu", "decode_tc.cu", "prefill.cu", "prefill_packed.cu", "prefill_paged.cu",
+           "prefill_cascade.cu", "noalloc.cu", "blocks.cu", "selftest.cu",
            "prefix_cache.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -350,7 +350,6 @@ static int prefill_entry(const void *q, const void *k, const void *v, const int3
     if (num_seqs < 0 || max_seqlen < 0 || max_blocks_per_seq < 0 || total_tokens < 0)
         return pkv_fail(PKV_EINVAL, "negative size");
     if (total_tokens > 0x7FFFFFFF) return pkv_fail(PKV_EUNSUPPORTED, "more than 2^31 - 1 packed tokens");
-    if (c->kv_dtype == PKV_FP8_E4M3) return pkv_fail(PKV_EUNSUPPORTED, "prefill writes fp16/bf16 caches only");
     if (num_seqs == 0 || max_seqlen == 0 || total_tokens == 0) return PKV_OK;
     if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads)
         return pkv_fail(PKV_EINVAL, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
@@ -396,8 +395,6 @@ int paged_decode_attention_cascade(const void *q, pkv_cache_t c, const int32_t *
     if (num_seqs == 0) return PKV_OK;
     if ((int64_t)shared_prefix_len > (int64_t)max_blocks_per_seq * c->block_size)
         return pkv_fail(PKV_EINVAL, "shared prefix longer than the tables");
-    if (c->kv_dtype == PKV_FP8_E4M3)
-        return pkv_fail(PKV_EUNSUPPORTED, "cascade decode reads fp16/bf16 caches only");
     if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads)
         return pkv_fail(PKV_EINVAL, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
                         c->num_kv_heads);

@@ -39,6 +39,7 @@ struct AppendArgs {
     const int64_t *slots; // given slots (plain append) ...
     const int32_t *tables, *seq_ids, *positions; // ... or computed here (fused append)
     const int32_t *cu, *ctx; // ... or from packed ranges: token j of [cu[i], cu[i+1]) at position ctx[i] + j - cu[i]
+                             // (ctx NULL: position j - cu[i])
     int64_t *slots_out;
     int rows, max_blocks;
     char *pool;
@@ -73,8 +74,9 @@ PKV_DEV int64_t append_slot(const AppendArgs &a, int64_t j) {
                 hi = mid;
         }
         const int64_t st = a.cu[lo], en = a.cu[lo + 1];
-        const int64_t pos = (int64_t)a.ctx[lo] + (j - st);
-        return (j >= st && j < en && a.ctx[lo] >= 0 && pos <= 0x7FFFFFFF)
+        const int c0 = a.ctx ? a.ctx[lo] : 0; // no context lengths: every sequence starts at position 0
+        const int64_t pos = (int64_t)c0 + (j - st);
+        return (j >= st && j < en && c0 >= 0 && pos <= 0x7FFFFFFF)
                    ? slot_of(a.tables, a.rows, a.max_blocks, lo, (int)pos, a.bs)
                    : -1;
     } else {

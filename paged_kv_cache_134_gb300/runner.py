@@ -103,7 +103,8 @@ def run_decode(w, keep_cache=False, fused=True, cascade_prefix=0):
 
 def run_prefill(w, keep_cache=False):
     md = TORCH_DT[w.dtype]
-    cache = new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.dtype, w.dtype)
+    cache = new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype, w.dtype, w.k_scale,
+                      w.v_scale)
     q, k, v = dev(w.q, md), dev(w.k, md), dev(w.v, md)
     out = P.packed_prefill_attention(q, k, v, dev(w.cu_seqlens), w.max_seqlen, dev(w.block_tables), cache,
                                      float(w.scale))
@@ -145,7 +146,8 @@ def context_prefill_step(cache, x: ContextPrefillInputs):
 
 
 def run_context_prefill(w, keep_cache=False):
-    cache = new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.dtype, w.dtype)
+    cache = new_cache(w, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype, w.dtype, w.k_scale,
+                      w.v_scale)
     fill_context(cache, w)
     x = ContextPrefillInputs(w)
     out = context_prefill_step(cache, x)

@@ -197,6 +197,13 @@ class PrefillWorkload:
     k: np.ndarray                   # uint16 [T, Hkv, D]
     v: np.ndarray
     block_tables: np.ndarray        # int32 [num_seqs, max_blocks], -1 padded
+    kv_dtype: Optional[str] = None  # cache dtype (None: the model dtype)
+    k_scale: Optional[np.ndarray] = None  # float32 [Hkv] (FP8 cache only)
+    v_scale: Optional[np.ndarray] = None
+
+    def __post_init__(self):
+        if self.kv_dtype is None:
+            self.kv_dtype = self.dtype
 
     @property
     def total_tokens(self) -> int:
@@ -239,6 +246,13 @@ class ContextPrefillWorkload:
     v: np.ndarray
     ref_count: np.ndarray           # int32 [NB]
     shared_prefix_len: int = 0      # tokens at the head of every table, stored once
+    kv_dtype: Optional[str] = None  # cache dtype (None: the model dtype)
+    k_scale: Optional[np.ndarray] = None  # float32 [Hkv] (FP8 cache only)
+    v_scale: Optional[np.ndarray] = None
+
+    def __post_init__(self):
+        if self.kv_dtype is None:
+            self.kv_dtype = self.dtype
 
     @property
     def num_seqs(self) -> int:
@@ -262,7 +276,7 @@ class ContextPrefillWorkload:
 
 def context_prefill(seed: int = 1006, context_lens=(0, 16, 37, 200), new_lens=(5, 130, 64, 1), shared_prefix: int = 0,
                     heads: int = 4, kv_heads: Optional[int] = None, d: int = 128, bs: int = 16, dtype: str = F16,
-                    pool_factor: float = 1.25) -> ContextPrefillWorkload:
+                    pool_factor: float = 1.25, kv_dtype: Optional[str] = None) -> ContextPrefillWorkload:
     """Sequences holding context_lens[i] cached tokens get new_lens[i] tail tokens.  With shared_prefix
     > 0 (a multiple of bs) the first shared_prefix tokens of every sequence live once, in blocks every
     table points at (the prefix-cache hit, 2kiu.com section 4.3 step 3); the rest is private."""
@@ -298,17 +312,23 @@ def context_prefill(seed: int = 1006, context_lens=(0, 16, 37, 200), new_lens=(5
     N, T = len(fill_ids), int(nl.sum())
     cu = np.zeros(S + 1, dtype=np.int32)
     cu[1:] = np.cumsum(nl)
+    fill_k, fill_v = normal_bits(rng, (N, hkv, d), dtype), normal_bits(rng, (N, hkv, d), dtype)
+    q, k, v = normal_bits(rng, (T, heads, d), dtype), normal_bits(rng, (T, hkv, d), dtype), \
+        normal_bits(rng, (T, hkv, d), dtype)
+    ks = vs = None
+    if kv_dtype == FP8:
+        ks, vs = _fp8_scales(fill_k, k, dtype), _fp8_scales(fill_v, v, dtype)
     return ContextPrefillWorkload(
         name=f"context_prefill_T{T}", context_lens=ctx, new_lens=nl, cu_seqlens=cu, num_q_heads=heads,
         num_kv_heads=hkv, head_dim=d, block_size=bs, num_blocks=nb, dtype=dtype,
         scale=np.float32(1.0 / math.sqrt(d)), block_tables=bt, fill_seq_ids=fill_ids, fill_positions=fill_pos,
-        fill_k=normal_bits(rng, (N, hkv, d), dtype), fill_v=normal_bits(rng, (N, hkv, d), dtype),
-        q=normal_bits(rng, (T, heads, d), dtype), k=normal_bits(rng, (T, hkv, d), dtype),
-        v=normal_bits(rng, (T, hkv, d), dtype), ref_count=alloc.ref_count.copy(), shared_prefix_len=shared_prefix)
+        fill_k=fill_k, fill_v=fill_v, q=q, k=k, v=v, ref_count=alloc.ref_count.copy(), shared_prefix_len=shared_prefix,
+        kv_dtype=kv_dtype or dtype, k_scale=ks, v_scale=vs)
 
 
 def prefix_hit_prefill(seed: int = 1006, num_seqs: int = 16, prompt: int = 1500, tail=(100, 300), heads: int = 32,
-                       d: int = 128, bs: int = 16, dtype: str = F16) -> ContextPrefillWorkload:
+                       d: int = 128, bs: int = 16, dtype: str = F16,
+                       kv_dtype: Optional[str] = None) -> ContextPrefillWorkload:
     """A 1500-token system prompt cached once (its whole blocks: 1488 tokens), then per request the
     prompt's remaining 12 tokens plus a tail of U{100..300} tokens to prefill (the scenario of
     2kiu.com section 3.3: only the tail after the prefix hit is prefilled)."""
@@ -316,7 +336,7 @@ def prefix_hit_prefill(seed: int = 1006, num_seqs: int = 16, prompt: int = 1500,
     hit = (prompt // bs) * bs
     nl = (prompt - hit) + rng.integers(tail[0], tail[1] + 1, size=num_seqs)
     return context_prefill(seed=seed, context_lens=[hit] * num_seqs, new_lens=nl, shared_prefix=hit, heads=heads,
-                           d=d, bs=bs, dtype=dtype, pool_factor=1.1)
+                           d=d, bs=bs, dtype=dtype, pool_factor=1.1, kv_dtype=kv_dtype)
 
 
 def _tables_array(tables: List[List[int]], max_blocks: Optional[int] = None) -> np.ndarray:
@@ -416,7 +436,8 @@ PACKED_LENGTHS = (128, 200, 512, 1024, 2048, 256, 64, 1024)
 
 
 def prefill(seed: int = 1003, lengths=PACKED_LENGTHS, heads: int = 32, kv_heads: Optional[int] = None,
-            d: int = 128, bs: int = 16, dtype: str = F16, pool_factor: float = 1.1) -> PrefillWorkload:
+            d: int = 128, bs: int = 16, dtype: str = F16, pool_factor: float = 1.1,
+            kv_dtype: Optional[str] = None) -> PrefillWorkload:
     rng = np.random.default_rng(seed)
     lengths = np.asarray(lengths, dtype=np.int32)
     hkv = heads if kv_heads is None else kv_heads
@@ -427,16 +448,21 @@ def prefill(seed: int = 1003, lengths=PACKED_LENGTHS, heads: int = 32, kv_heads:
     alloc = BlockAllocator(nb, rng)
     tables = [alloc.allocate(blocks_for(n, bs)) for n in lengths]
     T = int(cu[-1])
+    q, k, v = normal_bits(rng, (T, heads, d), dtype), normal_bits(rng, (T, hkv, d), dtype), \
+        normal_bits(rng, (T, hkv, d), dtype)
+    ks = vs = None
+    if kv_dtype == FP8:
+        empty = np.zeros((0, hkv, d), np.uint16)
+        ks, vs = _fp8_scales(empty, k, dtype), _fp8_scales(empty, v, dtype)
     return PrefillWorkload(
         name=f"prefill_T{T}", lengths=lengths, cu_seqlens=cu, num_q_heads=heads, num_kv_heads=hkv,
         head_dim=d, block_size=bs, num_blocks=nb, dtype=dtype, scale=np.float32(1.0 / math.sqrt(d)),
-        q=normal_bits(rng, (T, heads, d), dtype), k=normal_bits(rng, (T, hkv, d), dtype),
-        v=normal_bits(rng, (T, hkv, d), dtype), block_tables=_tables_array(tables))
+        q=q, k=k, v=v, block_tables=_tables_array(tables), kv_dtype=kv_dtype or dtype, k_scale=ks, v_scale=vs)
 
 
 def prefix13b(seed: int = 1004, num_seqs: int = 64, prefix_tokens: int = 4096, max_suffix: int = 512,
               heads: int = 40, d: int = 128, bs: int = 32, private_prefix: bool = False,
-              kv_heads: Optional[int] = None, dtype: str = F16) -> DecodeWorkload:
+              kv_heads: Optional[int] = None, dtype: str = F16, kv_dtype: Optional[str] = None) -> DecodeWorkload:
     """Shared-prefix decode.  ``private_prefix`` gives every sequence its own copy of the prefix
     blocks (same values, different physical blocks) for the shared-vs-private equality check."""
     rng = np.random.default_rng(seed)
@@ -483,13 +509,17 @@ def prefix13b(seed: int = 1004, num_seqs: int = 64, prefix_tokens: int = 4096, m
         # the creating sequence's reference is dropped once the prefill that wrote it is done
         alloc.free(shared)
     mb = max(len(t) for t in fill_tables)
+    fill_k, fill_v = np.concatenate(fk), np.concatenate(fv)
+    ks = vs = None
+    if kv_dtype == FP8:
+        ks, vs = _fp8_scales(fill_k, new_k, dtype), _fp8_scales(fill_v, new_v, dtype)
     return DecodeWorkload(
         name="prefix13b" + ("_private" if private_prefix else ""), num_seqs=num_seqs, num_q_heads=heads,
-        num_kv_heads=hkv, head_dim=d, block_size=bs, num_blocks=nb, kv_dtype=dtype, model_dtype=dtype,
+        num_kv_heads=hkv, head_dim=d, block_size=bs, num_blocks=nb, kv_dtype=kv_dtype or dtype, model_dtype=dtype,
         scale=np.float32(1.0 / math.sqrt(d)), context_lens=lens, block_tables=_tables_array(tables, mb),
         fill_tables=_tables_array(fill_tables, mb), fill_seq_ids=np.concatenate(ids),
-        fill_positions=np.concatenate(pos), fill_k=np.concatenate(fk), fill_v=np.concatenate(fv),
-        q=q, new_k=new_k, new_v=new_v, k_scale=None, v_scale=None, ref_count=alloc.ref_count.copy(),
+        fill_positions=np.concatenate(pos), fill_k=fill_k, fill_v=fill_v,
+        q=q, new_k=new_k, new_v=new_v, k_scale=ks, v_scale=vs, ref_count=alloc.ref_count.copy(),
         seq_fill_row=np.arange(num_seqs, dtype=np.int32) + (0 if private_prefix else 1),
         shared_prefix_len=0 if private_prefix else prefix_tokens)
 

@@ -28,12 +28,12 @@ ATOL, RTOL = 2e-3, 1e-2
 
 # ------------------------------------------------------------------------------ prefill over a cached prefix
 
-def check_context_prefill(w, tag):
+def check_context_prefill(w, tag, atol=ATOL):
     g = run_context_prefill(w)
     r = steps.context_prefill_step(w, strides=g["strides"], pool_elems=g["pool"].size)
     assert g["err"] == 0, f"device error bits {g['err']}"
     assert np.array_equal(g["pool"], r["pool"]), f"pool differs at {int(np.sum(g['pool'] != r['pool']))} elements"
-    mx, rel = assert_close(g["out"], r["out"], ATOL, RTOL, tag, out_dtype=OUT_DT(w))
+    mx, rel = assert_close(g["out"], r["out"], atol, RTOL, tag, out_dtype=OUT_DT(w))
     print(f"{tag}: max abs {mx:.2e} max rel {rel:.2e}")
     return g
 
@@ -60,6 +60,25 @@ def test_context_prefill_small_cases(case):
 def test_prefix_hit_prefill_config():
     w = W.prefix_hit_prefill()
     check_context_prefill(w, "prefix_hit")
+
+
+# FP8 cache: the tails are appended as E4M3 codes, and every key and value, cached or new, is read as
+# its code times the head's scale; the oracle reads the same stored codes (gate 5e-2 abs)
+FP8_CTX_CASES = [
+    dict(context_lens=(0, 16, 37, 200), new_lens=(5, 130, 64, 1), heads=4, kv_heads=4, d=128, bs=16),
+    dict(context_lens=(1, 300), new_lens=(255, 17), heads=8, kv_heads=2, d=128, bs=8, dtype="bf16"),
+    dict(context_lens=(63, 500), new_lens=(1, 200), heads=2, kv_heads=1, d=64, bs=32),
+]
+
+
+@pytest.mark.parametrize("case", FP8_CTX_CASES, ids=lambda c: f"G{c['heads'] // c['kv_heads']}_d{c['d']}_bs{c['bs']}")
+def test_fp8_cache_context_prefill(case):
+    check_context_prefill(W.context_prefill(seed=47, kv_dtype="fp8", **case), "fp8 ctx", atol=5e-2)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_fp8_cache_prefix_hit_prefill_config(dtype):
+    check_context_prefill(W.prefix_hit_prefill(kv_dtype="fp8", dtype=dtype), f"fp8 prefix_hit {dtype}", atol=5e-2)
 
 
 def test_zero_context_matches_the_packed_prefill_kernel():

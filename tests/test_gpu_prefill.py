@@ -104,3 +104,18 @@ def test_bad_cu_seqlens_reported_not_fatal():
     assert cache.check_error() & 8   # the 50-token sequence exceeds max_seqlen 45
     assert np.all(np.isfinite(out[:40].float().cpu().numpy()))
     cache.close()
+
+
+# FP8 cache (E4M3 with per-head scales): the attention reads the packed k, v as given (the 16-bit
+# tolerance applies), and the cache holds what the append writes (bit-exact against the oracle's
+# append): config 3's lengths, a bf16 model with grouped heads and bs 8, and D = 64 with bs 32
+FP8_CASES = [
+    dict(lengths=(128, 200, 512, 1024, 2048, 256, 64, 1024), heads=8, kv_heads=8, d=128, bs=16),
+    dict(lengths=(130, 17, 500), heads=4, kv_heads=2, d=128, dtype="bf16", bs=8),
+    dict(lengths=(33, 257, 64, 1), heads=4, kv_heads=2, d=64, bs=32),
+]
+
+
+@pytest.mark.parametrize("case", FP8_CASES, ids=lambda c: "_".join(f"{k}{v}" for k, v in c.items()).replace(" ", ""))
+def test_fp8_cache_packed_prefill(case):
+    check_prefill(W.prefill(seed=57, kv_dtype="fp8", **case), "fp8 cache packed")
