@@ -128,6 +128,19 @@ PKV_DEV bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint64_t limit_ns =
     return mbar_try_wait_sleep(b, parity) || mbar_wait_sleep_slow(b, parity, limit_ns);
 }
 
+// The same wait entirely inline, for kernels whose warps change their register budget
+// (setmaxnreg), where a call to the out-of-line loop cannot be register-allocated.
+PKV_DEV bool mbar_wait_hint(uint64_t *bar, uint32_t parity, uint64_t limit_ns = PKV_WAIT_LIMIT_NS) {
+    const uint32_t b = smem_u32(bar);
+    if (mbar_try_wait_sleep(b, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 0; i < 0x80000000u; ++i) {
+        if (mbar_try_wait_sleep(b, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return false;
+}
+
 // two-lane fp32 arithmetic (one instruction for both lanes): a * b + c and a + b; max of three
 // (the softmax of the prefill kernels issues these per key pair instead of two scalar operations)
 PKV_DEV float2 fma2(float2 a, float2 b, float2 c) {

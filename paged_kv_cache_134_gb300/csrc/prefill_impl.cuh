@@ -20,14 +20,15 @@
 //  * Tensor memory (512 columns): S_A, S_B (128 fp32 columns each) and O_A, O_B (D columns each).  P
 //    is written over S in place (fp16, or a bf16 hi + lo pair), and read by P V as the A operand from
 //    tensor memory.
-//  * The MMA warp issues, per key step j:  P_A V(j), S_A(j+1), P_B V(j), S_B(j+1).  While one tile's
-//    softmax runs, the tensor pipe works on the other tile's products, so each softmax has two MMAs'
-//    time (2 x 128 x 128 x D) to finish; S(j+1) of a tile is issued only after its P V(j), which frees
-//    the S columns P occupies (tcgen05 operations of one thread complete in issue order).
-//  * Warp roles: 0 scheduler, Q loads and K loads; 1 tensor-memory owner and MMA issuer; 2 V loads;
-//    3 the paged K/V write of packed mode, or the widening of E4M3 K tiles (FP8 caches, paged and
-//    cascade modes); 4-7 softmax of tile A, 8-11 softmax of tile B (one thread per query row, tensor
-//    memory lane = row); V tiles of FP8 caches are widened by warp 2 after they land.
+//  * Each tile has its own MMA-issuing warp, which issues per key step j: P V(j), then S(j+1).  While
+//    one tile's softmax runs, the tensor pipe works on the other tile's products, so each softmax has
+//    two MMAs' time (2 x 128 x 128 x D) to finish; S(j+1) of a tile is issued only after its P V(j),
+//    which frees the S columns P occupies (tcgen05 operations of one thread complete in issue order).
+//    Two issuing warps keep the pipe's queue fed while either waits for its softmax.
+//  * Warp roles: 0 scheduler, Q loads and K loads; 2 V loads (each loader also writes the packed
+//    mode's paged K/V rows, and widens the E4M3 tiles of FP8 caches); 1 and 3 the MMA issuers of tiles
+//    A and B (warp 1 also owns tensor memory); 4-7 softmax of tile A, 8-11 softmax of tile B (one
+//    thread per query row, tensor memory lane = row).
 //  * O is rescaled in tensor memory only when a row's running maximum grows by more than 2^8 (the
 //    exponent base stays fixed otherwise, which is exact algebra); the softmax thread does it, since
 //    S(j) complete implies P V(j-1) complete.
@@ -87,9 +88,9 @@ struct Layout {
     static constexpr int K0 = Q + 2 * Q_TILE;
     static constexpr int V0 = K0 + NKS * STAGE;
     static constexpr int BAR = V0 + NVS * STAGE;
-    static constexpr int NBARS = 2 + 2 + 2 + 2 + 4 * NKS + 4 * NVS + 2 + 2 + 2 + 2 + 1;
+    static constexpr int NBARS = 4 + 4 + 2 + 2 + 4 * NKS + 4 * NVS + 2 + 2 + 2 + 2 + 2;
     static constexpr int MISC = BAR + (NBARS * 8 + 15) / 16 * 16; // TMEM slot, abort flag; item slots at + 16
-    static constexpr int TOTAL = MISC + 16 + 32;
+    static constexpr int TOTAL = MISC + 16 + 64;
     static_assert(TOTAL + 1024 <= 232448, "shared memory");
     static_assert(!KV8 || D == 64 || kCodeOff + BN * D <= STAGE, "code region");
 };
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool PAGED = MODE != MODE_PACKED;    // keys from the pool through the block table
     constexpr bool CASCADE = MODE == MODE_CASCADE; // no causal mask, fp32 split partials out
     constexpr bool SHARED = !CASCADE;              // both tiles use the same key tiles
-    constexpr bool WRITER = MODE == MODE_PACKED;   // warp 3 writes the item's K/V rows into the pool
+    constexpr bool WRITER = MODE == MODE_PACKED;   // the loaders write the item's K/V rows into the pool
     constexpr int NP = MT == PKV_BF16 ? 2 : 1;     // P parts (bf16: hi + lo)
     constexpr int EB = KV8 ? 1 : 2;                // pool bytes per element
     constexpr int NKS = L::NKS, NVS = L::NVS;
@@ -274,15 +275,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (smem_u32(smem) & 1023u) return; // the swizzled tiles need 1024-byte alignment (always true)
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR);
-    uint64_t *item_full = bars, *item_empty = bars + 2;
-    uint64_t *q_full = bars + 4, *q_empty = bars + 6;
-    uint64_t *k_full = bars + 8, *k_empty = k_full + NKS, *kc_full = k_empty + NKS, *k_spare = kc_full + NKS;
+    // items go through a 4-slot ring: the scheduler publishes an item while the one before it is
+    // still being loaded, so that nobody waits for the next item at an item boundary
+    constexpr int kItemSlots = 4;
+    uint64_t *item_full = bars, *item_empty = bars + kItemSlots;
+    uint64_t *q_full = bars + 2 * kItemSlots, *q_empty = q_full + 2;
+    uint64_t *k_full = q_empty + 2, *k_empty = k_full + NKS, *kc_full = k_empty + NKS, *k_spare = kc_full + NKS;
     uint64_t *v_full = k_spare + NKS, *v_empty = v_full + NVS, *vc_full = v_empty + NVS, *v_spare = vc_full + NVS;
     uint64_t *s_full = v_spare + NVS, *p_full = s_full + 2, *o_full = p_full + 2, *o_free = o_full + 2;
     uint64_t *fin = o_free + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::MISC + 4);
-    volatile int4 *item_slot = reinterpret_cast<volatile int4 *>(smem + L::MISC + 16); // [2]
+    // exp phases the softmax of each tile has finished, counted per warp (4 per key step), monotonic
+    int *sm_prog = reinterpret_cast<int *>(smem + L::MISC + 8); // [2]
+    volatile int4 *item_slot = reinterpret_cast<volatile int4 *>(smem + L::MISC + 16); // [kItemSlots]
     (void)k_spare;
     (void)v_spare;
     // K / V tiles ready for the MMA: landed (16-bit) or landed and widened (E4M3)
@@ -290,14 +296,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *v_ready = KV8 ? vc_full : v_full;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // item consumers: V loader, MMA issuer, warp 3, eight softmax warps
+    // item consumers: V loader, the two MMA issuers, eight softmax warps
     constexpr int kItemConsumers = 11;
+    // a K or V stage frees once every MMA warp whose tile reads it has released it (both tiles read
+    // the shared key tiles of packed and paged modes; each cascade tile has key tiles of its own)
+    constexpr int kStageReleasers = SHARED ? 2 : 1;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kItemSlots; ++s) {
             mbar_init(item_full + s, 1);
             mbar_init(item_empty + s, kItemConsumers);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(q_full + s, 1);
-            mbar_init(q_empty + s, 1);
+            mbar_init(q_empty + s, CASCADE ? 2 : 1); // cascade: one Q tile, read by both MMA warps
             mbar_init(s_full + s, 1);
             mbar_init(p_full + s, 128);
             mbar_init(o_full + s, 1);
@@ -305,16 +316,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < NKS; ++s) {
             mbar_init(k_full + s, 1);
-            mbar_init(k_empty + s, WRITER ? 2 : 1);
+            mbar_init(k_empty + s, kStageReleasers);
             mbar_init(kc_full + s, 1);
         }
         for (int s = 0; s < NVS; ++s) {
             mbar_init(v_full + s, 1);
-            mbar_init(v_empty + s, WRITER ? 2 : 1);
+            mbar_init(v_empty + s, kStageReleasers);
             mbar_init(vc_full + s, 1);
         }
         mbar_init(fin, 1);
+        mbar_init(fin + 1, 1);
         *abort_flag = 0;
+        sm_prog[0] = 0;
+        sm_prog[1] = 0;
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -338,11 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         set_error(a.err, PKV_DEVERR_TIMEOUT);
         *abort_flag = 1;
     };
-    // the item in ring slot n % 2, once the scheduler has published it
+    // the item in ring slot n % 4, once the scheduler has published it
     auto take_item = [&](int n, bool &ok) -> Item {
-        ok = mbar_wait(item_full + (n & 1), (n >> 1) & 1);
+        const int sl = n & (kItemSlots - 1);
+        ok = mbar_wait_hint(item_full + sl, (n / kItemSlots) & 1);
         if (!ok) return decode_item(a, -1, 0, 0);
-        return decode_item(a, item_slot[n & 1].x, item_slot[n & 1].y, item_slot[n & 1].z);
+        return decode_item(a, item_slot[sl].x, item_slot[sl].y, item_slot[sl].z);
     };
     // the item's keys of ring entry e: key step j of tile t (packed / paged: one tile serves both)
     // (tiles are selected, not indexed, so that the item stays in registers)
@@ -355,23 +370,125 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 104;");
-    if (warp == 0) {
-        // ---------------------------------------------------------------- scheduler, Q and K loads
-        // lane 0 takes items and loads Q; packed mode: lane 0 loads each K tile (one box per half of
-        // D); paged and cascade modes: lane l loads block l of each K tile
+    if (warp == 0 || warp == 2) {
+        // ---------------------------------------------------------------- loaders
+        // Warp 0: the scheduler (lane 0), Q loads and K loads; warp 2: V loads.  Packed mode: lane 0
+        // loads each tile (one box per half of D).  Paged and cascade modes: lane l loads block l of
+        // each tile; blocks full of the keys' tokens arrive as TMA boxes, and every other row of a V
+        // tile is written with plain stores: the tokens of a partly filled last block copied from the
+        // pool, zeros for slots past the keys' end and for unusable block ids (P is 0 on those rows,
+        // but 0 * NaN is NaN, and the pool's unused slots may hold anything); K rows past the end are
+        // masked by the softmax instead.  FP8 caches: the codes land in the stage's code region, and
+        // the loader widens each tile once it has landed, before it issues the next one.  Packed mode:
+        // the paged write of an item's own rows (the keys of its last tiles) leaves a stage just before
+        // the loader refills it (whole blocks as tiled TMA stores, one lane per block and half of D;
+        // the rows of a partly filled last block as plain 16-byte stores, so no slot past the sequence
+        // is touched), or at the end.
+        const bool isK = warp == 0;
+        constexpr int NS = 0; // (stage counts differ per ring; see ns below)
+        (void)NS;
+        const int ns = isK ? NKS : NVS;
+        uint8_t *const ring = smem + (isK ? L::K0 : L::V0);
+        uint64_t *const full = isK ? k_full : v_full;
+        uint64_t *const empty = isK ? k_empty : v_empty;
+        uint64_t *const ready = isK ? kc_full : vc_full; // E4M3: widened
+        const int kvsel = isK ? 0 : 1;                   // K or V half of a pool block
+        constexpr int CPR = D * EB / 16;                  // 16-byte chunks per pool row
+        constexpr int RPI = 32 / CPR;                     // rows per warp instruction (never two blocks: bs >= 8)
+        const int cc = lane % CPR, rsub = lane / CPR;
         if (lane == 0) {
-            tc::prefetch_tmap(&tq);
-            tc::prefetch_tmap(PAGED ? &tp : &tk);
+            if (isK) tc::prefetch_tmap(&tq);
+            tc::prefetch_tmap(PAGED ? &tp : (isK ? &tk : &tv));
         }
+        // packed mode: the pending pool write of the entry each stage holds (j < 0: none), with the
+        // item's rows and (lane l) the table entry of its logical block lb0 + l
+        int wj[4] = {-1, -1, -1, -1}, wq0[4] = {}, wql[4] = {}, wkvh[4] = {}, wblk[4] = {}, wpar[4] = {};
+        auto flush_write = [&](int st) {
+            if constexpr (WRITER) {
+                if (wj[st] < 0) return;
+                const uint8_t *src = ring + st * L::STAGE;
+                // the tile has landed long ago (it was loaded ns entries back); the wait is for the
+                // rare case the loader is about to refill a stage whose tile still flies
+                mbar_wait_hint(full + st, (uint32_t)wpar[st]);
+                const int j = wj[st], q0 = wq0[st], qlast = wql[st], kvh = wkvh[st], blkv = wblk[st];
+                const int lb0 = q0 >> a.lg_bs;
+                const int lo = max(j * BN, q0), hi = min(j * BN + BN - 1, qlast);
+                if (lo <= hi) {
+                    const int bfirst = lo >> a.lg_bs;           // lo is a multiple of bs
+                    const int nfull = (hi + 1 - lo) >> a.lg_bs; // whole blocks among the rows
+                    {
+                        const int lb = bfirst + lane;
+                        const int blk = __shfl_sync(0xffffffffu, blkv, min(lb - lb0, 31));
+                        if (lane < nfull) {
+                            if (blk < 0 || blk >= a.num_blocks) {
+                                set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                            } else {
+                                const uint8_t *box = src + ((lb << a.lg_bs) - j * BN) * 128;
+                                const int y = ((blk * 2 + kvsel) * a.hkv + kvh) << a.lg_bs;
+#pragma unroll
+                                for (int c = 0; c < D / 64; ++c) tc::tma_store_2d(&tp, c * 64, y, box + c * BN * 128);
+                                tc::bulk_commit();
+                            }
+                        }
+                    }
+                    const int c2 = cc >> 3, u = cc & 7;
+                    for (int p0 = lo + (nfull << a.lg_bs); p0 <= hi; p0 += RPI) { // fewer than bs rows
+                        const int pp = p0 + rsub;
+                        const int lb = pp >> a.lg_bs;
+                        const int blk = __shfl_sync(0xffffffffu, blkv, min(lb - lb0, 31));
+                        if (pp > hi) continue;
+                        if (blk < 0 || blk >= a.num_blocks) {
+                            if (cc == 0) set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                            continue;
+                        }
+                        const int rr = pp - j * BN;
+                        const uint4 xv = *reinterpret_cast<const uint4 *>(src + c2 * BN * 128 + rr * 128 +
+                                                                          ((u ^ (rr & 7)) << 4));
+                        const int64_t dst = ((int64_t)(blk * 2 + kvsel) * a.hkv + kvh) * a.tile_elems +
+                                            (int64_t)(pp - (lb << a.lg_bs)) * D + cc * 8;
+                        *reinterpret_cast<uint4 *>(a.pool + dst * 2) = xv;
+                    }
+                }
+                tc::bulk_wait_read_all(); // the stores have read the stage; it may be refilled
+                __syncwarp();
+                wj[st] = -1;
+            }
+        };
+        // FP8: widen ring entry gw (landed), then release it to the MMAs
+        auto widen = [&](int64_t gw) -> bool {
+            const int st = (int)(gw % ns);
+            if (!__all_sync(0xffffffffu, mbar_wait_hint(full + st, (uint32_t)((gw / ns) & 1)))) return false;
+            uint8_t *stage = ring + st * L::STAGE;
+            for (int r = lane; r < BN; r += 32) widen_row<D, MT>(stage, r);
+            fence_proxy_async_smem(); // the MMAs read the widened tile through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ready + st);
+            return true;
+        };
         const int total = a.plan[0] * a.hq;
-        int64_t g = 0;        // K tiles issued so far (all items)
-        int nq[2] = {0, 0};   // Q loads per buffer so far
+        int64_t g = 0;      // tiles issued so far (all items)
+        int nq[2] = {0, 0}; // Q loads per buffer so far (warp 0)
+        int64_t pend = -1;  // FP8: the issued tile still to widen
+        // FP8: widen the pending tile; done before this warp can block on anything an MMA of that tile
+        // may be holding up (the next tile's stage, the next item, the next item's Q buffer)
+        auto widen_pending = [&]() -> bool {
+            if constexpr (KV8) {
+                if (pend >= 0) {
+                    const bool w = widen(pend);
+                    pend = -1;
+                    return w;
+                }
+            }
+            return true;
+        };
         bool ok = true;
-        for (int n = 0; ok; ++n) {
-            const int s = n & 1;
-            if (n >= 2) ok = __all_sync(0xffffffffu, mbar_wait(item_empty + s, ((n >> 1) - 1) & 1));
-            if (!ok) break;
+        // the scheduler (warp 0): take item m from the work list and publish it in ring slot m % 4
+        auto publish = [&](int m, bool &pok) -> Item {
+            const int sl = m & (kItemSlots - 1);
+            pok = true;
+            if (m >= kItemSlots) pok = __all_sync(0xffffffffu, mbar_wait_hint(item_empty + sl, ((m / kItemSlots) - 1) & 1));
             int4 raw = make_int4(-1, 0, 0, 0);
+            if (!pok) return decode_item(a, -1, 0, 0);
             if (lane == 0) {
                 const int idx = *abort_flag ? total : atomicAdd(a.plan + 1, 1);
                 if (idx < total) {
@@ -384,23 +501,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                         raw = make_int4(sq.x, sq.y, idx % a.hq, 0);
                     }
                 }
-                item_slot[s].x = raw.x;
-                item_slot[s].y = raw.y;
-                item_slot[s].z = raw.z;
-                mbar_arrive(item_full + s);
+                item_slot[sl].x = raw.x;
+                item_slot[sl].y = raw.y;
+                item_slot[sl].z = raw.z;
+                mbar_arrive(item_full + sl);
             }
             raw.x = __shfl_sync(0xffffffffu, raw.x, 0);
             raw.y = __shfl_sync(0xffffffffu, raw.y, 0);
             raw.z = __shfl_sync(0xffffffffu, raw.z, 0);
-            if (raw.x < 0) break;
-            const Item it = decode_item(a, raw.x, raw.y, raw.z);
+            return decode_item(a, raw.x, raw.y, raw.z);
+        };
+        for (int n = 0; ok; ++n) {
+            Item it;
+            if (!isK && !widen_pending()) ok = false; // before waiting for the next item
+            if (!ok) break;
+            if (isK) {
+                // ---- scheduler: take the next item and publish it.  This happens once the previous
+                // item's last K tile is issued, a few key steps before it ends; the item's Q tiles and
+                // first key tiles are prefetched into L2 now, so that their loads, which wait for the
+                // previous item's buffers to free up, come from L2
+                it = publish(n, ok);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                if (it.seq >= 0 && lane == 0) {
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        if (CASCADE ? b == 1 : it.t[b].n == 0) continue;
+#pragma unroll
+                        for (int c = 0; c < D / 64; ++c)
+                            tc::tma_prefetch_2d(&tq, it.h * D + c * 64, it.start + it.t[b].q0);
+                    }
+                    if constexpr (!PAGED) {
+                        const int nk = min(ring_count<SHARED>(it), 2);
+                        for (int e = 0; e < nk; ++e)
+#pragma unroll
+                            for (int c = 0; c < D / 64; ++c) {
+                                tc::tma_prefetch_2d(&tk, (it.h / G) * D + c * 64, it.start + e * BN);
+                                tc::tma_prefetch_2d(&tv, (it.h / G) * D + c * 64, it.start + e * BN);
+                            }
+                    }
+                }
+            } else {
+                it = take_item(n, ok);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            }
+            if (it.seq < 0) break;
             const int kvh = it.h / G;
-            // Q: buffer t holds tile t (cascade: buffer 0 holds the one query tile of both splits)
-            if (lane == 0) {
+            if (isK && !widen_pending()) ok = false; // before the Q loads wait for their buffers
+            if (isK && lane == 0 && ok) {
+                // ---- Q: buffer t holds tile t (cascade: buffer 0 holds the one query tile of both splits)
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
                     if (CASCADE ? b == 1 : it.t[b].n == 0) continue;
-                    if (nq[b] >= 1 && !mbar_wait(q_empty + b, (nq[b] - 1) & 1)) {
+                    if (nq[b] >= 1 && !mbar_wait_hint(q_empty + b, (nq[b] - 1) & 1)) {
                         ok = false;
                         break;
                     }
@@ -419,6 +573,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const int ne = ring_count<SHARED>(it);
+            // packed mode: this item writes the K/V of its own rows (the first query head of each KV
+            // group does), from the key tiles that hold them
+            const int q0 = it.t[0].q0, qlast = it.t[1].n > 0 ? it.t[1].qlast : it.t[0].qlast;
+            const bool writes = WRITER && a.write_pool && it.h % G == 0;
+            int blkv = -1;
+            if (writes) {
+                const int lb = (q0 >> a.lg_bs) + lane;
+                if ((lb << a.lg_bs) <= qlast && lb < a.max_blocks) blkv = a.tables[(int64_t)it.seq * a.max_blocks + lb];
+            }
             // paged / cascade: lane l's table entry of block l of ring entry e (-1: no token there)
             auto entry = [&](int e) -> int {
                 int t, j;
@@ -432,186 +595,112 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0;
             for (int e = 0; e < ne && ok; ++e) {
                 const int64_t gg = g + e;
-                const int st = (int)(gg % NKS);
-                const int64_t round = gg / NKS;
-                if (round >= 1) ok = __all_sync(0xffffffffu, mbar_wait(k_empty + st, (round - 1) & 1));
+                const int st = (int)(gg % ns);
+                const int64_t round = gg / ns;
+                // FP8: the previous tile is widened first (an MMA waits for it), then this one loads
+                if (!widen_pending()) ok = false;
+                flush_write(st); // the stage's previous tile leaves for the pool before the refill
+                if (ok && round >= 1) ok = __all_sync(0xffffffffu, mbar_wait_hint(empty + st, (round - 1) & 1));
                 if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) break;
-                uint8_t *stage = smem + L::K0 + st * L::STAGE;
+                uint8_t *stage = ring + st * L::STAGE;
                 if constexpr (PAGED) {
-                    // the tile's blocks that hold tokens, one box per block (and half of D for 16-bit
-                    // caches) from the pool; rows past the keys' end are masked by the softmax, and
-                    // unusable block ids (reported by the V loader) are skipped.  The table entries of
-                    // the next ring entry are read now, ahead of their use.
+                    int t, j;
+                    const int kbase = key_base(it, e, t, j), send = key_end(it, t);
+                    const int nbt = BN >> a.lg_bs;
                     int b = nxt;
                     if (e + 1 < ne) nxt = entry(e + 1);
-                    if (b >= a.num_blocks) b = -1;
-                    const unsigned have = __ballot_sync(0xffffffffu, b >= 0);
-                    if (lane == 0)
-                        mbar_arrive_expect_tx(k_full + st, (uint32_t)__popc(have) * (uint32_t)(a.bs * D * EB));
+                    const int lb = (kbase >> a.lg_bs) + lane;
+                    const bool has = lane < nbt && (lb << a.lg_bs) < send;
+                    const bool good = has && b >= 0 && b < a.num_blocks;
+                    if (!isK && has && !good) set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                    // K: every usable block whole (rows past the end are masked); V: only full blocks
+                    const bool full_blk = good && (isK || ((lb + 1) << a.lg_bs) <= send);
+                    const unsigned fullmask = __ballot_sync(0xffffffffu, full_blk);
+                    if (lane == 0) mbar_expect_tx(full + st, (uint32_t)__popc(fullmask) * (uint32_t)(a.bs * D * EB));
                     __syncwarp();
-                    if (b >= 0) {
-                        const int y = (b * 2 * a.hkv + kvh) << a.lg_bs;
+                    if (full_blk) {
+                        const int y = ((b * 2 + kvsel) * a.hkv + kvh) << a.lg_bs;
                         if constexpr (KV8) {
-                            tc::tma_load_2d(stage + kCodeOff + (lane << a.lg_bs) * D, &tp, 0, y, k_full + st);
+                            tc::tma_load_2d(stage + kCodeOff + (lane << a.lg_bs) * D, &tp, 0, y, full + st);
                         } else {
 #pragma unroll
                             for (int c = 0; c < D / 64; ++c)
                                 tc::tma_load_2d(stage + c * BN * 128 + ((lane << a.lg_bs) * 128), &tp, c * 64, y,
-                                                k_full + st);
+                                                full + st);
                         }
                     }
+                    const unsigned allmask = nbt == 32 ? 0xffffffffu : (1u << nbt) - 1u;
+                    if (!isK) {
+                        for (int r0 = 0; fullmask != allmask && r0 < BN; r0 += RPI) {
+                            const int r = r0 + rsub, l = r >> a.lg_bs;
+                            const int bl = __shfl_sync(0xffffffffu, good ? b : -1, l);
+                            if ((fullmask >> l) & 1u) continue;
+                            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                            if (bl >= 0 && kbase + r < send)
+                                x = *reinterpret_cast<const uint4 *>(
+                                    a.pool + ((((int64_t)bl * 2 + 1) * a.hkv + kvh) * a.tile_elems +
+                                              (int64_t)(r - (l << a.lg_bs)) * D) * EB + cc * 16);
+                            if constexpr (KV8) {
+                                *reinterpret_cast<uint4 *>(stage + kCodeOff + r * D + cc * 16) = x;
+                            } else {
+                                const int c2 = cc >> 3, u = cc & 7;
+                                *reinterpret_cast<uint4 *>(stage + c2 * BN * 128 + r * 128 + ((u ^ (r & 7)) << 4)) = x;
+                            }
+                        }
+                        if constexpr (!KV8) fence_proxy_async_smem(); // the plain stores are read by the MMA
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full + st);
                 } else {
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(k_full + st, L::TILE);
+                        mbar_arrive_expect_tx(full + st, L::TILE);
 #pragma unroll
                         for (int c = 0; c < D / 64; ++c)
-                            tc::tma_load_2d(stage + c * BN * 128, &tk, kvh * D + c * 64, it.start + e * BN,
-                                            k_full + st);
+                            tc::tma_load_2d(stage + c * BN * 128, isK ? &tk : &tv, kvh * D + c * 64, it.start + e * BN,
+                                            full + st);
+                    }
+                    if (writes && e >= q0 / BN) {
+                        // the tile holds some of the item's own rows: write them before the stage is refilled
+                        wj[st] = e;
+                        wq0[st] = q0;
+                        wql[st] = qlast;
+                        wkvh[st] = kvh;
+                        wblk[st] = blkv;
+                        wpar[st] = (int)(round & 1);
                     }
                 }
                 issued = e + 1;
+                if constexpr (KV8) pend = gg;
             }
             g += issued; // tiles issued so far, all items
+            if (!isK && lane == 0) mbar_arrive(item_empty + (n & (kItemSlots - 1)));
             if (!ok) {
                 if (lane == 0) fail();
                 break;
             }
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
         }
+        // FP8: the last tile issued is widened too (an MMA may still be waiting for it)
+        if (ok && !widen_pending() && lane == 0) fail();
+        // pending pool writes leave now; every store has completed before the CTA exits
+        for (int st = 0; st < ns; ++st) flush_write(st);
+        if constexpr (WRITER) tc::bulk_wait_all();
         // the last loads must land before this CTA's shared memory goes away
         if (lane == 0) {
-            for (int64_t gg = g > NKS ? g - NKS : 0; gg < g; ++gg)
-                if (!mbar_wait(k_full + gg % NKS, (gg / NKS) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
-            for (int b = 0; b < 2; ++b)
-                if (nq[b] >= 1 && !mbar_wait(q_full + b, (nq[b] - 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            for (int64_t gg = g > ns ? g - ns : 0; gg < g; ++gg)
+                if (!mbar_wait_hint(full + gg % ns, (gg / ns) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            if (isK)
+                for (int b = 0; b < 2; ++b)
+                    if (nq[b] >= 1 && !mbar_wait_hint(q_full + b, (nq[b] - 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
         }
-    } else if (warp == 2) {
-        // ---------------------------------------------------------------- V loads (whole warp)
-        // Packed mode: lane 0 loads each V tile.  Paged and cascade modes: lane l handles block l of a
-        // tile; blocks full of the keys' tokens arrive as TMA boxes, and every other row of the tile is
-        // written with plain stores: the tokens of a partly filled last block copied from the pool,
-        // zeros for slots past the keys' end and for unusable block ids.  P is 0 on those rows, but
-        // 0 * NaN is NaN, and the pool's unused slots may hold anything.  FP8 caches: the codes land in
-        // the stage's code region and this warp widens each tile once it has landed, one tile behind
-        // its loads (a tile is widened before the next one is issued).
-        constexpr int CPR = D * EB / 16;  // 16-byte chunks per pool row
-        constexpr int RPI = 32 / CPR;     // rows per warp instruction (never two blocks: bs >= 8)
-        const int cc = lane % CPR, rsub = lane / CPR;
-        if (lane == 0) tc::prefetch_tmap(PAGED ? &tp : &tv);
-        int64_t g = 0;
-        bool ok = true;
-        // FP8: widen ring entry gw (landed), then release it to the MMA
-        auto widen = [&](int64_t gw) -> bool {
-            const int st = (int)(gw % NVS);
-            if (!__all_sync(0xffffffffu, mbar_wait(v_full + st, (gw / NVS) & 1))) return false;
-            uint8_t *stage = smem + L::V0 + st * L::STAGE;
-            for (int r = lane; r < BN; r += 32) widen_row<D, MT>(stage, r);
-            fence_proxy_async_smem(); // the MMA reads the widened tile through the async proxy
-            __syncwarp();
-            if (lane == 0) mbar_arrive(vc_full + st);
-            return true;
-        };
-        for (int n = 0;; ++n) {
-            const Item it = take_item(n, ok);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok || it.seq < 0) break;
-            const int kvh = it.h / G;
-            const int ne = ring_count<SHARED>(it);
-            auto entry = [&](int e) -> int {
-                int t, j;
-                const int kb = key_base(it, e, t, j);
-                const int lb = (kb >> a.lg_bs) + lane;
-                return (lane < (BN >> a.lg_bs) && (lb << a.lg_bs) < key_end(it, t))
-                           ? a.tables[(int64_t)it.trow * a.max_blocks + lb]
-                           : -1;
-            };
-            int nxt = PAGED && ne > 0 ? entry(0) : -1;
-            int issued = 0;
-            for (int e = 0; e < ne && ok; ++e) {
-                const int64_t gg = g + e;
-                const int st = (int)(gg % NVS);
-                const int64_t round = gg / NVS;
-                // FP8: the previous tile is widened first (the MMA waits for it), then this one loads
-                if constexpr (KV8) {
-                    if (gg >= 1 && !widen(gg - 1)) ok = false;
-                }
-                if (ok && round >= 1) ok = __all_sync(0xffffffffu, mbar_wait(v_empty + st, (round - 1) & 1));
-                if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) break;
-                uint8_t *stage = smem + L::V0 + st * L::STAGE;
-                if constexpr (PAGED) {
-                    int t, j;
-                    const int kbase = key_base(it, e, t, j), send = key_end(it, t);
-                    const int nbt = BN >> a.lg_bs;
-                    const int b = nxt;
-                    if (e + 1 < ne) nxt = entry(e + 1);
-                    const int lb = (kbase >> a.lg_bs) + lane;
-                    const bool has = lane < nbt && (lb << a.lg_bs) < send;
-                    const bool good = has && b >= 0 && b < a.num_blocks;
-                    if (has && !good) set_error(a.err, PKV_DEVERR_BLOCK_ID);
-                    const bool full = good && ((lb + 1) << a.lg_bs) <= send;
-                    const unsigned fullmask = __ballot_sync(0xffffffffu, full);
-                    if (lane == 0) mbar_expect_tx(v_full + st, (uint32_t)__popc(fullmask) * (uint32_t)(a.bs * D * EB));
-                    __syncwarp();
-                    if (full) {
-                        const int y = ((b * 2 + 1) * a.hkv + kvh) << a.lg_bs;
-                        if constexpr (KV8) {
-                            tc::tma_load_2d(stage + kCodeOff + (lane << a.lg_bs) * D, &tp, 0, y, v_full + st);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < D / 64; ++c)
-                                tc::tma_load_2d(stage + c * BN * 128 + ((lane << a.lg_bs) * 128), &tp, c * 64, y,
-                                                v_full + st);
-                        }
-                    }
-                    for (int r0 = 0; fullmask != (nbt == 32 ? 0xffffffffu : (1u << nbt) - 1u) && r0 < BN; r0 += RPI) {
-                        const int r = r0 + rsub, l = r >> a.lg_bs;
-                        const int bl = __shfl_sync(0xffffffffu, good ? b : -1, l);
-                        if ((fullmask >> l) & 1u) continue;
-                        uint4 x = make_uint4(0u, 0u, 0u, 0u);
-                        if (bl >= 0 && kbase + r < send)
-                            x = *reinterpret_cast<const uint4 *>(
-                                a.pool + ((((int64_t)bl * 2 + 1) * a.hkv + kvh) * a.tile_elems +
-                                          (int64_t)(r - (l << a.lg_bs)) * D) * EB + cc * 16);
-                        if constexpr (KV8) {
-                            *reinterpret_cast<uint4 *>(stage + kCodeOff + r * D + cc * 16) = x;
-                        } else {
-                            const int c2 = cc >> 3, u = cc & 7;
-                            *reinterpret_cast<uint4 *>(stage + c2 * BN * 128 + r * 128 + ((u ^ (r & 7)) << 4)) = x;
-                        }
-                    }
-                    if constexpr (!KV8) fence_proxy_async_smem(); // the plain stores are read by the MMA
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(v_full + st);
-                } else {
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(v_full + st, L::TILE);
-#pragma unroll
-                        for (int c = 0; c < D / 64; ++c)
-                            tc::tma_load_2d(stage + c * BN * 128, &tv, kvh * D + c * 64, it.start + e * BN,
-                                            v_full + st);
-                    }
-                }
-                issued = e + 1;
-            }
-            g += issued; // tiles issued so far, all items
-            if (lane == 0) mbar_arrive(item_empty + (n & 1));
-            if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) break;
-        }
-        if (!ok && lane == 0) fail();
-        // FP8: the last tile issued is widened too (the MMA may still be waiting for it)
-        if constexpr (KV8) {
-            if (ok && g >= 1 && !widen(g - 1) && lane == 0) fail();
-        }
-        if (lane == 0)
-            for (int64_t gg = g > NVS ? g - NVS : 0; gg < g; ++gg)
-                if (!mbar_wait(v_full + gg % NVS, (gg / NVS) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        // The whole warp runs the issue loop in step (waits agreed with __all_sync); one elected lane
-        // issues each MMA and commit.  An MMA issue blocks while the tensor pipe's queue is full, and
-        // the pipe idles once this warp stops feeding it, so the work between two groups of MMAs is
-        // kept short: ring positions advance by one stage at a time, phase parities are single bits,
-        // the operand descriptors are built once.
+    } else if (warp == 1 || warp == 3) {
+        // ---------------------------------------------------------------- MMA issuers
+        // Warp 1 issues the products of tile A, warp 3 those of tile B, each from a converged warp with
+        // one elected lane issuing (waits agreed with __all_sync).  Per tile: S(0), then per key step
+        // j: P V(j), S(j+1).  S(j+1) follows P V(j) from the same thread, so it overwrites the S
+        // columns only after P V(j) has read P from them.  Two issuers keep the tensor pipe's queue fed
+        // while either waits for its softmax.  Commits track the issuing thread's own MMAs.
+        const int t = warp == 1 ? 0 : 1;
         constexpr uint32_t IQK = tc::idesc_f16(MT == PKV_BF16 ? 1u : 0u, 0u, BM, BN);
         constexpr uint32_t IPV = tc::idesc_f16(MT == PKV_BF16 ? 1u : 0u, 1u, BM, D);
         // one descriptor per operand layout; the address field counts 16-byte units, so a tile at byte
@@ -619,104 +708,152 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dQ = tc::smem_desc(smem_u32(smem + L::Q), 16, 1024);
         const uint64_t dK = tc::smem_desc(smem_u32(smem + L::K0), 16, 1024);
         const uint64_t dV = tc::smem_desc(smem_u32(smem + L::V0), BN * 128, 1024);
+        const uint32_t tS = tmem + (uint32_t)(t * BN), tO = tmem + (uint32_t)(2 * BN + t * D);
         bool any_mma = false, ok = true;
-        // the K (V) entry the next S (P V) reads: its stage and the parity of its phase
+        // ring cursors: the stage of the K (V) entry to look at next and the parity of its phase
         uint32_t kst = 0, kph = 0, vst = 0, vph = 0;
-        // phase parities of the per-tile barriers
-        uint32_t pph[2] = {0, 0}, oph[2] = {0, 0}, qph[2] = {0, 0};
-        bool o_used[2] = {false, false};
+        uint32_t pph = 0, oph = 0, qph = 0; // phase parities of this tile's barriers
+        bool o_used = false;
+        auto adv = [](uint32_t &st, uint32_t &ph, int nstage) {
+            if (++st == (uint32_t)nstage) {
+                st = 0;
+                ph ^= 1u;
+            }
+        };
         for (int n = 0; ok; ++n) {
             const Item it = take_item(n, ok);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok || it.seq < 0) break;
-            const int n0 = it.t[0].n, n1 = it.t[1].n;
-            // S products still to issue that read each Q buffer (cascade: buffer 0 serves both tiles)
-            int rem0 = CASCADE ? n0 + n1 : n0, rem1 = CASCADE ? 0 : n1;
-            // S_t(j) = Q K^T into the tile's S columns
-            auto issue_s = [&](int t, int j) -> bool {
-                const int qb = CASCADE ? 0 : t;
-                bool w = mbar_wait(k_ready + kst, kph);
-                if (j == 0 && (!CASCADE || t == 0)) w = w && mbar_wait(q_full + qb, qph[qb]);
-                if (!__all_sync(0xffffffffu, w)) return false;
-                tc::fence_after_sync();
-                any_mma = true;
+            const int nt = t ? it.t[1].n : it.t[0].n;
+            const int ne = ring_count<SHARED>(it);
+            const int qb = CASCADE ? 0 : t;
+            // ring entries of the item this warp has passed (cascade: the other tile's are skipped)
+            int ke = 0, ve = 0;
+            auto owner = [&](int e) -> int {
+                int tt, jj;
+                ring_entry<SHARED>(it, e, tt, jj);
+                return tt;
+            };
+            // move a cursor to this tile's next entry (cascade: over the other tile's entries)
+            auto skip_others = [&](int &pos, uint32_t &st, uint32_t &ph, int nstage) {
+                if (!SHARED) {
+                    while (pos < ne && owner(pos) != t) {
+                        adv(st, ph, nstage);
+                        ++pos;
+                    }
+                }
+            };
+            // S(j) = Q K^T into the tile's S columns (its MMAs only; the caller commits)
+            auto mmas_s = [&]() {
                 const uint64_t a0 = dQ + (uint64_t)((qb * L::Q_TILE) >> 4);
                 const uint64_t b0 = dK + (uint64_t)(kst * (L::STAGE >> 4));
-                const uint32_t d = tmem + (uint32_t)(t * BN);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const int c = k >> 2, kk = k & 3;
-                    tc::mma_f16_warp(d, a0 + (uint64_t)((c * BM * 128 + kk * 32) >> 4),
+                    tc::mma_f16_warp(tS, a0 + (uint64_t)((c * BM * 128 + kk * 32) >> 4),
                                      b0 + (uint64_t)((c * BN * 128 + kk * 32) >> 4), IQK, k > 0 ? 1u : 0u);
                 }
+            };
+            // after S(j): S complete, this warp's share of the K stage, and Q after the tile's last S
+            auto commit_s = [&](int j) {
                 tc::commit_warp(s_full + t);
-                // the K stage frees once every S that reads it has been issued (and completes)
-                if (!SHARED || t == 1 || j >= n1) {
-                    tc::commit_warp(k_empty + kst);
-                    if (++kst == (uint32_t)NKS) {
-                        kst = 0;
-                        kph ^= 1u;
-                    }
+                tc::commit_warp(k_empty + kst); // this warp's share of the K stage
+                adv(kst, kph, NKS);
+                ++ke;
+                if (j == nt - 1) {
+                    tc::commit_warp(q_empty + qb); // the last S of the tile has read Q
+                    qph ^= 1u;
                 }
-                // the Q buffer frees after the last S that reads it
-                int &rem = qb == 0 ? rem0 : rem1;
-                if (--rem == 0) {
-                    tc::commit_warp(q_empty + qb);
-                    qph[qb] ^= 1u;
-                }
+            };
+            // S(0): Q and the first K tile
+            auto first_s = [&]() -> bool {
+                skip_others(ke, kst, kph, NKS);
+                if (!__all_sync(0xffffffffu, mbar_wait(k_ready + kst, kph) && mbar_wait(q_full + qb, qph))) return false;
+                tc::fence_after_sync();
+                any_mma = true;
+                mmas_s();
+                commit_s(0);
                 return true;
             };
-            // O_t += P_t(j) V(j), P read from tensor memory where the softmax left it (over S_t)
-            auto issue_pv = [&](int t, int j) -> bool {
-                bool w = mbar_wait(p_full + t, pph[t]) && mbar_wait(v_ready + vst, vph);
+            // O += P(j) V(j), then S(j + 1) right behind it: the pipe gets both groups back to back.
+            // P is read from tensor memory where the softmax left it (over S), and S(j + 1) overwrites
+            // those columns only after P V(j) has read them (one thread's MMAs complete in order).
+            auto step = [&](int j) -> bool {
+                skip_others(ve, vst, vph, NVS);
+                const bool more = j + 1 < nt;
+                // the next K tile is normally in place already; checked first, so that nothing but the
+                // softmax is waited for between the two groups
+                if (more) {
+                    skip_others(ke, kst, kph, NKS);
+                    if (!__all_sync(0xffffffffu, mbar_wait(k_ready + kst, kph))) return false;
+                }
+                bool w = mbar_wait(v_ready + vst, vph) && mbar_wait(p_full + t, pph);
                 // the previous item's epilogue of this tile has read O out of tensor memory
-                if (j == 0 && o_used[t]) w = w && mbar_wait(o_free + t, oph[t] ^ 1u);
+                if (j == 0 && o_used) w = w && mbar_wait(o_free + t, oph ^ 1u);
                 if (!__all_sync(0xffffffffu, w)) return false;
-                pph[t] ^= 1u;
+                pph ^= 1u;
                 tc::fence_after_sync();
-                const uint32_t ap = tmem + (uint32_t)(t * BN);
-                const uint32_t d = tmem + (uint32_t)(2 * BN + t * D);
                 const uint64_t b0 = dV + (uint64_t)(vst * (L::STAGE >> 4));
 #pragma unroll
                 for (int part = 0; part < NP; ++part)
 #pragma unroll
                     for (int k = 0; k < BN / 16; ++k)
-                        tc::mma_f16_ts_warp(d, ap + (uint32_t)(part * (BN / 2) + k * 8), b0 + (uint64_t)((k * 2048) >> 4),
+                        tc::mma_f16_ts_warp(tO, tS + (uint32_t)(part * (BN / 2) + k * 8), b0 + (uint64_t)((k * 2048) >> 4),
                                             IPV, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
-                if (!SHARED || t == 1 || j >= n1) {
-                    tc::commit_warp(v_empty + vst);
-                    if (++vst == (uint32_t)NVS) {
-                        vst = 0;
-                        vph ^= 1u;
-                    }
-                }
-                if (j == it.t[t].n - 1) {
+                // the V stage share goes out before S(j + 1) is issued (a commit covers every earlier MMA of
+                // this thread, so issued later it would hold the stage until S(j + 1) completes too); the
+                // P V MMAs queued ahead keep the pipe busy meanwhile
+                tc::commit_warp(v_empty + vst); // this warp's share of the V stage
+                adv(vst, vph, NVS);
+                ++ve;
+                if (more) mmas_s();
+                if (!more) {
                     tc::commit_warp(o_full + t); // the tile's O is complete once this commit arrives
-                    oph[t] ^= 1u;
-                    o_used[t] = true;
+                    oph ^= 1u;
+                    o_used = true;
+                } else {
+                    commit_s(j + 1);
                 }
                 return true;
             };
-            if (n0 > 0) ok = issue_s(0, 0);
-            if (ok && n1 > 0) ok = issue_s(1, 0);
-            const int steps = max(n0, n1);
-            for (int j = 0; j < steps && ok; ++j) {
-                if (j < n0) ok = issue_pv(0, j);
-                if (ok && j + 1 < n0) ok = issue_s(0, j + 1);
-                if (ok && j < n1) ok = issue_pv(1, j);
-                if (ok && j + 1 < n1) ok = issue_s(1, j + 1);
+            if (nt > 0) ok = first_s();
+            for (int j = 0; j < nt && ok; ++j) ok = step(j);
+            if constexpr (SHARED) {
+                // key tiles only the other tile reads: this warp's share of each K and V stage is given
+                // once the tile has landed (waiting for the load keeps the arrival in the stage's current
+                // phase), K and V of one key step together, in ring order: a later K load can depend on
+                // an earlier V release (the other tile's S(j + 1) follows its P V(j)), so all K shares
+                // first would deadlock
+                for (; ok && ke < ne; ++ke, ++ve) {
+                    ok = __all_sync(0xffffffffu, mbar_wait_hint(k_full + kst, kph));
+                    if (ok && lane == 0) mbar_arrive(k_empty + kst);
+                    adv(kst, kph, NKS);
+                    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_hint(v_full + vst, vph));
+                    if (ok && lane == 0) mbar_arrive(v_empty + vst);
+                    adv(vst, vph, NVS);
+                }
+            } else {
+                // the other tile's remaining entries
+                for (; ke < ne; ++ke) adv(kst, kph, NKS);
+                for (; ve < ne; ++ve) adv(vst, vph, NVS);
+                if (nt == 0 && ok) {
+                    // cascade: no split for this tile; its share of the Q buffer once Q has landed
+                    ok = __all_sync(0xffffffffu, mbar_wait_hint(q_full + qb, qph));
+                    if (ok && lane == 0) mbar_arrive(q_empty + qb);
+                    qph ^= 1u;
+                }
             }
-            if (lane == 0) mbar_arrive(item_empty + (n & 1));
+            if (lane == 0) mbar_arrive(item_empty + (n & (kItemSlots - 1)));
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
         }
         if (!ok && lane == 0) fail();
-        // every MMA issued by the elected lane has completed before TMEM is released (a CTA that found
-        // no item issued none and has nothing to wait for)
+        // every MMA issued by this warp's elected lane has completed before TMEM is released (a warp that
+        // issued none has nothing to wait for)
         if (any_mma) {
-            tc::commit_warp(fin);
-            if (!__all_sync(0xffffffffu, mbar_wait(fin, 0)) && lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
+            tc::commit_warp(fin + t);
+            if (!__all_sync(0xffffffffu, mbar_wait_hint(fin + t, 0)) && lane == 0) set_error(a.err, PKV_DEVERR_TIMEOUT);
         }
-    } else if (warp >= 4) {
+    } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
         // ---------------------------------------------------------------- softmax, one thread per row
         const int t = (warp - 4) >> 2;          // tile A (warps 4-7) or B (warps 8-11)
@@ -726,17 +863,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + (uint32_t)(2 * BN + t * D);
         bool ok = true;
         int ns = 0, no = 0;
+        int steps0 = 0, steps1 = 0; // key steps of tiles A and B in earlier items
+        // The two tiles' softmaxes take turns on the exponentials (they share the SMSPs and their
+        // transcendental units; run together, each takes twice as long and the MMAs of both tiles
+        // wait): in an item, A's step j follows B's step j - 1, and B's step j follows A's step j.
+        // The wait reads the other tile's monotonic count of finished steps, polled with a bound.
+        auto wait_turn = [&](int other, int target) -> bool {
+            volatile int *prog = sm_prog + other;
+            if (*prog >= target) return true;
+            const uint64_t t0 = global_timer_ns();
+            for (uint32_t i = 0; i < 0x80000000u; ++i) {
+                if (*prog >= target) return true;
+                __nanosleep(32);
+                if ((i & 63u) == 0u && global_timer_ns() - t0 > PKV_WAIT_LIMIT_NS) return false;
+            }
+            return false;
+        };
         for (int n = 0; ok; ++n) {
             const Item it = take_item(n, ok);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok || it.seq < 0) break;
             const Tile x = t ? it.t[1] : it.t[0];
+            const int n0 = it.t[0].n, n1 = it.t[1].n;
             if (x.n > 0) {
                 const int kvh = it.h / G;
                 const float sl = KV8 ? a.scale_log2 * a.k_scale[kvh] : a.scale_log2;
                 const int qpos = x.qpos0 + r; // absolute position of this row (causal modes)
                 float m_use = -INFINITY, l = 0.f;
                 for (int j = 0; j < x.n && ok; ++j) {
+                    // (spinning: S complete is on the critical path; a suspended wait wakes later)
                     ok = __all_sync(0xffffffffu, mbar_wait(s_full + t, ns & 1));
                     if (!ok) break;
                     ++ns;
@@ -762,13 +917,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < BN; ++c)
                             if (c >= lim) sr[c] = 0xFF800000u; // -inf
                     }
-                    float mx0 = -INFINITY, mx1 = -INFINITY;
+                    // row maximum: eight independent chains of three-input maxima, then a short tree
+                    float mc[8];
 #pragma unroll
-                    for (int c = 0; c < BN; c += 4) {
-                        mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-                        mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                    for (int q = 0; q < 8; ++q) mc[q] = __uint_as_float(sr[q]);
+#pragma unroll
+                    for (int c = 8; c < BN; c += 16) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) mc[q] = max3(mc[q], __uint_as_float(sr[c + q]), __uint_as_float(sr[c + 8 + q]));
                     }
-                    const float mx = fmaxf(mx0, mx1) * sl; // scale > 0 keeps the order
+                    const float mx = fmaxf(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], max3(mc[5], mc[6], mc[7]))) *
+                                     sl; // scale > 0 keeps the order
                     const bool up = mx > m_use + kRescale;
                     const float m_new = up ? mx : m_use;
                     const float alpha = up ? fast_exp2(m_use - m_new) : 1.f;
@@ -785,6 +944,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                             tc::st16(tO + cc * 16, o);
                         }
+                    }
+                    // this tile's turn on the exponentials (see wait_turn)
+                    if (t == 0 ? (j >= 1 && j - 1 < n1) : (j < n0)) {
+                        const int target = 4 * (t == 0 ? steps1 + j : steps0 + j + 1);
+                        ok = __all_sync(0xffffffffu, wait_turn(1 - t, target));
+                        if (!ok) break;
                     }
                     float2 rs = make_float2(0.f, 0.f);
                     const float2 sc2 = make_float2(sl, sl), nb2 = make_float2(nbase, nbase);
@@ -817,9 +982,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::wait_st();
                     tc::fence_before_sync();
                     mbar_arrive(p_full + t);
+                    __syncwarp();
+                    if (lane == 0) atomicAdd(sm_prog + t, 1); // this warp's exp phase of the step is done
                 }
                 // the tile's O is complete
-                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full + t, no & 1));
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait_hint(o_full + t, no & 1));
                 if (!ok) break;
                 ++no;
                 tc::fence_after_sync();
@@ -869,124 +1036,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_before_sync();
                 mbar_arrive(o_free + t); // O has been read out; the tile's next first P V may overwrite it
             }
+            steps0 += n0;
+            steps1 += n1;
             __syncwarp();
-            if (lane == 0) mbar_arrive(item_empty + (n & 1));
+            if (lane == 0) mbar_arrive(item_empty + (n & (kItemSlots - 1)));
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
         }
         if (!ok) fail();
-    } else {
-        // ---------------------------------------------------------------- warp 3
-        // Packed mode: the paged K/V write of the item's rows.  The item's own rows q0(A)..qlast are the
-        // keys of its last K/V tiles.  This warp follows every K tile and every V tile of the rings in
-        // order (so a stage's phase is never more than one ahead of it) and holds each stage until it is
-        // done with it: a stage frees only after the MMAs that read it and this warp.  Whole blocks of
-        // the item's rows leave shared memory as tiled TMA stores (one lane per block; one box of bs
-        // rows x 64 dims per half of D, the 128-byte swizzle undone by the copy engine) into their
-        // (block, K|V, head) tile of the pool; the rows of a partly filled last block (a sequence whose
-        // length is not a multiple of bs) go out as plain 16-byte stores, so no slot past the sequence
-        // is touched.  FP8 caches are written by the ranged append instead (write_pool = 0).
-        // FP8 caches in paged and cascade modes: widening of every K tile once it has landed.
-        constexpr int CPR = D / 8;    // 16-byte chunks per row
-        constexpr int RPI = 32 / CPR; // rows per warp instruction
-        const int cc = lane % CPR, rsub = lane / CPR;
-        const int c2 = cc >> 3, u = cc & 7;
-        if (WRITER && lane == 0) tc::prefetch_tmap(&tp);
-        bool ok = true;
-        int64_t g = 0;
-        for (int n = 0; ok; ++n) {
-            const Item it = take_item(n, ok);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok || it.seq < 0) break;
-            const int ne = ring_count<SHARED>(it);
-            if constexpr (WRITER) {
-                const int qlast = it.t[1].n > 0 ? it.t[1].qlast : it.t[0].qlast;
-                const int q0 = it.t[0].q0;
-                const bool writes = a.write_pool && it.h % G == 0;
-                const int kvh = it.h / G, lb0 = q0 >> a.lg_bs;
-                // lane l: table entry of logical block lb0 + l (at most 2 BM / bs <= 32 of them)
-                int blkv = -1;
-                {
-                    const int lb = lb0 + lane;
-                    if (writes && (lb << a.lg_bs) <= qlast && lb < a.max_blocks)
-                        blkv = a.tables[(int64_t)it.seq * a.max_blocks + lb];
-                }
-                // the item's rows of tile j, from `src` (a K or a V stage) into the K (kv = 0) or V half
-                auto write_tile = [&](int j, const uint8_t *src, int kv) {
-                    const int lo = max(j * BN, q0), hi = min(j * BN + BN - 1, qlast);
-                    if (lo > hi) return;
-                    const int bfirst = lo >> a.lg_bs;           // lo is a multiple of bs
-                    const int nfull = (hi + 1 - lo) >> a.lg_bs; // whole blocks among the rows
-                    {
-                        const int lb = bfirst + lane;
-                        const int blk = __shfl_sync(0xffffffffu, blkv, min(lb - lb0, 31));
-                        if (lane < nfull) {
-                            if (blk < 0 || blk >= a.num_blocks) {
-                                set_error(a.err, PKV_DEVERR_BLOCK_ID);
-                            } else {
-                                const uint8_t *box = src + ((lb << a.lg_bs) - j * BN) * 128;
-                                const int y = ((blk * 2 + kv) * a.hkv + kvh) << a.lg_bs;
-#pragma unroll
-                                for (int c = 0; c < D / 64; ++c) tc::tma_store_2d(&tp, c * 64, y, box + c * BN * 128);
-                                tc::bulk_commit();
-                            }
-                        }
-                    }
-                    for (int p0 = lo + (nfull << a.lg_bs); p0 <= hi; p0 += RPI) { // fewer than bs rows
-                        const int p = p0 + rsub;
-                        const int lb = p >> a.lg_bs;
-                        const int blk = __shfl_sync(0xffffffffu, blkv, min(lb - lb0, 31));
-                        if (p > hi) continue;
-                        if (blk < 0 || blk >= a.num_blocks) {
-                            if (cc == 0) set_error(a.err, PKV_DEVERR_BLOCK_ID);
-                            continue;
-                        }
-                        const int rr = p - j * BN;
-                        const int sw = c2 * BN * 128 + rr * 128 + ((u ^ (rr & 7)) << 4);
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(src + sw);
-                        const int64_t dst = ((int64_t)(blk * 2 + kv) * a.hkv + kvh) * a.tile_elems +
-                                            (int64_t)(p - (lb << a.lg_bs)) * D + cc * 8;
-                        *reinterpret_cast<uint4 *>(a.pool + dst * 2) = xv;
-                    }
-                    tc::bulk_wait_read_all(); // the stores have read the stage; it may be released
-                };
-                for (int e = 0; e < ne && ok; ++e) {
-                    const int64_t gg = g + e;
-                    const bool mine = writes && e >= q0 / BN;
-                    const int sk = (int)(gg % NKS), sv = (int)(gg % NVS);
-                    ok = __all_sync(0xffffffffu, mbar_wait(k_full + sk, (gg / NKS) & 1));
-                    if (!ok) break;
-                    if (mine) write_tile(e, smem + L::K0 + sk * L::STAGE, 0);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(k_empty + sk);
-                    ok = __all_sync(0xffffffffu, mbar_wait(v_full + sv, (gg / NVS) & 1));
-                    if (!ok) break;
-                    if (mine) write_tile(e, smem + L::V0 + sv * L::STAGE, 1);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(v_empty + sv);
-                }
-            } else if constexpr (KV8) {
-                for (int e = 0; e < ne && ok; ++e) {
-                    const int64_t gg = g + e;
-                    const int st = (int)(gg % NKS);
-                    ok = __all_sync(0xffffffffu, mbar_wait(k_full + st, (gg / NKS) & 1));
-                    if (!ok) break;
-                    uint8_t *stage = smem + L::K0 + st * L::STAGE;
-                    for (int rr = lane; rr < BN; rr += 32) widen_row<D, MT>(stage, rr);
-                    fence_proxy_async_smem(); // the MMA reads the widened tile through the async proxy
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(kc_full + st);
-                }
-            }
-            if (!ok) break;
-            g += ne;
-            if (lane == 0) mbar_arrive(item_empty + (n & 1));
-            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-        }
-        if constexpr (WRITER) tc::bulk_wait_all(); // the pool writes have completed before the CTA exits
-        if (!ok && lane == 0) fail();
-        (void)c2;
-        (void)u;
-        (void)rsub;
     }
 
     tc::fence_before_sync();

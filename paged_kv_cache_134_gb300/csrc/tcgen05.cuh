@@ -239,6 +239,13 @@ PKV_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 
 // every bulk store this thread committed has completed
 PKV_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// L2 prefetch of one box of a tiled tensor (no shared memory, no completion to wait for)
+PKV_DEV void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 PKV_DEV void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
