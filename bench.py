@@ -235,19 +235,21 @@ def _time_loop(fn, steps, stream):
 
 
 class L2Flush:
-    """Writes a device buffer of twice the L2 size, so that the next kernel finds none of its inputs
-    in L2.  Called between timed launches, outside the library's events around its kernels."""
+    """Reads a device buffer of twice the L2 size, so that the next kernel finds none of its inputs
+    in L2.  A read leaves L2 holding clean lines: the dirty lines of the previous launch are written
+    back during the flush, not during the next timed kernel (a flush that writes its buffer would
+    leave 2 x L2 of dirty lines to be written back inside the timed launch).  Called between timed
+    launches, outside the library's events around its kernels."""
 
     def __init__(self):
         l2 = int(getattr(torch.cuda.get_device_properties(torch.cuda.current_device()), "L2_cache_size", 0) or
                  (128 << 20))
         self.bytes = 2 * l2
-        self.buf = torch.empty(self.bytes // 4, dtype=torch.int32, device="cuda")
-        self.n = 0
+        self.buf = torch.zeros(self.bytes // 4, dtype=torch.int32, device="cuda")
+        self.acc = torch.zeros((), dtype=torch.int64, device="cuda")
 
     def __call__(self):
-        self.n += 1
-        self.buf.fill_(self.n)
+        torch.sum(self.buf, dtype=torch.int64, out=self.acc)
 
 
 def _kernel_loop_flushed(fn, reps, flush):
