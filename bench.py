@@ -249,7 +249,7 @@ class L2Flush:
         self.acc = torch.zeros((), dtype=torch.int64, device="cuda")
 
     def __call__(self):
-        torch.sum(self.buf, dtype=torch.int64, out=self.acc)
+        torch.sum(self.buf, dim=0, dtype=torch.int64, out=self.acc)
 
 
 def _kernel_loop_flushed(fn, reps, flush):

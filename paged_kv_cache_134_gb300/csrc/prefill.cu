@@ -170,14 +170,13 @@ bool pool_map(CUtensorMap *m, const pkv_cache *c) {
 }
 
 template <int MODE, bool KV8>
-cudaError_t dispatch(int D, int mt, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                     const CUtensorMap &tp, const Args &a, int64_t max_ctas, int num_sms, cudaStream_t st) {
+cudaError_t dispatch(int D, int mt, const Maps &m, const Args &a, int64_t max_ctas, int num_sms, cudaStream_t st) {
     if (D == 128)
-        return mt == PKV_BF16 ? launch_attn<128, PKV_BF16, MODE, KV8>(tq, tk, tv, tp, a, max_ctas, num_sms, st)
-                              : launch_attn<128, PKV_F16, MODE, KV8>(tq, tk, tv, tp, a, max_ctas, num_sms, st);
+        return mt == PKV_BF16 ? launch_attn<128, PKV_BF16, MODE, KV8>(m, a, max_ctas, num_sms, st)
+                              : launch_attn<128, PKV_F16, MODE, KV8>(m, a, max_ctas, num_sms, st);
     if (D == 64)
-        return mt == PKV_BF16 ? launch_attn<64, PKV_BF16, MODE, KV8>(tq, tk, tv, tp, a, max_ctas, num_sms, st)
-                              : launch_attn<64, PKV_F16, MODE, KV8>(tq, tk, tv, tp, a, max_ctas, num_sms, st);
+        return mt == PKV_BF16 ? launch_attn<64, PKV_BF16, MODE, KV8>(m, a, max_ctas, num_sms, st)
+                              : launch_attn<64, PKV_F16, MODE, KV8>(m, a, max_ctas, num_sms, st);
     return cudaErrorInvalidValue;
 }
 
@@ -277,10 +276,11 @@ cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st
     // blocks; row coordinates are 32-bit
     const int64_t pool_rows = c->num_blocks * 2 * c->num_kv_heads * c->block_size;
     if (pool_rows > 0x7FFFFFFFLL) return cudaErrorNotSupported;
-    CUtensorMap tq, tk, tv, tp;
-    if (!make_map(&tq, p.q, mt, p.total_tokens, (int64_t)p.num_q_heads * D, BM) ||
-        !make_map(&tk, p.k, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN) ||
-        !make_map(&tv, p.v, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN) || !pool_map(&tp, c))
+    Maps m;
+    if (!make_map(&m.q, p.q, mt, p.total_tokens, (int64_t)p.num_q_heads * D, BM) ||
+        !make_map(&m.k, p.k, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN) ||
+        !make_map(&m.v, p.v, mt, p.total_tokens, (int64_t)c->num_kv_heads * D, BN) || !pool_map(&m.pool, c) ||
+        !make_map(&m.out, p.out, mt, p.total_tokens, (int64_t)p.num_q_heads * D, BM))
         return cudaErrorInvalidValue;
     if (p.ctx || kv8) {
         // A cached prefix: the new tokens' K/V go to their slots first, then attention reads every key
@@ -295,11 +295,11 @@ cudaError_t launch_prefill(pkv_cache *c, const PrefillLaunch &p, cudaStream_t st
     if (e != cudaSuccess) return e;
     const int64_t max_ctas = items * p.num_q_heads;
     if (!p.ctx)
-        e = dispatch<MODE_PACKED, false>(D, mt, tq, tk, tv, tp, a, max_ctas, c->num_sms, st);
+        e = dispatch<MODE_PACKED, false>(D, mt, m, a, max_ctas, c->num_sms, st);
     else if (kv8)
-        e = dispatch<MODE_PAGED, true>(D, mt, tq, tk, tv, tp, a, max_ctas, c->num_sms, st);
+        e = dispatch<MODE_PAGED, true>(D, mt, m, a, max_ctas, c->num_sms, st);
     else
-        e = dispatch<MODE_PAGED, false>(D, mt, tq, tk, tv, tp, a, max_ctas, c->num_sms, st);
+        e = dispatch<MODE_PAGED, false>(D, mt, m, a, max_ctas, c->num_sms, st);
     g_pkv_launches++;
     return e;
 }
@@ -350,16 +350,17 @@ cudaError_t launch_cascade_prefix(pkv_cache *c, const CascadePrefixLaunch &p, cu
     const int64_t pool_rows = c->num_blocks * 2 * c->num_kv_heads * c->block_size;
     if (pool_rows > 0x7FFFFFFFLL) return cudaErrorNotSupported;
     // q [S][Hq][D] as rows of sequences: a box of 128 sequences x 64 dims of one head
-    CUtensorMap tq, tp;
-    if (!make_map(&tq, p.q, mt, p.num_seqs, (int64_t)p.num_q_heads * D, BM) || !pool_map(&tp, c))
+    Maps m; // cascade: q and the pool (k, v, out unused)
+    if (!make_map(&m.q, p.q, mt, p.num_seqs, (int64_t)p.num_q_heads * D, BM) || !pool_map(&m.pool, c))
         return cudaErrorInvalidValue;
     if (part == 1) {
         e = launch_plan(a, st);
         g_pkv_launches++;
         return e;
     }
-    e = kv8 ? dispatch<MODE_CASCADE, true>(D, mt, tq, tp, tp, tp, a, pairs * p.num_q_heads, c->num_sms, st)
-            : dispatch<MODE_CASCADE, false>(D, mt, tq, tp, tp, tp, a, pairs * p.num_q_heads, c->num_sms, st);
+    m.k = m.v = m.out = m.pool;
+    e = kv8 ? dispatch<MODE_CASCADE, true>(D, mt, m, a, pairs * p.num_q_heads, c->num_sms, st)
+            : dispatch<MODE_CASCADE, false>(D, mt, m, a, pairs * p.num_q_heads, c->num_sms, st);
     g_pkv_launches++;
     return e;
 }

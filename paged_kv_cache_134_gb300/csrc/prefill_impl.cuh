@@ -72,6 +72,13 @@ struct Args {
     int max_splits = 0, prefix_tokens = 0, split_tokens = 0, nps = 0;
 };
 
+// TMA descriptors of one launch: q (and out) as [rows][Hq * D] with 64-column boxes of BM rows; packed
+// k and v as [T][Hkv * D] with boxes of BN rows; the pool's rows (16-bit: bs rows x 64 dims; E4M3: bs
+// whole rows)
+struct Maps {
+    CUtensorMap q, k, v, pool, out;
+};
+
 // Shared memory: two Q tiles, the K ring and the V ring.  A 16-bit tile is [D/64 halves][rows][128 B],
 // 128-byte swizzled.  FP8 caches: the codes of a K or V tile land at stage + kCodeOff (row r at r * D)
 // and are widened into the 16-bit layout of the same stage: for D = 128 the codes are the upper half
@@ -88,7 +95,7 @@ struct Layout {
     static constexpr int K0 = Q + 2 * Q_TILE;
     static constexpr int V0 = K0 + NKS * STAGE;
     static constexpr int BAR = V0 + NVS * STAGE;
-    static constexpr int NBARS = 4 + 4 + 2 + 2 + 4 * NKS + 4 * NVS + 2 + 2 + 2 + 2 + 2;
+    static constexpr int NBARS = 4 + 4 + 2 + 2 + 4 * NKS + 4 * NVS + 2 + 2 + 2 + 2 + 2 + 2;
     static constexpr int MISC = BAR + (NBARS * 8 + 15) / 16 * 16; // TMEM slot, abort flag; item slots at + 16
     static constexpr int TOTAL = MISC + 16 + 64;
     static_assert(TOTAL + 1024 <= 232448, "shared memory");
@@ -258,9 +265,8 @@ PKV_DEV void ring_entry(const Item &it, int e, int &t, int &j) {
 }
 
 template <int D, int MT, int MODE, bool KV8>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tp, const Args a) {
+__global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ Maps maps, const Args a) {
+    const CUtensorMap &tq = maps.q, &tk = maps.k, &tv = maps.v, &tp = maps.pool, &to = maps.out;
     using L = Layout<D, KV8>;
     constexpr bool PAGED = MODE != MODE_PACKED;    // keys from the pool through the block table
     constexpr bool CASCADE = MODE == MODE_CASCADE; // no causal mask, fp32 split partials out
@@ -284,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *v_full = k_spare + NKS, *v_empty = v_full + NVS, *vc_full = v_empty + NVS, *v_spare = vc_full + NVS;
     uint64_t *s_full = v_spare + NVS, *p_full = s_full + 2, *o_full = p_full + 2, *o_free = o_full + 2;
     uint64_t *fin = o_free + 2;
+    uint64_t *epi = fin + 2; // a tile's output rows are staged (one arrival per softmax warp)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::MISC + 4);
     // exp phases the softmax of each tile has finished, counted per warp (4 per key step), monotonic
@@ -310,9 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(q_full + s, 1);
             mbar_init(q_empty + s, CASCADE ? 2 : 1); // cascade: one Q tile, read by both MMA warps
             mbar_init(s_full + s, 1);
-            mbar_init(p_full + s, 128);
+            mbar_init(p_full + s, 4); // one arrival per softmax warp
             mbar_init(o_full + s, 1);
-            mbar_init(o_free + s, 128);
+            mbar_init(o_free + s, 4);
         }
         for (int s = 0; s < NKS; ++s) {
             mbar_init(k_full + s, 1);
@@ -326,6 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(fin, 1);
         mbar_init(fin + 1, 1);
+        mbar_init(epi, 4);
+        mbar_init(epi + 1, 4);
         *abort_flag = 0;
         sm_prog[0] = 0;
         sm_prog[1] = 0;
@@ -516,29 +525,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!isK && !widen_pending()) ok = false; // before waiting for the next item
             if (!ok) break;
             if (isK) {
-                // ---- scheduler: take the next item and publish it.  This happens once the previous
-                // item's last K tile is issued, a few key steps before it ends; the item's Q tiles and
-                // first key tiles are prefetched into L2 now, so that their loads, which wait for the
-                // previous item's buffers to free up, come from L2
+                // ---- scheduler: take the next item and publish it (once the previous item's last K
+                // tile is issued, a few key steps before that item ends)
                 it = publish(n, ok);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                if (it.seq >= 0 && lane == 0) {
+                if (n > 0 && it.seq >= 0 && lane == 0) {
+                    // the item's Q tiles load only once the previous item's last S of each tile is done:
+                    // staged in L2 now, they then arrive from L2
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
                         if (CASCADE ? b == 1 : it.t[b].n == 0) continue;
 #pragma unroll
-                        for (int c = 0; c < D / 64; ++c)
-                            tc::tma_prefetch_2d(&tq, it.h * D + c * 64, it.start + it.t[b].q0);
-                    }
-                    if constexpr (!PAGED) {
-                        const int nk = min(ring_count<SHARED>(it), 2);
-                        for (int e = 0; e < nk; ++e)
-#pragma unroll
-                            for (int c = 0; c < D / 64; ++c) {
-                                tc::tma_prefetch_2d(&tk, (it.h / G) * D + c * 64, it.start + e * BN);
-                                tc::tma_prefetch_2d(&tv, (it.h / G) * D + c * 64, it.start + e * BN);
-                            }
+                        for (int c = 0; c < D / 64; ++c) tc::tma_prefetch_2d(&tq, it.h * D + c * 64, it.start + it.t[b].q0);
                     }
                 }
             } else {
@@ -549,29 +548,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it.seq < 0) break;
             const int kvh = it.h / G;
             if (isK && !widen_pending()) ok = false; // before the Q loads wait for their buffers
-            if (isK && lane == 0 && ok) {
-                // ---- Q: buffer t holds tile t (cascade: buffer 0 holds the one query tile of both splits)
-#pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    if (CASCADE ? b == 1 : it.t[b].n == 0) continue;
-                    if (nq[b] >= 1 && !mbar_wait_hint(q_empty + b, (nq[b] - 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(q_full + b, L::Q_TILE);
-                    const int row = it.start + it.t[b].q0;
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c)
-                        tc::tma_load_2d(smem + L::Q + b * L::Q_TILE + c * BM * 128, &tq, it.h * D + c * 64, row,
-                                        q_full + b);
-                    ++nq[b];
-                }
-            }
-            ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 if (lane == 0) fail();
                 break;
             }
+            // ---- Q (warp 0): buffer b holds tile b (cascade: buffer 0 holds the one query tile of both
+            // splits).  Each load waits for the previous item's last S of that tile, so the loads are
+            // interleaved with the K tiles in the order their buffers free up: K tile 0 (its stage frees
+            // a few key steps before the previous item ends), Q_A, K tile 1, Q_B, the rest.  The first S
+            // of each tile then finds both operands in place.
+            // query row of each buffer's tile, -1: nothing to load
+            const int qrow0 = it.t[0].n > 0 ? it.start + it.t[0].q0 : -1;
+            const int qrow1 = !CASCADE && it.t[1].n > 0 ? it.start + it.t[1].q0 : -1;
+            const int qcol = it.h * D;
+            int qnext = 0; // next Q buffer to load
+            auto issue_q = [&](int upto) {
+                for (; qnext <= upto && qnext < 2 && ok; ++qnext) {
+                    const int b = qnext;
+                    const int row = b ? qrow1 : qrow0;
+                    if (row < 0) continue;
+                    if (lane == 0) {
+                        const bool w = nq[b] < 1 || mbar_wait_hint(q_empty + b, (nq[b] - 1) & 1);
+                        if (w) {
+                            mbar_arrive_expect_tx(q_full + b, L::Q_TILE);
+#pragma unroll
+                            for (int c = 0; c < D / 64; ++c)
+                                tc::tma_load_2d(smem + L::Q + b * L::Q_TILE + c * BM * 128, &tq, qcol + c * 64, row,
+                                                q_full + b);
+                        } else {
+                            fail();
+                        }
+                        ok = w;
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    ++nq[b];
+                }
+            };
             const int ne = ring_count<SHARED>(it);
             // packed mode: this item writes the K/V of its own rows (the first query head of each KV
             // group does), from the key tiles that hold them
@@ -671,7 +683,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 issued = e + 1;
                 if constexpr (KV8) pend = gg;
+                if (isK && e < 2) issue_q(e); // Q_A after K tile 0, Q_B after K tile 1
             }
+            if (isK) issue_q(1); // items of fewer than two key tiles
             g += issued; // tiles issued so far, all items
             if (!isK && lane == 0) mbar_arrive(item_empty + (n & (kItemSlots - 1)));
             if (!ok) {
@@ -725,6 +739,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok || it.seq < 0) break;
             const int nt = t ? it.t[1].n : it.t[0].n;
+            // shared modes: key entries j >= n_other are read by this tile alone, which then gives the
+            // stage's release for both tiles (two commits), so the other tile's issuer skips them
+            // without waiting for their loads
+            const int n_other = t ? it.t[0].n : it.t[1].n;
             const int ne = ring_count<SHARED>(it);
             const int qb = CASCADE ? 0 : t;
             // ring entries of the item this warp has passed (cascade: the other tile's are skipped)
@@ -758,10 +776,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto commit_s = [&](int j) {
                 tc::commit_warp(s_full + t);
                 tc::commit_warp(k_empty + kst); // this warp's share of the K stage
+                if (SHARED && j >= n_other) tc::commit_warp(k_empty + kst); // and the other tile's
                 adv(kst, kph, NKS);
                 ++ke;
                 if (j == nt - 1) {
-                    tc::commit_warp(q_empty + qb); // the last S of the tile has read Q
+                    // cascade: the last S of the tile has read Q (other modes: the epilogue, which stages
+                    // the tile's output in the Q buffer, frees it)
+                    if constexpr (CASCADE) tc::commit_warp(q_empty + qb);
                     qph ^= 1u;
                 }
             };
@@ -804,6 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // this thread, so issued later it would hold the stage until S(j + 1) completes too); the
                 // P V MMAs queued ahead keep the pipe busy meanwhile
                 tc::commit_warp(v_empty + vst); // this warp's share of the V stage
+                if (SHARED && j >= n_other) tc::commit_warp(v_empty + vst); // and the other tile's
                 adv(vst, vph, NVS);
                 ++ve;
                 if (more) mmas_s();
@@ -819,17 +841,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nt > 0) ok = first_s();
             for (int j = 0; j < nt && ok; ++j) ok = step(j);
             if constexpr (SHARED) {
-                // key tiles only the other tile reads: this warp's share of each K and V stage is given
-                // once the tile has landed (waiting for the load keeps the arrival in the stage's current
-                // phase), K and V of one key step together, in ring order: a later K load can depend on
-                // an earlier V release (the other tile's S(j + 1) follows its P V(j)), so all K shares
-                // first would deadlock
-                for (; ok && ke < ne; ++ke, ++ve) {
-                    ok = __all_sync(0xffffffffu, mbar_wait_hint(k_full + kst, kph));
-                    if (ok && lane == 0) mbar_arrive(k_empty + kst);
+                // key tiles only the other tile reads: released by that tile (see n_other)
+                for (; ke < ne; ++ke, ++ve) {
                     adv(kst, kph, NKS);
-                    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_hint(v_full + vst, vph));
-                    if (ok && lane == 0) mbar_arrive(v_empty + vst);
                     adv(vst, vph, NVS);
                 }
             } else {
@@ -862,7 +876,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_off + (uint32_t)(t * BN);
         const uint32_t tO = tmem + lane_off + (uint32_t)(2 * BN + t * D);
         bool ok = true;
-        int ns = 0, no = 0;
+        int ns = 0, no = 0, nepi = 0;
         int steps0 = 0, steps1 = 0; // key steps of tiles A and B in earlier items
         // The two tiles' softmaxes take turns on the exponentials (they share the SMSPs and their
         // transcendental units; run together, each takes twice as long and the MMAs of both tiles
@@ -981,9 +995,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l = l * alpha + (rs.x + rs.y);
                     tc::wait_st();
                     tc::fence_before_sync();
-                    mbar_arrive(p_full + t);
-                    __syncwarp();
-                    if (lane == 0) atomicAdd(sm_prog + t, 1); // this warp's exp phase of the step is done
+                    __syncwarp(); // every lane's P is stored; one arrival for the warp
+                    if (lane == 0) {
+                        mbar_arrive(p_full + t);
+                        atomicAdd(sm_prog + t, 1); // this warp's exp phase of the step is done
+                    }
                 }
                 // the tile's O is complete
                 if (ok) ok = __all_sync(0xffffffffu, mbar_wait_hint(o_full + t, no & 1));
@@ -998,43 +1014,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool valid = r < it.n;
                     const int64_t idx = ((int64_t)(it.start + r) * a.hq + it.h) * a.max_splits + 2 * it.pr + t;
                     float *wo = a.ws_o + idx * D;
+                    uint32_t o[D]; // the whole row in one tensor-memory round trip
 #pragma unroll
-                    for (int cc = 0; cc < D / 16; ++cc) {
-                        uint32_t o[16];
-                        tc::ld16(tO + cc * 16, o);
-                        tc::wait_ld();
-                        if (valid) {
-                            float4 *dst = reinterpret_cast<float4 *>(wo + cc * 16);
+                    for (int cc = 0; cc < D / 32; ++cc) tc::ld32(tO + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[cc * 32]));
+                    tc::wait_ld();
+                    if (valid) {
+                        float4 *dst = reinterpret_cast<float4 *>(wo);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                dst[e] = make_float4(__uint_as_float(o[4 * e]) * vs, __uint_as_float(o[4 * e + 1]) * vs,
-                                                     __uint_as_float(o[4 * e + 2]) * vs,
-                                                     __uint_as_float(o[4 * e + 3]) * vs);
-                        }
+                        for (int e = 0; e < D / 4; ++e)
+                            dst[e] = make_float4(__uint_as_float(o[4 * e]) * vs, __uint_as_float(o[4 * e + 1]) * vs,
+                                                 __uint_as_float(o[4 * e + 2]) * vs, __uint_as_float(o[4 * e + 3]) * vs);
                     }
                     if (valid) reinterpret_cast<float2 *>(a.ws_ml)[idx] = make_float2(m_use, l);
                 } else {
                     const int row = x.q0 + r;
                     const float inv = vs / l;
-                    T *orow = static_cast<T *>(a.out) + ((int64_t)(it.start + row) * a.hq + it.h) * D;
+                    uint32_t o[D]; // the whole row in one tensor-memory round trip
 #pragma unroll
-                    for (int cc = 0; cc < D / 16; ++cc) {
-                        uint32_t o[16];
-                        tc::ld16(tO + cc * 16, o);
-                        tc::wait_ld();
-                        uint32_t w[8];
+                    for (int cc = 0; cc < D / 32; ++cc) tc::ld32(tO + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[cc * 32]));
+                    tc::wait_ld();
+                    const bool lead = (warp & 3) == 0 && lane == 0;
+                    if (x.q0 + BM <= it.n) {
+                        // a whole tile of the sequence's rows: staged in this tile's Q buffer (free, since the
+                        // tile's last S has completed) in the Q tile's own 128-byte swizzled layout, then one TMA
+                        // store per 64 columns writes coalesced rows; the buffer goes back to the Q loader once
+                        // the stores have read it
+                        uint8_t *stage = smem + L::Q + t * L::Q_TILE;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            w[e] = pack2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv, MT);
+                        for (int cc = 0; cc < D / 8; ++cc) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                w[e] = pack2(__uint_as_float(o[8 * cc + 2 * e]) * inv, __uint_as_float(o[8 * cc + 2 * e + 1]) * inv, MT);
+                            const int h = cc >> 3, u = cc & 7;
+                            *reinterpret_cast<uint4 *>(stage + h * BM * 128 + r * 128 + ((u ^ (r & 7)) << 4)) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                        fence_proxy_async_smem(); // the stores read the tile through the async proxy
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(epi + t);
+                        if (lead) {
+                            // the four warps' rows are staged (bounded wait: a warp that gave up never arrives)
+                            if (mbar_wait(epi + t, nepi & 1)) {
+#pragma unroll
+                                for (int h = 0; h < D / 64; ++h)
+                                    tc::tma_store_2d(&to, it.h * D + h * 64, it.start + x.q0, stage + h * BM * 128);
+                                tc::bulk_commit();
+                                tc::bulk_wait_read_all();
+                                mbar_arrive(q_empty + t);
+                            } else {
+                                ok = false;
+                            }
+                        }
+                        ++nepi;
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                    } else {
+                        // the sequence's last, partial tile: row by row, so that no row of the next sequence is
+                        // written; the Q buffer is not used here and is free already
+                        if (lead) mbar_arrive(q_empty + t);
                         if (row < it.n) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 16);
-                            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                            T *orow = static_cast<T *>(a.out) + ((int64_t)(it.start + row) * a.hq + it.h) * D;
+#pragma unroll
+                            for (int cc = 0; cc < D / 8; ++cc) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    w[e] = pack2(__uint_as_float(o[8 * cc + 2 * e]) * inv,
+                                                 __uint_as_float(o[8 * cc + 2 * e + 1]) * inv, MT);
+                                reinterpret_cast<uint4 *>(orow)[cc] = make_uint4(w[0], w[1], w[2], w[3]);
+                            }
                         }
                     }
                 }
                 tc::fence_before_sync();
-                mbar_arrive(o_free + t); // O has been read out; the tile's next first P V may overwrite it
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free + t); // O has been read out; the tile's next first P V may overwrite it
             }
             steps0 += n0;
             steps1 += n1;
@@ -1043,6 +1097,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
         }
         if (!ok) fail();
+        // the output tiles' TMA stores have completed before the CTA exits
+        if (!CASCADE && (warp & 3) == 0 && lane == 0) tc::bulk_wait_all();
     }
 
     tc::fence_before_sync();
@@ -1056,42 +1112,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // launch of one instantiation (prefill_packed.cu, prefill_paged.cu, prefill_cascade.cu)
 template <int D, int MT, int MODE, bool KV8>
-cudaError_t launch_attn(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tp,
-                        const Args &a, int64_t max_ctas, int num_sms, cudaStream_t st) {
+cudaError_t launch_attn(const Maps &m, const Args &a, int64_t max_ctas, int num_sms, cudaStream_t st) {
     auto kern = attn_kernel<D, MT, MODE, KV8>;
     const int smem = Layout<D, KV8>::TOTAL;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = std::min<int64_t>(max_ctas, (int64_t)num_sms);
-    return pdl_launch(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, tq, tk, tv, tp, a);
+    return pdl_launch(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, m, a);
 }
 
 #define PKV_ATTN_EXTERN(MODE, KV8)                                                                                     \
-    extern template cudaError_t launch_attn<128, PKV_F16, MODE, KV8>(const CUtensorMap &, const CUtensorMap &,       \
-                                                                     const CUtensorMap &, const CUtensorMap &,       \
-                                                                     const Args &, int64_t, int, cudaStream_t);      \
-    extern template cudaError_t launch_attn<128, PKV_BF16, MODE, KV8>(const CUtensorMap &, const CUtensorMap &,      \
-                                                                      const CUtensorMap &, const CUtensorMap &,      \
-                                                                      const Args &, int64_t, int, cudaStream_t);     \
-    extern template cudaError_t launch_attn<64, PKV_F16, MODE, KV8>(const CUtensorMap &, const CUtensorMap &,        \
-                                                                    const CUtensorMap &, const CUtensorMap &,        \
-                                                                    const Args &, int64_t, int, cudaStream_t);       \
-    extern template cudaError_t launch_attn<64, PKV_BF16, MODE, KV8>(const CUtensorMap &, const CUtensorMap &,       \
-                                                                     const CUtensorMap &, const CUtensorMap &,       \
-                                                                     const Args &, int64_t, int, cudaStream_t);
-#define PKV_ATTN_INSTANTIATE(MODE, KV8)                                                                                \
-    template cudaError_t launch_attn<128, PKV_F16, MODE, KV8>(const CUtensorMap &, const CUtensorMap &,              \
-                                                              const CUtensorMap &, const CUtensorMap &, const Args &, \
-                                                              int64_t, int, cudaStream_t);                            \
-    template cudaError_t launch_attn<128, PKV_BF16, MODE, KV8>(const CUtensorMap &, const CUtensorMap &,             \
-                                                               const CUtensorMap &, const CUtensorMap &,              \
-                                                               const Args &, int64_t, int, cudaStream_t);             \
-    template cudaError_t launch_attn<64, PKV_F16, MODE, KV8>(const CUtensorMap &, const CUtensorMap &,               \
-                                                             const CUtensorMap &, const CUtensorMap &, const Args &,  \
-                                                             int64_t, int, cudaStream_t);                             \
-    template cudaError_t launch_attn<64, PKV_BF16, MODE, KV8>(const CUtensorMap &, const CUtensorMap &,              \
-                                                              const CUtensorMap &, const CUtensorMap &, const Args &, \
-                                                              int64_t, int, cudaStream_t);
+    extern template cudaError_t launch_attn<128, PKV_F16, MODE, KV8>(const Maps &, const Args &, int64_t, int, cudaStream_t);  \
+    extern template cudaError_t launch_attn<128, PKV_BF16, MODE, KV8>(const Maps &, const Args &, int64_t, int, cudaStream_t); \
+    extern template cudaError_t launch_attn<64, PKV_F16, MODE, KV8>(const Maps &, const Args &, int64_t, int, cudaStream_t);   \
+    extern template cudaError_t launch_attn<64, PKV_BF16, MODE, KV8>(const Maps &, const Args &, int64_t, int, cudaStream_t);
+#define PKV_ATTN_INSTANTIATE(MODE, KV8)                                                                         \
+    template cudaError_t launch_attn<128, PKV_F16, MODE, KV8>(const Maps &, const Args &, int64_t, int, cudaStream_t);  \
+    template cudaError_t launch_attn<128, PKV_BF16, MODE, KV8>(const Maps &, const Args &, int64_t, int, cudaStream_t); \
+    template cudaError_t launch_attn<64, PKV_F16, MODE, KV8>(const Maps &, const Args &, int64_t, int, cudaStream_t);   \
+    template cudaError_t launch_attn<64, PKV_BF16, MODE, KV8>(const Maps &, const Args &, int64_t, int, cudaStream_t);
 
 PKV_ATTN_EXTERN(MODE_PACKED, false)
 PKV_ATTN_EXTERN(MODE_PAGED, false)
