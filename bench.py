@@ -559,18 +559,22 @@ def run_ours(args):
     sampler = ClockSampler(local, os.path.join(clock_dir, f"pkv_clocks_rank{rank}.csv"))
     time.sleep(0.2)
     launches0 = P.kernel_launches()
-    # events around every 10th decode kernel only: the kernel's duration is sampled live while the
-    # other steps keep the append -> decode -> merge overlap of programmatic dependent launch
-    # (every 10th launch over long runs; at least 10 launches bracketed when the run is short)
-    every = max(1, min(10, args.steps // 10))
-    cache.profile_start(kinds=("decode",), every=every)
+    # no events inside the timed region: an event between two kernels stops the append -> decode ->
+    # merge overlap of programmatic dependent launch
     _barrier(ws)
     torch.cuda.synchronize()
     elapsed = _time_loop(step, args.steps, stream)
     torch.cuda.synchronize()
     _barrier(ws)
-    prof = cache.profile_read()
     launches = P.kernel_launches() - launches0
+    assert cache.check_error() == 0
+    # the decode kernel's own duration (the roofline's denominator): a second pass of at least 10
+    # steps with events around every decode launch, still under the clock sampler
+    rsteps = max(10, min(args.steps, 200))
+    cache.profile_start(kinds=("decode",))
+    _time_loop(step, rsteps, stream)
+    torch.cuda.synchronize()
+    prof = cache.profile_read()
     clocks = sampler.stop()
     assert cache.check_error() == 0
 

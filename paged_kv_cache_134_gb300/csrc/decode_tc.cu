@@ -36,11 +36,11 @@ cudaError_t pkv_decode_tc_launch(const pkv_cache *c, const pkv_decode::Args &a, 
     const int mt = c->model_dtype;
     const bool f8 = c->kv_dtype == PKV_FP8_E4M3;
     if (!pkv_tmap_2d(&tq, q, mt, (int64_t)a.num_seqs * a.hq, D, G)) return cudaErrorInvalidValue;
-    // the pool as [rows][D] of the cache dtype: one box per (block, K|V, head) tile of bs rows, as
-    // [row group][half][8 rows][128 bytes] (16-bit), or bs rows x 128 one-byte codes (E4M3, read
-    // this way for K; V goes by 1-D bulk copies and is widened)
+    // the pool: 16-bit caches, one box per (block, K|V, head) tile of bs rows, as
+    // [row group][half][8 rows][128 bytes]; E4M3 caches, one box per (block, head) holding its K and
+    // its V tile, as [row group][K, V][8 rows][128 codes] (half the copies of one box per tile)
     const int64_t pool_rows = (int64_t)c->num_blocks * 2 * c->num_kv_heads * c->block_size;
-    if (!(f8 ? pkv_tmap_2d(&tkv, c->pool, (int)PKV_FP8_E4M3, pool_rows, D, c->block_size)
+    if (!(f8 ? pkv_tmap_kv_pairs_e4m3(&tkv, c->pool, c->num_blocks, c->num_kv_heads, c->block_size)
              : pkv_tmap_rows128_grouped(&tkv, c->pool, mt, pool_rows, c->block_size)))
         return cudaErrorInvalidValue;
     const size_t smem = smem_bytes(operand_dtype(c), f8, a.num_seqs);

@@ -9,17 +9,22 @@
 // fills the MMA's M = 128 rows:
 //   S^T [128 tokens x 16] = K [128 tokens x D] . Q^T [D x 16]      (heads padded from G to 16)
 //   O^T [D x 16]         += V^T [D x 128 tokens] . P^T [128 tokens x 16]
-// K and V come straight from the paged pool by tiled TMA (one box of bs rows x 64 dims per block
-// and half of D, 128-byte swizzle), landing in the K-major layout the first MMA reads as A and the
-// MN-major layout the second MMA reads as A.  Q sits in shared memory K-major, P is written there
-// by the softmax threads.  Accumulators live in tensor memory.
+// K and V come straight from the paged pool by tiled TMA (16-bit caches: one box of bs rows x 64
+// dims per block and half of D, 128-byte swizzle), landing in the K-major layout the first MMA
+// reads as A and the MN-major layout the second MMA reads as A.  E4M3 caches: one box per block
+// brings its K and its V codes together (the SM issues copies one after another, so a step's copy
+// count, not its bytes, set the pace); K is read by the MMA as it lands and V is widened to fp16 by
+// converter warps.  Q sits in shared memory K-major, P is written there by the softmax threads.
+// Accumulators live in tensor memory.
 //
 // Work unit = (sequence, KV head, split of up to split_blocks blocks), the same unit list as the
 // CUDA-core kernel (full splits first), round-robin over one persistent CTA per SM.  A unit is
 // processed in steps of 128 tokens.  Roles:
-//   warp 0     loads: block-table entries (one lane per block of the step, read a step ahead), Q of
-//              the unit, and the K boxes of every block into a ring of 3 K stages;
-//   warp 6     the same walk for the V boxes (ring of 3 V stages);
+//   warp 0     loads: block-table entries (read a unit ahead into registers, one lane per block of
+//              the step), Q of the unit, and the K boxes of every block into a ring of 3 K stages
+//              (E4M3: the K + V boxes into a ring of 4 code stages);
+//   warp 6     the same walk for the V boxes (ring of 3 V stages; no role for E4M3 caches);
+//   warps 11-14 (E4M3) q to three E4M3 terms, V codes widened into a ring of 2 fp16 V stages;
 //   warp 1     tensor-memory owner and MMA issuer (one thread);
 //   warps 2-5  one thread per token row of S^T (a TMEM lane): mask, scale, tile max over the 128
 //              rows (shuffles + shared memory), online softmax with a lazily moved base (the base
@@ -67,19 +72,21 @@ struct UnitRec {
 
 template <int MT, bool F8 = false>
 struct Layout {
-    // K stages and V stages: an E4M3 K stage (128 rows of 128 codes) takes half the room of a 16-bit
-    // one, which pays for a fourth stage of each ring
+    // K stages and V stages.  16-bit caches: three of each, K and V loaded by their own copies.  E4M3
+    // caches: four code stages, each holding the K and the V codes of a step as they land (one copy per
+    // block brings both), and two stages of V widened to fp16 for the P V MMA
     static constexpr int NS = F8 ? 4 : 3;
+    static constexpr int NSV = F8 ? 2 : 3;
     static constexpr int NP = MT == PKV_BF16 ? 2 : 1;      // P parts (hi, lo for bf16)
     // rows of the P^T operand: the group's heads (padded to NQ), and for bf16 the lo parts as rows
     // NQ.. 2 NQ - 1, so that one N = 2 NQ MMA per K step covers both parts (the two O^T column
     // groups are added in the epilogue)
     static constexpr int NPR = NQ * NP;
     static constexpr int STAGE = TOK * D * 2;              // V (and 16-bit K): [half][128 rows][128 B] = 32 KB
-    static constexpr int KSTAGE = F8 ? TOK * D : STAGE;    // E4M3 K: [128 rows][128 B] = 16 KB
+    static constexpr int KSTAGE = STAGE;                   // E4M3: [row group][K, V][8 rows][128 B] = 32 KB
     static constexpr int K0 = 0;
     static constexpr int V0 = K0 + NS * KSTAGE;
-    static constexpr int Q = V0 + NS * STAGE;              // [2 buffers][half][16 rows][128 B]
+    static constexpr int Q = V0 + NSV * STAGE;             // [2 buffers][half][16 rows][128 B]
     static constexpr int Q_BYTES = NQ * D * 2;
     static constexpr int P = Q + 2 * Q_BYTES;                  // [buffer][part][64-token chunk][16 rows][128 B]
     static constexpr int P_BYTES = NPR * TOK * 2;          // one buffer
@@ -194,10 +201,10 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
     // FP8 caches: the exponent of unit nu's q scale in slot nu % 8, published with "Q converted"
     // (q_ready, a ring of 8: unit nu + 8's Q cannot be loaded before the softmax has read the scores
     // of unit nu + 4, so the MMA and the softmax, which wait for unit nu, never see a later phase),
-    // the converters' partial maxima, and "E4M3 V tile landed" (v8_full, before the widening)
+    // and the converters' partial maxima
     volatile int *qexp = reinterpret_cast<volatile int *>(fin + 5);              // [8]
     volatile float *qred = reinterpret_cast<volatile float *>(fin + 9);          // [2 unit parities][4 warps]
-    uint64_t *v8_full = fin + 13 + NS, *q_ready = fin + 13 + 2 * NS; // q_ready [8]
+    uint64_t *q_ready = fin + 13 + 2 * NS; // [8]
     float *red_max = reinterpret_cast<float *>(smem + LY::RED);                  // [2][4][NQ]
     float *red_sum = red_max + 2 * 4 * NQ;                                      // [2][4][NQ]
     float *m_base = red_sum + 2 * 4 * NQ;                                       // [2][NQ]
@@ -208,11 +215,16 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(k_full + i, 1);             // the TMA arrival (E4M3 K is read by the MMA as is)
-            mbar_init(k_empty + i, 1);
-            mbar_init(v_full + i, F8 ? 128 : 1);
+            mbar_init(k_full + i, 1); // the TMA arrival (E4M3 K is read by the MMA as is)
+            // free once the four softmax warps have read the S^T its K gave (so the MMA has read K) and,
+            // E4M3, the four converter warps its V codes: arrivals instead of a commit per step (the
+            // MMA warp issues every MMA and commit of a step in a row, and a commit costs about as
+            // much as two MMAs)
+            mbar_init(k_empty + i, F8 ? 8 : 4);
+        }
+        for (int i = 0; i < LY::NSV; ++i) {
+            mbar_init(v_full + i, F8 ? 128 : 1);  // the converters' rows (E4M3) or the TMA arrival
             mbar_init(v_empty + i, 1);
-            if constexpr (F8) mbar_init(v8_full + i, 1);
         }
         if constexpr (F8)
             for (int b = 0; b < 8; ++b) mbar_init(q_ready + b, 128);
@@ -296,17 +308,40 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
     if (warp == 0 || warp == 6) {
         // ---------------------------------------------------------------- loads
         // Warp 0 loads Q of each unit and the K boxes, warp 6 the V boxes (one warp issuing both
-        // spent most of each step issuing boxes one after another).  Both walk this CTA's steps in
+        // spent most of each step issuing boxes one after another).  E4M3 caches: a block's box brings
+        // its K and its V codes (one copy, not two), and the two warps take alternate steps, warp 0
+        // the even ones: a step's walk (table entries, waits, copy issue) takes about as long as the
+        // step's bytes take to arrive, so one warp alone would set the pace.  Both walk this CTA's steps in
         // the same order, one lane per block of a step, and read the block-table entries of the
         // next step before issuing the current one, so the table read latency stays off the path.
         const bool is_k = warp == 0;
         const uint64_t policy = l2_policy_evict_first();
         if (lane == 0) tc::prefetch_tmap(&tkv);
         if (lane == 0 && is_k) tc::prefetch_tmap(&tq);
-        // table entry of this lane's block in step i of unit `un` (0 for lanes past the step's blocks)
-        auto entry = [&](const Unit &un, int i) -> int {
-            const int nblk = min(bpstep, un.ntiles - i * bpstep);
-            return lane < nblk ? a.tables[(int64_t)un.s * a.max_blocks + un.blk0 + i * bpstep + lane] : 0;
+        // A unit's block-table entries are read once, a unit ahead, into registers: lane l holds the
+        // entries of the unit's blocks l, l + 32, l + 64, l + 96 (a step picks its own with shuffles).
+        // A per-step read would leave the loader waiting for it at every step.  Units of more blocks
+        // (longer splits set through the tuning variables) read the rest directly.
+        constexpr int kER = 4;
+        int ecur[kER], enx[kER];
+        auto load_entries = [&](const Unit &x, int (&e)[kER]) {
+#pragma unroll
+            for (int k = 0; k < kER; ++k) {
+                const int idx = k * 32 + lane;
+                e[k] = idx < x.ntiles ? a.tables[(int64_t)x.s * a.max_blocks + x.blk0 + idx] : 0;
+            }
+        };
+        // table entry of this lane's block in step i of unit `x` (0 for lanes past the step's blocks)
+        auto entry = [&](const Unit &x, const int (&e)[kER], int i) -> int {
+            const int idx = i * bpstep + lane;
+            int v = 0;
+#pragma unroll
+            for (int k = 0; k < kER; ++k) {
+                const int t = __shfl_sync(0xffffffffu, e[k], idx & 31);
+                if ((idx >> 5) == k) v = t;
+            }
+            if (idx >= kER * 32 && idx < x.ntiles) v = a.tables[(int64_t)x.s * a.max_blocks + x.blk0 + idx];
+            return lane < min(bpstep, x.ntiles - i * bpstep) ? v : 0;
         };
         int64_t gs = 0; // steps issued so far, all units
         int nu = 0, q_next = 0; // q_next: this CTA's next unit (in its order) whose Q is still to load
@@ -338,14 +373,15 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 un = unit_at(u);
                 if (lane == 0) write_rec(0, un, a.lens[un.s], F8 ? a.k_scale[un.kvh] : 1.f);
                 look_ahead(u + (int)gridDim.x);
+                if (u + (int)gridDim.x < U) load_entries(nx, enx);
             } else {
                 int te;
                 float ks;
                 ok = read_rec(0, un, te, ks);
             }
             nsteps = (un.ntiles + bpstep - 1) / bpstep;
+            if (ok) load_entries(un, ecur);
         }
-        int cur = u < U && ok ? entry(un, 0) : 0;
         while (u < U && ok) {
             if (is_k) {
                 // this unit's Q is loaded by its first step at the latest (waiting for its buffer); the
@@ -381,59 +417,62 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                             ok = false;
                             break;
                         }
+                        load_entries(un2, enx); // used from the next step on
                     }
                     nsteps2 = (un2.ntiles + bpstep - 1) / bpstep;
                 }
             }
-            const int nxt = u2 < U ? entry(un2, i2) : 0;
-            // this step
+            // this step (E4M3: only every other one is this warp's)
+            const bool my_step = !F8 || (int)(gs & 1) == (is_k ? 0 : 1);
             const int st = (int)(gs % NS);
             const int64_t round = gs / NS;
             const int nblk = min(bpstep, un.ntiles - i * bpstep);
-            const int b = cur;
-            const bool good = lane < nblk && b >= 0 && b < a.num_blocks;
-            const unsigned goodmask = __ballot_sync(0xffffffffu, good);
-            const unsigned bad = __ballot_sync(0xffffffffu, lane < nblk && !good);
-            const uint32_t bytes = (uint32_t)__popc(goodmask) * (uint32_t)a.bs * (uint32_t)(F8 ? D : D * 2);
-            // FP8: the E4M3 K tile lands as it is (the MMA reads E4M3); the E4M3 V tile lands in the
-            // upper half of the stage (v8_full) and the converters widen it in place, then arrive on v_full
-            uint64_t *full = is_k ? k_full + st : (F8 ? v8_full + st : v_full + st);
-            uint64_t *empty = is_k ? k_empty + st : v_empty + st;
-            if (lane == 0) {
-                if (round >= 1 && !mbar_wait_sleep(empty, (round - 1) & 1)) ok = false;
-                if (ok) {
-                    if (!is_k && bad) set_error(a.err, PKV_DEVERR_BLOCK_ID);
-                    mbar_arrive_expect_tx(full, bytes);
+            if (my_step) {
+                const int b = entry(un, ecur, i);
+                const bool good = lane < nblk && b >= 0 && b < a.num_blocks;
+                const unsigned goodmask = __ballot_sync(0xffffffffu, good);
+                const unsigned bad = __ballot_sync(0xffffffffu, lane < nblk && !good);
+                // bs rows of 2 D bytes a block: a 16-bit K or V tile, or an E4M3 K tile and its V tile
+                const uint32_t bytes = (uint32_t)__popc(goodmask) * (uint32_t)a.bs * (uint32_t)(2 * D);
+                // E4M3: the K codes are read by the MMA as they land; the converters widen the V codes into
+                // a V stage of their own
+                const bool kring = is_k || F8; // the ring this warp fills: K (E4M3: the code stages) or V
+                uint64_t *full = kring ? k_full + st : v_full + st;
+                uint64_t *empty = kring ? k_empty + st : v_empty + st;
+                if (lane == 0) {
+                    if (round >= 1 && !mbar_wait_sleep(empty, (round - 1) & 1)) ok = false;
+                    if (ok) {
+                        // bad block ids: reported by the V loader (16-bit) or by the step's loader (E4M3)
+                        if ((F8 || !is_k) && bad) set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                        mbar_arrive_expect_tx(full, bytes);
+                    }
                 }
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok || *abort_flag) break;
-            // row of (block b, K or V, KV head) in the pool's [rows][D] view
-            const int row = ((b * 2 + (is_k ? 0 : 1)) * a.hkv + un.kvh) * a.bs;
-            // 16-bit stage layout: [row group of 8][half][8 rows][128 bytes], a block's bs rows at
-            // lane * bs * 256; E4M3 K: [row][128 bytes]
-            uint8_t *dst0 = smem + (is_k ? LY::K0 + st * LY::KSTAGE : LY::V0 + st * LY::STAGE) + lane * a.bs * (F8 ? 128 : 256);
-            if (good) {
-                if (F8 && is_k) {
-                    // the block's bs rows of 128 E4M3 codes, 128-byte swizzled: the MMA's K-major layout
-                    tc::tma_load_2d_hint(dst0, &tkv, 0, row, full, policy);
-                } else if constexpr (F8) {
-                    // one (block, V, head) tile of bs rows x 128 one-byte dims is contiguous in the pool
-                    const char *src = a.pool + (int64_t)row / a.bs * a.tile_bytes;
-                    bulk_g2s_hint(smem + LY::V0 + st * LY::STAGE + TOK * 128 + lane * a.bs * 128, src,
-                                  (uint32_t)a.tile_bytes, full, policy);
-                } else {
-                    tc::tma_load_4d_hint(dst0, &tkv, 0, 0, 0, row / 8, full, policy);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok || *abort_flag) break;
+                // 16-bit stage layout: [row group of 8][half][8 rows][128 bytes]; E4M3 code stage:
+                // [row group of 8][K, V][8 rows][128 bytes]; a block's bs rows at lane * bs * 256
+                uint8_t *dst0 = smem + (kring ? LY::K0 + st * LY::KSTAGE : LY::V0 + st * LY::STAGE) + lane * a.bs * 256;
+                if (good) {
+                    if constexpr (F8) {
+                        // the K and V codes of (block b, KV head), 128-byte swizzled: K in the MMA's K-major layout
+                        tc::tma_load_5d_hint(dst0, &tkv, 0, 0, 0, un.kvh * (a.bs >> 3), b, full, policy);
+                    } else {
+                        // row group of (block b, K or V, KV head) in the pool's [rows][D] view
+                        const int row = ((b * 2 + (is_k ? 0 : 1)) * a.hkv + un.kvh) * a.bs;
+                        tc::tma_load_4d_hint(dst0, &tkv, 0, 0, 0, row / 8, full, policy);
+                    }
                 }
             }
             ++gs;
-            cur = nxt;
             if (i2 == 0) {
                 ++nu;
+#pragma unroll
+                for (int k = 0; k < kER; ++k) ecur[k] = enx[k]; // read a unit ago (K) or a step ago (V)
                 if (is_k && u2 < U) {
                     // entering unit nu (its Q may still be loading): publish it, look up the next one
                     if (lane == 0) write_rec(nu, un2, nx_len, nx_ks);
                     look_ahead(u2 + (int)gridDim.x);
+                    if (u2 + (int)gridDim.x < U) load_entries(nx, enx);
                 }
             }
             u = u2;
@@ -447,7 +486,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         // the copies of the last stages must land before this CTA's shared memory goes away
         if (lane == 0) {
             for (int64_t g = gs > NS ? gs - NS : 0; g < gs; ++g)
-                if (!mbar_wait_sleep((is_k ? k_full : (F8 ? v8_full : v_full)) + g % NS, (g / NS) & 1))
+                if (!mbar_wait_sleep((is_k || F8 ? k_full : v_full) + g % NS, (g / NS) & 1))
                     set_error(a.err, PKV_DEVERR_TIMEOUT);
             const int last_q = q_next - 1;
             if (is_k)
@@ -466,9 +505,9 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             // one descriptor per operand layout; the address field counts 16-byte units, so a tile at
             // byte offset `off` from the base is the base descriptor plus off / 16 (shared memory stays
             // below the field's 256 KB): each MMA adds a constant instead of rebuilding its descriptors
-            // K: groups of 8 token rows 1024 bytes apart (E4M3) or 2048 (16-bit: the second 64-dim
-            // half of a group sits 1024 bytes after the first)
-            const uint64_t dK = tc::smem_desc(smem_u32(smem + LY::K0), 16, F8 ? 1024 : 2048);
+            // K: groups of 8 token rows 2048 bytes apart (16-bit: the second 64-dim half of a group sits
+            // 1024 bytes after the first; E4M3: the group's V codes do)
+            const uint64_t dK = tc::smem_desc(smem_u32(smem + LY::K0), 16, 2048);
             const uint64_t dQ = tc::smem_desc(smem_u32(smem + LY::Q), 16, 1024);
             // V^T (MN-major): the two 64-dim halves LBO apart, groups of 8 tokens SBO apart
             const uint64_t dV = F8 ? tc::smem_desc(smem_u32(smem + LY::V0), TOK * 128, 1024)
@@ -499,7 +538,6 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                     }
                 }
                 tc::commit_warp(s_full + b);
-                tc::commit_warp(k_empty + st);
                 return true;
             };
             // Q of unit n in place: loaded (q_full), or for FP8 caches converted (q_ready, ring of 8)
@@ -538,22 +576,25 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                         ok = issue_s(g + 1, qn);
                         if (!ok) break;
                     }
-                    const int st = (int)(g % NS), b = (int)(g & 1);
-                    ok = __all_sync(0xffffffffu, mbar_wait_sleep(p_full + b, (g >> 1) & 1) && mbar_wait_sleep(v_full + st, (g / NS) & 1));
+                    const int sv = (int)(g % LY::NSV), b = (int)(g & 1);
+                    ok = __all_sync(0xffffffffu, mbar_wait_sleep(p_full + b, (g >> 1) & 1) &&
+                                                     mbar_wait_sleep(v_full + sv, (g / LY::NSV) & 1));
                     // O^T of this unit's parity was read out by the epilogue warps for unit nu - 2
                     if (ok && i == 0 && nu >= 2)
                         ok = __all_sync(0xffffffffu, mbar_wait_sleep(o_free + (nu & 1), ((nu >> 1) - 1) & 1));
                     if (!ok) break;
                     const uint32_t tO = tmem + OB + (uint32_t)((nu & 1) * 32);
                     tc::fence_after_sync();
-                    const uint64_t a0 = dV + (uint64_t)((st * LY::STAGE) >> 4), b0 = dP + (uint64_t)((b * LY::P_BYTES) >> 4);
+                    const uint64_t a0 = dV + (uint64_t)((sv * LY::STAGE) >> 4), b0 = dP + (uint64_t)((b * LY::P_BYTES) >> 4);
 #pragma unroll
                     for (int k = 0; k < TOK / 16; ++k)
                         tc::mma_f16_warp(tO, a0 + (uint64_t)((k * kVStep) >> 4),
                                          b0 + (uint64_t)(((k >> 2) * (LY::NPR * 128) + (k & 3) * 32) >> 4), IPV,
                                          (i > 0 || k > 0) ? 1u : 0u);
                     tc::commit_warp(t_full + b);
-                    tc::commit_warp(v_empty + st);
+                    // 16-bit: the V stage's release for the V loader (E4M3: the converters wait for
+                    // t_full, the same event with two V stages)
+                    if constexpr (!F8) tc::commit_warp(v_empty + sv);
                     if (i + 1 == nsteps) tc::commit_warp(o_full + (nu & 1));
                 }
                 gs += nsteps;
@@ -608,7 +649,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             // `ok` agreement: the four warps stop together, at a barrier (see named_barrier_and)
             for (int i = 0; i < nsteps; ++i) {
                 const int64_t g0 = gs + i;
-                const int st = (int)(g0 % NS), b = (int)(g0 & 1);
+                const int b = (int)(g0 & 1);
                 // the next step's table entry (the next unit's first one after the last step)
                 bool rec_ok = true;
                 if (i + 1 == nsteps && u2 < U) rec_ok = read_rec(nu + 1, un2, tok_end2, ksc2);
@@ -646,6 +687,8 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                     tc::wait_ld();
                     tc::fence_before_sync();
                     mbar_arrive(s_free + b);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(k_empty + (int)(g0 % NS)); // S^T is done: the MMA has read the step's K
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         sc[g] = valid ? __uint_as_float(sr[g]) * qsc : -INFINITY;
@@ -733,7 +776,8 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                     // a row without a token holds an unused slot, a skipped block's stale row or (FP8)
                     // widened garbage: zero its V once the stage has landed, so that no NaN reaches the
                     // MMA (only these steps wait for V here; P V waits for it in the MMA warp)
-                    if (!__all_sync(0xffffffffu, mbar_wait_sleep(v_full + st, (g0 / NS) & 1))) {
+                    const int sv = (int)(g0 % LY::NSV);
+                    if (!__all_sync(0xffffffffu, mbar_wait_sleep(v_full + sv, (g0 / LY::NSV) & 1))) {
                         ok = false;
                         continue; // carried to the next barrier
                     }
@@ -741,7 +785,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
 #pragma unroll
                         for (int c = 0; c < D / 64; ++c) {
                             uint4 *vr = reinterpret_cast<uint4 *>(
-                                smem + LY::V0 + st * LY::STAGE +
+                                smem + LY::V0 + sv * LY::STAGE +
                                 (F8 ? c * (TOK * 128) + r * 128 : (r >> 3) * 2048 + c * 1024 + (r & 7) * 128));
 #pragma unroll
                             for (int e = 0; e < 8; ++e) vr[e] = make_uint4(0u, 0u, 0u, 0u);
@@ -843,20 +887,19 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         if (!ok && lane == 0) fail();
     } else if constexpr (F8) {
         // ---------------------------------------------------------------- E4M3 V -> fp16, q -> E4M3 (warps 11-14)
-        // Thread r owns row r of every V stage (token r of the step) and dimension r of q.  A V
-        // stage's E4M3 tile (128 rows of 128 bytes) sits in the stage's upper half; row r is read into
-        // registers whole before its two fp16 halves are written (the second one over the E4M3 row
-        // itself), so the widening runs in place.  E4M3 values are exact in fp16.  K stays E4M3: the
-        // S^T MMA reads it as it landed.
+        // Thread r owns token r of every step and dimension r of q.  Token r's V codes sit in the code
+        // stage as row r & 7 of the V half of row group r >> 3, 128-byte swizzled as they landed; they
+        // are widened into row r of a V stage (fp16, the P V MMA's MN-major layout).  E4M3 values are
+        // exact in fp16.  K stays E4M3: the S^T MMA reads it as it landed.
         const int cw = warp - 11, r = cw * 32 + lane;
-        auto widen_row = [&](uint8_t *stage) {
-            const uint8_t *src = stage + TOK * 128 + r * 128;
+        auto widen_row = [&](const uint8_t *codes, uint8_t *stage) {
+            const uint8_t *src = codes + (r >> 3) * 2048 + 1024 + (r & 7) * 128;
             uint4 w[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) w[c] = *reinterpret_cast<const uint4 *>(src + (((c + lane) & 7) << 4));
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const int ch = (c + lane) & 7; // 16 dims: 16 ch .. 16 ch + 15
+                const int ch = ((c + lane) & 7) ^ (r & 7); // 16 dims: 16 ch .. 16 ch + 15 (the swizzled chunk read)
                 const uint32_t in[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
                 uint32_t o[8];
 #pragma unroll
@@ -955,16 +998,21 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             // ---- the unit's V stages
             for (int i = 0; i < nsteps && ok; ++i) {
                 const int64_t g = gs + i;
-                const int st = (int)(g % NS);
+                const int st = (int)(g % NS), sv = (int)(g % LY::NSV);
                 if (i + 1 == nsteps && u + (int)gridDim.x < U) {
                     ok = convert_q(nu + 1, *abort_flag == 0);
                     if (!ok) break;
                 }
-                ok = __all_sync(0xffffffffu, mbar_wait_sleep(v8_full + st, (g / NS) & 1));
+                // the step's codes have landed, and P V of the step that used this V stage before is done
+                ok = __all_sync(0xffffffffu, mbar_wait_sleep(k_full + st, (g / NS) & 1));
+                static_assert(!F8 || LY::NSV == 2, "V stage g % 2 frees with P V of step g - 2 (t_full)");
+                if (ok && g >= 2) ok = __all_sync(0xffffffffu, mbar_wait_sleep(t_full + (g & 1), ((g >> 1) - 1) & 1));
                 if (!ok) break;
-                widen_row(smem + LY::V0 + st * LY::STAGE);
+                widen_row(smem + LY::K0 + st * LY::KSTAGE, smem + LY::V0 + sv * LY::STAGE);
                 fence_proxy_async_smem();
-                mbar_arrive(v_full + st);
+                mbar_arrive(v_full + sv);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(k_empty + st); // this warp's V codes are read
             }
             gs += nsteps;
             // the four warps leave together (the next unit's barrier would wait for a warp gone)

@@ -174,3 +174,7 @@ bool pkv_tmap_2d(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t
 // multiple of 8) lands as [row group of 8][64-element half][8 rows][128 bytes], 128-byte swizzled:
 // one copy per block tile where two 2-D boxes (one per half) were needed
 bool pkv_tmap_rows128_grouped(CUtensorMap *m, const void *base, int mt, int64_t rows, int box_rows);
+// E4M3 pool: one box = the K and the V tile of one (block, KV head), bs rows of 128 codes each,
+// landing as [slot / 8][K, V][8 rows][128 bytes], 128-byte swizzled; coordinates
+// (0, 0, 0, head * bs / 8, block) (prefill.cu)
+bool pkv_tmap_kv_pairs_e4m3(CUtensorMap *m, const void *pool, int64_t num_blocks, int hkv, int bs);

@@ -207,6 +207,25 @@ bool pkv_tmap_2d(CUtensorMap *m, const void *base, int mt, int64_t rows, int64_t
     return pkv_prefill::make_map(m, base, mt, rows, cols, box_rows);
 }
 
+bool pkv_tmap_kv_pairs_e4m3(CUtensorMap *m, const void *pool, int64_t num_blocks, int hkv, int bs) {
+    using namespace pkv_prefill;
+    EncodeFn enc = encode_fn();
+    if (!enc || bs % 8 || bs / 8 > 256 || num_blocks < 1 || (int64_t)hkv * bs / 8 > 0x7FFFFFFFLL) return false;
+    // the pool's E4M3 rows [(block, K|V, head, slot)][128 codes] seen as (code, slot % 8, K|V,
+    // head * bs / 8 + slot / 8, block): a box of (128, 8, 2, bs / 8, 1) at (0, 0, 0, head * bs / 8,
+    // block) is the K tile and the V tile of one (block, head) in one copy, landing as
+    // [slot / 8][K, V][8 rows][128 bytes] (each 8-row group of K followed by the same rows of V)
+    const cuuint64_t row = 128, kv = (cuuint64_t)hkv * bs * row;
+    const cuuint64_t dims[5] = {128, 8, 2, (cuuint64_t)hkv * bs / 8, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[4] = {row, kv, 8 * row, 2 * kv};
+    const cuuint32_t box[5] = {128u, 8u, 2u, (cuuint32_t)(bs / 8), 1u};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(pool), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool pkv_tmap_rows128_grouped(CUtensorMap *m, const void *base, int mt, int64_t rows, int box_rows) {
     using namespace pkv_prefill;
     EncodeFn enc = encode_fn();

@@ -216,6 +216,16 @@ PKV_DEV void tma_load_2d_hint(void *dst, const CUtensorMap *map, int x, int y, u
                  : "memory");
 }
 
+// 5-D tiled load with an L2 cache-policy hint (coordinates innermost first)
+PKV_DEV void tma_load_5d_hint(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3, int c4, uint64_t *bar,
+                              uint64_t policy) {
+    asm volatile("cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar)),
+                 "l"(policy)
+                 : "memory");
+}
+
 // 4-D tiled load with an L2 cache-policy hint (coordinates innermost first)
 PKV_DEV void tma_load_4d_hint(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3, uint64_t *bar,
                               uint64_t policy) {
