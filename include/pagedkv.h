@@ -252,7 +252,9 @@ int paged_block_copy(pkv_cache_t cache, const int32_t *src_blocks, const int32_t
  * B = the block size in bytes (kv_cache_view's num_bytes / num_blocks).  dst must be device
  * accessible: device memory, or page-locked host memory (cudaHostAlloc / cudaHostRegister; with
  * unified addressing its host pointer is also its device pointer), at least num_ids*B bytes,
- * 16-byte aligned.  block_ids: device int32 [num_ids].  Bad ids are skipped as above. */
+ * 16-byte aligned.  block_ids: device int32 [num_ids].  Bad ids are skipped as above (their
+ * bytes of dst are left as they were).  The copy kernel reads the pool and writes dst directly
+ * (host memory over the host link, at the link's rate). */
 int paged_block_swap_out(pkv_cache_t cache, const int32_t *block_ids, int64_t num_ids, void *dst, void *stream);
 
 /* Swap in, the inverse: physical block block_ids[i] := bytes [i*B, (i+1)*B) of src (same rules for

@@ -207,6 +207,7 @@ int kv_cache_destroy(pkv_cache_t c) {
 }
 
 int kv_cache_set_scales(pkv_cache_t c, const float *k_scale, const float *v_scale, void *stream) {
+    PKV_RANGE("kv_cache_set_scales");
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     if (c->kv_dtype != PKV_FP8_E4M3) return pkv_fail(PKV_EINVAL, "scales apply to FP8 caches only");
     if (!k_scale || !v_scale) return pkv_fail(PKV_EINVAL, "scale pointer is NULL");
@@ -263,6 +264,7 @@ int kv_cache_check_error(pkv_cache_t c, int *device_code) {
 int paged_slot_mapping(const int32_t *block_tables, int num_rows, int max_blocks_per_seq, const int32_t *seq_ids,
                        const int32_t *positions, int64_t num_tokens, int block_size, int64_t *slot_mapping,
                        void *stream) {
+    PKV_RANGE("paged_slot_mapping");
     if (num_tokens < 0 || num_rows < 0 || max_blocks_per_seq < 0) return pkv_fail(PKV_EINVAL, "negative size");
     if (block_size <= 0) return pkv_fail(PKV_EINVAL, "block_size must be > 0");
     if (num_tokens == 0) return PKV_OK;
@@ -276,6 +278,7 @@ int paged_slot_mapping(const int32_t *block_tables, int num_rows, int max_blocks
 
 int paged_kv_append(pkv_cache_t c, const void *k, const void *v, const int64_t *slot_mapping, int64_t num_tokens,
                     void *stream) {
+    PKV_RANGE("paged_kv_append");
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     if (num_tokens < 0) return pkv_fail(PKV_EINVAL, "num_tokens < 0");
     if (num_tokens == 0) return PKV_OK;
@@ -290,6 +293,7 @@ int paged_kv_append(pkv_cache_t c, const void *k, const void *v, const int64_t *
 int paged_kv_append_at(pkv_cache_t c, const void *k, const void *v, const int32_t *block_tables, int num_rows,
                        int max_blocks_per_seq, const int32_t *seq_ids, const int32_t *positions, int64_t num_tokens,
                        int64_t *slot_mapping, void *stream) {
+    PKV_RANGE("paged_kv_append_at");
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     if (num_tokens < 0 || num_rows < 0 || max_blocks_per_seq < 0) return pkv_fail(PKV_EINVAL, "negative size");
     if (num_tokens == 0) return PKV_OK;
@@ -306,6 +310,7 @@ int paged_kv_append_at(pkv_cache_t c, const void *k, const void *v, const int32_
 int paged_decode_attention(const void *q, pkv_cache_t c, const int32_t *block_tables, int max_blocks_per_seq,
                            const int32_t *context_lens, int num_seqs, int num_q_heads, float scale, void *out,
                            void *stream) {
+    PKV_RANGE("paged_decode_attention");
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     if (num_seqs < 0 || max_blocks_per_seq < 0) return pkv_fail(PKV_EINVAL, "negative size");
     if (num_seqs == 0) return PKV_OK;
@@ -384,6 +389,7 @@ static int prefill_entry(const void *q, const void *k, const void *v, const int3
 int paged_decode_attention_cascade(const void *q, pkv_cache_t c, const int32_t *block_tables, int max_blocks_per_seq,
                                    const int32_t *context_lens, int num_seqs, int num_q_heads, int shared_prefix_len,
                                    float scale, void *out, void *stream) {
+    PKV_RANGE("paged_decode_attention_cascade");
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     if (shared_prefix_len < 0 || shared_prefix_len % c->block_size)
         return pkv_fail(PKV_EINVAL, "shared_prefix_len %d is not a non-negative multiple of block_size %d",
@@ -453,6 +459,7 @@ int packed_prefill_attention(const void *q, const void *k, const void *v, const 
                              int max_seqlen, int64_t total_tokens, const int32_t *block_tables,
                              int max_blocks_per_seq, pkv_cache_t c, int num_q_heads, float scale, void *out,
                              void *stream) {
+    PKV_RANGE("packed_prefill_attention");
     return prefill_entry(q, k, v, cu_seqlens, nullptr, num_seqs, max_seqlen, total_tokens, block_tables,
                          max_blocks_per_seq, c, num_q_heads, scale, out, stream);
 }
@@ -461,6 +468,7 @@ int paged_prefill_attention(const void *q, const void *k, const void *v, const i
                             const int32_t *context_lens, int num_seqs, int max_seqlen, int64_t total_tokens,
                             const int32_t *block_tables, int max_blocks_per_seq, pkv_cache_t c, int num_q_heads,
                             float scale, void *out, void *stream) {
+    PKV_RANGE("paged_prefill_attention");
     if (!context_lens && num_seqs > 0) return pkv_fail(PKV_EINVAL, "NULL pointer");
     return prefill_entry(q, k, v, cu_seqlens, context_lens, num_seqs, max_seqlen, total_tokens, block_tables,
                          max_blocks_per_seq, c, num_q_heads, scale, out, stream);
@@ -468,6 +476,7 @@ int paged_prefill_attention(const void *q, const void *k, const void *v, const i
 
 int paged_block_copy(pkv_cache_t c, const int32_t *src_blocks, const int32_t *dst_blocks, int64_t num_pairs,
                      void *stream) {
+    PKV_RANGE("paged_block_copy");
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     if (num_pairs < 0) return pkv_fail(PKV_EINVAL, "num_pairs < 0");
     if (num_pairs == 0) return PKV_OK;
@@ -480,6 +489,7 @@ int paged_block_copy(pkv_cache_t c, const int32_t *src_blocks, const int32_t *ds
 }
 
 int paged_block_swap_out(pkv_cache_t c, const int32_t *block_ids, int64_t num_ids, void *dst, void *stream) {
+    PKV_RANGE("paged_block_swap_out");
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     if (num_ids < 0) return pkv_fail(PKV_EINVAL, "num_ids < 0");
     if (num_ids == 0) return PKV_OK;
@@ -493,6 +503,7 @@ int paged_block_swap_out(pkv_cache_t c, const int32_t *block_ids, int64_t num_id
 }
 
 int paged_block_swap_in(pkv_cache_t c, const int32_t *block_ids, int64_t num_ids, const void *src, void *stream) {
+    PKV_RANGE("paged_block_swap_in");
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     if (num_ids < 0) return pkv_fail(PKV_EINVAL, "num_ids < 0");
     if (num_ids == 0) return PKV_OK;

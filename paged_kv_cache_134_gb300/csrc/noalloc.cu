@@ -54,6 +54,7 @@ int pkv_noalloc_scratch_prepare(int device) {
 extern "C" int paged_decode_attention_noalloc(const void *q, pkv_cache_t c, const int32_t *block_tables,
                                               int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                                               int num_q_heads, float scale, void *out, void *stream) {
+    PKV_RANGE("paged_decode_attention_noalloc");
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     if (num_seqs < 0 || max_blocks_per_seq < 0) return pkv_fail(PKV_EINVAL, "negative size");
     if (num_seqs == 0) return PKV_OK;

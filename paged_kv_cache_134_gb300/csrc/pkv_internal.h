@@ -1,6 +1,7 @@
 // Host-side internals shared by the translation units of the library.
 #pragma once
 
+#include <nvtx3/nvToolsExt.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -117,6 +118,17 @@ struct DecodeLaunch {
     // plan kernel went before the decode)
     const CascadePrefixLaunch *prefix = nullptr;
 };
+
+// One NVTX range per C-ABI call that launches GPU work, named after the call: a profiler attached
+// to the process shows the library's calls on its timeline (NVTX v3 is header-only; with no tool
+// attached a range costs a branch).
+struct PkvRange {
+    explicit PkvRange(const char *name) { nvtxRangePushA(name); }
+    ~PkvRange() { nvtxRangePop(); }
+    PkvRange(const PkvRange &) = delete;
+    PkvRange &operator=(const PkvRange &) = delete;
+};
+#define PKV_RANGE(name) PkvRange pkv_nvtx_range_(name)
 
 // The prefix phase of a cascade decode (prefill.cu): the decode queries of every sequence against the
 // first prefix_tokens tokens of table row 0, cut into splits of split_tokens keys (a multiple of 64);

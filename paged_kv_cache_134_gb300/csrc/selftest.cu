@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(64) wait_timeout_kernel(unsigned int *err, uin
 } // namespace
 
 extern "C" int kv_cache_selftest_wait_timeout(pkv_cache_t c, uint64_t limit_ns, void *stream) {
+    PKV_RANGE("kv_cache_selftest_wait_timeout");
     if (!c) return pkv_fail(PKV_EINVAL, "cache is NULL");
     if (limit_ns == 0 || limit_ns > 1000000000ull)
         return pkv_fail(PKV_EINVAL, "limit_ns %llu not in [1, 1e9]", (unsigned long long)limit_ns);

@@ -169,6 +169,44 @@ def test_swap_out_and_in_match_oracle(where):
     cache.close()
 
 
+def test_large_swap_with_host_memory_keeps_bad_pairs():
+    """A swap of 300 blocks of 256 KB (75 MB) to page-locked host memory and back into other blocks
+    of a fresh cache is bit-exact; a bad block id leaves its host bytes as they were and sets the
+    error bit (2kiu.com section 5.2: swap-out on preemption, swap-in on resumption)."""
+    nb = 640
+    cache = P.KVCache(nb, 16, 32, 128, "f16")
+    B = cache.block_bytes
+    gen = torch.Generator().manual_seed(612)
+    raw, _ = cache.view()                             # the pool's bytes
+    raw.copy_(torch.randint(0, 256, raw.shape, generator=gen, dtype=torch.uint8))
+    torch.cuda.synchronize()
+    before = raw.reshape(nb, B).cpu().clone()
+    perm = torch.randperm(nb, generator=gen)
+    ids = perm[:300].to(torch.int32).clone()
+    ids[7] = nb + 5                                   # bad id: pair 7 skipped
+    host = torch.full((300 * B,), 0xAB, dtype=torch.uint8).pin_memory()
+    P.paged_block_swap_out(cache, ids.cuda(), host)
+    torch.cuda.synchronize()
+    assert cache.check_error() & 1, "block-id error bit not set"
+    got = host.reshape(300, B)
+    for i in range(300):
+        if i == 7:
+            assert bool((got[i] == 0xAB).all()), "a skipped pair's host bytes changed"
+        else:
+            assert torch.equal(got[i], before[int(ids[i])]), f"block {i}"
+    cache.close()
+    # swap back into other blocks of a fresh cache: every good pair lands bit-exact
+    cache = P.KVCache(nb, 16, 32, 128, "f16")
+    new_ids = perm[300:600].to(torch.int32).clone()
+    P.paged_block_swap_in(cache, new_ids.cuda(), host)
+    torch.cuda.synchronize()
+    assert cache.check_error() == 0
+    after = cache.view()[0].reshape(nb, B).cpu()
+    for i in range(300):
+        assert torch.equal(after[int(new_ids[i])], got[i]), f"block {i}"
+    cache.close()
+
+
 def test_copy_on_write_decode_is_bitwise_equal():
     w, g, free = _setup()
     cache, x = g["cache"], g["inputs"]
