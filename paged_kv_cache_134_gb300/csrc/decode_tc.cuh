@@ -703,7 +703,9 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 float alpha[G], p[G];
 #pragma unroll
                 for (int g = 0; g < G; ++g) alpha[g] = 1.f;
-                if (named_barrier_or(1, 128, need)) {
+                // (a unit's first step always sets the base: its scores are the first, so the exchange runs
+                // without asking)
+                if (i == 0 || named_barrier_or(1, 128, need)) {
                     if (mine) {
                         float tmx[G];
 #pragma unroll
@@ -981,8 +983,9 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             mbar_arrive(q_ready + (n & 7));
             return true;
         };
-        // unit 0's q first; each later unit's at the previous unit's last step, before that step's V
-        // tile (which lands last), so that the unit's first S^T does not wait for it
+        // unit 0's q first; each later unit's once the previous unit's V tile of step max(0, n - 4) is
+        // widened (its first step for units of up to four steps), so that it is ready when the softmax
+        // starts that unit
         bool ok = (int)blockIdx.x < U ? convert_q(0, *abort_flag == 0) : true;
         int64_t gs = 0;
         int nu = 0;
@@ -999,10 +1002,6 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             for (int i = 0; i < nsteps && ok; ++i) {
                 const int64_t g = gs + i;
                 const int st = (int)(g % NS), sv = (int)(g % LY::NSV);
-                if (i + 1 == nsteps && u + (int)gridDim.x < U) {
-                    ok = convert_q(nu + 1, *abort_flag == 0);
-                    if (!ok) break;
-                }
                 // the step's codes have landed, and P V of the step that used this V stage before is done
                 ok = __all_sync(0xffffffffu, mbar_wait_sleep(k_full + st, (g / NS) & 1));
                 static_assert(!F8 || LY::NSV == 2, "V stage g % 2 frees with P V of step g - 2 (t_full)");
@@ -1013,6 +1012,14 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 mbar_arrive(v_full + sv);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(k_empty + st); // this warp's V codes are read
+                // not before step nsteps - 4: convert_q waits for the next unit's Q, which warp 0 issues at
+                // the latest with the next unit's first step, and warp 0 gets there only if it is at most
+                // NS = 4 steps ahead of the code stages this warp has released (releases come first)
+                static_assert(NS == 4, "the conversion point assumes four code stages");
+                if (i == (nsteps > NS ? nsteps - NS : 0) && u + (int)gridDim.x < U) {
+                    ok = convert_q(nu + 1, *abort_flag == 0);
+                    if (!ok) break;
+                }
             }
             gs += nsteps;
             // the four warps leave together (the next unit's barrier would wait for a warp gone)
