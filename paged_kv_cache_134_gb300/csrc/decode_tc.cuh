@@ -23,7 +23,8 @@
 //   warp 0     loads: block-table entries (read a unit ahead into registers, one lane per block of
 //              the step), Q of the unit, and the K boxes of every block into a ring of 3 K stages
 //              (E4M3: the K + V boxes into a ring of 4 code stages);
-//   warp 6     the same walk for the V boxes (ring of 3 V stages; no role for E4M3 caches);
+//   warp 6     the same walk for the V boxes (ring of 3 V stages); each ring has a second loader
+//              taking the odd steps: warps 11 (K) and 12 (V), or for E4M3 caches warp 6 (codes);
 //   warps 11-14 (E4M3) q to three E4M3 terms, V codes widened into a ring of 2 fp16 V stages;
 //   warp 1     tensor-memory owner and MMA issuer (one thread);
 //   warps 2-5  one thread per token row of S^T (a TMEM lane): mask, scale, tile max over the 128
@@ -47,10 +48,11 @@ using pkv_decode::Unit;
 constexpr int D = 128;
 constexpr int TOK = 128;             // tokens per step: MMA M of S^T, MMA K of O^T
 constexpr int NQ = 16;               // MMA N: the group's query heads, padded
-// warp 0 Q and K loads, 1 MMA, 2-5 softmax, 6 V loads, 7-10 epilogue; FP8 caches: 11-14 converters
+// warp 0 Q and K loads, 1 MMA, 2-5 softmax, 6 V loads, 7-10 epilogue; 16-bit caches: 11 and 12
+// second K and V loaders (odd steps); FP8 caches: 11-14 converters
 template <bool F8>
 __host__ __device__ constexpr int threads_for() {
-    return F8 ? 480 : 352;
+    return F8 ? 480 : 416;
 }
 constexpr uint32_t kTmemCols = 128;  // two S^T buffers, then O^T of even and odd units (see NSC, OB)
 constexpr float kRescale = 8.0f;     // log2 units
@@ -305,19 +307,21 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         return okr;
     };
 
-    if (warp == 0 || warp == 6) {
+    if (warp == 0 || warp == 6 || (!F8 && (warp == 11 || warp == 12))) {
         // ---------------------------------------------------------------- loads
-        // Warp 0 loads Q of each unit and the K boxes, warp 6 the V boxes (one warp issuing both
-        // spent most of each step issuing boxes one after another).  E4M3 caches: a block's box brings
-        // its K and its V codes (one copy, not two), and the two warps take alternate steps, warp 0
-        // the even ones: a step's walk (table entries, waits, copy issue) takes about as long as the
-        // step's bytes take to arrive, so one warp alone would set the pace.  Both walk this CTA's steps in
-        // the same order, one lane per block of a step, and read the block-table entries of the
-        // next step before issuing the current one, so the table read latency stays off the path.
-        const bool is_k = warp == 0;
+        // Every ring is filled by two warps taking alternate steps, the first of each pair the even
+        // ones: a step's walk (table entries, waits, copy issue, one copy per lane after another)
+        // takes about as long as the step's bytes take to arrive, so one warp alone would set the
+        // pace.  16-bit caches: warps 0 and 11 the K boxes, 6 and 12 the V boxes; E4M3 caches: a
+        // block's box brings its K and its V codes (one copy, not two), warps 0 and 6.  Warp 0 also
+        // loads Q of each unit and publishes the unit records the other roles read.  All walk this
+        // CTA's steps in the same order, one lane per block of a step.
+        const bool boss = warp == 0;                             // Q loads, unit records, look-ahead
+        const bool kring = F8 || warp == 0 || warp == 11;        // the K ring (E4M3: code stages) or V
+        const int parity = (warp == 0 || (!F8 && warp == 6)) ? 0 : 1; // its steps: even or odd
         const uint64_t policy = l2_policy_evict_first();
         if (lane == 0) tc::prefetch_tmap(&tkv);
-        if (lane == 0 && is_k) tc::prefetch_tmap(&tq);
+        if (lane == 0 && boss) tc::prefetch_tmap(&tq);
         // A unit's block-table entries are read once, a unit ahead, into registers: lane l holds the
         // entries of the unit's blocks l, l + 32, l + 64, l + 96 (a step picks its own with shuffles).
         // A per-step read would leave the loader waiting for it at every step.  Units of more blocks
@@ -369,7 +373,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             }
         };
         if (u < U) {
-            if (is_k) {
+            if (boss) {
                 un = unit_at(u);
                 if (lane == 0) write_rec(0, un, a.lens[un.s], F8 ? a.k_scale[un.kvh] : 1.f);
                 look_ahead(u + (int)gridDim.x);
@@ -383,7 +387,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             if (ok) load_entries(un, ecur);
         }
         while (u < U && ok) {
-            if (is_k) {
+            if (boss) {
                 // this unit's Q is loaded by its first step at the latest (waiting for its buffer); the
                 // next unit's goes as soon as its buffer is free, tested at every step without waiting
                 const bool first = i == 0 && q_next == nu;
@@ -408,7 +412,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 u2 = u + gridDim.x;
                 i2 = 0;
                 if (u2 < U) {
-                    if (is_k) {
+                    if (boss) {
                         un2 = nx;
                     } else {
                         int te;
@@ -423,7 +427,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 }
             }
             // this step (E4M3: only every other one is this warp's)
-            const bool my_step = !F8 || (int)(gs & 1) == (is_k ? 0 : 1);
+            const bool my_step = (int)(gs & 1) == parity;
             const int st = (int)(gs % NS);
             const int64_t round = gs / NS;
             const int nblk = min(bpstep, un.ntiles - i * bpstep);
@@ -436,14 +440,13 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 const uint32_t bytes = (uint32_t)__popc(goodmask) * (uint32_t)a.bs * (uint32_t)(2 * D);
                 // E4M3: the K codes are read by the MMA as they land; the converters widen the V codes into
                 // a V stage of their own
-                const bool kring = is_k || F8; // the ring this warp fills: K (E4M3: the code stages) or V
                 uint64_t *full = kring ? k_full + st : v_full + st;
                 uint64_t *empty = kring ? k_empty + st : v_empty + st;
                 if (lane == 0) {
                     if (round >= 1 && !mbar_wait_sleep(empty, (round - 1) & 1)) ok = false;
                     if (ok) {
                         // bad block ids: reported by the V loader (16-bit) or by the step's loader (E4M3)
-                        if ((F8 || !is_k) && bad) set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                        if ((F8 || !kring) && bad) set_error(a.err, PKV_DEVERR_BLOCK_ID);
                         mbar_arrive_expect_tx(full, bytes);
                     }
                 }
@@ -458,7 +461,7 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                         tc::tma_load_5d_hint(dst0, &tkv, 0, 0, 0, un.kvh * (a.bs >> 3), b, full, policy);
                     } else {
                         // row group of (block b, K or V, KV head) in the pool's [rows][D] view
-                        const int row = ((b * 2 + (is_k ? 0 : 1)) * a.hkv + un.kvh) * a.bs;
+                        const int row = ((b * 2 + (kring ? 0 : 1)) * a.hkv + un.kvh) * a.bs;
                         tc::tma_load_4d_hint(dst0, &tkv, 0, 0, 0, row / 8, full, policy);
                     }
                 }
@@ -467,8 +470,8 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
             if (i2 == 0) {
                 ++nu;
 #pragma unroll
-                for (int k = 0; k < kER; ++k) ecur[k] = enx[k]; // read a unit ago (K) or a step ago (V)
-                if (is_k && u2 < U) {
+                for (int k = 0; k < kER; ++k) ecur[k] = enx[k]; // read a unit ago (warp 0) or a step ago
+                if (boss && u2 < U) {
                     // entering unit nu (its Q may still be loading): publish it, look up the next one
                     if (lane == 0) write_rec(nu, un2, nx_len, nx_ks);
                     look_ahead(u2 + (int)gridDim.x);
@@ -482,14 +485,14 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         }
         if (!ok && lane == 0) fail();
         // the next kernel (the split merge) may start launching once every CTA has issued its last load
-        if (is_k) pdl_trigger();
+        if (boss) pdl_trigger();
         // the copies of the last stages must land before this CTA's shared memory goes away
         if (lane == 0) {
             for (int64_t g = gs > NS ? gs - NS : 0; g < gs; ++g)
-                if (!mbar_wait_sleep((is_k || F8 ? k_full : v_full) + g % NS, (g / NS) & 1))
+                if (!mbar_wait_sleep((kring ? k_full : v_full) + g % NS, (g / NS) & 1))
                     set_error(a.err, PKV_DEVERR_TIMEOUT);
             const int last_q = q_next - 1;
-            if (is_k)
+            if (boss)
                 for (int n = last_q > 0 ? last_q - 1 : 0; n <= last_q; ++n)
                     if (!mbar_wait_sleep(q_full + (n & 1), (n >> 1) & 1)) set_error(a.err, PKV_DEVERR_TIMEOUT);
         }
