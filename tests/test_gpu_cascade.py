@@ -108,6 +108,7 @@ def test_back_to_back_cascade_steps_agree(kv_heads):
         for i, o in enumerate(outs[1:], 1):
             assert torch.equal(o, first), f"step {i} differs from step 0"
         r = steps.decode_step(w, strides=cache.view()[1], pool_elems=int(cache.pool_elems().numel()))
-        assert_close(first.float().cpu().double().numpy(), r["out"], ATOL, RTOL, "back-to-back cascade")
+        assert_close(first.float().cpu().double().numpy(), r["out"], ATOL, RTOL, "back-to-back cascade",
+                     out_dtype=OUT_DT(w))
     finally:
         cache.close()

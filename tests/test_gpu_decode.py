@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 if not torch.cuda.is_available():  # collected on CPU too; every test here needs the device
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-from gpu_path import assert_close, run_decode  # noqa: E402
+from gpu_path import OUT_DT, assert_close, run_decode  # noqa: E402
 
 ATOL = {"f16": 2e-3, "bf16": 2e-3, "fp8": 5e-2}
 RTOL = 1e-2
@@ -127,7 +127,7 @@ def test_invalid_block_id_is_reported_not_fatal():
     assert g["err"] & 1, "block-id error bit not set"
     r = steps.decode_step(W.small_decode("bad", [40, 40], hq=2, hkv=2, d=64, bs=16, seed=45),
                           strides=g["strides"], pool_elems=g["pool"].size)
-    assert_close(g["out"][0], r["out"][0], 2e-3, RTOL, "unaffected sequence")
+    assert_close(g["out"][0], r["out"][0], 2e-3, RTOL, "unaffected sequence", out_dtype=OUT_DT(w))
 
 
 def test_append_out_of_pool_slot_is_reported_and_skipped():

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-from gpu_path import assert_close, run_decode  # noqa: E402
+from gpu_path import OUT_DT, assert_close, run_decode  # noqa: E402
 
 ATOL = {"f16": 2e-3, "bf16": 2e-3, "fp8": 5e-2}
 RTOL = 1e-2
@@ -64,7 +64,7 @@ def test_tensor_core_and_cuda_core_paths_agree(kv, monkeypatch):
     monkeypatch.setenv("PAGEDKV_DECODE_TC", "0")
     cc = check(w, f"{kv} CUDA cores")
     assert os.environ["PAGEDKV_DECODE_TC"] == "0"
-    assert_close(tc["out"], cc["out"], ATOL[kv], RTOL, "paths")
+    assert_close(tc["out"], cc["out"], ATOL[kv], RTOL, "paths", out_dtype=OUT_DT(w))
 
 
 @pytest.mark.parametrize("kv", ["fp8", "bf16"])
@@ -78,4 +78,4 @@ def test_invalid_block_id_on_the_tensor_core_path(kv):
     r = steps.decode_step(W.small_decode("badtc", lens, hq=8, hkv=2, d=128, bs=16, kv_dtype=kv, seed=520),
                           strides=g["strides"], pool_elems=g["pool"].size)
     for s in (0, 2):
-        assert_close(g["out"][s], r["out"][s], ATOL[kv], RTOL, f"unaffected sequence {s}")
+        assert_close(g["out"][s], r["out"][s], ATOL[kv], RTOL, f"unaffected sequence {s}", out_dtype=OUT_DT(w))
