@@ -618,20 +618,30 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
         bool ok = true;
         int64_t gs = 0;
         int nu = 0;
-        // table entry of this thread's block (row r of the step) in step i of unit un; -1 past the unit
+        // table entry of this thread's block (row r of the step) in step i of a unit, and whether that
+        // block belongs to the unit
         const int jb = r / a.bs;
-        auto blk_entry = [&](const Unit &x, int i) -> int {
-            return i * bpstep + jb < x.ntiles ? a.tables[(int64_t)x.s * a.max_blocks + x.blk0 + i * bpstep + jb] : -1;
+        // (the read is always made, from an index kept inside the table row, and whether the block
+        // belongs to the unit is kept apart: a select between the loaded value and -1 would wait for
+        // the load on the spot, while here the value is first used a step later)
+        auto blk_read = [&](const Unit &x, int i) -> int {
+            const int idx = min(x.blk0 + i * bpstep + jb, a.max_blocks - 1);
+            return a.tables[(int64_t)x.s * a.max_blocks + max(idx, 0)];
         };
+        auto blk_in = [&](const Unit &x, int i) -> bool { return i * bpstep + jb < x.ntiles; };
         // the units come from the K loader's records: the next one is read at the last step of the
         // current one, with the table entry of its first step; entries are read a step ahead
         int u = blockIdx.x;
         Unit un{};
         int tok_end = 0, ent = -1;
+        bool ent_in = false;
         float ksc = 1.f;
         if (u < U) {
             ok = read_rec(0, un, tok_end, ksc);
-            if (ok) ent = blk_entry(un, 0);
+            if (ok) {
+                ent = blk_read(un, 0);
+                ent_in = blk_in(un, 0);
+            }
         }
         for (; u < U && ok; u += gridDim.x, ++nu) {
             const int nsteps = (un.ntiles + bpstep - 1) / bpstep;
@@ -656,7 +666,9 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 // the next step's table entry (the next unit's first one after the last step)
                 bool rec_ok = true;
                 if (i + 1 == nsteps && u2 < U) rec_ok = read_rec(nu + 1, un2, tok_end2, ksc2);
-                const int ent_nx = i + 1 < nsteps ? blk_entry(un, i + 1) : (u2 < U && rec_ok ? blk_entry(un2, 0) : -1);
+                const bool last = i + 1 == nsteps;
+                const int ent_nx = blk_read(last ? un2 : un, last ? 0 : i + 1);
+                const bool ent_nx_in = last ? u2 < U && rec_ok && blk_in(un2, 0) : blk_in(un, i + 1);
                 bool mine = ok && rec_ok && *abort_flag == 0;
                 if constexpr (F8) {
                     // the unit's q exponent, published with its "Q converted" barrier
@@ -669,8 +681,9 @@ __global__ void __launch_bounds__(threads_for<KVT == PKV_FP8_E4M3>(), 1)
                 const int step0 = tok0 + i * TOK;
                 // a row holds a token of the unit if it lies before the unit's end and in a block whose
                 // table entry names a block of the pool (the loaders skip the others)
-                const bool valid = step0 + r < tok_end && ent >= 0 && ent < a.num_blocks;
+                const bool valid = step0 + r < tok_end && ent_in && ent >= 0 && ent < a.num_blocks;
                 ent = ent_nx;
+                ent_in = ent_nx_in;
                 float sc[G];
                 bool need = !mine; // a failed wait takes the exchange path, where `ok` is agreed
                 if (mine) {
