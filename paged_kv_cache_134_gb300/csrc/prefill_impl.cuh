@@ -32,6 +32,9 @@
 //  * O is rescaled in tensor memory only when a row's running maximum grows by more than 2^8 (the
 //    exponent base stays fixed otherwise, which is exact algebra); the softmax thread does it, since
 //    S(j) complete implies P V(j-1) complete.
+//  * Item boundaries: the K loader issues the next item's first K tile, then its Q tiles as their
+//    buffers free up; a tile's output (a whole tile of the sequence's rows) is staged in its own Q
+//    buffer and written by TMA stores, and the Q buffer returns to the loader once they have read it.
 //  * Every mbarrier wait is bounded; a timeout sets PKV_DEVERR_TIMEOUT and the CTA winds down.
 #pragma once
 
