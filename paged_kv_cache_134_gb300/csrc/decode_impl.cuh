@@ -24,10 +24,12 @@
 //    token (16-byte vector loads from shared memory, conflict-free), partial dot products are
 //    reduced with xor-shuffles, and an online softmax (running max m, sum l, rescaled
 //    accumulator) runs per 16-token chunk with exp2 on prescaled scores.
-//  * At the end of a unit the four warps' (m, l, acc) are merged through shared memory.  A
-//    sequence with one split writes its output row directly; otherwise the unit writes an
-//    fp32 partial (m, l, unnormalised o) and a merge kernel combines the splits in split
-//    order.
+//  * At the end of a unit each warp hands its (m, l, acc) to one of two merge slots in shared
+//    memory (by the parity of the CTA's unit count) and goes on to its next unit's tiles; the
+//    warp that hands in last merges the four in warp order and writes the result, so no warp
+//    waits for the others at a unit boundary while its next tiles land.  A sequence with one
+//    split writes its output row directly; otherwise the unit writes an fp32 partial (m, l,
+//    unnormalised o) and a merge kernel combines the splits in split order.
 //  * Every mbarrier wait is bounded (PKV_WAIT_LIMIT_NS); a timeout sets PKV_DEVERR_TIMEOUT
 //    and the CTA winds down without further waiting on work that will not arrive.
 #pragma once
@@ -357,6 +359,18 @@ PKV_DEV void build_unit_list(const Args &a, int *pf, int *pp, int *nb, int warp,
     __syncthreads();
 }
 
+// wait (bounded) until a shared-memory counter reaches n or the CTA aborts; false after the limit
+PKV_DEV bool wait_at_least(const int *x, int n, const int *abort_flag) {
+    const volatile int *v = x;
+    if (*v >= n) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (*v < n && !*reinterpret_cast<const volatile int *>(abort_flag)) {
+        if (global_timer_ns() - t0 > PKV_WAIT_LIMIT_NS) return false;
+        __nanosleep(32);
+    }
+    return true;
+}
+
 template <int D, int G, int MT, int KVT>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     using M = ModelT<MT>;
@@ -370,8 +384,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     uint64_t *empty = full + NST;
     int *flags = reinterpret_cast<int *>(empty + NST);
     int *abort_flag = flags + NST;
-    float *mrg = reinterpret_cast<float *>(abort_flag + 4);
-    int *pf = reinterpret_cast<int *>(mrg + NCW * G * (D + 2));
+    int *mcount = abort_flag + 1;                               // [2] warps handed in to merge slot p
+    int *mdone = abort_flag + 3;                                // [2] merges of slot p completed
+    float *mrg = reinterpret_cast<float *>(abort_flag + 8);     // [2 slots][NCW warps][G][D + 2]
+    int *pf = reinterpret_cast<int *>(mrg + 2 * NCW * G * (D + 2));
     int *pp = pf + (S + 1);
     int *nb = pp + (S + 1);
 
@@ -381,7 +397,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
-        *abort_flag = 0;
+        for (int i = 0; i < 8; ++i) abort_flag[i] = 0;
         fence_mbarrier_init();
     }
     pdl_wait(); // the previous kernel (e.g. the append of this step) has finished
@@ -451,9 +467,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     constexpr int LT = (G == 1) ? LY::LT : D / 8;
     constexpr int GS = (G == 1) ? 1 : G; // heads a lane carries
     const int sub = lane % LH, gl = (G == 1) ? 0 : 0, tg = lane / LT;
-    const int tid = threadIdx.x; // 0 .. NCW*32-1
     uint32_t tau = 0;
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+    int nu = 0; // this CTA's units so far
+    for (int u = blockIdx.x; u < U; u += gridDim.x, ++nu) {
         const Unit un = unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
         const int L = a.lens[un.s];
         float qs = a.qk_scale_log2;
@@ -517,10 +533,25 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
 #pragma unroll
                 for (int e = 0; e < DL; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
         }
+        // merge slot nu % 2 is free once the merge of this CTA's unit nu - 2 is done
+        const int sp = nu & 1;
+        float *slot = mrg + sp * (NCW * G * (D + 2));
+        bool ok = true;
+        if (lane == 0) {
+            ok = wait_at_least(mdone + sp, nu >> 1, abort_flag);
+            __threadfence_block(); // the merger's reads of the slot come before this warp's writes
+        }
+        __syncwarp();
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            set_error(a.err, PKV_DEVERR_TIMEOUT);
+            *reinterpret_cast<volatile int *>(abort_flag) = 1;
+        }
+        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
         if (tg == 0) {
 #pragma unroll
             for (int g = 0; g < GS; ++g) {
-                float *r = mrg + (warp * G + g + gl) * (D + 2);
+                float *r = slot + (warp * G + g + gl) * (D + 2);
 #pragma unroll
                 for (int e = 0; e < DL; ++e) r[sub * DL + e] = acc[g][e];
                 if (sub == 0) {
@@ -529,21 +560,30 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
                 }
             }
         }
-        named_barrier_sync(1, NCW * 32);
-        if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block(); // this warp's partial, then its hand-in
+            last = atomicAdd(mcount + sp, 1) == NCW - 1;
+            __threadfence_block(); // the last hand-in, then the other warps' partials
+        }
+        __syncwarp();
+        if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+        // the last warp to hand in: merge the four warps' partials in warp order
+        if (lane == 0) mcount[sp] = 0; // no warp hands in to this slot before mdone[sp] moves on
         const float vs = (KVT == PKV_FP8_E4M3) ? a.v_scale[un.kvh] : 1.f;
-        for (int o = tid; o < G * D; o += NCW * 32) {
+        for (int o = lane; o < G * D; o += 32) {
             const int g = o / D, d = o - g * D;
             float Mx = -INFINITY;
 #pragma unroll
             for (int w = 0; w < NCW; ++w) {
-                const float *r = mrg + (w * G + g) * (D + 2);
+                const float *r = slot + (w * G + g) * (D + 2);
                 if (r[D + 1] > 0.f) Mx = fmaxf(Mx, r[D]);
             }
             float num = 0.f, den = 0.f;
 #pragma unroll
             for (int w = 0; w < NCW; ++w) {
-                const float *r = mrg + (w * G + g) * (D + 2);
+                const float *r = slot + (w * G + g) * (D + 2);
                 if (r[D + 1] > 0.f) {
                     const float wt = fast_exp2(r[D] - Mx);
                     num = fmaf(wt, r[d], num);
@@ -560,7 +600,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
                 if (d == 0) reinterpret_cast<float2 *>(a.ws_ml)[idx] = make_float2(Mx, den);
             }
         }
-        named_barrier_sync(1, NCW * 32);
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            *reinterpret_cast<volatile int *>(mdone + sp) = mdone[sp] + 1;
+        }
     }
 }
 
@@ -656,7 +700,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const Args a) {
 }
 
 inline size_t smem_bytes(int D, int G, int nst, int tile_bytes, int S) {
-    return (size_t)nst * 2 * tile_bytes + (size_t)nst * (8 + 8 + 4) + 16 + (size_t)kConsumerWarps * G * (D + 2) * 4 +
+    return (size_t)nst * 2 * tile_bytes + (size_t)nst * (8 + 8 + 4) + 32 + (size_t)2 * kConsumerWarps * G * (D + 2) * 4 +
            (size_t)(3 * S + 2) * 4;
 }
 

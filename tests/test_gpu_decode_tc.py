@@ -26,8 +26,9 @@ from gpu_path import OUT_DT, assert_close, run_decode  # noqa: E402
 ATOL = {"f16": 2e-3, "bf16": 2e-3, "fp8": 5e-2}
 RTOL = 1e-2
 
-# token counts around the 128-token MMA step and the 512-token split
-LENS = [0, 1, 127, 128, 129, 511, 512, 513, 2000, 37]
+# token counts around the 128-token MMA step and the split (512 tokens for 16-bit caches, 1024 for
+# E4M3 ones)
+LENS = [0, 1, 127, 128, 129, 511, 512, 513, 1023, 1025, 2000, 37]
 
 
 def check(w, tag):
