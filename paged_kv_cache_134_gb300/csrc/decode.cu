@@ -83,6 +83,16 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
     a.err = c->err;
     a.num_blocks = c->num_blocks;
     a.tile_bytes = static_cast<int>(c->tile_bytes);
+    // a stage of the CUDA-core kernel holds at most PAGEDKV_DECODE_STAGE_BYTES of K plus V (8 KB:
+    // 16 tokens at fp16 and D=128), so that bs=32 blocks go in two stages and as many CTAs fit an
+    // SM as with bs=16 (the consumer warps' per-stage work is latency bound; more warps hide it)
+    {
+        const int64_t cap = env_int("PAGEDKV_DECODE_STAGE_BYTES", 8192);
+        int t = c->block_size;
+        while (t > 8 && (t & 1) == 0 && 2 * (int64_t)t * c->head_dim * c->elem_bytes > cap) t >>= 1;
+        a.sub_tokens = t;
+        a.sub_bytes = static_cast<int>((int64_t)t * c->head_dim * c->elem_bytes);
+    }
     a.kv_stride = (int64_t)c->num_kv_heads * c->tile_bytes;
     a.blk_stride = 2 * a.kv_stride;
     a.max_blocks = d.max_blocks;
@@ -124,13 +134,13 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
         return e;
     }
     // stages: fill the per-CTA shared-memory budget
-    const size_t fixed = smem_bytes(c->head_dim, G, 0, a.tile_bytes, d.num_seqs);
-    const size_t per_stage = smem_bytes(c->head_dim, G, 1, a.tile_bytes, d.num_seqs) - fixed;
+    const size_t fixed = smem_bytes(c->head_dim, G, 0, a.sub_bytes, d.num_seqs);
+    const size_t per_stage = smem_bytes(c->head_dim, G, 1, a.sub_bytes, d.num_seqs) - fixed;
     // CTAs per SM: the target, or fewer when registers allow fewer (grouped heads); the stage ring
     // then takes that many CTAs' share of shared memory, so the bytes in flight per SM stay high
     int want = ctas_per_sm();
     {
-        const int fit = occ(c->head_dim, G, smem_bytes(c->head_dim, G, kConsumerWarps, a.tile_bytes, d.num_seqs));
+        const int fit = occ(c->head_dim, G, smem_bytes(c->head_dim, G, kConsumerWarps, a.sub_bytes, d.num_seqs));
         if (fit >= 1 && fit < want) want = fit;
     }
     const size_t budget = (size_t)(233472 / want) - 1024;
@@ -141,7 +151,7 @@ cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st) 
     if (nst > 32) nst = 32;
     if (nst < kConsumerWarps) nst = kConsumerWarps;
     a.nstages = nst;
-    const size_t smem = smem_bytes(c->head_dim, G, nst, a.tile_bytes, d.num_seqs);
+    const size_t smem = smem_bytes(c->head_dim, G, nst, a.sub_bytes, d.num_seqs);
     int per_sm = occ(c->head_dim, G, smem);
     if (per_sm < 1) per_sm = 1;
     const int grid = c->num_sms * per_sm;

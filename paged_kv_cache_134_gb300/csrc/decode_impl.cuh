@@ -19,7 +19,10 @@
 //    tile into a ring of shared-memory stages, completion tracked by mbarrier transaction
 //    counts.  The pool layout [block][K|V][head][offset][dim] makes each tile one contiguous
 //    bs*D*elt-byte run (4 KB for bs=16, D=128, fp16), so one table lookup yields two large
-//    aligned copies.  The copies carry an L2 evict-first hint: KV is streamed once.
+//    aligned copies.  Blocks whose K plus V tile would exceed a stage's bytes (bs=32 at fp16,
+//    D=128) go in equal parts of consecutive tokens, one part per stage, so that a stage stays
+//    small and more CTAs fit an SM; parts wholly past the sequence's end are not loaded.  The
+//    copies carry an L2 evict-first hint: KV is streamed once.
 //  * Four consumer warps take the tiles round-robin by their index in the CTA's tile stream.  In a warp, D/8 lanes share a
 //    token (16-byte vector loads from shared memory, conflict-free), partial dot products are
 //    reduced with xor-shuffles, and an online softmax (running max m, sum l, rescaled
@@ -55,6 +58,9 @@ struct Args {
     int64_t blk_stride;  // bytes between consecutive physical blocks
     int64_t kv_stride;   // bytes between the K and V halves of a block
     int tile_bytes;      // one (block, K|V, head) tile
+    // one stage of the CUDA-core kernel's ring: sub_tokens consecutive tokens of a block (the
+    // whole block, or an equal part of it) of one head, K then V, sub_bytes each
+    int sub_tokens, sub_bytes;
     int max_blocks, num_seqs, hq, hkv, bs;
     int split_blocks, max_splits, nstages;
     float qk_scale_log2; // scale * log2(e)
@@ -380,7 +386,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     const int NST = a.nstages;
     const int S = a.num_seqs;
     char *ring = reinterpret_cast<char *>(smem);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NST * 2 * a.tile_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NST * 2 * a.sub_bytes);
     uint64_t *empty = full + NST;
     int *flags = reinterpret_cast<int *>(empty + NST);
     int *abort_flag = flags + NST;
@@ -407,6 +413,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     const int bps = a.split_blocks;
     build_unit_list(a, pf, pp, nb, warp, lane);
     const int U = (pf[S] + pp[S]) * a.hkv;
+    const int ST = a.sub_tokens, spb = a.bs / a.sub_tokens; // stage tokens, stages per block
 
     if (warp == NCW) {
         // ---------------------------------------------------------------- producer warp
@@ -417,33 +424,37 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
             const Unit un = unit_info(u, pf, pp, nb, S, a.hkv, bps, a.start_block);
             const int32_t *trow = a.tables + (int64_t)un.s * a.max_blocks + un.blk0;
             const char *head_base = a.pool + (int64_t)un.kvh * a.tile_bytes;
+            // stages of this unit: spb per block, less the parts wholly past the sequence's end
+            const int nt = spb > 1 ? min(un.ntiles * spb, (a.lens[un.s] - un.blk0 * a.bs + ST - 1) / ST) : un.ntiles;
             for (int i0 = 0; i0 < un.ntiles && ok; i0 += 32) {
                 const int cnt = min(32, un.ntiles - i0);
                 const int myb = lane < cnt ? trow[i0 + lane] : 0;
-                for (int i = 0; i < cnt; ++i) {
+                for (int i = 0; i < cnt && ok; ++i) {
                     const int b = __shfl_sync(0xffffffffu, myb, i);
-                    if (lane == 0) {
-                        const uint32_t stage = tau % NST, round = tau / NST;
-                        if (round > 0 && !mbar_wait(&empty[stage], (round - 1) & 1)) {
-                            // stop issuing; the consumers time out on the stages that never fill
-                            set_error(a.err, PKV_DEVERR_TIMEOUT);
-                            ok = false;
-                        } else if (b >= 0 && b < a.num_blocks) {
-                            flags[stage] = 0;
-                            char *dst = ring + (size_t)stage * 2 * a.tile_bytes;
-                            const char *src = head_base + (int64_t)b * a.blk_stride;
-                            mbar_arrive_expect_tx(&full[stage], 2u * a.tile_bytes);
-                            bulk_g2s_hint(dst, src, a.tile_bytes, &full[stage], policy);
-                            bulk_g2s_hint(dst + a.tile_bytes, src + a.kv_stride, a.tile_bytes, &full[stage], policy);
-                        } else {
-                            flags[stage] = 1;
-                            set_error(a.err, PKV_DEVERR_BLOCK_ID);
-                            mbar_arrive(&full[stage]);
+                    for (int h = 0, k = (i0 + i) * spb; h < spb && k < nt; ++h, ++k) {
+                        if (lane == 0) {
+                            const uint32_t stage = tau % NST, round = tau / NST;
+                            if (round > 0 && !mbar_wait(&empty[stage], (round - 1) & 1)) {
+                                // stop issuing; the consumers time out on the stages that never fill
+                                set_error(a.err, PKV_DEVERR_TIMEOUT);
+                                ok = false;
+                            } else if (b >= 0 && b < a.num_blocks) {
+                                flags[stage] = 0;
+                                char *dst = ring + (size_t)stage * 2 * a.sub_bytes;
+                                const char *src = head_base + (int64_t)b * a.blk_stride + (int64_t)h * a.sub_bytes;
+                                mbar_arrive_expect_tx(&full[stage], 2u * a.sub_bytes);
+                                bulk_g2s_hint(dst, src, a.sub_bytes, &full[stage], policy);
+                                bulk_g2s_hint(dst + a.sub_bytes, src + a.kv_stride, a.sub_bytes, &full[stage], policy);
+                            } else {
+                                flags[stage] = 1;
+                                set_error(a.err, PKV_DEVERR_BLOCK_ID);
+                                mbar_arrive(&full[stage]);
+                            }
                         }
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) break;
+                        ++tau;
                     }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) break;
-                    ++tau;
                 }
             }
         }
@@ -497,7 +508,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
         // the parity wait unambiguous.
         int i0 = warp - static_cast<int>(tau % NCW);
         if (i0 < 0) i0 += NCW;
-        for (int i = i0; i < un.ntiles; i += NCW) {
+        const int nt = spb > 1 ? min(un.ntiles * spb, (L - un.blk0 * a.bs + ST - 1) / ST) : un.ntiles;
+        for (int i = i0; i < nt; i += NCW) {
             const uint32_t t = tau + i;
             const uint32_t stage = t % NST;
             if (!mbar_wait(&full[stage], (t / NST) & 1)) {
@@ -506,17 +518,17 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
             }
             if (*reinterpret_cast<volatile int *>(abort_flag)) break;
             if (!flags[stage]) {
-                const char *ks = ring + (size_t)stage * 2 * a.tile_bytes;
-                const int valid = min(a.bs, L - (un.blk0 + i) * a.bs);
+                const char *ks = ring + (size_t)stage * 2 * a.sub_bytes;
+                const int valid = min(ST, L - un.blk0 * a.bs - i * ST);
                 if constexpr (G == 1)
-                    process_tile<D, 1, KVT>(ks, ks + a.tile_bytes, a.bs, valid, qf[0], m[0], l[0], acc[0], lane);
+                    process_tile<D, 1, KVT>(ks, ks + a.sub_bytes, ST, valid, qf[0], m[0], l[0], acc[0], lane);
                 else
-                    process_tile_tp<D, G, KVT>(ks, ks + a.tile_bytes, a.bs, valid, qf, m, l, acc, lane);
+                    process_tile_tp<D, G, KVT>(ks, ks + a.sub_bytes, ST, valid, qf, m, l, acc, lane);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
         }
-        tau += un.ntiles;
+        tau += nt;
         // combine the token groups of this warp (same heads, same dims); for G >= 2 the row sums are
         // spread over all lanes
 #pragma unroll
@@ -699,8 +711,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const Args a) {
     }
 }
 
-inline size_t smem_bytes(int D, int G, int nst, int tile_bytes, int S) {
-    return (size_t)nst * 2 * tile_bytes + (size_t)nst * (8 + 8 + 4) + 32 + (size_t)2 * kConsumerWarps * G * (D + 2) * 4 +
+inline size_t smem_bytes(int D, int G, int nst, int stage_part_bytes, int S) {
+    return (size_t)nst * 2 * stage_part_bytes + (size_t)nst * (8 + 8 + 4) + 32 + (size_t)2 * kConsumerWarps * G * (D + 2) * 4 +
            (size_t)(3 * S + 2) * 4;
 }
 

@@ -76,6 +76,23 @@ def test_edge_cases(case):
     check_decode(W.small_decode("edge", case.pop("lens"), seed=41, **case), "edge")
 
 
+# A block whose K plus V tiles exceed a stage of the CUDA-core kernel goes in parts of consecutive
+# tokens (16 at fp16 and D=128 with the default 8 KB stage, 8 with a 4 KB one, the whole block with
+# a 64 KB one); parts wholly past a sequence's end are not loaded.  Lengths around the parts' and
+# the blocks' ends, one head per KV head and four (grouped heads kept off the tensor cores).
+PARTS_LENS = [1, 7, 8, 9, 15, 16, 17, 24, 31, 32, 33, 48, 49, 257, 300, 513]
+
+
+@pytest.mark.parametrize("stage_bytes", [None, "4096", "65536"])
+@pytest.mark.parametrize("hq,kv", [(4, "f16"), (16, "bf16")], ids=["G1_f16", "G4_bf16"])
+def test_blocks_in_stage_parts(stage_bytes, hq, kv, monkeypatch):
+    if stage_bytes:
+        monkeypatch.setenv("PAGEDKV_DECODE_STAGE_BYTES", stage_bytes)
+    monkeypatch.setenv("PAGEDKV_DECODE_TC", "0")
+    w = W.small_decode("parts", PARTS_LENS, hq=hq, hkv=4, d=128, bs=32, kv_dtype=kv, seed=48)
+    check_decode(w, f"parts {stage_bytes} {kv}")
+
+
 def test_single_token_returns_v0_bit_exact():
     w = W.small_decode("one", [0, 0, 0, 0], hq=8, hkv=2, d=128, bs=16, kv_dtype="bf16", seed=42)
     g = run_decode(w)
