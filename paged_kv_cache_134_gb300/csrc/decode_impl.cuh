@@ -623,8 +623,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
 // Merge of the per-split partials of sequences with more than one split; zero rows for
 // L_s == 0.  One CTA of four warps per (sequence, query head) row: every warp forms the common
 // max M from all splits' (m, l), then accumulates the splits j = warp, warp + 4, ... (lane = D/32
-// dims, vector loads, loads issued ahead of their use); the four warp sums are added in warp order
-// through shared memory, so the result is deterministic.
+// dims, vector loads; the first 16 splits' loads go out with those of the maxima); the four warp
+// sums are added in warp order through shared memory, so the result is deterministic.
 template <int D, int MT>
 __global__ void __launch_bounds__(128) merge_kernel(const Args a) {
     using M = ModelT<MT>;
@@ -655,20 +655,11 @@ __global__ void __launch_bounds__(128) merge_kernel(const Args a) {
     }
     const int64_t base = (int64_t)row * a.max_splits;
     const float2 *ml = reinterpret_cast<const float2 *>(a.ws_ml) + base;
-    float Mx = -INFINITY;
-    for (int j = lane; j < nsplit; j += 32) {
-        const float2 v = ml[j];
-        if (v.y > 0.f) Mx = fmaxf(Mx, v.x);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
-    float num[PER], den = 0.f;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) num[e] = 0.f;
+    // this warp's splits j0, j0 + 4, ... (U of them): (m, l) and its lane's dims of o
     constexpr int U = 4;
-    for (int j0 = warp; j0 < nsplit; j0 += 4 * U) {
-        float2 mlj[U];
-        float vj[U][PER];
+    float2 mlj[U];
+    float vj[U][PER];
+    auto load_group = [&](int j0) {
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const int j = j0 + 4 * k;
@@ -690,6 +681,22 @@ __global__ void __launch_bounds__(128) merge_kernel(const Args a) {
                 mlj[k] = make_float2(0.f, 0.f);
             }
         }
+    };
+    // the first group (all splits of a row with up to 16) is loaded with the maxima's (m, l), so the
+    // row takes one round trip to memory instead of two
+    load_group(warp);
+    float Mx = -INFINITY;
+    for (int j = lane; j < nsplit; j += 32) {
+        const float2 v = ml[j];
+        if (v.y > 0.f) Mx = fmaxf(Mx, v.x);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
+    float num[PER], den = 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) num[e] = 0.f;
+    for (int j0 = warp; j0 < nsplit; j0 += 4 * U) {
+        if (j0 != warp) load_group(j0);
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             if (mlj[k].y > 0.f) {
