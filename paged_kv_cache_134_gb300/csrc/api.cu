@@ -425,7 +425,7 @@ int paged_decode_attention_cascade(const void *q, pkv_cache_t c, const int32_t *
     d.num_seqs = num_seqs;
     d.num_q_heads = num_q_heads;
     d.scale = scale;
-    d.split_blocks = decode_split_blocks(c);
+    d.split_blocks = cascade_suffix_split_blocks(c);
     d.max_splits = nps + (max_blocks_per_seq - pb + d.split_blocks - 1) / d.split_blocks;
     d.start_block = pb;
     d.slot0 = nps;

@@ -50,6 +50,15 @@ int decode_split_blocks(const pkv_cache *c) {
     return b > 0 ? b : 1;
 }
 
+int cascade_suffix_split_blocks(const pkv_cache *c) {
+    // the suffixes of a cascade batch are short (a few hundred tokens): 128-token splits give the
+    // CTAs twice as many, half as long units, which evens out their finish times (prefix13b: step
+    // 101.5-102.3 -> 100.2-101.5 us); the tensor-core decode keeps its own longer splits
+    const int tokens = env_int("PAGEDKV_CASCADE_SUFFIX_TOKENS", 128);
+    const int b = tokens / c->block_size;
+    return b > 0 ? b : 1;
+}
+
 int decode_seqs_per_launch(const pkv_cache *c, int G) {
     // Both decode kernels keep a per-sequence unit table (3 ints a sequence) in shared memory: the
     // CUDA-core kernel takes up to kMaxSeqs sequences a launch; the tensor-core kernel, whose stage

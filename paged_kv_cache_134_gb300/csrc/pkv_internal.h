@@ -159,6 +159,7 @@ cudaError_t launch_decode_chunked(pkv_cache *c, DecodeLaunch d, cudaStream_t st)
 // takes the rest of the device memory.
 int pkv_noalloc_scratch_prepare(int device);
 int decode_split_blocks(const pkv_cache *c);
+int cascade_suffix_split_blocks(const pkv_cache *c); // blocks per split of a cascade's suffix decode
 cudaError_t launch_decode(pkv_cache *c, const DecodeLaunch &d, cudaStream_t st);
 // tensor-core decode for grouped-query heads (decode_tc.cu)
 namespace pkv_decode {
