@@ -82,6 +82,22 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    def wait_running(self, limit_s: float = 10.0):
+        """Until nvidia-smi has written its first sample (its start-up talks to the driver at length,
+        which would otherwise fall into the timed region), or it has exited, or limit_s has passed."""
+        if self.proc is None:
+            return
+        t0 = time.time()
+        while time.time() - t0 < limit_s and self.proc.poll() is None:
+            self.f.flush()
+            try:
+                if os.path.getsize(self.path) > 0:
+                    break
+            except OSError:
+                break
+            time.sleep(0.02)
+        time.sleep(0.1) # past the first sample's own driver queries
+
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
@@ -568,7 +584,7 @@ def run_ours(args):
     # ---- timed region: inputs resident in HBM; KV (1.07 GB/step) is larger than L2 (129 MB)
     clock_dir = args.clocks_dir or tempfile.gettempdir()
     sampler = ClockSampler(local, os.path.join(clock_dir, f"pkv_clocks_rank{rank}.csv"))
-    time.sleep(0.2)
+    sampler.wait_running()
     launches0 = P.kernel_launches()
     # no events inside the timed region: an event between two kernels stops the append -> decode ->
     # merge overlap of programmatic dependent launch
