@@ -29,3 +29,40 @@ def test_recorded_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     assert bench._recorded_traffic("k.md") is None
     assert bench._recorded_traffic("missing.md") is None
 
+
+
+def _fake_smi(tmp_path, line):
+    """A stand-in `nvidia-smi` on PATH that prints one CSV sample line every 20 ms."""
+    d = tmp_path / "bin"
+    d.mkdir()
+    exe = d / "nvidia-smi"
+    exe.write_text(f"#!{sys.executable}\nimport sys, time\n"
+                   f"while True:\n    print({line!r}, flush=True)\n    time.sleep(0.02)\n")
+    exe.chmod(0o755)
+    return str(d)
+
+
+@pytest.mark.parametrize("line,reasons", [
+    ("0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Active", ["sw_power_cap"]),
+    ("0, 1500, 2070, 1390.0, 0x8, Active, Not Active, Not Active, Not Active", ["hw_slowdown"]),
+])
+def test_clock_sampler_waits_for_its_first_sample_and_reads_reasons(tmp_path, monkeypatch, line, reasons):
+    import time
+    monkeypatch.setenv("PATH", _fake_smi(tmp_path, line) + os.pathsep + os.environ.get("PATH", ""))
+    path = str(tmp_path / "clk.csv")
+    c = bench.ClockSampler(0, path)
+    c.wait_running(limit_s=10)
+    assert os.path.getsize(path) > 0  # the timed region starts only once a sample is in
+    time.sleep(0.1)
+    r = c.stop()
+    assert r["samples"] >= 1
+    assert r["sm_max_mhz"] == 2070.0
+    assert r["sm_mhz"] == float(line.split(",")[1])
+    assert r["reasons"] == reasons
+
+
+def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
+    monkeypatch.setenv("PATH", str(tmp_path))  # nothing named nvidia-smi there
+    c = bench.ClockSampler(0, str(tmp_path / "clk.csv"))
+    c.wait_running(limit_s=1)
+    assert c.stop()["reasons"] == ["nvidia-smi unavailable"]
